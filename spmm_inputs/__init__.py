@@ -1,0 +1,196 @@
+"""Seeded synthetic inputs for the SpMM workloads.
+
+This module only draws random numbers and lays them out as plain arrays
+(dense matrices as raw 16-bit / 8-bit patterns, CSR arrays, kept-column
+lists).  It holds none of the SpMM arithmetic and none of the format
+builders: both the CPU oracle and the CUDA path receive exactly the arrays
+produced here.
+
+Every generator uses numpy's PCG64 (``numpy.random.default_rng(seed)``).
+Floating-point values are drawn in fp32 from N(0, std) and rounded to
+bf16 / fp16 with round-to-nearest-even; both sides read the rounded bits.
+
+Workload recipes (sizes follow the five configurations the library is
+measured on):
+
+* ``bcsr_problem``   block-sparse A: an exact number of bh x bw blocks,
+  positions drawn uniformly without replacement, every entry of a drawn
+  block N(0, std); dense B N(0, 1).
+* ``mask24_problem`` 2:4 int8 A: in every group of 4 consecutive K entries
+  exactly 2 positions (uniform among the 6 pairs) hold values uniform on
+  {-127..-1, 1..127}; B uniform on [-127, 127].
+* ``csr_lognormal_problem`` irregular CSR A: row lengths
+  clip(round(LogNormal(ln(mean) - sigma^2/2, sigma)), 1, clip), columns
+  uniform without duplicates per row (ascending), values N(0, 1); B N(0, 1).
+* ``tvw_problem``    tile-vector-wise A: per tile of ``tile_rows`` rows a
+  uniform random kept subset of K columns (ascending), then inside every
+  group of 4 consecutive kept columns exactly 2 positions per row hold
+  N(0, 1) values; B N(0, 1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BF16, F16, I8 = "bf16", "f16", "i8"
+
+__all__ = [
+    "BF16", "F16", "I8", "round_f32_to_bf16_bits", "normal_bits",
+    "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem",
+    "CONFIGS", "config_problem",
+]
+
+
+def round_f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round-to-nearest-even (NaN kept quiet)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    nan = (u & 0x7FFFFFFF) > 0x7F800000
+    bias = ((u >> 16) & 1) + np.uint32(0x7FFF)
+    r = ((u + bias) >> 16).astype(np.uint16)
+    if nan.any():
+        r[nan] = ((u[nan] >> 16) | 0x0040).astype(np.uint16)
+    return r
+
+
+def normal_bits(rng: np.random.Generator, shape, dtype: str, std: float = 1.0) -> np.ndarray:
+    """N(0, std) drawn in fp32, returned as uint16 bit patterns of ``dtype``."""
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    if dtype == BF16:
+        return round_f32_to_bf16_bits(x)
+    if dtype == F16:
+        return x.astype(np.float16).view(np.uint16)
+    raise ValueError(dtype)
+
+
+def bcsr_problem(M: int, K: int, N: int, bh: int, bw: int, nnzb: int, seed: int,
+                 dtype: str = BF16, std: float = 1.0, b_std: float = 1.0) -> dict:
+    """Dense A (bits, M x K) with exactly ``nnzb`` nonzero blocks, and B (K x N)."""
+    rng = np.random.default_rng(seed)
+    gm, gk = M // bh, K // bw
+    nblocks = gm * gk
+    pos = np.sort(rng.choice(nblocks, size=nnzb, replace=False)) if nnzb else np.zeros(0, np.int64)
+    A = np.zeros((M, K), dtype=np.uint16)
+    vals = normal_bits(rng, (nnzb, bh, bw), dtype, std)
+    Ab = A.reshape(gm, bh, gk, bw)
+    for t, p in enumerate(pos.tolist()):
+        Ab[p // gk, :, p % gk, :] = vals[t]
+    B = normal_bits(rng, (K, N), dtype, b_std)
+    return {"A": A, "B": B, "M": M, "K": K, "N": N, "bh": bh, "bw": bw,
+            "dtype": dtype, "block_pos": pos}
+
+
+def mask24_problem(M: int, K: int, N: int, seed: int) -> dict:
+    """int8 A with exactly 2 nonzeros in each group of 4 along K; int8 B."""
+    assert K % 4 == 0
+    rng = np.random.default_rng(seed)
+    pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)], dtype=np.int64)
+    G = K // 4
+    A = np.zeros((M, K), dtype=np.int8)
+    chunk = max(1, (1 << 24) // max(1, K))
+    for r0 in range(0, M, chunk):
+        r1 = min(M, r0 + chunk)
+        sel = pairs[rng.integers(0, 6, size=(r1 - r0, G))]          # (rows, G, 2)
+        mag = rng.integers(1, 128, size=(r1 - r0, G, 2), dtype=np.int16)
+        sgn = rng.integers(0, 2, size=(r1 - r0, G, 2), dtype=np.int16) * 2 - 1
+        v = (mag * sgn).astype(np.int8)
+        cols = sel + (np.arange(G, dtype=np.int64) * 4)[None, :, None]
+        rows = np.arange(r0, r1, dtype=np.int64)[:, None, None]
+        A[np.broadcast_to(rows, cols.shape), cols] = v
+    B = rng.integers(-127, 128, size=(K, N), dtype=np.int16).astype(np.int8)
+    return {"A": A, "B": B, "M": M, "K": K, "N": N, "dtype": I8}
+
+
+def _unique_sorted_rows(rng, lengths: np.ndarray, K: int):
+    """Per row, ``lengths[r]`` distinct columns uniform on [0, K), ascending."""
+    M = lengths.shape[0]
+    row_ptr = np.zeros(M + 1, dtype=np.int64)
+    np.cumsum(lengths, out=row_ptr[1:])
+    nnz = int(row_ptr[-1])
+    rows = np.repeat(np.arange(M, dtype=np.int64), lengths)
+    cols = rng.integers(0, K, size=nnz, dtype=np.int64)
+    while True:
+        order = np.lexsort((cols, rows))
+        rs, cs = rows[order], cols[order]
+        dup = np.zeros(nnz, dtype=bool)
+        if nnz > 1:
+            dup[1:] = (rs[1:] == rs[:-1]) & (cs[1:] == cs[:-1])
+        rows, cols = rs, cs
+        nd = int(dup.sum())
+        if nd == 0:
+            break
+        cols = cols.copy()
+        cols[dup] = rng.integers(0, K, size=nd, dtype=np.int64)
+    return row_ptr, cols
+
+
+def csr_lognormal_problem(M: int, K: int, N: int, seed: int, mean: float = 16.0,
+                          sigma: float = 1.5, clip: int = 4096, dtype: str = F16) -> dict:
+    """CSR A with log-normal row lengths (mean ``mean``), values N(0,1); B (K x N)."""
+    rng = np.random.default_rng(seed)
+    mu = np.log(mean) - sigma * sigma / 2.0
+    X = rng.lognormal(mean=mu, sigma=sigma, size=M)
+    L = np.clip(np.rint(X), 1, min(clip, K)).astype(np.int64)
+    row_ptr, cols = _unique_sorted_rows(rng, L, K)
+    val = normal_bits(rng, (cols.shape[0],), dtype)
+    B = normal_bits(rng, (K, N), dtype)
+    return {"row_ptr": row_ptr.astype(np.int32), "col": cols.astype(np.int32), "val": val,
+            "B": B, "M": M, "K": K, "N": N, "dtype": dtype}
+
+
+def tvw_problem(M: int, K: int, N: int, tile_rows: int, keep: int, seed: int,
+                dtype: str = F16) -> dict:
+    """Dense A (bits) in tile-vector-wise form plus the per-tile kept columns."""
+    assert keep % 4 == 0 and keep <= K
+    rng = np.random.default_rng(seed)
+    nt = (M + tile_rows - 1) // tile_rows
+    pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)], dtype=np.int64)
+    tile_ptr = np.arange(nt + 1, dtype=np.int64) * keep
+    cols = np.zeros(nt * keep, dtype=np.int64)
+    A = np.zeros((M, K), dtype=np.uint16)
+    G = keep // 4
+    for t in range(nt):
+        kc = np.sort(rng.choice(K, size=keep, replace=False))
+        cols[t * keep:(t + 1) * keep] = kc
+        r0, r1 = t * tile_rows, min(M, (t + 1) * tile_rows)
+        sel = pairs[rng.integers(0, 6, size=(r1 - r0, G))]
+        kidx = sel + (np.arange(G, dtype=np.int64) * 4)[None, :, None]
+        v = normal_bits(rng, (r1 - r0, G, 2), dtype)
+        rows = np.arange(r0, r1, dtype=np.int64)[:, None, None]
+        A[np.broadcast_to(rows, kidx.shape), kc[kidx]] = v
+    B = normal_bits(rng, (K, N), dtype)
+    return {"A": A, "B": B, "tile_ptr": tile_ptr.astype(np.int32), "cols": cols.astype(np.int32),
+            "M": M, "K": K, "N": N, "tile_rows": tile_rows, "dtype": dtype}
+
+
+# The five measured workloads.  ``nnzb`` for the block-sparse ones is the exact
+# count round((1 - sparsity) * number_of_blocks).
+CONFIGS = {
+    "bcsr_tiny": dict(kind="bcsr", M=256, K=256, N=64, bh=16, bw=16, nnzb=64, seed=1,
+                      dtype=BF16, std=1.0),
+    "mask24_int8": dict(kind="24", M=8192, K=8192, N=4096, seed=2),
+    "wcsr_lognormal": dict(kind="wcsr", M=65536, K=65536, N=128, seed=3, mean=16.0,
+                           sigma=1.5, clip=4096, dtype=F16),
+    "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
+                     dtype=BF16, std=0.02),
+    "tvw": dict(kind="tvw", M=4096, K=4096, N=4096, tile_rows=128, keep=2048, seed=5, dtype=F16),
+}
+
+
+def config_problem(name: str, **overrides) -> dict:
+    """Generate the named workload (keyword overrides shrink it for tests)."""
+    c = dict(CONFIGS[name])
+    c.update(overrides)
+    kind = c.pop("kind")
+    if kind == "bcsr":
+        return bcsr_problem(c["M"], c["K"], c["N"], c["bh"], c["bw"], c["nnzb"], c["seed"],
+                            c.get("dtype", BF16), c.get("std", 1.0))
+    if kind == "24":
+        return mask24_problem(c["M"], c["K"], c["N"], c["seed"])
+    if kind == "wcsr":
+        return csr_lognormal_problem(c["M"], c["K"], c["N"], c["seed"], c.get("mean", 16.0),
+                                     c.get("sigma", 1.5), c.get("clip", 4096), c.get("dtype", F16))
+    if kind == "tvw":
+        return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
+                           c.get("dtype", F16))
+    raise ValueError(kind)

@@ -1,0 +1,43 @@
+"""The seeded input generators produce the stated structure."""
+import numpy as np
+
+import spmm_inputs as gen
+
+
+def test_bcsr_problem_exact_block_count_and_determinism():
+    p = gen.bcsr_problem(256, 256, 64, 16, 16, 64, seed=1)
+    blocks = (p["A"].reshape(16, 16, 16, 16) & 0x7FFF).any(axis=(1, 3))
+    assert blocks.sum() == 64
+    q = gen.bcsr_problem(256, 256, 64, 16, 16, 64, seed=1)
+    assert np.array_equal(p["A"], q["A"]) and np.array_equal(p["B"], q["B"])
+
+
+def test_mask24_problem_two_per_group():
+    p = gen.mask24_problem(64, 256, 8, seed=2)
+    g = p["A"].reshape(64, 64, 4)
+    assert np.all((g != 0).sum(axis=2) == 2)
+    assert p["A"].min() >= -127 and p["A"].max() <= 127
+    assert p["B"].min() >= -127 and p["B"].max() <= 127
+
+
+def test_csr_lognormal_rows_sorted_unique_and_mean():
+    p = gen.csr_lognormal_problem(20000, 65536, 4, seed=3)
+    rp, col = p["row_ptr"], p["col"]
+    L = np.diff(rp)
+    assert L.min() >= 1 and L.max() <= 4096
+    assert 13.0 < L.mean() < 19.0
+    rows = np.repeat(np.arange(20000), L)
+    same = rows[1:] == rows[:-1]
+    assert np.all(col[1:][same] > col[:-1][same])
+
+
+def test_tvw_problem_structure():
+    p = gen.tvw_problem(256, 512, 8, tile_rows=128, keep=256, seed=5)
+    for t in range(2):
+        kc = p["cols"][p["tile_ptr"][t]:p["tile_ptr"][t + 1]]
+        assert len(kc) == 256 and np.all(np.diff(kc) > 0)
+        rows = p["A"][t * 128:(t + 1) * 128]
+        outside = np.setdiff1d(np.arange(512), kc)
+        assert not (rows[:, outside] & 0x7FFF).any()
+        g = (rows[:, kc] & 0x7FFF).reshape(128, 64, 4) != 0
+        assert np.all(g.sum(axis=2) == 2)

@@ -1,0 +1,280 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+* fp16 / bf16 decoding: exhaustive over all 65536 bit patterns, against numpy.
+* hand-worked fixtures under tests/golden/ (each cites the passage it reads).
+* brute-force dense GEMM (numpy) on the densified operand.
+* format round trips, invariants, and reductions to textbook routines
+  (scipy CSR SpMM for one-row windows; dense GEMM when every block is stored;
+  dense GEMM on the even-compressed K when every nibble is (0, 1)).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import spmm_inputs as gen
+from tests._helpers import bits_to_f64, golden, to_bits
+
+
+# ---------------------------------------------------------------- decoding
+def test_decode_f16_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode(bits, "f16")
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_decode_bf16_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode(bits, "bf16")
+    ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_bf16_rounding_is_rne():
+    # the input generator's rounding: ties to even, checked on hand-picked values
+    x = np.array([1.0, 1.00390625, 1.01171875, -2.5, 3.0e38], dtype=np.float32)
+    b = gen.round_f32_to_bf16_bits(x)
+    # 1 + 2^-8 is a tie between 1 and 1+2^-7 -> even (1.0);
+    # 1 + 3*2^-8 is a tie between 1+2^-7 and 1+2^-6 -> even (1+2^-6)
+    assert b.tolist() == [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x7F62]
+
+
+# ---------------------------------------------------------------- BCSR
+def test_bcsr_golden():
+    g = golden("bcsr_bf16_4x6.json")
+    A, B = to_bits(g["A"], "bf16"), to_bits(g["B"], "bf16")
+    F = oracle.bcsr_build(A, g["bh"], g["bw"], "bf16")
+    assert F["row_ptr"].tolist() == g["row_ptr"]
+    assert F["col_idx"].tolist() == g["col_idx"]
+    assert np.array_equal(F["vals"], to_bits(g["vals"], "bf16"))
+    assert np.array_equal(oracle.bcsr_spmm(F, B), np.array(g["C"], dtype=np.float64))
+
+
+def _dense_ref(A_bits, B_bits, dtype):
+    return bits_to_f64(A_bits, dtype) @ bits_to_f64(B_bits, dtype)
+
+
+@pytest.mark.parametrize("bh,bw", [(16, 16), (2, 4), (8, 8)])
+def test_bcsr_vs_dense_gemm(bh, bw):
+    p = gen.bcsr_problem(64, 96, 40, bh, bw, nnzb=(64 // bh) * (96 // bw) // 3, seed=7)
+    F = oracle.bcsr_build(p["A"], bh, bw, "bf16")
+    got = oracle.bcsr_spmm(F, p["B"])
+    ref = _dense_ref(p["A"], p["B"], "bf16")
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # round trip and the exact block count
+    assert np.array_equal(oracle.bcsr_densify(F), p["A"])
+    blocks = (p["A"].reshape(64 // bh, bh, 96 // bw, bw) & 0x7FFF).any(axis=(1, 3))
+    assert F["nnzb"] == int(blocks.sum()) == len(p["block_pos"])
+
+
+def test_bcsr_all_blocks_is_dense_gemm_and_row_col_selection():
+    rng = np.random.default_rng(3)
+    A = gen.normal_bits(rng, (32, 48), "f16")
+    B = gen.normal_bits(rng, (48, 20), "f16")
+    F = oracle.bcsr_build(A, 8, 16, "f16")
+    assert F["nnzb"] == (32 // 8) * (48 // 16)
+    ref = _dense_ref(A, B, "f16")
+    np.testing.assert_allclose(oracle.bcsr_spmm(F, B), ref, rtol=1e-12, atol=1e-12)
+    cols = [19, 0, 7]
+    np.testing.assert_allclose(oracle.bcsr_spmm(F, B, rows=(5, 17), cols=cols), ref[5:17][:, cols],
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_bcsr_identity_blocks_copy_rows_and_zero():
+    A = np.zeros((32, 32), dtype=np.float32)
+    A[0:16, 16:32] = np.eye(16)            # block (0,1) = I
+    A[16:32, 0:16] = np.eye(16)            # block (1,0) = I
+    Ab = to_bits(A, "bf16")
+    rng = np.random.default_rng(5)
+    B = gen.normal_bits(rng, (32, 24), "bf16")
+    F = oracle.bcsr_build(Ab, 16, 16, "bf16")
+    out = oracle.bcsr_spmm(F, B)
+    Bf = bits_to_f64(B, "bf16")
+    assert np.array_equal(out[0:16], Bf[16:32]) and np.array_equal(out[16:32], Bf[0:16])
+    Z = oracle.bcsr_build(np.zeros((32, 32), np.uint16), 16, 16, "bf16")
+    assert Z["nnzb"] == 0 and not oracle.bcsr_spmm(Z, B).any()
+
+
+def test_bcsr_nan_block_is_stored_and_shape_error():
+    A = np.zeros((4, 4), dtype=np.uint16)
+    A[3, 3] = 0x7FC0                      # NaN counts as nonzero
+    A[0, 0] = 0x8000                      # -0.0 does not
+    F = oracle.bcsr_build(A, 2, 2, "bf16")
+    assert F["col_idx"].tolist() == [1] and F["row_ptr"].tolist() == [0, 0, 1]
+    with pytest.raises(oracle.OracleError):
+        oracle.bcsr_build(np.zeros((6, 4), np.uint16), 4, 4, "bf16")
+
+
+# ---------------------------------------------------------------- WCSR
+def test_wcsr_golden():
+    g = golden("wcsr_f16_h2_s1.json")
+    val = to_bits(g["csr_val"], "f16")
+    F = oracle.wcsr_build(g["M"], g["K"], np.array(g["csr_row_ptr"]), np.array(g["csr_col"]), val,
+                          "f16", h=g["h"], S=g["S"])
+    for k in ("wcol_ptr", "wcols", "wnz_ptr", "unit_ptr", "unit_win", "unit_nz_ptr", "lrow", "slot"):
+        assert F[k].tolist() == g[k], k
+    assert np.array_equal(F["val"], to_bits(g["val"], "f16"))
+
+
+def _small_csr(M=70, K=300, N=24, seed=11, sigma=1.5, mean=6.0, clip=200):
+    return gen.csr_lognormal_problem(M, K, N, seed, mean=mean, sigma=sigma, clip=clip)
+
+
+def _csr_dense(p):
+    D = np.zeros((p["M"], p["K"]), dtype=np.float64)
+    rows = np.repeat(np.arange(p["M"]), np.diff(p["row_ptr"]))
+    D[rows, p["col"]] = bits_to_f64(p["val"], p["dtype"])
+    return D
+
+
+@pytest.mark.parametrize("h,S", [(16, 32), (4, 1), (1, 2), (7, 1)])
+def test_wcsr_round_trip_invariants_and_dense(h, S):
+    p = _small_csr()
+    F = oracle.wcsr_build(p["M"], p["K"], p["row_ptr"], p["col"], p["val"], "f16", h=h, S=S)
+    rp, col, val = oracle.wcsr_to_csr(F)
+    assert np.array_equal(rp, p["row_ptr"]) and np.array_equal(col, p["col"])
+    assert np.array_equal(val, p["val"])
+    # units cover every window once, contiguous, in window order
+    nw = F["nw"]
+    assert F["unit_ptr"][0] == 0 and F["unit_ptr"][-1] == F["n_units"]
+    for w in range(nw):
+        us = range(F["unit_ptr"][w], F["unit_ptr"][w + 1])
+        assert len(us) >= 1 and all(F["unit_win"][u] == w for u in us)
+        assert F["unit_nz_ptr"][us[0]] == F["wnz_ptr"][w]
+        assert F["unit_nz_ptr"][us[-1] + 1] == F["wnz_ptr"][w + 1]
+        T = F["wcol_ptr"][w + 1] - F["wcol_ptr"][w]
+        assert len(us) == max(1, -(-T // (16 * S)))
+        # per-window nnz equals the CSR row-range nnz
+        r1 = min(p["M"], (w + 1) * h)
+        assert F["wnz_ptr"][w + 1] - F["wnz_ptr"][w] == p["row_ptr"][r1] - p["row_ptr"][w * h]
+        wc = F["wcols"][F["wcol_ptr"][w]:F["wcol_ptr"][w + 1]]
+        assert np.all(np.diff(wc) > 0)
+    got = oracle.wcsr_spmm(F, p["B"])
+    ref = _csr_dense(p) @ bits_to_f64(p["B"], "f16")
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_wcsr_h1_is_csr_spmm_scipy():
+    sp = pytest.importorskip("scipy.sparse")
+    p = _small_csr(M=50, K=120, N=9, seed=4)
+    F = oracle.wcsr_build(p["M"], p["K"], p["row_ptr"], p["col"], p["val"], "f16", h=1, S=1)
+    A = sp.csr_matrix((bits_to_f64(p["val"], "f16"), p["col"], p["row_ptr"]), shape=(p["M"], p["K"]))
+    ref = A @ bits_to_f64(p["B"], "f16")
+    np.testing.assert_allclose(oracle.wcsr_spmm(F, p["B"]), ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.csr_spmm(p["M"], p["row_ptr"], p["col"], p["val"], p["B"], "f16"),
+                               ref, rtol=1e-12, atol=1e-12)
+
+
+def test_csr_check_rejects_bad_input():
+    assert oracle.csr_check(2, 5, [0, 2, 3], [1, 1, 4]) != 0       # duplicate column
+    assert oracle.csr_check(2, 5, [0, 2, 3], [2, 1, 4]) != 0       # unsorted
+    assert oracle.csr_check(2, 5, [0, 2, 1], [1, 2, 4]) != 0       # row_ptr not monotone
+    assert oracle.csr_check(2, 5, [0, 2, 3], [1, 2, 5]) != 0       # out of range
+    assert oracle.csr_check(2, 5, [0, 2, 3], [1, 2, 4]) == 0
+    with pytest.raises(oracle.OracleError):
+        oracle.wcsr_build(2, 5, np.array([0, 2, 3]), np.array([2, 1, 4]), np.zeros(3, np.uint16), "f16")
+
+
+# ---------------------------------------------------------------- 2:4
+def test_24_golden():
+    g = golden("mask24_int8_2x8.json")
+    A, B = np.array(g["A"], np.int8), np.array(g["B"], np.int8)
+    F = oracle.compress24(A, "i8")
+    assert F["vals"].tolist() == g["vals"] and F["meta"].tolist() == g["meta"]
+    assert oracle.spmm24(F, B).tolist() == g["C"]
+
+
+def test_24_int8_exact_vs_int64_gemm_and_invariants():
+    p = gen.mask24_problem(48, 128, 33, seed=9)
+    nz = (p["A"].reshape(48, 32, 4) != 0).sum(axis=2)
+    assert np.all(nz == 2)
+    F = oracle.compress24(p["A"], "i8")
+    assert np.array_equal(oracle.densify24(F), p["A"])
+    nib = np.stack([F["meta"] & 15, F["meta"] >> 4], axis=-1).reshape(48, 32)
+    assert np.all((nib & 3) < (nib >> 2))
+    got = oracle.spmm24(F, p["B"])
+    assert got.dtype == np.int64
+    assert np.array_equal(got, p["A"].astype(np.int64) @ p["B"].astype(np.int64))
+
+
+def test_24_linearity_and_zero():
+    p = gen.mask24_problem(16, 64, 12, seed=10)
+    F = oracle.compress24(p["A"], "i8")
+    rng = np.random.default_rng(1)
+    B1 = rng.integers(-60, 60, size=(64, 12)).astype(np.int8)
+    B2 = rng.integers(-60, 60, size=(64, 12)).astype(np.int8)
+    assert np.array_equal(oracle.spmm24(F, (B1 + B2).astype(np.int8)),
+                          oracle.spmm24(F, B1) + oracle.spmm24(F, B2))
+    Z = oracle.compress24(np.zeros((16, 64), np.int8), "i8")
+    assert not oracle.spmm24(Z, B1).any()
+    assert np.all(Z["meta"] == 0x44)
+
+
+def test_24_meta01_is_dense_on_even_compressed_k():
+    rng = np.random.default_rng(2)
+    M, K, N = 8, 32, 5
+    A = np.zeros((M, K), np.float32)
+    A[:, 0::4] = rng.standard_normal((M, K // 4))
+    A[:, 1::4] = rng.standard_normal((M, K // 4))
+    Ab = to_bits(A, "bf16")
+    F = oracle.compress24(Ab, "bf16")
+    assert np.all(F["meta"] == 0x44)
+    B = gen.normal_bits(rng, (K, N), "bf16")
+    Bsel = bits_to_f64(B, "bf16").reshape(K // 4, 4, N)[:, :2, :].reshape(K // 2, N)
+    ref = bits_to_f64(F["vals"], "bf16") @ Bsel
+    np.testing.assert_allclose(oracle.spmm24(F, B), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_24_errors():
+    A = np.zeros((2, 8), np.int8)
+    A[1, 4:7] = 1                          # three nonzeros in a group
+    with pytest.raises(oracle.OracleError):
+        oracle.compress24(A, "i8")
+    with pytest.raises(oracle.OracleError):
+        oracle.compress24(np.zeros((2, 6), np.int8), "i8")
+
+
+# ---------------------------------------------------------------- TVW
+def test_tvw_golden():
+    g = golden("tvw_f16_2x8.json")
+    A, B = to_bits(g["A"], "f16"), to_bits(g["B"], "f16")
+    F = oracle.tvw_build(A, g["tile_rows"], g["tile_ptr"], g["cols"], "f16", Kp=g["Kp"])
+    assert np.array_equal(F["vals"], to_bits(g["vals"], "f16"))
+    assert F["meta"].tolist() == g["meta"]
+    assert np.array_equal(oracle.tvw_spmm(F, B), np.array(g["C"], np.float64))
+
+
+def test_tvw_round_trip_and_dense():
+    p = gen.tvw_problem(40, 64, 17, tile_rows=16, keep=32, seed=12)
+    F = oracle.tvw_build(p["A"], 16, p["tile_ptr"], p["cols"], "f16")
+    assert np.array_equal(oracle.tvw_densify(F), p["A"])
+    for t in range(3):
+        c = p["cols"][p["tile_ptr"][t]:p["tile_ptr"][t + 1]]
+        assert np.all(np.diff(c) > 0)
+    ref = _dense_ref(p["A"], p["B"], "f16")
+    np.testing.assert_allclose(oracle.tvw_spmm(F, p["B"]), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_tvw_all_kept_reduces_to_24():
+    p = gen.mask24_problem(16, 32, 6, seed=13)
+    Ab = to_bits(p["A"].astype(np.float32), "f16")
+    Bb = to_bits(p["B"].astype(np.float32), "f16")
+    F = oracle.tvw_build(Ab, 16, [0, 32], np.arange(32), "f16")
+    G = oracle.compress24(Ab, "f16")
+    assert np.array_equal(F["vals"], G["vals"]) and np.array_equal(F["meta"], G["meta"])
+    assert np.array_equal(oracle.tvw_spmm(F, Bb), oracle.spmm24(G, Bb))
+
+
+def test_tvw_errors():
+    g = golden("tvw_f16_2x8.json")
+    A = to_bits(g["A"], "f16")
+    A[0, 0] = to_bits([1.0], "f16")[0]     # nonzero outside the kept set
+    with pytest.raises(oracle.OracleError):
+        oracle.tvw_build(A, 2, g["tile_ptr"], g["cols"], "f16")
+    with pytest.raises(oracle.OracleError):  # kept columns not ascending
+        oracle.tvw_build(to_bits(g["A"], "f16"), 2, g["tile_ptr"], [2, 1, 5, 7], "f16")
