@@ -1,0 +1,252 @@
+/*
+ * spmm_gb300.h -- C ABI of the GB300 (sm_103a) sparse x dense matrix multiply
+ * library:  C = A_sparse * B_dense.
+ *
+ * A is stored in one of four formats:
+ *   BCSR  block compressed sparse row       ("AsyncSparse", abstract, Fig. 2)
+ *   WCSR  CSR regrouped into row windows     ("AsyncSparse", abstract, Fig. 2)
+ *   2:4   semi-structured, 2 of every 4      ("Accelerating Sparse DNNs Based on
+ *         consecutive K entries kept           Tiled GEMM", abstract)
+ *   TVW   tile-vector-wise: per row tile a   ("Accelerating Sparse DNNs Based on
+ *         kept column set, 2:4 inside it       Tiled GEMM", abstract)
+ *
+ * Conventions shared by every entry point
+ *   - All matrix pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees device memory.  Scratch space, where an
+ *     operation needs it, is a caller-provided workspace whose size a
+ *     *_workspace_size() query returns.
+ *   - B is K x N row-major with leading dimension ldb (elements); C is M x N
+ *     row-major with leading dimension ldc.  Every element of C[0:M, 0:N] is
+ *     written (rows without stored entries get 0).
+ *   - Floating-point inputs are bf16 or fp16 with fp32 accumulation and fp32 C;
+ *     int8 2:4 accumulates exactly and writes int32 C.
+ *   - Every call validates its scalar arguments on the host first and returns a
+ *     status without launching anything when they are invalid.  SpMM calls are
+ *     asynchronous on `stream`; builders that must report sizes or
+ *     data-dependent format errors synchronise `stream` (stated per call).
+ *   - Kernels never wait without bound: a pipeline wait that exceeds its limit
+ *     (about 2 s) records SPMM_DEVERR_TIMEOUT in a sticky per-device error word
+ *     and the kernel returns; spmm_last_device_error() reads and clears it.
+ *   - Alignment: B, C, format value arrays and 2:4 metadata must be 16-byte
+ *     aligned, and ldb must make a row 16-byte aligned (TMA requirement).
+ *     Violations return SPMM_ERR_SHAPE.
+ */
+#ifndef SPMM_GB300_H
+#define SPMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPMM_API __attribute__((visibility("default")))
+#else
+#define SPMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *spmm_stream_t;
+
+typedef enum {
+    SPMM_OK = 0,
+    SPMM_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    SPMM_ERR_SHAPE = 2,       /* bad dimension, leading dimension or alignment       */
+    SPMM_ERR_DTYPE = 3,       /* dtype not supported by this call                    */
+    SPMM_ERR_FORMAT = 4,      /* format data invalid (builders detect it on device)  */
+    SPMM_ERR_WORKSPACE = 5,   /* workspace NULL or too small                         */
+    SPMM_ERR_TIMEOUT = 6,     /* a device pipeline wait exceeded its bound           */
+    SPMM_ERR_CUDA = 7,        /* CUDA runtime / driver error                         */
+    SPMM_ERR_UNSUPPORTED = 8  /* valid request outside what the kernels implement    */
+} spmm_status;
+
+typedef enum { SPMM_BF16 = 0, SPMM_F16 = 1, SPMM_I8 = 2 } spmm_dtype;
+
+/* Bits of the sticky device error word. */
+#define SPMM_DEVERR_TIMEOUT 1 /* a bounded pipeline wait gave up                        */
+#define SPMM_DEVERR_INDEX 2   /* an out-of-range index was skipped                      */
+#define SPMM_DEVERR_FORMAT 4  /* a builder found invalid data                           */
+
+/* ---------------------------------------------------------------- formats */
+
+/* Block compressed sparse row ("AsyncSparse", abstract and Fig. 2).
+ * A (M x K) is cut into bh x bw blocks; a block is stored iff one entry is
+ * nonzero (IEEE compare: -0.0 is zero, NaN is not).  Block rows ascending,
+ * block columns ascending inside a block row.
+ *   row_ptr[M/bh + 1]   first stored block of each block row
+ *   col_idx[nnzb]       block-column index (element column / bw)
+ *   vals[nnzb][bh][bw]  block values, row-major inside a block
+ * GPU SpMM supports bh in {16, 32, ..., 256} (multiple of 16), bw in {16, 32, 64}. */
+typedef struct {
+    int64_t M, K;
+    int32_t bh, bw;
+    int64_t nnzb;
+    int32_t dtype; /* SPMM_BF16 or SPMM_F16 */
+    int32_t *row_ptr;
+    int32_t *col_idx;
+    void *vals;
+} spmm_bcsr_t;
+
+/* Plain CSR (input of the row-window builder): row_ptr[M+1], col[nnz]
+ * strictly ascending inside a row, val[nnz]. */
+typedef struct {
+    int64_t M, K, nnz;
+    int32_t dtype; /* SPMM_F16 or SPMM_BF16 */
+    int32_t *row_ptr;
+    int32_t *col;
+    void *val;
+} spmm_csr_t;
+
+/* Row-window CSR ("AsyncSparse", abstract: sparse operand loaded per row
+ * window, long windows split across thread blocks).  Rows are grouped into
+ * windows of h rows (the last may be shorter).  Per window w:
+ *   wcols[wcol_ptr[w] .. wcol_ptr[w+1])  distinct columns, ascending (T_w of them)
+ *   units unit_ptr[w] .. unit_ptr[w+1]-1: U_w = max(1, ceil(T_w / (16 S)))
+ *     work units; unit u of the window covers column slots [16 S u, 16 S (u+1)).
+ * Per nonzero (window-major; inside a window unit-major, then row, then
+ * column): lrow (row - h w), slot (index into the window's wcols), val.
+ * wnz_ptr[w] is the window's first nonzero, unit_win[u] the window of unit u,
+ * unit_nz_ptr[u] the unit's first nonzero (unit_nz_ptr[n_units] = nnz). */
+typedef struct {
+    int64_t M, K, nnz;
+    int32_t h, S;
+    int32_t dtype; /* SPMM_F16 or SPMM_BF16 */
+    int64_t n_windows, n_wcols, n_units;
+    int32_t *wcol_ptr;    /* [n_windows + 1] */
+    int32_t *wcols;       /* [n_wcols]       */
+    int32_t *wnz_ptr;     /* [n_windows + 1] */
+    int32_t *unit_ptr;    /* [n_windows + 1] */
+    int32_t *unit_win;    /* [n_units]       */
+    int32_t *unit_nz_ptr; /* [n_units + 1]   */
+    uint8_t *lrow;        /* [nnz]           */
+    int32_t *slot;        /* [nnz]           */
+    void *val;            /* [nnz]           */
+} spmm_wcsr_t;
+
+/* 2:4 semi-structured ("Accelerating Sparse DNNs Based on Tiled GEMM",
+ * abstract).  In every group of 4 consecutive K entries two positions are
+ * stored: vals[M][K/2] (group g's entries at 2g, 2g+1), meta[M][K/8] with
+ * group g's nibble idx0 | idx1 << 2 (idx0 < idx1) in byte g/2, low nibble for
+ * even g.  A group with fewer than two nonzeros stores its nonzero positions
+ * plus the lowest-index zero positions. */
+typedef struct {
+    int64_t M, K;
+    int32_t dtype; /* SPMM_I8 (-> int32 C), SPMM_F16 or SPMM_BF16 (-> fp32 C) */
+    void *vals;
+    uint8_t *meta;
+} spmm_24_t;
+
+/* Tile-vector-wise ("Accelerating Sparse DNNs Based on Tiled GEMM",
+ * abstract).  Rows form tiles of tile_rows rows; tile t keeps the ascending
+ * columns cols[tile_ptr[t] .. tile_ptr[t+1]) (Kt entries, Kt % 4 == 0); each
+ * row is 2:4 over its tile's kept columns in that order.  vals[M][Kp/2] and
+ * meta[M][Kp/8] use the common pitch Kp >= max Kt; entries past a tile's Kt
+ * hold value 0 and nibble (0, 1).  The GPU SpMM needs tile_rows == 128 and
+ * Kp % 128 == 0. */
+typedef struct {
+    int64_t M, K;
+    int32_t tile_rows;
+    int32_t dtype; /* SPMM_F16 or SPMM_BF16 */
+    int64_t n_tiles, Kp;
+    int32_t *tile_ptr; /* [n_tiles + 1] */
+    int32_t *cols;     /* [tile_ptr[n_tiles]] */
+    void *vals;
+    uint8_t *meta;
+} spmm_tvw_t;
+
+/* ---------------------------------------------------------------- utilities */
+
+SPMM_API const char *spmm_status_string(spmm_status s);
+/* Library version (major * 100 + minor). */
+SPMM_API int spmm_version(void);
+/* Reads and clears the sticky device error word of the current device
+ * (SPMM_DEVERR_* bits).  Synchronises the device. */
+SPMM_API spmm_status spmm_last_device_error(int32_t *bits);
+/* Tests the bounded-wait path: launches one CTA that waits on an mbarrier no
+ * one arrives on, with the given limit; the kernel gives up, records
+ * SPMM_DEVERR_TIMEOUT and returns.  Synchronises `stream`. */
+SPMM_API spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t stream);
+
+/* ---------------------------------------------------------------- SpMM */
+
+/* C = A * B with A in BCSR ("AsyncSparse": warp-specialised TMA -> tensor core
+ * pipeline over nonzero blocks).  bf16/fp16 in, fp32 C. */
+SPMM_API spmm_status spmm_bcsr(const spmm_bcsr_t *A, const void *B, int64_t ldb, float *C, int64_t ldc, int64_t N,
+                               spmm_stream_t stream);
+
+/* Workspace bytes spmm_wcsr needs for this operand and N (partials of split
+ * windows plus one arrival counter per split window). */
+SPMM_API spmm_status spmm_wcsr_workspace_size(const spmm_wcsr_t *A, int64_t N, size_t *bytes);
+/* C = A * B with A in row-window CSR ("AsyncSparse": per-window loads, long
+ * windows split across CTAs).  Split windows are summed in split order by the
+ * last CTA to finish, so results are run-to-run identical.  The workspace must
+ * be zero-filled before its first use; a successful call leaves its counters
+ * at zero again.  fp16/bf16 in, fp32 C. */
+SPMM_API spmm_status spmm_wcsr(const spmm_wcsr_t *A, const void *B, int64_t ldb, float *C, int64_t ldc, int64_t N,
+                               void *workspace, size_t workspace_bytes, spmm_stream_t stream);
+
+/* Workspace bytes spmm_24 needs (int8 operands are widened to fp16 for the
+ * tensor core; 0 for fp16/bf16). */
+SPMM_API spmm_status spmm_24_workspace_size(const spmm_24_t *A, int64_t N, size_t *bytes);
+/* C = A * B with A 2:4 ("Accelerating Sparse DNNs Based on Tiled GEMM": 2:4
+ * executed inside the sparse tensor core).  int8: C is int32 and exact (the
+ * kernel accumulates 512-wide K chunks in fp32, every partial an integer of
+ * magnitude at most 2^22, and sums the chunks in int32).  fp16/bf16: C is fp32.
+ * Needs K % 128 == 0. */
+SPMM_API spmm_status spmm_24(const spmm_24_t *A, const void *B, int64_t ldb, void *C, int64_t ldc, int64_t N,
+                             void *workspace, size_t workspace_bytes, spmm_stream_t stream);
+
+/* C = A * B with A tile-vector-wise ("Accelerating Sparse DNNs Based on Tiled
+ * GEMM": tile-wise column selection at global-memory level, 2:4 in the sparse
+ * tensor core).  Each tile gathers its kept rows of B.  fp32 C. */
+SPMM_API spmm_status spmm_tvw(const spmm_tvw_t *A, const void *B, int64_t ldb, float *C, int64_t ldc, int64_t N,
+                              spmm_stream_t stream);
+
+/* ---------------------------------------------------------------- builders */
+
+/* dense (M x K, leading dim ld) -> BCSR, phase 1: row_ptr[M/bh + 1] on the
+ * device and the block count in *nnzb.  Synchronises `stream`. */
+SPMM_API spmm_status spmm_build_bcsr_count(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t bh,
+                                           int32_t bw, int32_t dtype, int32_t *row_ptr, int64_t *nnzb,
+                                           spmm_stream_t stream);
+/* Phase 2: col_idx[nnzb] and vals[nnzb][bh][bw] (values copied bit for bit). */
+SPMM_API spmm_status spmm_build_bcsr_fill(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t bh,
+                                          int32_t bw, int32_t dtype, const int32_t *row_ptr, int32_t *col_idx,
+                                          void *vals, spmm_stream_t stream);
+
+/* CSR -> row windows.  Workspace for both phases (must be the same buffer,
+ * untouched between them). */
+SPMM_API spmm_status spmm_build_wcsr_workspace_size(const spmm_csr_t *A, int32_t h, size_t *bytes);
+/* Phase 1: validates the CSR (row_ptr monotone, columns strictly ascending
+ * and in range: SPMM_ERR_FORMAT otherwise), and returns the total number of
+ * window columns and of work units.  Synchronises `stream`. */
+SPMM_API spmm_status spmm_build_wcsr_count(const spmm_csr_t *A, int32_t h, int32_t S, void *workspace,
+                                           size_t workspace_bytes, int64_t *n_wcols, int64_t *n_units,
+                                           spmm_stream_t stream);
+/* Phase 2: fills every array of *out (allocated by the caller from the
+ * counts; out->M/K/nnz/h/S/dtype/n_* are set by this call).  Bit-exact with
+ * the layout described at spmm_wcsr_t. */
+SPMM_API spmm_status spmm_build_wcsr_fill(const spmm_csr_t *A, int32_t h, int32_t S, void *workspace,
+                                          size_t workspace_bytes, spmm_wcsr_t *out, spmm_stream_t stream);
+
+/* dense (M x K) -> 2:4 vals[M][K/2] + meta[M][K/8].  K % 8 == 0.  More than
+ * two nonzeros in a group -> SPMM_ERR_FORMAT.  Synchronises `stream`. */
+SPMM_API spmm_status spmm_compress_24(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
+                                      void *vals, uint8_t *meta, spmm_stream_t stream);
+
+/* dense (M x K) + kept columns -> TVW vals[M][Kp/2] + meta[M][Kp/8].
+ * tile_ptr/cols are device arrays (tile_ptr has n_tiles + 1 entries).  Kept
+ * columns not ascending or out of range, a nonzero outside the kept set, or
+ * more than two nonzeros in a group -> SPMM_ERR_FORMAT.  Synchronises
+ * `stream`. */
+SPMM_API spmm_status spmm_build_tvw(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
+                                    int32_t tile_rows, const int32_t *tile_ptr, const int32_t *cols,
+                                    int64_t n_tiles, int64_t Kp, void *vals, uint8_t *meta, spmm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPMM_GB300_H */

@@ -1,0 +1,242 @@
+// api.cu -- the extern "C" boundary: argument validation, per-device state,
+// tensor-map encoding and dispatch to the kernels of each format.
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace spmm {
+
+// Sticky per-device error word (SPMM_DEVERR_* bits), written by kernels.
+__device__ int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxKernelSlots = 16;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+bool g_attr_done[kMaxDevices][kMaxKernelSlots];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+__global__ void timeout_selftest_kernel(int* err, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on this barrier: the wait must give up by itself.
+    if (threadIdx.x == 0) ptx::mbar_wait(b, 0, timeout_ns, err, SPMM_DEVERR_TIMEOUT);
+    __syncthreads();
+}
+
+}  // namespace
+
+const DeviceInfo* device_info() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_info_ok[d]) {
+        DeviceInfo info;
+        if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) !=
+            cudaSuccess)
+            return nullptr;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        info.err = static_cast<int*>(p);
+        g_info[d] = info;
+        g_info_ok[d] = true;
+    }
+    return &g_info[d];
+}
+
+bool set_smem_attr_once(const void* kernel, int bytes, int slot) {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices || slot < 0 || slot >= kMaxKernelSlots)
+        return false;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_attr_done[d][slot]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+            return false;
+        g_attr_done[d][slot] = true;
+    }
+    return true;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    std::memset(map, 0, sizeof(*map));
+    return f(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace spmm
+
+using namespace spmm;
+
+extern "C" {
+
+const char* spmm_status_string(spmm_status s) {
+    switch (s) {
+        case SPMM_OK: return "ok";
+        case SPMM_ERR_NULL: return "null pointer";
+        case SPMM_ERR_SHAPE: return "invalid shape, leading dimension or alignment";
+        case SPMM_ERR_DTYPE: return "unsupported dtype";
+        case SPMM_ERR_FORMAT: return "invalid sparse format data";
+        case SPMM_ERR_WORKSPACE: return "workspace missing or too small";
+        case SPMM_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case SPMM_ERR_CUDA: return "CUDA error";
+        case SPMM_ERR_UNSUPPORTED: return "unsupported configuration";
+    }
+    return "unknown status";
+}
+
+int spmm_version(void) { return 100; }
+
+spmm_status spmm_last_device_error(int32_t* bits) {
+    if (!bits) return SPMM_ERR_NULL;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SPMM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, dev->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SPMM_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SPMM_ERR_CUDA;
+    *bits = v;
+    return SPMM_OK;
+}
+
+spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (timeout_ns > 4000000000ull) return SPMM_ERR_SHAPE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    timeout_selftest_kernel<<<1, 32, 0, s>>>(dev->err, timeout_ns);
+    if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                      spmm_stream_t stream) {
+    if (!A || !B || !C) return SPMM_ERR_NULL;
+    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || N < 0 || A->bh <= 0 || A->bw <= 0 || A->nnzb < 0) return SPMM_ERR_SHAPE;
+    if (A->M % A->bh || A->K % A->bw) return SPMM_ERR_SHAPE;
+    if (ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B) || (A->nnzb > 0 && !aligned16(A->vals)))
+        return SPMM_ERR_SHAPE;
+    if (A->nnzb > 0 && (!A->row_ptr || !A->col_idx || !A->vals)) return SPMM_ERR_NULL;
+    if (A->bh % 16 || A->bh > 256 || (A->bw != 16 && A->bw != 32 && A->bw != 64)) return SPMM_ERR_UNSUPPORTED;
+    if (A->nnzb * A->bh >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    return launch_bcsr(A, B, ldb, C, ldc, N, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- builders
+
+spmm_status spmm_build_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t bh, int32_t bw,
+                                  int32_t dtype, int32_t* row_ptr, int64_t* nnzb, spmm_stream_t stream) {
+    if (!row_ptr || !nnzb || (M > 0 && K > 0 && !dense)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (M < 0 || K < 0 || bh <= 0 || bw <= 0 || M % bh || K % bw || ld < K) return SPMM_ERR_SHAPE;
+    if (K / bw > 40000 || M / bh >= (int64_t(1) << 31)) return SPMM_ERR_UNSUPPORTED;
+    return run_bcsr_count(dense, M, K, ld, bh, bw, dtype, row_ptr, nnzb, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_build_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t bh, int32_t bw,
+                                 int32_t dtype, const int32_t* row_ptr, int32_t* col_idx, void* vals,
+                                 spmm_stream_t stream) {
+    if (!row_ptr || (M > 0 && K > 0 && !dense)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (M < 0 || K < 0 || bh <= 0 || bw <= 0 || M % bh || K % bw || ld < K) return SPMM_ERR_SHAPE;
+    if (K / bw > 8000) return SPMM_ERR_UNSUPPORTED;
+    return run_bcsr_fill(dense, M, K, ld, bh, bw, dtype, row_ptr, col_idx, vals,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_compress_24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
+                             uint8_t* meta, spmm_stream_t stream) {
+    if (M > 0 && K > 0 && (!dense || !vals || !meta)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (M < 0 || K < 0 || K % 8 || ld < K) return SPMM_ERR_SHAPE;
+    return run_compress24(dense, M, K, ld, dtype, vals, meta, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
+                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
+                           uint8_t* meta, spmm_stream_t stream) {
+    if (M > 0 && (!dense || !tile_ptr || !vals || !meta)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (M < 0 || K < 0 || ld < K || tile_rows <= 0 || Kp < 0 || Kp % 8) return SPMM_ERR_SHAPE;
+    if (n_tiles != (M + tile_rows - 1) / tile_rows) return SPMM_ERR_SHAPE;
+    if (M == 0) return SPMM_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // tile_ptr is small: check it on the host (starts at 0, monotone, Kt % 4 == 0, Kt <= Kp)
+    std::vector<int32_t> tp(static_cast<size_t>(n_tiles + 1));
+    if (cudaMemcpyAsync(tp.data(), tile_ptr, tp.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    if (tp[0] != 0) return SPMM_ERR_FORMAT;
+    for (int64_t t = 0; t < n_tiles; ++t) {
+        const int64_t kt = int64_t(tp[t + 1]) - tp[t];
+        if (kt < 0 || kt % 4 || kt > Kp) return SPMM_ERR_FORMAT;
+    }
+    if (tp[n_tiles] > 0 && !cols) return SPMM_ERR_NULL;
+    return run_build_tvw(dense, M, K, ld, dtype, tile_rows, tile_ptr, cols, n_tiles, Kp, vals, meta, s);
+}
+
+// ---------------------------------------------------------------- not yet built
+
+spmm_status spmm_wcsr_workspace_size(const spmm_wcsr_t*, int64_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
+spmm_status spmm_wcsr(const spmm_wcsr_t*, const void*, int64_t, float*, int64_t, int64_t, void*, size_t,
+                      spmm_stream_t) {
+    return SPMM_ERR_UNSUPPORTED;
+}
+spmm_status spmm_24_workspace_size(const spmm_24_t*, int64_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
+spmm_status spmm_24(const spmm_24_t*, const void*, int64_t, void*, int64_t, int64_t, void*, size_t, spmm_stream_t) {
+    return SPMM_ERR_UNSUPPORTED;
+}
+spmm_status spmm_tvw(const spmm_tvw_t*, const void*, int64_t, float*, int64_t, int64_t, spmm_stream_t) {
+    return SPMM_ERR_UNSUPPORTED;
+}
+spmm_status spmm_build_wcsr_workspace_size(const spmm_csr_t*, int32_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
+spmm_status spmm_build_wcsr_count(const spmm_csr_t*, int32_t, int32_t, void*, size_t, int64_t*, int64_t*,
+                                  spmm_stream_t) {
+    return SPMM_ERR_UNSUPPORTED;
+}
+spmm_status spmm_build_wcsr_fill(const spmm_csr_t*, int32_t, int32_t, void*, size_t, spmm_wcsr_t*,
+                                 spmm_stream_t) {
+    return SPMM_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

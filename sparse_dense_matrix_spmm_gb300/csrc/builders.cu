@@ -1,0 +1,367 @@
+// builders.cu -- GPU format builders: dense -> BCSR, dense -> 2:4, dense -> TVW.
+//
+// Every builder is bit-exact with respect to its format definition: stored
+// values are copied bit for bit, and the order of stored items comes from
+// prefix sums (never from atomics), so the output does not depend on thread
+// scheduling.  A stored element is "zero" iff it compares equal to zero
+// (16-bit types: (bits & 0x7FFF) == 0, so -0.0 is zero and NaN is not).
+#include <mutex>
+
+#include "internal.h"
+
+namespace spmm {
+
+__device__ int g_build_error;  // data-dependent builder errors (SPMM_DEVERR_FORMAT)
+
+namespace {
+
+std::mutex g_build_mu;  // builders share g_build_error: one at a time per process
+
+template <typename T>
+__device__ __forceinline__ bool nz(T v);
+template <>
+__device__ __forceinline__ bool nz<uint16_t>(uint16_t v) { return (v & 0x7FFFu) != 0; }
+template <>
+__device__ __forceinline__ bool nz<int8_t>(int8_t v) { return v != 0; }
+
+// ---------------------------------------------------------------- scan
+// In-place exclusive prefix sum of a[0..n) with one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) exclusive_scan_kernel(int32_t* a, int64_t n) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < n; base += 1024) {
+        const int64_t i = base + tid;
+        int32_t v = i < n ? a[i] : 0;
+        int32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int32_t s = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_sums[lane] = s;
+        }
+        __syncthreads();
+        const int32_t before = carry + (wid ? warp_sums[wid - 1] : 0) + x - v;
+        if (i < n) a[i] = before;
+        __syncthreads();
+        if (tid == 1023) carry = before + v;
+        __syncthreads();
+    }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ int32_t block_exclusive_scan(int32_t v, int32_t* total, int32_t* sh /* >= 33 ints */) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = (blockDim.x + 31) >> 5;
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t s = lane < nw ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        sh[lane] = s;
+    }
+    __syncthreads();
+    const int32_t r = (wid ? sh[wid - 1] : 0) + x - v;
+    if (total) *total = sh[nw - 1];
+    __syncthreads();
+    return r;
+}
+
+// ---------------------------------------------------------------- BCSR
+// One CTA per block row; flags[bc] = 1 iff block (br, bc) holds a nonzero.
+template <typename T>
+__device__ void bcsr_flags(const T* dense, int64_t ld, int br, int bh, int gk, int bw, uint8_t* flags) {
+    for (int bc = threadIdx.x; bc < gk; bc += blockDim.x) flags[bc] = 0;
+    __syncthreads();
+    const int64_t K = static_cast<int64_t>(gk) * bw;
+    const int64_t total = static_cast<int64_t>(bh) * K;
+    const T* base = dense + static_cast<int64_t>(br) * bh * ld;
+    for (int64_t e = threadIdx.x; e < total; e += blockDim.x) {
+        const int64_t r = e / K, c = e % K;
+        if (nz<T>(base[r * ld + c])) flags[c / bw] = 1;  // benign same-value race
+    }
+    __syncthreads();
+}
+
+template <typename T>
+__global__ void bcsr_count_kernel(const T* dense, int64_t ld, int bh, int bw, int gk, int32_t* row_ptr) {
+    extern __shared__ uint8_t flags[];
+    __shared__ int32_t sh[33];
+    const int br = blockIdx.x;
+    bcsr_flags<T>(dense, ld, br, bh, gk, bw, flags);
+    int32_t cnt = 0;
+    for (int bc = threadIdx.x; bc < gk; bc += blockDim.x) cnt += flags[bc];
+    int32_t total = 0;
+    block_exclusive_scan(cnt, &total, sh);
+    if (threadIdx.x == 0) row_ptr[br] = total;
+}
+
+template <typename T>
+__global__ void bcsr_fill_kernel(const T* dense, int64_t ld, int bh, int bw, int gk, const int32_t* row_ptr,
+                                 int32_t* col_idx, T* vals) {
+    extern __shared__ uint8_t smem[];
+    uint8_t* flags = smem;
+    int32_t* pos = reinterpret_cast<int32_t*>(smem + ((gk + 15) & ~15));
+    __shared__ int32_t sh[33];
+    const int br = blockIdx.x;
+    bcsr_flags<T>(dense, ld, br, bh, gk, bw, flags);
+    // positions of the stored blocks inside this block row, in ascending bc
+    const int per = (gk + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(gk, static_cast<int>(threadIdx.x) * per), b1 = min(gk, b0 + per);
+    int32_t cnt = 0;
+    for (int bc = b0; bc < b1; ++bc) cnt += flags[bc];
+    int32_t run = block_exclusive_scan(cnt, nullptr, sh);
+    for (int bc = b0; bc < b1; ++bc) {
+        pos[bc] = run;
+        run += flags[bc];
+    }
+    __syncthreads();
+    const int64_t first = row_ptr[br];
+    for (int bc = threadIdx.x; bc < gk; bc += blockDim.x)
+        if (flags[bc]) col_idx[first + pos[bc]] = bc;
+    const int64_t blk = static_cast<int64_t>(bh) * bw;
+    const int64_t K = static_cast<int64_t>(gk) * bw;
+    const T* base = dense + static_cast<int64_t>(br) * bh * ld;
+    for (int64_t e = threadIdx.x; e < static_cast<int64_t>(bh) * K; e += blockDim.x) {
+        const int64_t r = e / K, c = e % K;
+        const int bc = static_cast<int>(c / bw);
+        if (!flags[bc]) continue;
+        vals[(first + pos[bc]) * blk + r * bw + (c % bw)] = base[r * ld + c];
+    }
+}
+
+// ---------------------------------------------------------------- 2:4
+// Keep the nonzero positions of a 4-group, padded with the lowest-index zero
+// positions; nibble = idx0 | idx1 << 2.  Returns false on > 2 nonzeros.
+__device__ __forceinline__ bool pick2(unsigned mask, int& i0, int& i1) {
+    if (__popc(mask) > 2) return false;
+    unsigned keep = mask;
+    for (int p = 0; p < 4 && __popc(keep) < 2; ++p) keep |= 1u << p;  // lowest zero positions
+    i0 = __ffs(keep) - 1;
+    i1 = __ffs(keep & ~(1u << i0)) - 1;
+    return true;
+}
+
+// One thread per (row, meta byte) = 2 groups = 8 dense columns.
+template <typename T>
+__global__ void compress24_kernel(const T* dense, int64_t M, int64_t K, int64_t ld, T* vals, uint8_t* meta,
+                                  int* err) {
+    const int64_t nb = K / 8;
+    const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (id >= M * nb) return;
+    const int64_t i = id / nb, j = id % nb;
+    const T* src = dense + i * ld + 8 * j;
+    T* dst = vals + i * (K / 2) + 4 * j;
+    uint8_t byte = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        unsigned mask = 0;
+        T v[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            v[p] = src[4 * h + p];
+            if (nz<T>(v[p])) mask |= 1u << p;
+        }
+        int i0 = 0, i1 = 1;
+        if (!pick2(mask, i0, i1)) {
+            atomicOr(err, SPMM_DEVERR_FORMAT);
+            i0 = 0;
+            i1 = 1;
+        }
+        dst[2 * h] = v[i0];
+        dst[2 * h + 1] = v[i1];
+        byte |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
+    }
+    meta[i * nb + j] = byte;
+}
+
+// ---------------------------------------------------------------- TVW
+// Kept columns of every tile must be ascending and inside [0, K).
+__global__ void tvw_check_cols_kernel(const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t K,
+                                      int* err) {
+    const int64_t t = blockIdx.x;
+    if (t >= n_tiles) return;
+    const int32_t b = tile_ptr[t], e = tile_ptr[t + 1];
+    for (int32_t q = b + threadIdx.x; q < e; q += blockDim.x) {
+        const int32_t c = cols[q];
+        if (c < 0 || c >= K || (q > b && cols[q - 1] >= c)) atomicOr(err, SPMM_DEVERR_FORMAT);
+    }
+}
+
+// One CTA per row.  Every nonzero of the row must sit in a kept column; then
+// each group of 4 kept columns is compressed to 2:4.
+template <typename T>
+__global__ void tvw_build_kernel(const T* dense, int64_t M, int64_t K, int64_t ld, int tile_rows,
+                                 const int32_t* tile_ptr, const int32_t* cols, int64_t Kp, T* vals, uint8_t* meta,
+                                 int* err) {
+    __shared__ int32_t sh[33];
+    const int64_t i = blockIdx.x;
+    const int64_t t = i / tile_rows;
+    const int32_t kb = tile_ptr[t], Kt = tile_ptr[t + 1] - kb;
+    const T* row = dense + i * ld;
+    int32_t all = 0, kept = 0;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) all += nz<T>(row[k]);
+    for (int32_t q = threadIdx.x; q < Kt; q += blockDim.x) {
+        const int32_t c = cols[kb + q];
+        if (c >= 0 && c < K) kept += nz<T>(row[c]);
+    }
+    int32_t tall = 0, tkept = 0;
+    block_exclusive_scan(all, &tall, sh);
+    block_exclusive_scan(kept, &tkept, sh);
+    if (threadIdx.x == 0 && tall != tkept) atomicOr(err, SPMM_DEVERR_FORMAT);
+    const int64_t nb = Kp / 8;
+    for (int64_t j = threadIdx.x; j < nb; j += blockDim.x) {
+        uint8_t byte = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t g = 2 * j + h;
+            int i0 = 0, i1 = 1;
+            if (4 * g < Kt) {
+                T v[4];
+                unsigned mask = 0;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int32_t c = cols[kb + 4 * g + p];
+                    v[p] = (c >= 0 && c < K) ? row[c] : T(0);
+                    if (nz<T>(v[p])) mask |= 1u << p;
+                }
+                if (!pick2(mask, i0, i1)) {
+                    atomicOr(err, SPMM_DEVERR_FORMAT);
+                    i0 = 0;
+                    i1 = 1;
+                }
+                vals[i * (Kp / 2) + 2 * g] = v[i0];
+                vals[i * (Kp / 2) + 2 * g + 1] = v[i1];
+            } else {
+                vals[i * (Kp / 2) + 2 * g] = T(0);
+                vals[i * (Kp / 2) + 2 * g + 1] = T(0);
+            }
+            byte |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
+        }
+        meta[i * nb + j] = byte;
+    }
+}
+
+int* build_err_ptr() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_build_error) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+// Clear the builder error word before a launch, read it back after.
+spmm_status build_begin(int* e, cudaStream_t s) { return cuda_status(cudaMemsetAsync(e, 0, sizeof(int), s)); }
+spmm_status build_end(int* e, cudaStream_t s) {
+    int v = 0;
+    if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, e, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SPMM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPMM_ERR_CUDA;
+    return v ? SPMM_ERR_FORMAT : SPMM_OK;
+}
+
+}  // namespace
+
+spmm_status run_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
+                           int32_t* row_ptr, int64_t* nnzb, cudaStream_t s) {
+    const int nbr = static_cast<int>(M / bh), gk = static_cast<int>(K / bw);
+    const int smem = gk;
+    if (nbr > 0 && gk > 0) {
+        if (dtype == SPMM_I8)
+            bcsr_count_kernel<int8_t>
+                <<<nbr, 256, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk, row_ptr);
+        else
+            bcsr_count_kernel<uint16_t>
+                <<<nbr, 256, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw, gk, row_ptr);
+        if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
+    } else if (nbr > 0) {
+        if (cudaMemsetAsync(row_ptr, 0, sizeof(int32_t) * nbr, s) != cudaSuccess) return SPMM_ERR_CUDA;
+    }
+    if (cudaMemsetAsync(row_ptr + nbr, 0, sizeof(int32_t), s) != cudaSuccess) return SPMM_ERR_CUDA;
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(row_ptr, nbr + 1);
+    if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
+    int32_t total = 0;
+    if (cudaMemcpyAsync(&total, row_ptr + nbr, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPMM_ERR_CUDA;
+    *nnzb = total;
+    return SPMM_OK;
+}
+
+spmm_status run_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
+                          const int32_t* row_ptr, int32_t* col_idx, void* vals, cudaStream_t s) {
+    const int nbr = static_cast<int>(M / bh), gk = static_cast<int>(K / bw);
+    const int smem = ((gk + 15) & ~15) + 4 * gk;
+    if (nbr == 0 || gk == 0) return SPMM_OK;
+    if (dtype == SPMM_I8)
+        bcsr_fill_kernel<int8_t><<<nbr, 256, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk, row_ptr,
+                                                        col_idx, static_cast<int8_t*>(vals));
+    else
+        bcsr_fill_kernel<uint16_t><<<nbr, 256, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw, gk,
+                                                          row_ptr, col_idx, static_cast<uint16_t*>(vals));
+    return cuda_status(cudaGetLastError());
+}
+
+spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
+                           uint8_t* meta, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_build_mu);
+    int* e = build_err_ptr();
+    if (!e) return SPMM_ERR_CUDA;
+    spmm_status st = build_begin(e, s);
+    if (st != SPMM_OK) return st;
+    const int64_t n = M * (K / 8);
+    if (n > 0) {
+        const int64_t blocks = (n + 255) / 256;
+        if (dtype == SPMM_I8)
+            compress24_kernel<int8_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                static_cast<const int8_t*>(dense), M, K, ld, static_cast<int8_t*>(vals), meta, e);
+        else
+            compress24_kernel<uint16_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                static_cast<const uint16_t*>(dense), M, K, ld, static_cast<uint16_t*>(vals), meta, e);
+    }
+    return build_end(e, s);
+}
+
+spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
+                          const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
+                          uint8_t* meta, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_build_mu);
+    int* e = build_err_ptr();
+    if (!e) return SPMM_ERR_CUDA;
+    spmm_status st = build_begin(e, s);
+    if (st != SPMM_OK) return st;
+    if (n_tiles > 0)
+        tvw_check_cols_kernel<<<static_cast<unsigned>(n_tiles), 256, 0, s>>>(tile_ptr, cols, n_tiles, K, e);
+    if (M > 0) {
+        if (dtype == SPMM_I8)
+            tvw_build_kernel<int8_t><<<static_cast<unsigned>(M), 256, 0, s>>>(
+                static_cast<const int8_t*>(dense), M, K, ld, tile_rows, tile_ptr, cols, Kp,
+                static_cast<int8_t*>(vals), meta, e);
+        else
+            tvw_build_kernel<uint16_t><<<static_cast<unsigned>(M), 256, 0, s>>>(
+                static_cast<const uint16_t*>(dense), M, K, ld, tile_rows, tile_ptr, cols, Kp,
+                static_cast<uint16_t*>(vals), meta, e);
+    }
+    return build_end(e, s);
+}
+
+}  // namespace spmm

@@ -1,0 +1,57 @@
+// internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "spmm_gb300.h"
+
+namespace spmm {
+
+// Per-device facts and the device address of the sticky error word.
+struct DeviceInfo {
+    int sms = 0;
+    int max_smem_optin = 0;
+    int* err = nullptr;  // device address of the error word (SPMM_DEVERR_* bits)
+};
+
+// Facts for the current device; nullptr if the CUDA runtime is unusable.
+const DeviceInfo* device_info();
+
+// Default bound on any single pipeline wait inside a kernel.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// 2-D tiled tensor map: `inner` elements per row (contiguous), `outer` rows,
+// `row_bytes` between rows; box of box_inner x box_outer elements.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle swizzle);
+
+inline spmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline CUtensorMapDataType half_type(int32_t dtype) {
+    return dtype == SPMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// Raise a kernel's dynamic shared memory limit once per device.
+bool set_smem_attr_once(const void* kernel, int bytes, int slot);
+
+// Kernel launchers implemented in the per-format translation units.  Arguments
+// are already validated by the C-ABI layer.
+spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                        cudaStream_t stream);
+
+spmm_status run_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
+                           int32_t* row_ptr, int64_t* nnzb, cudaStream_t s);
+spmm_status run_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
+                          const int32_t* row_ptr, int32_t* col_idx, void* vals, cudaStream_t s);
+spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
+                           uint8_t* meta, cudaStream_t s);
+spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
+                          const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
+                          uint8_t* meta, cudaStream_t s);
+
+}  // namespace spmm

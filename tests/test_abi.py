@@ -1,0 +1,74 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h declares (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        names |= set(re.findall(r"SPMM_API\s+[^;(]*?\b(spmm_\w+)\s*\(", txt))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_dense_matrix_spmm_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("spmm_bcsr", "spmm_wcsr", "spmm_24", "spmm_tvw", "spmm_build_bcsr_count", "spmm_build_bcsr_fill",
+              "spmm_build_wcsr_count", "spmm_build_wcsr_fill", "spmm_compress_24", "spmm_build_tvw"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_the_header():
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    assert sorted(_lib.SIGNATURES) == _declared()
+
+
+def test_host_only_calls(lib):
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    L = _lib.load()
+    assert L.spmm_version() >= 100
+    assert L.spmm_status_string(0) == b"ok"
+    assert L.spmm_status_string(4) == b"invalid sparse format data"
+
+
+def test_struct_layouts_match_c():
+    # sizes of the format structs as laid out by the C compiler (x86-64 / aarch64 LP64)
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    assert ctypes.sizeof(_lib.BcsrT) == 8 * 2 + 4 * 2 + 8 + 8 + 8 * 3
+    assert ctypes.sizeof(_lib.T24) == 8 * 2 + 8 + 8 * 2
+    assert ctypes.sizeof(_lib.TvwT) == 8 * 2 + 4 * 2 + 8 * 2 + 8 * 4
+    assert ctypes.sizeof(_lib.WcsrT) == 8 * 3 + 4 * 3 + 4 + 8 * 3 + 8 * 9
+
+
+def test_host_validation_rejects_bad_arguments_before_launch():
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    L = _lib.load()
+    a = _lib.BcsrT(256, 256, 16, 16, 64, 0, None, None, None)
+    # null B / C -> SPMM_ERR_NULL
+    assert L.spmm_bcsr(ctypes.byref(a), None, 64, None, 64, 64, None) == 1
+    # M not divisible by bh -> SPMM_ERR_SHAPE (checked before any device work)
+    b = _lib.BcsrT(250, 256, 16, 16, 64, 0, 16, 16, 16)
+    assert L.spmm_bcsr(ctypes.byref(b), 16, 64, 16, 64, 64, None) == 2
+    # int8 BCSR SpMM -> SPMM_ERR_DTYPE
+    c = _lib.BcsrT(256, 256, 16, 16, 64, 2, 16, 16, 16)
+    assert L.spmm_bcsr(ctypes.byref(c), 16, 64, 16, 64, 64, None) == 3
+    # K % 8 for the 2:4 compressor -> SPMM_ERR_SHAPE
+    assert L.spmm_compress_24(16, 4, 12, 12, 2, 16, 16, None) == 2
