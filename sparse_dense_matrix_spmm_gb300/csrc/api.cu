@@ -222,12 +222,49 @@ spmm_status spmm_wcsr(const spmm_wcsr_t*, const void*, int64_t, float*, int64_t,
                       spmm_stream_t) {
     return SPMM_ERR_UNSUPPORTED;
 }
-spmm_status spmm_24_workspace_size(const spmm_24_t*, int64_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
-spmm_status spmm_24(const spmm_24_t*, const void*, int64_t, void*, int64_t, int64_t, void*, size_t, spmm_stream_t) {
-    return SPMM_ERR_UNSUPPORTED;
+static spmm_status check_24(const spmm_24_t* A, int64_t N) {
+    if (!A) return SPMM_ERR_NULL;
+    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || N < 0) return SPMM_ERR_SHAPE;
+    if (A->K % 128) return SPMM_ERR_SHAPE;
+    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    return SPMM_OK;
 }
-spmm_status spmm_tvw(const spmm_tvw_t*, const void*, int64_t, float*, int64_t, int64_t, spmm_stream_t) {
-    return SPMM_ERR_UNSUPPORTED;
+
+spmm_status spmm_24_workspace_size(const spmm_24_t* A, int64_t N, size_t* bytes) {
+    if (!bytes) return SPMM_ERR_NULL;
+    spmm_status st = check_24(A, N);
+    if (st != SPMM_OK) return st;
+    *bytes = spmm24_workspace_bytes(A, N);
+    return SPMM_OK;
+}
+
+spmm_status spmm_24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
+                    void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
+    spmm_status st = check_24(A, N);
+    if (st != SPMM_OK) return st;
+    if (!B || !C || (A->M > 0 && (!A->vals || !A->meta))) return SPMM_ERR_NULL;
+    if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
+    if (A->dtype != SPMM_I8 && ((ldb * 2) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
+    const size_t need = spmm24_workspace_bytes(A, N);
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SPMM_ERR_WORKSPACE;
+    return launch_spmm24(A, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                     spmm_stream_t stream) {
+    if (!A || !B || !C) return SPMM_ERR_NULL;
+    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || N < 0 || A->Kp < 0 || A->tile_rows <= 0) return SPMM_ERR_SHAPE;
+    if (A->n_tiles != (A->M + A->tile_rows - 1) / A->tile_rows) return SPMM_ERR_SHAPE;
+    if (A->M > 0 && (!A->tile_ptr || !A->cols || !A->vals || !A->meta)) return SPMM_ERR_NULL;
+    if (ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B) || !aligned16(A->vals) || !aligned16(A->meta))
+        return SPMM_ERR_SHAPE;
+    if (A->tile_rows != 128 || A->Kp % 128 || A->Kp == 0) return SPMM_ERR_UNSUPPORTED;
+    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    return launch_tvw(A, B, ldb, C, ldc, N, reinterpret_cast<cudaStream_t>(stream));
 }
 spmm_status spmm_build_wcsr_workspace_size(const spmm_csr_t*, int32_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
 spmm_status spmm_build_wcsr_count(const spmm_csr_t*, int32_t, int32_t, void*, size_t, int64_t*, int64_t*,

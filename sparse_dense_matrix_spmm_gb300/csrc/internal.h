@@ -44,6 +44,12 @@ bool set_smem_attr_once(const void* kernel, int bytes, int slot);
 spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
                         cudaStream_t stream);
 
+size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N);
+spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
+                          void* ws, cudaStream_t stream);
+spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                       cudaStream_t stream);
+
 spmm_status run_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
                            int32_t* row_ptr, int64_t* nnzb, cudaStream_t s);
 spmm_status run_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,

@@ -1,0 +1,510 @@
+// spmm24.cu -- C = A * B for A in 2:4 form (dense B) and in tile-vector-wise
+// form (each 128-row tile gathers its kept rows of B), on the sparse tensor
+// core: tcgen05.mma.sp, kind::f16, fp32 accumulation in TMEM.
+//
+// "Accelerating Sparse DNNs Based on Tiled GEMM" (abstract): tile-wise pruning
+// is applied at the global-memory level (here: TMA tile::gather4 of the kept B
+// rows into shared memory) and the 2:4 pattern executes inside the sparse
+// tensor core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
+//
+// Roles (224 threads, one CTA per SM, persistent over 128 x 128 output tiles):
+//   warp 0     producer: per 128-wide dense-K step, TMA loads of the compressed A
+//              tile (128 x 64, K-major, 128B swizzle), its metadata (128 x 16 B)
+//              and the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle;
+//              for TVW one gather4 per 4 kept rows).
+//   warp 1     MMA issuer: tcgen05.cp of the stage's metadata into TMEM, then four
+//              sparse MMAs (M=128, N=128, K=32 dense each), commit frees the stage.
+//   warp 2     metadata warp: rewrites the stage's canonical metadata into the
+//              tensor core's TMEM order (below) and zeroes B rows past a tile's
+//              kept-column count.
+//   warps 3-6  epilogue: tcgen05.ld the accumulator and write C.
+//
+// Metadata order in TMEM (measured on the device for kind::f16, M = 128,
+// selector 0): within each 16-row block, TMEM lane l (l < 8) holds in its low
+// half the indices of row l for K columns 0-15 of the MMA and in its high half
+// those of row l+8; lane l+8 holds the same for K columns 16-31.  The stored
+// format keeps one little-endian 32-bit word per row and MMA, so the rewrite is
+// a swap of 16-bit halves between rows l and l^8.
+//
+// int8 operands: the tensor core on sm_103a has no integer MMA, so int8 values
+// (exact in fp16) are widened to fp16 in a workspace and multiplied with fp32
+// accumulation.  Every product is an integer of magnitude at most 127*127; the
+// accumulator is drained every 512 dense K (256 products, |partial| <= 2^22,
+// all partial sums exact) and the chunks are summed in int32 by the epilogue,
+// so C is exact.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace spmm {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 224;
+constexpr int BM = 128, BN = 128, KS = 128;                 // KS: dense K per stage
+constexpr uint32_t A_BYTES = BM * (KS / 2) * 2;             // 16 KB
+constexpr uint32_t B_BYTES = KS * BN * 2;                   // 32 KB: two 64-column chunks
+constexpr uint32_t B_CHUNK = KS * 128;                      // 16 KB
+constexpr uint32_t M_BYTES = BM * (KS / 8);                 // 2 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + 2 * M_BYTES;  // 52 KB
+constexpr int STAGES = 4;
+constexpr int NACC = 2;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t META_COL = NACC * BN;                    // metadata columns after the accumulators
+constexpr int INT_CHUNK_STEPS = 4;                          // 4 x 128 = 512 dense K per int chunk
+constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + M_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+
+struct SpArgs {
+    int64_t M, N, K;          // K: dense depth of the 2:4 operand (multiple of 128)
+    int32_t n_mtiles, n_ntiles;
+    const int32_t* tile_ptr;  // TVW only
+    const int32_t* cols;      // TVW only
+    void* C;
+    int64_t ldc;
+    uint32_t idesc;
+    int32_t vec_ok;           // C rows 16-byte aligned
+    int* err;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int& kt, bool gather) {
+    if (gather) {
+        kb = __ldg(a.tile_ptr + mt);
+        kt = __ldg(a.tile_ptr + mt + 1) - kb;
+        return (kt + KS - 1) / KS;
+    }
+    kb = 0;
+    kt = static_cast<int>(a.K);
+    return static_cast<int>(a.K / KS);
+}
+
+template <bool GATHER, bool INT_EXACT>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
+                       const __grid_constant__ CUtensorMap tmB, const SpArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
+    // stage s: [A | B chunk 0 | B chunk 1 | canonical meta | TMEM-order meta]
+    auto a_s = [&](int s) { return s0 + s * STAGE_BYTES; };
+    auto b_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES; };
+    auto mc_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES + B_BYTES; };
+    auto mp_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES + B_BYTES + M_BYTES; };
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto mready_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + NACC + b); };
+    const uint32_t done_bar = bar0 + 8u * (3 * STAGES + 2 * NACC);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(mready_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < NACC; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmMeta);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tslot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int64_t total = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
+    constexpr int CH = INT_EXACT ? INT_CHUNK_STEPS : (1 << 30);
+
+    if (warp == 0) {
+        // -------------------------------------------------------- producer
+        int s = 0;
+        uint32_t ph = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            const int mt = static_cast<int>(u % a.n_mtiles), nt = static_cast<int>(u / a.n_mtiles);
+            const int m0 = mt * BM, n0 = nt * BN;
+            int kb, kt;
+            const int nk = tile_steps(a, mt, kb, kt, GATHER);
+            for (int ks = 0; ks < nk; ++ks) {
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
+                    tma_load_2d(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0);
+                    tma_load_2d(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0);
+                    if (!GATHER) {
+                        tma_load_2d(b_s(s), &tmB, full_bar(s), n0, ks * KS);
+                        tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, ks * KS);
+                    }
+                }
+                if (GATHER) {
+                    __syncwarp();
+                    // lane l brings kept rows 4l..4l+3 of this step (both 64-column chunks);
+                    // rows past the tile's kept count re-read its first kept row and are
+                    // zeroed in shared memory by the metadata warp.
+                    int32_t r[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int k = ks * KS + 4 * lane + i;
+                        r[i] = __ldg(a.cols + kb + (k < kt ? k : 0));
+                    }
+                    tma_gather4(b_s(s) + lane * 512u, &tmB, full_bar(s), n0, r[0], r[1], r[2], r[3]);
+                    tma_gather4(b_s(s) + B_CHUNK + lane * 512u, &tmB, full_bar(s), n0 + 64, r[0], r[1], r[2],
+                                r[3]);
+                }
+                ++issued;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        // Leave no copy in flight: wait for the last phase armed on each slot.
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+            const int slot = (s - 1 - i + 2 * STAGES) % STAGES;
+            const uint32_t par = (slot < s) ? ph : (ph ^ 1u);
+            mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int s = 0, acc_i = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                const int mt = static_cast<int>(u % a.n_mtiles);
+                int kb, kt;
+                const int nk = tile_steps(a, mt, kb, kt, GATHER);
+                const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
+                for (int c = 0; c < nch && ok; ++c, ++acc_i) {
+                    const int b = acc_i & 1;
+                    const uint32_t aph = static_cast<uint32_t>(acc_i >> 1) & 1u;
+                    if (!mbar_wait(acce_bar(b), aph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                    const int k_lo = c * CH, k_hi = min(nk, k_lo + CH);
+                    for (int ks = k_lo; ks < k_hi; ++ks) {
+                        if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT) ||
+                            !mbar_wait(mready_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t mcol = tmem + META_COL + 4u * s;
+                        tmem_cp_128x128b(mcol, smem_desc(mp_s(s), 128u, 128u, SWZ_NONE));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint64_t ad = smem_desc(a_s(s) + 32u * i, 16u, 1024u, SWZ_128B);
+                            const uint64_t bd = smem_desc(b_s(s) + 4096u * i, B_CHUNK, 1024u, SWZ_128B);
+                            mma_sp_f16(d, ad, bd, mcol + i, a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
+                        }
+                        mma_commit(empty_bar(s));
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    mma_commit(accf_bar(b));
+                }
+            }
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------------------- metadata warp
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            const int mt = static_cast<int>(u % a.n_mtiles);
+            int kb, kt;
+            const int nk = tile_steps(a, mt, kb, kt, GATHER);
+            for (int ks = 0; ks < nk; ++ks) {
+                if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* mc = smem + s * STAGE_BYTES + A_BYTES + B_BYTES;
+                uint8_t* mp = smem + s * STAGE_BYTES + A_BYTES + B_BYTES + M_BYTES;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = lane + 32 * j;
+                    uint4 w = *reinterpret_cast<const uint4*>(mc + 16 * r);
+                    // rows past M arrive zero-filled; give them the valid (0, 1) pattern
+                    if (static_cast<int64_t>(mt) * BM + r >= a.M) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+                    uint4 o;
+                    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t out[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t p = __shfl_xor_sync(0xffffffffu, in[i], 8);
+                        out[i] = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
+                    }
+                    o.x = out[0];
+                    o.y = out[1];
+                    o.z = out[2];
+                    o.w = out[3];
+                    *reinterpret_cast<uint4*>(mp + 16 * r) = o;
+                }
+                if (GATHER && (ks + 1) * KS > kt) {
+                    // rows past the kept count must contribute nothing
+                    const int r0 = kt - ks * KS;
+                    uint8_t* bs = smem + s * STAGE_BYTES + A_BYTES;
+                    for (int idx = r0 * 8 + lane; idx < KS * 8; idx += 32) {
+                        const int r = idx / 8, c = idx % 8;
+                        *reinterpret_cast<uint4*>(bs + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(bs + B_CHUNK + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(mready_bar(s));
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        int acc_i = 0;
+        for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+            const int mt = static_cast<int>(u % a.n_mtiles), nt = static_cast<int>(u / a.n_mtiles);
+            int kb, kt;
+            const int nk = tile_steps(a, mt, kb, kt, GATHER);
+            const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
+            const int64_t row = static_cast<int64_t>(mt) * BM + q * 32 + lane;
+            const int64_t n0 = static_cast<int64_t>(nt) * BN;
+            const bool row_live = row < a.M;
+            const bool full_n = n0 + BN <= a.N && a.vec_ok;
+            const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            int32_t run[INT_EXACT ? BN : 1];
+#pragma unroll
+            for (int i = 0; i < (INT_EXACT ? BN : 1); ++i) run[i] = 0;
+            bool ok = true;
+            for (int c = 0; c < nch; ++c, ++acc_i) {
+                const int b = acc_i & 1;
+                const uint32_t aph = static_cast<uint32_t>(acc_i >> 1) & 1u;
+                if (!mbar_wait(accf_bar(b), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tl + static_cast<uint32_t>(b * BN);
+#pragma unroll
+                for (int j = 0; j < BN / 16; ++j) {
+                    uint32_t v[16];
+                    if (nk > 0) {
+                        tmem_ld16(tb + 16 * j, v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0u;
+                    }
+                    if constexpr (INT_EXACT) {
+                        // integer-valued fp32 with |x| <= 2^22: x + 1.5 * 2^23 has the bits
+                        // 0x4B400000 + x
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            run[16 * j + i] += __float_as_int(__uint_as_float(v[i]) + 12582912.0f) - 0x4B400000;
+                    } else if (row_live) {
+                        float* cp = static_cast<float*>(a.C) + row * a.ldc + n0 + 16 * j;
+                        if (full_n) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4)
+                                __stcs(reinterpret_cast<float4*>(cp + i),
+                                       make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                   __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (n0 + 16 * j + i < a.N) cp[i] = __uint_as_float(v[i]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(b));
+            }
+            if (!ok) break;
+            if constexpr (INT_EXACT) {
+                if (row_live) {
+                    int32_t* cp = static_cast<int32_t*>(a.C) + row * a.ldc + n0;
+                    if (full_n) {
+#pragma unroll
+                        for (int i = 0; i < BN; i += 4)
+                            __stcs(reinterpret_cast<int4*>(cp + i),
+                                   make_int4(run[i], run[i + 1], run[i + 2], run[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BN; ++i)
+                            if (n0 + i < a.N) cp[i] = run[i];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// int8 -> fp16, exact (|v| <= 127).  8 elements per thread; rows of `cols`
+// elements with leading dimensions lds (source) and ldd (destination).
+__global__ void widen_i8_kernel(const int8_t* __restrict__ src, int64_t lds, __half* __restrict__ dst, int64_t ldd,
+                                int64_t rows, int64_t cols) {
+    const int64_t per_row = (cols + 7) / 8;
+    const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (id >= rows * per_row) return;
+    const int64_t r = id / per_row, c = (id % per_row) * 8;
+    const int8_t* sp = src + r * lds + c;
+    __half* dp = dst + r * ldd + c;
+    if (c + 8 <= cols && (reinterpret_cast<uintptr_t>(sp) & 7) == 0 && (reinterpret_cast<uintptr_t>(dp) & 15) == 0) {
+        const int2 w = *reinterpret_cast<const int2*>(sp);
+        const int8_t* b = reinterpret_cast<const int8_t*>(&w);
+        __align__(16) __half h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = __int2half_rn(b[i]);
+        *reinterpret_cast<uint4*>(dp) = *reinterpret_cast<const uint4*>(h);
+    } else {
+        for (int i = 0; i < 8 && c + i < cols; ++i) dp[i] = __int2half_rn(sp[i]);
+        for (int i = static_cast<int>(cols - c); i < 8 && c + i < ldd; ++i)
+            if (i >= 0) dp[i] = __float2half(0.f);
+    }
+}
+
+template <bool GATHER, bool INT_EXACT>
+spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const CUtensorMap& tmB, const SpArgs& a,
+                          cudaStream_t stream, int slot) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (dev->max_smem_optin < SMEM_BYTES) return SPMM_ERR_UNSUPPORTED;
+    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT>;
+    if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), SMEM_BYTES, slot)) return SPMM_ERR_CUDA;
+    const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
+    const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
+    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(tmA, tmM, tmB, a);
+    return cuda_status(cudaGetLastError());
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N) {
+    if (A->dtype != SPMM_I8) return 0;
+    const int64_t np = (N + 7) / 8 * 8;
+    return align256(static_cast<size_t>(A->M) * (A->K / 2) * 2) + align256(static_cast<size_t>(A->K) * np * 2);
+}
+
+spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
+                          void* ws, cudaStream_t stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (A->M == 0 || N == 0) return SPMM_OK;
+    const bool i8 = A->dtype == SPMM_I8;
+    const void* vals = A->vals;
+    const void* bsrc = B;
+    int64_t bld = ldb;
+    const CUtensorMapDataType t = i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : half_type(A->dtype);
+    if (i8) {
+        __half* wa = static_cast<__half*>(ws);
+        __half* wb = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) +
+                                               align256(static_cast<size_t>(A->M) * (A->K / 2) * 2));
+        const int64_t np = (N + 7) / 8 * 8;
+        const int64_t na = A->M * ((A->K / 2 + 7) / 8), nb = A->K * (np / 8);
+        widen_i8_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, stream>>>(
+            static_cast<const int8_t*>(A->vals), A->K / 2, wa, A->K / 2, A->M, A->K / 2);
+        widen_i8_kernel<<<static_cast<unsigned>((nb + 255) / 256), 256, 0, stream>>>(
+            static_cast<const int8_t*>(B), ldb, wb, np, A->K, N);
+        if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
+        vals = wa;
+        bsrc = wb;
+        bld = np;
+    }
+    CUtensorMap tmA, tmM, tmB;
+    if (!encode_tmap_2d(&tmA, t, vals, static_cast<uint64_t>(A->K / 2), static_cast<uint64_t>(A->M),
+                        static_cast<uint64_t>(A->K), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->meta, static_cast<uint64_t>(A->K / 8),
+                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(A->K / 8), 16, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_2d(&tmB, t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+                        static_cast<uint64_t>(bld) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPMM_ERR_CUDA;
+    SpArgs a{};
+    a.M = A->M;
+    a.N = N;
+    a.K = A->K;
+    a.n_mtiles = static_cast<int32_t>((A->M + BM - 1) / BM);
+    a.n_ntiles = static_cast<int32_t>((N + BN - 1) / BN);
+    a.C = C;
+    a.ldc = ldc;
+    a.idesc = idesc_f16(128, BN, A->dtype == SPMM_BF16, false, true, true, 0);
+    a.vec_ok = (ldc % 4 == 0) && aligned16(C);
+    a.err = dev->err;
+    a.timeout_ns = kWaitTimeoutNs;
+    if (i8) return launch_sparse<false, true>(tmA, tmM, tmB, a, stream, 2);
+    return launch_sparse<false, false>(tmA, tmM, tmB, a, stream, 1);
+}
+
+spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                       cudaStream_t stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (A->M == 0 || N == 0) return SPMM_OK;
+    const CUtensorMapDataType t = half_type(A->dtype);
+    CUtensorMap tmA, tmM, tmB;
+    if (!encode_tmap_2d(&tmA, t, A->vals, static_cast<uint64_t>(A->Kp / 2), static_cast<uint64_t>(A->M),
+                        static_cast<uint64_t>(A->Kp), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->meta, static_cast<uint64_t>(A->Kp / 8),
+                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(A->Kp / 8), 16, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_2d(&tmB, t, B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+                        static_cast<uint64_t>(ldb) * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPMM_ERR_CUDA;
+    SpArgs a{};
+    a.M = A->M;
+    a.N = N;
+    a.K = A->Kp;
+    a.n_mtiles = static_cast<int32_t>(A->n_tiles);
+    a.n_ntiles = static_cast<int32_t>((N + BN - 1) / BN);
+    a.tile_ptr = A->tile_ptr;
+    a.cols = A->cols;
+    a.C = C;
+    a.ldc = ldc;
+    a.idesc = idesc_f16(128, BN, A->dtype == SPMM_BF16, false, true, true, 0);
+    a.vec_ok = (ldc % 4 == 0) && aligned16(C);
+    a.err = dev->err;
+    a.timeout_ns = kWaitTimeoutNs;
+    return launch_sparse<true, false>(tmA, tmM, tmB, a, stream, 3);
+}
+
+}  // namespace spmm

@@ -138,20 +138,25 @@ def csr_lognormal_problem(M: int, K: int, N: int, seed: int, mean: float = 16.0,
             "B": B, "M": M, "K": K, "N": N, "dtype": dtype}
 
 
-def tvw_problem(M: int, K: int, N: int, tile_rows: int, keep: int, seed: int,
+def tvw_problem(M: int, K: int, N: int, tile_rows: int, keep, seed: int,
                 dtype: str = F16) -> dict:
-    """Dense A (bits) in tile-vector-wise form plus the per-tile kept columns."""
-    assert keep % 4 == 0 and keep <= K
+    """Dense A (bits) in tile-vector-wise form plus the per-tile kept columns.
+
+    ``keep`` is the kept-column count of every tile, or one count per tile."""
     rng = np.random.default_rng(seed)
     nt = (M + tile_rows - 1) // tile_rows
+    keeps = [int(keep)] * nt if np.isscalar(keep) else [int(k) for k in keep]
+    assert len(keeps) == nt and all(k % 4 == 0 and 0 <= k <= K for k in keeps)
     pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)], dtype=np.int64)
-    tile_ptr = np.arange(nt + 1, dtype=np.int64) * keep
-    cols = np.zeros(nt * keep, dtype=np.int64)
+    tile_ptr = np.zeros(nt + 1, dtype=np.int64)
+    np.cumsum(keeps, out=tile_ptr[1:])
+    cols = np.zeros(int(tile_ptr[-1]), dtype=np.int64)
     A = np.zeros((M, K), dtype=np.uint16)
-    G = keep // 4
     for t in range(nt):
+        keep = keeps[t]
+        G = keep // 4
         kc = np.sort(rng.choice(K, size=keep, replace=False))
-        cols[t * keep:(t + 1) * keep] = kc
+        cols[tile_ptr[t]:tile_ptr[t + 1]] = kc
         r0, r1 = t * tile_rows, min(M, (t + 1) * tile_rows)
         sel = pairs[rng.integers(0, 6, size=(r1 - r0, G))]
         kidx = sel + (np.arange(G, dtype=np.int64) * 4)[None, :, None]

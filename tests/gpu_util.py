@@ -44,3 +44,14 @@ def assert_close(got, ref, what=""):
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; first at {tuple(i)} "
                              f"gpu={got[tuple(i)]} oracle={ref[tuple(i)]}")
+
+
+def padded_b(bits, dtype):
+    """B on the device with its row pitch rounded up to 8 elements (16 bytes), as a K x N view."""
+    import torch
+    K, N = bits.shape
+    ld = -(-N // 8) * 8
+    full = torch.zeros((K, ld), dtype=torch.int16, device="cuda")
+    full[:, :N] = dev(bits)
+    full = full.view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return full[:, :N]

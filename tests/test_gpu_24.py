@@ -1,0 +1,97 @@
+"""2:4 on the GPU vs the CPU oracle: compression bit-exact, int8 SpMM exact,
+fp16/bf16 SpMM within tolerance."""
+import numpy as np
+import pytest
+
+import oracle
+import spmm_inputs as gen
+from tests.gpu_util import assert_close, dev, dev_half, host_bits, need_gpu, padded_b
+
+pytestmark = pytest.mark.gpu
+
+
+def _compress(p, dtype):
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    A = dev(p["A"]) if dtype == "i8" else dev_half(p["A"], dtype)
+    F = spmm.spmm_compress_24(A)
+    O = oracle.compress24(p["A"], dtype)
+    assert np.array_equal(host_bits(F.vals), O["vals"])
+    assert np.array_equal(F.meta.cpu().numpy(), O["meta"])
+    return F, O
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 512, 256), (200, 1024, 300), (128, 128, 8), (384, 2048, 520)])
+def test_24_int8_exact(M, K, N):
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.mask24_problem(M, K, N, seed=M + K + N)
+    F, O = _compress(p, "i8")
+    C = spmm.spmm_24(F, dev(p["B"]))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    ref = oracle.spmm24(O, p["B"])
+    assert np.array_equal(C.cpu().numpy().astype(np.int64), ref)
+
+
+def test_24_int8_extreme_values_stay_exact():
+    """Every product 127*127 with equal signs: each 512-wide chunk reaches its
+    largest partial sum (256 * 16129), so any lost bit would show."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    M, K, N = 128, 4096, 128
+    A = np.zeros((M, K), np.int8)
+    A[:, 0::4] = 127
+    A[:, 3::4] = 127
+    A[1::2, 0::4] = -127          # odd rows mix signs
+    B = np.full((K, N), 127, np.int8)
+    B[:, 1::2] = -127
+    p = {"A": A, "B": B}
+    F, O = _compress(p, "i8")
+    C = spmm.spmm_24(F, dev(B))
+    torch.cuda.synchronize()
+    ref = oracle.spmm24(O, B)
+    assert ref.max() == 2048 * 16129
+    assert np.array_equal(C.cpu().numpy().astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,K,N", [(256, 512, 256), (136, 1024, 200)])
+def test_24_float(dtype, M, K, N):
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    rng = np.random.default_rng(M * K + N)
+    mask = gen.mask24_problem(M, K, 1, seed=7)["A"] != 0
+    Abits = gen.normal_bits(rng, (M, K), dtype)
+    Abits[~mask] = 0
+    Bbits = gen.normal_bits(rng, (K, N), dtype)
+    F, O = _compress({"A": Abits}, dtype)
+    C = spmm.spmm_24(F, padded_b(Bbits, dtype))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert_close(C.cpu().numpy(), oracle.spmm24(O, Bbits), f"2:4 {dtype}")
+
+
+def test_24_compress_rejects_three_nonzeros():
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    A = torch.zeros((16, 64), dtype=torch.int8, device="cuda")
+    A[3, 8:11] = 1
+    with pytest.raises(spmm.SpmmError) as e:
+        spmm.spmm_compress_24(A)
+    assert e.value.name == "SPMM_ERR_FORMAT"
+
+
+def test_24_int8_full_size_sampled_rows():
+    """A 8192 x 8192 int8 (2:4), B 8192 x 4096 int8: the oracle recomputes 96
+    seeded rows exactly (all 4096 columns)."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.config_problem("mask24_int8")
+    F, O = _compress(p, "i8")
+    C = spmm.spmm_24(F, dev(p["B"]))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    rows = np.sort(np.random.default_rng(21).choice(p["M"], size=96, replace=False))
+    got = C[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.int64)
+    ref = np.concatenate([oracle.spmm24(O, p["B"], rows=(int(r), int(r) + 1)) for r in rows])
+    assert np.array_equal(got, ref)

@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import spmm_inputs as gen
-from tests.gpu_util import assert_close, dev_half, host_bits, need_gpu
+from tests.gpu_util import assert_close, dev_half, host_bits, need_gpu, padded_b
 
 pytestmark = pytest.mark.gpu
 
@@ -13,7 +13,7 @@ def _run(p, dtype="bf16"):
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     A = dev_half(p["A"], dtype)
-    B = dev_half(p["B"], dtype)
+    B = padded_b(p["B"], dtype)
     F = spmm.build_bcsr(A, p["bh"], p["bw"])
     O = oracle.bcsr_build(p["A"], p["bh"], p["bw"], dtype)
     assert F.nnzb == O["nnzb"]
