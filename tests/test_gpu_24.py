@@ -50,7 +50,7 @@ def test_24_int8_extreme_values_stay_exact():
     C = spmm.spmm_24(F, dev(B))
     torch.cuda.synchronize()
     ref = oracle.spmm24(O, B)
-    assert ref.max() == 4096 * 16129
+    assert ref.max() == (K // 2) * 16129
     assert np.array_equal(C.cpu().numpy().astype(np.int64), ref)
 
 
