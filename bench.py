@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Throughput of C = A_sparse @ B_dense on GB300, one JSON line on stdout.
+
+Headline workload: A 8192 x 8192 int8 in 2:4 form (exactly two nonzeros in
+every group of four along K), B 8192 x 4096 int8, C int32 (exact).  A step is
+one spmm_24 call with A (already compressed) and B resident in HBM; the L2 is
+flushed (256 MiB written) before every timed step.  Metric: effective
+TFLOP/s = 2 * nnz * N / time.
+
+The same line carries, per other format (BCSR LLM-shaped, tile-vector-wise,
+row-window CSR, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+replicas: the path has no exchange step); time is the max over ranks and
+`value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SpMM effective TFLOP/s (2·nnz·N/time) and % of roofline, per sparse format"
+HEADLINE = "mask24_int8"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "sparse_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/spmm24.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
+    "bcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/bcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
+    "wcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu",),
+}
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}|{workload}")
+    if not e:
+        return None
+    try:
+        if e.get("source_sha") != source_sha(*KERNEL_SOURCES[kernel]):
+            return None
+    except OSError:
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workloads (ours)
+def to_dev(bits, torch_dtype=None):
+    import torch
+    if bits.dtype == np.int8:
+        return torch.from_numpy(np.ascontiguousarray(bits)).cuda()
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+    return t.view(torch_dtype) if torch_dtype is not None else t
+
+
+def timed_steps(step, steps, warmup, flush_buf, ws):
+    """Warm up, then time exactly `steps` steps with CUDA events (L2 flushed before each)."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush_buf.zero_()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def roofline(flops, alg_bytes, t_s, peaks, prefer=None, traffic=None, peak_kind="burst"):
+    """Roofline object for one kernel: bound = the larger of the two time floors."""
+    P = peaks["bf16_tflops"] if peak_kind == "burst" else peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    BW = peaks["hbm_gbs"]
+    t_tensor = flops / (P * 1e12)
+    t_hbm = alg_bytes / (BW * 1e9)
+    bound = prefer or ("tensor" if t_tensor >= t_hbm else "hbm")
+    if bound == "tensor":
+        ach = flops / t_s / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": P, "unit": "TFLOP/s",
+                "frac": round(ach / P, 4), "traffic": traffic}
+    ach = alg_bytes / t_s / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": BW, "unit": "GB/s", "frac": round(ach / BW, 4),
+            "traffic": traffic}
+
+
+def run_headline(args, ws, rank, local, peaks, flush_buf):
+    import torch
+    import spmm_inputs as gen
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.config_problem(HEADLINE)
+    M, K, N = p["M"], p["K"], p["N"]
+    nnz = M * K // 2
+    flops = 2.0 * nnz * N
+    A = to_dev(p["A"])
+    B = to_dev(p["B"])
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    F = spmm.spmm_compress_24(A)
+    torch.cuda.synchronize()
+    build_ms = (time.perf_counter() - t0) * 1e3
+    del A
+    Cd = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    wsz = spmm.spmm_24_workspace_size(F, N)
+    wsp = torch.empty(wsz, dtype=torch.uint8, device="cuda")
+
+    def step():
+        spmm.spmm_24(F, B, Cd, wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    spmm.trace_enable(True)  # trace exactly the timed steps
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    total_ms = timed_steps(step, args.steps, 0, flush_buf, ws)
+    clocks = sampler.stop()
+    n_sp, ms_sp = spmm.trace_read(spmm._lib.KERNEL_SPARSE)
+    n_wd, ms_wd = spmm.trace_read(spmm._lib.KERNEL_WIDEN)
+    spmm.trace_enable(False)
+    total_ms = max_over_ranks(total_ms, ws, "cuda")
+    ms_step = total_ms / args.steps
+    value = ws * flops * args.steps / (total_ms / 1e3) / 1e12
+    t_kernel = ms_sp / max(n_sp, 1) / 1e3
+    alg_bytes = nnz * 1 + M * K // 8 + K * N + M * N * 4
+    rl = roofline(flops, alg_bytes, t_kernel, peaks, prefer="tensor",
+                  traffic=measured_traffic("sparse_spmm_kernel", HEADLINE))
+    rl["kernel"] = "sparse_spmm_kernel<dense B, int-exact>"
+    rl["kernel_ms"] = round(t_kernel * 1e3, 4)
+    rl["widen_ms"] = round(ms_wd / max(n_wd, 1), 4)
+
+    # end to end through the public API: pinned host B in, int32 C out, every step
+    Bh = torch.from_numpy(p["B"]).pin_memory()
+    Ch = torch.empty((M, N), dtype=torch.int32).pin_memory()
+    Bd = torch.empty_like(B)
+
+    def e2e_step():
+        Bd.copy_(Bh, non_blocking=True)
+        spmm.spmm_24(F, Bd, Cd, wsp)
+        Ch.copy_(Cd, non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 10))
+    e2e_ms = timed_steps(e2e_step, n_e2e, 2, flush_buf, ws)
+    e2e_ms = max_over_ranks(e2e_ms, ws, "cuda")
+    e2e = {"value": round(ws * flops * n_e2e / (e2e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(Bh.numel() * Bh.element_size()),
+           "d2h_bytes_per_step": int(Ch.numel() * Ch.element_size()),
+           "ms_per_step": round(e2e_ms / n_e2e, 4)}
+    launches = (n_sp + 2 * n_wd) * ws
+    return {"value": value, "ms_step": ms_step, "roofline": rl, "clocks": clocks, "e2e": e2e,
+            "build_ms": build_ms, "launches": launches, "M": M, "K": K, "N": N, "nnz": nnz, "problem": p}
+
+
+def run_extra(name, args, ws, peaks, flush_buf):
+    """One of the other measured workloads: time, TFLOP/s, GB/s, roofline."""
+    import torch
+    import spmm_inputs as gen
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    c = gen.CONFIGS[name]
+    steps = max(3, min(args.steps, 10))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(int(c["seed"]))
+    if c["kind"] == "bcsr":
+        p = gen.bcsr_problem(c["M"], c["K"], 8, c["bh"], c["bw"], c["nnzb"], c["seed"], c["dtype"], c["std"])
+        dt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float16
+        A = to_dev(p["A"], dt)
+        Bx = torch.randn((c["K"], c["N"]), generator=g, device="cuda", dtype=torch.float32).to(dt)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        F = spmm.build_bcsr(A, c["bh"], c["bw"])
+        torch.cuda.synchronize()
+        build_ms = (time.perf_counter() - t0) * 1e3
+        del A
+        Cd = torch.empty((c["M"], c["N"]), dtype=torch.float32, device="cuda")
+        nnz = F.nnzb * c["bh"] * c["bw"]
+        alg = nnz * 2 + F.nnzb * 4 + (c["M"] // c["bh"] + 1) * 4 + c["K"] * c["N"] * 2 + c["M"] * c["N"] * 4
+        kern, kid = "bcsr_spmm_kernel", spmm._lib.KERNEL_BCSR
+
+        def step():
+            spmm.spmm_bcsr(F, Bx, Cd)
+    elif c["kind"] == "tvw":
+        p = gen.config_problem(name)
+        A = to_dev(p["A"], torch.float16)
+        Bx = to_dev(p["B"], torch.float16)
+        tp = to_dev(p["tile_ptr"])
+        cl = to_dev(p["cols"])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        F = spmm.spmm_build_tvw(A, c["tile_rows"], tp, cl, Kp=c["keep"])
+        torch.cuda.synchronize()
+        build_ms = (time.perf_counter() - t0) * 1e3
+        del A
+        Cd = torch.empty((c["M"], c["N"]), dtype=torch.float32, device="cuda")
+        nnz = c["M"] * c["keep"] // 2
+        alg = nnz * 2 + c["M"] * c["keep"] // 8 + int(p["cols"].size) * 4 + c["K"] * c["N"] * 2 + \
+            c["M"] * c["N"] * 4
+        kern, kid = "sparse_spmm_kernel", spmm._lib.KERNEL_SPARSE
+
+        def step():
+            spmm.spmm_tvw(F, Bx, Cd)
+    elif c["kind"] == "wcsr":
+        p = gen.config_problem(name)
+        dt = torch.float16
+        csr = spmm.CSR(c["M"], c["K"], int(p["row_ptr"][-1]), dt, to_dev(p["row_ptr"]), to_dev(p["col"]),
+                       to_dev(p["val"], dt))
+        Bx = to_dev(p["B"], dt)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        F = spmm.build_wcsr(csr, 16, 32)
+        torch.cuda.synchronize()
+        build_ms = (time.perf_counter() - t0) * 1e3
+        Cd = torch.empty((c["M"], c["N"]), dtype=torch.float32, device="cuda")
+        wsp = torch.zeros(max(1, spmm.spmm_wcsr_workspace_size(F, c["N"])), dtype=torch.uint8, device="cuda")
+        nnz = csr.nnz
+        # CSR-equivalent stored A (row_ptr, col, val) + B read once + C written once
+        alg = (c["M"] + 1) * 4 + nnz * 4 + nnz * 2 + c["K"] * c["N"] * 2 + c["M"] * c["N"] * 4
+        kern, kid = "wcsr_spmm_kernel", spmm._lib.KERNEL_WCSR
+
+        def step():
+            spmm.spmm_wcsr(F, Bx, Cd, wsp)
+    else:
+        raise ValueError(name)
+    flops = 2.0 * nnz * c["N"]
+    spmm.trace_enable(True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    spmm.trace_enable(True)
+    total_ms = timed_steps(step, steps, 0, flush_buf, ws)
+    n, ms = spmm.trace_read(kid)
+    spmm.trace_enable(False)
+    total_ms = max_over_ranks(total_ms, ws, "cuda")
+    t_kernel = ms / max(n, 1) / 1e3
+    rl = roofline(flops, alg, t_kernel, peaks, traffic=measured_traffic(kern, name))
+    rl["kernel"] = kern
+    rl["kernel_ms"] = round(t_kernel * 1e3, 4)
+    t_step = total_ms / steps / 1e3
+    return {"workload": name, "ms_per_step": round(t_step * 1e3, 4),
+            "tflops": round(ws * flops / t_step / 1e12, 3), "gbs": round(alg / t_step / 1e9, 1),
+            "nnz": int(nnz), "build_ms": round(build_ms, 2), "roofline": rl, "launches": n}
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_sample_run(p, rows):
+    import oracle
+    F = oracle.compress24(p["A"], "i8")
+    t0 = time.perf_counter()
+    oracle.spmm24(F, p["B"], rows=rows)
+    return time.perf_counter() - t0, F
+
+
+def cpu_baseline(p, target_s=12.0):
+    """The oracle (as it stands) on a bounded row sample of the headline workload."""
+    import oracle
+    F = oracle.compress24(p["A"], "i8")
+    K, N = p["K"], p["N"]
+    r = 8
+    t0 = time.perf_counter()
+    oracle.spmm24(F, p["B"], rows=(0, r))
+    dt = time.perf_counter() - t0
+    rows = int(min(p["M"], max(r, r * target_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.spmm24(F, p["B"], rows=(0, rows))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * (K // 2) * N
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {p['M']}x{K} int8 2:4 operand times the full {K}x{N} B "
+                      f"(int64 accumulation), {dt:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the CPU oracle timed on the host cores, bounded sample per step."""
+    if rank != 0:
+        return 0
+    import oracle
+    import spmm_inputs as gen
+    p = gen.config_problem(HEADLINE)
+    F = oracle.compress24(p["A"], "i8")
+    K, N = p["K"], p["N"]
+    # size one step to about 2 s of CPU work
+    t0 = time.perf_counter()
+    oracle.spmm24(F, p["B"], rows=(0, 4))
+    dt = time.perf_counter() - t0
+    rows = int(min(p["M"], max(4, 4 * 2.0 / max(dt, 1e-3))))
+    for i in range(args.warmup):
+        oracle.spmm24(F, p["B"], rows=(0, rows))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows) % (p["M"] - rows + 1)
+        oracle.spmm24(F, p["B"], rows=(r0, r0 + rows))
+    total = time.perf_counter() - t0
+    flops = 2.0 * rows * (K // 2) * N
+    value = flops * args.steps / total / 1e12
+    sample = f"{rows} rows of the {p['M']}x{K} int8 2:4 operand times the full {K}x{N} B per step (int64)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+            "config": {"workload": f"{HEADLINE}: A {p['M']}x{K} int8 2:4, B {K}x{N} int8, C int32",
+                       "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other formats")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import torch
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(ws)
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    spmm._lib.load()
+    peaks, peak_src = load_peaks()
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    h = run_headline(args, ws, rank, local, peaks, flush_buf)
+    extra = []
+    if not args.no_extra:
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "bcsr_tiny"):
+            try:
+                extra.append(run_extra(name, args, ws, peaks, flush_buf))
+            except Exception as e:  # a format whose kernel is missing is reported, not hidden
+                extra.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
+            torch.cuda.empty_cache()
+    if spmm.last_device_error() != 0:
+        raise RuntimeError("device error word set during the benchmark")
+    if rank != 0:
+        return 0
+    cpu = None if args.no_cpu_baseline else cpu_baseline(h["problem"])
+    rl = h["roofline"]
+    rl["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json bf16 burst; fp16 tensor rate = bf16 rate)" \
+        if rl["bound"] == "tensor" else peak_src
+    line = {
+        "metric": METRIC, "value": round(h["value"], 3), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(h["ms_step"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+        "config": {"workload": f"{HEADLINE}: A {h['M']}x{h['K']} int8 2:4 (2 nonzeros per 4-group), "
+                               f"B {h['K']}x{h['N']} int8, C int32 exact",
+                   "M": h["M"], "K": h["K"], "N": h["N"], "nnz": h["nnz"],
+                   "compute": "fp16 sparse tensor core on int8-valued operands, fp32 partials <= 2^22, int32 sum",
+                   "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{ws}",
+                   "build_ms": round(h["build_ms"], 2)},
+        "roofline": rl, "cpu_baseline": cpu, "e2e": h["e2e"], "gpu_launches": h["launches"],
+        "clocks": h["clocks"], "formats": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -169,6 +169,20 @@ SPMM_API spmm_status spmm_last_device_error(int32_t *bits);
  * SPMM_DEVERR_TIMEOUT and returns.  Synchronises `stream`. */
 SPMM_API spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t stream);
 
+/* Kernel-level tracing.  While enabled, the library records a pair of CUDA
+ * events on the launch stream around every kernel it launches; the reads below
+ * return how many launches of one kernel kind were traced and their summed
+ * device time.  Used by the benchmark to time the dominant kernel alone. */
+#define SPMM_KERNEL_BCSR 1    /* tcgen05 BCSR SpMM                                 */
+#define SPMM_KERNEL_SPARSE 2  /* tcgen05.mma.sp SpMM (2:4 and tile-vector-wise)    */
+#define SPMM_KERNEL_WIDEN 3   /* int8 -> fp16 operand widening (int8 2:4)          */
+#define SPMM_KERNEL_WCSR 4    /* row-window SpMM                                   */
+/* Turns tracing on (clearing earlier records) or off. */
+SPMM_API spmm_status spmm_trace_enable(int32_t on);
+/* Synchronises the traced events and reports launches and total milliseconds
+ * of `kernel` (an SPMM_KERNEL_* id) since tracing was enabled. */
+SPMM_API spmm_status spmm_trace_read(int32_t kernel, int64_t *launches, double *total_ms);
+
 /* ---------------------------------------------------------------- SpMM */
 
 /* C = A * B with A in BCSR ("AsyncSparse": warp-specialised TMA -> tensor core

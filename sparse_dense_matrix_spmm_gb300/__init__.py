@@ -28,7 +28,7 @@ __all__ = ["BCSR", "Mat24", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bcsr", "spm
            "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_24", "spmm_24_workspace_size",
            "spmm_build_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
-           "last_device_error", "selftest_timeout", "library_path"]
+           "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
 
 _DT = {torch.bfloat16: _lib.SPMM_BF16, torch.float16: _lib.SPMM_F16, torch.int8: _lib.SPMM_I8}
 
@@ -160,6 +160,18 @@ def last_device_error() -> int:
 
 def selftest_timeout(timeout_ns: int = 1_000_000, stream=None) -> None:
     _lib.call("spmm_selftest_timeout", C.c_uint64(timeout_ns), _stream(stream))
+
+
+def trace_enable(on: bool = True) -> None:
+    """Record CUDA events around every library kernel launch (see spmm_trace_read)."""
+    _lib.call("spmm_trace_enable", 1 if on else 0)
+
+
+def trace_read(kernel: int):
+    """(launches, total_ms) of one kernel kind since tracing was enabled."""
+    n, ms = C.c_int64(0), C.c_double(0.0)
+    _lib.call("spmm_trace_read", kernel, C.byref(n), C.byref(ms))
+    return n.value, ms.value
 
 
 def _out(C_, M, N, dtype, device):

@@ -9,6 +9,7 @@ LIB_PATH = os.path.join(_PKG, "libspmm_gb300.so")
 
 SPMM_BF16, SPMM_F16, SPMM_I8 = 0, 1, 2
 DEVERR_TIMEOUT, DEVERR_INDEX, DEVERR_FORMAT = 1, 2, 4
+KERNEL_BCSR, KERNEL_SPARSE, KERNEL_WIDEN, KERNEL_WCSR = 1, 2, 3, 4
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_NULL", 2: "SPMM_ERR_SHAPE", 3: "SPMM_ERR_DTYPE", 4: "SPMM_ERR_FORMAT",
           5: "SPMM_ERR_WORKSPACE", 6: "SPMM_ERR_TIMEOUT", 7: "SPMM_ERR_CUDA", 8: "SPMM_ERR_UNSUPPORTED"}
 
@@ -53,6 +54,8 @@ SIGNATURES = {
     "spmm_version": (C.c_int, []),
     "spmm_last_device_error": (I32, [C.POINTER(I32)]),
     "spmm_selftest_timeout": (I32, [C.c_uint64, P]),
+    "spmm_trace_enable": (I32, [I32]),
+    "spmm_trace_read": (I32, [I32, C.POINTER(I64), C.POINTER(C.c_double)]),
     "spmm_bcsr": (I32, [C.POINTER(BcsrT), P, I64, P, I64, I64, P]),
     "spmm_wcsr_workspace_size": (I32, [C.POINTER(WcsrT), I64, C.POINTER(SZ)]),
     "spmm_wcsr": (I32, [C.POINTER(WcsrT), P, I64, P, I64, I64, P, SZ, P]),

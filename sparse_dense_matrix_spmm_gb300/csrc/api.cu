@@ -53,7 +53,50 @@ __global__ void timeout_selftest_kernel(int* err, uint64_t timeout_ns) {
     __syncthreads();
 }
 
+// ---------------------------------------------------------------- tracing
+struct TraceRec {
+    int kernel;
+    cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;        // records of the current session
+std::vector<cudaEvent_t> g_ev_pool;   // events reused across sessions
+size_t g_ev_used = 0;
+int g_open_kernel = 0;
+cudaEvent_t g_open_ev = nullptr;
+
+cudaEvent_t take_event() {
+    if (g_ev_used == g_ev_pool.size()) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        g_ev_pool.push_back(e);
+    }
+    return g_ev_pool[g_ev_used++];
+}
+
 }  // namespace
+
+void trace_begin(int kernel, cudaStream_t s) {
+    if (!g_trace_on) return;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    cudaEvent_t e = take_event();
+    if (!e) return;
+    cudaEventRecord(e, s);
+    g_open_kernel = kernel;
+    g_open_ev = e;
+}
+
+void trace_end(int kernel, cudaStream_t s) {
+    if (!g_trace_on) return;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (!g_open_ev || g_open_kernel != kernel) return;
+    cudaEvent_t e = take_event();
+    if (!e) return;
+    cudaEventRecord(e, s);
+    g_trace.push_back({kernel, g_open_ev, e});
+    g_open_ev = nullptr;
+}
 
 const DeviceInfo* device_info() {
     int d = 0;
@@ -144,6 +187,33 @@ spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t stream) {
     timeout_selftest_kernel<<<1, 32, 0, s>>>(dev->err, timeout_ns);
     if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));
+}
+
+spmm_status spmm_trace_enable(int32_t on) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    g_trace.clear();
+    g_ev_used = 0;
+    g_open_ev = nullptr;
+    g_trace_on = on != 0;
+    return SPMM_OK;
+}
+
+spmm_status spmm_trace_read(int32_t kernel, int64_t* launches, double* total_ms) {
+    if (!launches || !total_ms) return SPMM_ERR_NULL;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    int64_t n = 0;
+    double ms = 0.0;
+    for (const TraceRec& r : g_trace) {
+        if (r.kernel != kernel) continue;
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return SPMM_ERR_CUDA;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return SPMM_ERR_CUDA;
+        ms += t;
+        ++n;
+    }
+    *launches = n;
+    *total_ms = ms;
+    return SPMM_OK;
 }
 
 spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,

@@ -281,8 +281,11 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
     if (!set_smem_attr_once(reinterpret_cast<const void*>(bcsr_spmm_kernel), max_smem, 0)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_brows) * a.n_ntiles;
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
+    trace_begin(SPMM_KERNEL_BCSR, stream);
     bcsr_spmm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmW, a);
-    return cuda_status(cudaGetLastError());
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_BCSR, stream);
+    return cuda_status(e);
 }
 
 }  // namespace spmm

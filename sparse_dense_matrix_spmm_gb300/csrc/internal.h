@@ -36,6 +36,10 @@ inline CUtensorMapDataType half_type(int32_t dtype) {
     return dtype == SPMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
+// Tracing hooks: no-ops unless spmm_trace_enable(1) is in effect.
+void trace_begin(int kernel, cudaStream_t s);
+void trace_end(int kernel, cudaStream_t s);
+
 // Raise a kernel's dynamic shared memory limit once per device.
 bool set_smem_attr_once(const void* kernel, int bytes, int slot);
 

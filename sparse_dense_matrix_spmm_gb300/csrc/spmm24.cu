@@ -407,8 +407,11 @@ spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const 
     if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), SMEM_BYTES, slot)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
+    trace_begin(SPMM_KERNEL_SPARSE, stream);
     kern<<<grid, kThreads, SMEM_BYTES, stream>>>(tmA, tmM, tmB, a);
-    return cuda_status(cudaGetLastError());
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_SPARSE, stream);
+    return cuda_status(e);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -437,11 +440,14 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
                                                align256(static_cast<size_t>(A->M) * (A->K / 2) * 2));
         const int64_t np = (N + 7) / 8 * 8;
         const int64_t na = A->M * ((A->K / 2 + 7) / 8), nb = A->K * (np / 8);
+        trace_begin(SPMM_KERNEL_WIDEN, stream);
         widen_i8_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, stream>>>(
             static_cast<const int8_t*>(A->vals), A->K / 2, wa, A->K / 2, A->M, A->K / 2);
         widen_i8_kernel<<<static_cast<unsigned>((nb + 255) / 256), 256, 0, stream>>>(
             static_cast<const int8_t*>(B), ldb, wb, np, A->K, N);
-        if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
+        const cudaError_t e = cudaGetLastError();
+        trace_end(SPMM_KERNEL_WIDEN, stream);
+        if (e != cudaSuccess) return SPMM_ERR_CUDA;
         vals = wa;
         bsrc = wb;
         bld = np;
