@@ -212,6 +212,26 @@ SPMM_API spmm_status spmm_24_workspace_size(const spmm_24_t *A, int64_t N, size_
 SPMM_API spmm_status spmm_24(const spmm_24_t *A, const void *B, int64_t ldb, void *C, int64_t ldc, int64_t N,
                              void *workspace, size_t workspace_bytes, spmm_stream_t stream);
 
+/* spmm_24 without a workspace argument, for callers that cannot allocate
+ * device memory: for example code running inside another runtime that is
+ * handed only its input and output buffers, a service that reserves all
+ * device memory at start-up and forbids allocation afterwards, or a
+ * latency-critical path that cannot afford cudaMalloc's implicit
+ * synchronisation.  (The papers have no counterpart; this is a library
+ * convenience.)  The scratch that int8 operands need (the same amount
+ * spmm_24_workspace_size reports) comes from a fixed 32 MiB array inside the
+ * library's device image, which every GPU that loads the library holds until
+ * the process exits.  A call whose scratch would exceed 32 MiB returns
+ * SPMM_ERR_WORKSPACE without launching; fp16/bf16 operands need no scratch.
+ * The call allocates nothing.  Its first call on a device looks up the array's
+ * device address for that device; make that first call before any stream
+ * capture.  All calls share the one array, and each call rewrites every byte
+ * it later reads, so nothing has to be cleared between calls; calls that can
+ * overlap on the GPU (different streams, or different host threads) race on
+ * the array and must be serialised by the caller. */
+SPMM_API spmm_status spmm_24_noalloc(const spmm_24_t *A, const void *B, int64_t ldb, void *C, int64_t ldc,
+                                     int64_t N, spmm_stream_t stream);
+
 /* C = A * B with A tile-vector-wise ("Accelerating Sparse DNNs Based on Tiled
  * GEMM": tile-wise column selection at global-memory level, 2:4 in the sparse
  * tensor core).  Each tile gathers its kept rows of B.  fp32 C. */

@@ -61,6 +61,7 @@ SIGNATURES = {
     "spmm_wcsr": (I32, [C.POINTER(WcsrT), P, I64, P, I64, I64, P, SZ, P]),
     "spmm_24_workspace_size": (I32, [C.POINTER(T24), I64, C.POINTER(SZ)]),
     "spmm_24": (I32, [C.POINTER(T24), P, I64, P, I64, I64, P, SZ, P]),
+    "spmm_24_noalloc": (I32, [C.POINTER(T24), P, I64, P, I64, I64, P]),
     "spmm_tvw": (I32, [C.POINTER(TvwT), P, I64, P, I64, I64, P]),
     "spmm_build_bcsr_count": (I32, [P, I64, I64, I64, I32, I32, I32, P, C.POINTER(I64), P]),
     "spmm_build_bcsr_fill": (I32, [P, I64, I64, I64, I32, I32, I32, P, P, P, P]),
