@@ -285,13 +285,86 @@ spmm_status spmm_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, 
     return run_build_tvw(dense, M, K, ld, dtype, tile_rows, tile_ptr, cols, n_tiles, Kp, vals, meta, s);
 }
 
-// ---------------------------------------------------------------- not yet built
-
-spmm_status spmm_wcsr_workspace_size(const spmm_wcsr_t*, int64_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
-spmm_status spmm_wcsr(const spmm_wcsr_t*, const void*, int64_t, float*, int64_t, int64_t, void*, size_t,
-                      spmm_stream_t) {
-    return SPMM_ERR_UNSUPPORTED;
+static spmm_status check_csr(const spmm_csr_t* A, int32_t h, int32_t S) {
+    if (!A) return SPMM_ERR_NULL;
+    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || A->nnz < 0 || h <= 0 || h > 256 || S <= 0) return SPMM_ERR_SHAPE;
+    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || A->nnz >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    if (!A->row_ptr || (A->nnz > 0 && (!A->col || !A->val))) return SPMM_ERR_NULL;
+    return SPMM_OK;
 }
+
+spmm_status spmm_build_wcsr_workspace_size(const spmm_csr_t* A, int32_t h, size_t* bytes) {
+    if (!bytes) return SPMM_ERR_NULL;
+    spmm_status st = check_csr(A, h, 1);
+    if (st != SPMM_OK) return st;
+    *bytes = wcsr_build_ws_bytes(A->M, A->nnz, h);
+    return SPMM_OK;
+}
+
+spmm_status spmm_build_wcsr_count(const spmm_csr_t* A, int32_t h, int32_t S, void* workspace, size_t workspace_bytes,
+                                  int64_t* n_wcols, int64_t* n_units, spmm_stream_t stream) {
+    if (!n_wcols || !n_units) return SPMM_ERR_NULL;
+    spmm_status st = check_csr(A, h, S);
+    if (st != SPMM_OK) return st;
+    if (!workspace || workspace_bytes < wcsr_build_ws_bytes(A->M, A->nnz, h) || !aligned16(workspace))
+        return SPMM_ERR_WORKSPACE;
+    return run_wcsr_count(A, h, S, workspace, n_wcols, n_units, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_build_wcsr_fill(const spmm_csr_t* A, int32_t h, int32_t S, void* workspace, size_t workspace_bytes,
+                                 spmm_wcsr_t* out, spmm_stream_t stream) {
+    if (!out) return SPMM_ERR_NULL;
+    spmm_status st = check_csr(A, h, S);
+    if (st != SPMM_OK) return st;
+    if (!workspace || workspace_bytes < wcsr_build_ws_bytes(A->M, A->nnz, h) || !aligned16(workspace))
+        return SPMM_ERR_WORKSPACE;
+    const int64_t nw = (A->M + h - 1) / h;
+    if (!out->wcol_ptr || !out->wnz_ptr || !out->unit_ptr || !out->unit_nz_ptr) return SPMM_ERR_NULL;
+    if (A->nnz > 0 && (!out->wcols || !out->lrow || !out->slot || !out->val || !out->unit_win))
+        return SPMM_ERR_NULL;
+    out->M = A->M;
+    out->K = A->K;
+    out->nnz = A->nnz;
+    out->h = h;
+    out->S = S;
+    out->dtype = A->dtype;
+    out->n_windows = nw;
+    return run_wcsr_fill(A, h, S, workspace, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static spmm_status check_wcsr(const spmm_wcsr_t* A) {
+    if (!A) return SPMM_ERR_NULL;
+    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || A->nnz < 0 || A->h <= 0 || A->S <= 0) return SPMM_ERR_SHAPE;
+    if (A->n_windows != (A->M + A->h - 1) / A->h || A->n_units < A->n_windows) return SPMM_ERR_SHAPE;
+    if (A->h > wcsr_max_h()) return SPMM_ERR_UNSUPPORTED;
+    return SPMM_OK;
+}
+
+spmm_status spmm_wcsr_workspace_size(const spmm_wcsr_t* A, int64_t N, size_t* bytes) {
+    if (!bytes) return SPMM_ERR_NULL;
+    spmm_status st = check_wcsr(A);
+    if (st != SPMM_OK) return st;
+    if (N < 0) return SPMM_ERR_SHAPE;
+    *bytes = wcsr_spmm_ws_bytes(A, N);
+    return SPMM_OK;
+}
+
+spmm_status spmm_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                      void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
+    spmm_status st = check_wcsr(A);
+    if (st != SPMM_OK) return st;
+    if (!B || !C) return SPMM_ERR_NULL;
+    if (N < 0 || ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B)) return SPMM_ERR_SHAPE;
+    if (A->M > 0 && (!A->wcol_ptr || !A->unit_ptr || !A->unit_win || !A->unit_nz_ptr)) return SPMM_ERR_NULL;
+    if (A->nnz > 0 && (!A->wcols || !A->lrow || !A->slot || !A->val)) return SPMM_ERR_NULL;
+    if (!workspace || workspace_bytes < wcsr_spmm_ws_bytes(A, N) || !aligned16(workspace))
+        return SPMM_ERR_WORKSPACE;
+    return launch_wcsr(A, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 static spmm_status check_24(const spmm_24_t* A, int64_t N) {
     if (!A) return SPMM_ERR_NULL;
     if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
@@ -336,14 +409,4 @@ spmm_status spmm_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, 
         return SPMM_ERR_UNSUPPORTED;
     return launch_tvw(A, B, ldb, C, ldc, N, reinterpret_cast<cudaStream_t>(stream));
 }
-spmm_status spmm_build_wcsr_workspace_size(const spmm_csr_t*, int32_t, size_t*) { return SPMM_ERR_UNSUPPORTED; }
-spmm_status spmm_build_wcsr_count(const spmm_csr_t*, int32_t, int32_t, void*, size_t, int64_t*, int64_t*,
-                                  spmm_stream_t) {
-    return SPMM_ERR_UNSUPPORTED;
-}
-spmm_status spmm_build_wcsr_fill(const spmm_csr_t*, int32_t, int32_t, void*, size_t, spmm_wcsr_t*,
-                                 spmm_stream_t) {
-    return SPMM_ERR_UNSUPPORTED;
-}
-
 }  // extern "C"

@@ -54,6 +54,15 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
 spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
                        cudaStream_t stream);
 
+size_t wcsr_build_ws_bytes(int64_t M, int64_t nnz, int32_t h);
+spmm_status run_wcsr_count(const spmm_csr_t* A, int32_t h, int32_t S, void* ws, int64_t* n_wcols, int64_t* n_units,
+                           cudaStream_t s);
+spmm_status run_wcsr_fill(const spmm_csr_t* A, int32_t h, int32_t S, void* ws, spmm_wcsr_t* out, cudaStream_t s);
+size_t wcsr_spmm_ws_bytes(const spmm_wcsr_t* A, int64_t N);
+spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                        void* ws, cudaStream_t s);
+int wcsr_max_h();
+
 spmm_status run_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
                            int32_t* row_ptr, int64_t* nnzb, cudaStream_t s);
 spmm_status run_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
