@@ -291,6 +291,10 @@ __global__ void __launch_bounds__(kThreads) wcsr_spmm_kernel(const WcsrArgs a) {
     const int u = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = a.unit_win[u];
+    if (w < 0 || static_cast<int64_t>(w) * a.h >= a.M) {  // malformed unit list: skip the unit
+        if (threadIdx.x == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);
+        return;
+    }
     const int64_t r0 = static_cast<int64_t>(w) * a.h;
     const int64_t rem = a.M - r0;
     const int nrows = rem < a.h ? static_cast<int>(rem) : a.h;
