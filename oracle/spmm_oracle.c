@@ -262,10 +262,13 @@ int orc_wcsr_fill(int64_t M, int64_t K, int dtype, const int32_t *row_ptr, const
     if (orc_csr_check(M, K, row_ptr, col) != ORC_OK) return ORC_ERR_FORMAT;
     int64_t nw = (M + h - 1) / h, span = 16 * (int64_t)S;
     int64_t cw = 0, cu = 0, cz = 0;
+    int32_t *tmp = (int32_t *)malloc(sizeof(int32_t) * (size_t)(row_ptr[M] + 1));
     for (int64_t w = 0; w < nw; w++) {
         int64_t rb = w * h, re = rb + h < M ? rb + h : M;
         int32_t *wc = wcols + cw;
-        int64_t T = window_unique(row_ptr, col, rb, re, wc);
+        /* collect and de-duplicate in scratch, then copy the T distinct columns */
+        int64_t T = window_unique(row_ptr, col, rb, re, tmp);
+        for (int64_t t = 0; t < T; t++) wc[t] = tmp[t];
         int64_t U = T ? (T + span - 1) / span : 1;
         wcol_ptr[w] = (int32_t)cw;
         wnz_ptr[w] = (int32_t)cz;
@@ -286,6 +289,7 @@ int orc_wcsr_fill(int64_t M, int64_t K, int dtype, const int32_t *row_ptr, const
         cw += T;
         cu += U;
     }
+    free(tmp);
     wcol_ptr[nw] = (int32_t)cw;
     wnz_ptr[nw] = (int32_t)cz;
     unit_ptr[nw] = (int32_t)cu;

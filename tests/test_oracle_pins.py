@@ -278,3 +278,16 @@ def test_tvw_errors():
         oracle.tvw_build(A, 2, g["tile_ptr"], g["cols"], "f16")
     with pytest.raises(oracle.OracleError):  # kept columns not ascending
         oracle.tvw_build(to_bits(g["A"], "f16"), 2, g["tile_ptr"], [2, 1, 5, 7], "f16")
+
+
+def test_wcsr_windows_with_repeated_columns():
+    # many rows share columns (K small): windows hold far fewer distinct columns
+    # than nonzeros; the builder must still produce the exact layout
+    p = gen.csr_lognormal_problem(200, 40, 8, seed=5, mean=10.0, sigma=1.0, clip=40)
+    for h, S in ((32, 1), (16, 4), (7, 2)):
+        F = oracle.wcsr_build(p["M"], p["K"], p["row_ptr"], p["col"], p["val"], "f16", h=h, S=S)
+        rp, col, val = oracle.wcsr_to_csr(F)
+        assert np.array_equal(rp, p["row_ptr"]) and np.array_equal(col, p["col"])
+        assert F["n_wcols"] < p["row_ptr"][-1]
+        np.testing.assert_allclose(oracle.wcsr_spmm(F, p["B"]), _csr_dense(p) @ bits_to_f64(p["B"], "f16"),
+                                   rtol=1e-12, atol=1e-12)
