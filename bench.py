@@ -277,7 +277,9 @@ def run_extra(name, args, ws, peaks, flush_buf):
     import torch
     import spmm_inputs as gen
     import sparse_dense_matrix_spmm_gb300 as spmm
-    c = gen.CONFIGS[name]
+    c = dict(gen.CONFIGS[name])
+    if args.n:
+        c["N"] = args.n
     steps = max(3, min(args.steps, 10))
     g = torch.Generator(device="cuda")
     g.manual_seed(int(c["seed"]))
@@ -300,7 +302,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
         def step():
             spmm.spmm_bcsr(F, Bx, Cd)
     elif c["kind"] == "tvw":
-        p = gen.config_problem(name)
+        p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
         A = to_dev(p["A"], torch.float16)
         Bx = to_dev(p["B"], torch.float16)
         tp = to_dev(p["tile_ptr"])
@@ -320,7 +322,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
         def step():
             spmm.spmm_tvw(F, Bx, Cd)
     elif c["kind"] == "wcsr":
-        p = gen.config_problem(name)
+        p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
         dt = torch.float16
         csr = spmm.CSR(c["M"], c["K"], int(p["row_ptr"][-1]), dt, to_dev(p["row_ptr"]), to_dev(p["col"]),
                        to_dev(p["val"], dt))
@@ -436,6 +438,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other formats")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, bcsr_tiny) and print its result; "
+                         "for profiling runs, not the benchmark line")
+    ap.add_argument("--n", type=int, default=0, help="with --only: override the workload's N")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -457,6 +463,11 @@ def main():
     peaks, peak_src = load_peaks()
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
+    if args.only:
+        r = run_extra(args.only, args, ws, peaks, flush_buf)
+        if rank == 0:
+            print(json.dumps({"only": args.only, **r}), flush=True)
+        return 0
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:

@@ -140,45 +140,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         int64_t issued = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        // Steps are visited as a flat sequence of (tile, k-step).  For TVW the
+        // kept-row indices of the next step are loaded right after the current
+        // step is issued, so their latency overlaps the wait for a free stage.
+        int64_t u = blockIdx.x;
+        int ks = 0, kb = 0, kt = 0, nk = 0;
+        int32_t rnext[4] = {0, 0, 0, 0};
+        auto load_rows = [&](int kb_, int kt_, int ks_) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = ks_ * KS + 4 * lane + i;
+                rnext[i] = __ldg(a.cols + kb_ + (k < kt_ ? k : 0));
+            }
+        };
+        // first tile with at least one step
+        while (u < total) {
+            nk = tile_steps(a, static_cast<int>(u % a.n_mtiles), kb, kt, GATHER);
+            if (nk > 0) break;
+            u += gridDim.x;
+        }
+        if (GATHER && u < total) load_rows(kb, kt, 0);
+        while (u < total && ok) {
             const int mt = static_cast<int>(u % a.n_mtiles), nt = static_cast<int>(u / a.n_mtiles);
             const int m0 = mt * BM, n0 = nt * BN;
-            int kb, kt;
-            const int nk = tile_steps(a, mt, kb, kt, GATHER);
-            for (int ks = 0; ks < nk; ++ks) {
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
-                    ok = false;
-                    break;
+            int32_t r[4] = {rnext[0], rnext[1], rnext[2], rnext[3]};
+            const int cur_ks = ks;
+            // advance to the next step and prefetch its rows
+            if (++ks >= nk) {
+                ks = 0;
+                u += gridDim.x;
+                while (u < total) {
+                    nk = tile_steps(a, static_cast<int>(u % a.n_mtiles), kb, kt, GATHER);
+                    if (nk > 0) break;
+                    u += gridDim.x;
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
-                    tma_load_2d(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0);
-                    tma_load_2d(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0);
-                    if (!GATHER) {
-                        tma_load_2d(b_s(s), &tmB, full_bar(s), n0, ks * KS);
-                        tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, ks * KS);
-                    }
+            }
+            if (GATHER && u < total) load_rows(kb, kt, ks);
+            if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
+                tma_load_2d(a_s(s), &tmA, full_bar(s), cur_ks * (KS / 2), m0);
+                tma_load_2d(mc_s(s), &tmMeta, full_bar(s), cur_ks * (KS / 8), m0);
+                if (!GATHER) {
+                    tma_load_2d(b_s(s), &tmB, full_bar(s), n0, cur_ks * KS);
+                    tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, cur_ks * KS);
                 }
-                if (GATHER) {
-                    __syncwarp();
-                    // lane l brings kept rows 4l..4l+3 of this step (both 64-column chunks);
-                    // rows past the tile's kept count re-read its first kept row and are
-                    // zeroed in shared memory by the metadata warp.
-                    int32_t r[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int k = ks * KS + 4 * lane + i;
-                        r[i] = __ldg(a.cols + kb + (k < kt ? k : 0));
-                    }
-                    tma_gather4(b_s(s) + lane * 512u, &tmB, full_bar(s), n0, r[0], r[1], r[2], r[3]);
-                    tma_gather4(b_s(s) + B_CHUNK + lane * 512u, &tmB, full_bar(s), n0 + 64, r[0], r[1], r[2],
-                                r[3]);
-                }
-                ++issued;
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+            }
+            if (GATHER) {
+                __syncwarp();
+                // lane l brings kept rows 4l..4l+3 of the step (both 64-column chunks);
+                // rows past the tile's kept count re-read its first kept row and are
+                // zeroed in shared memory by the metadata warps.
+                tma_gather4(b_s(s) + lane * 512u, &tmB, full_bar(s), n0, r[0], r[1], r[2], r[3]);
+                tma_gather4(b_s(s) + B_CHUNK + lane * 512u, &tmB, full_bar(s), n0 + 64, r[0], r[1], r[2], r[3]);
+            }
+            ++issued;
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
             }
         }
         // Leave no copy in flight: wait for the last phase armed on each slot.

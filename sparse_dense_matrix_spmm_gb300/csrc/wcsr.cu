@@ -19,10 +19,11 @@
 // SpMM.  On the synthetic power-law workload the windows are about 6% dense
 // (uniform columns), so the contraction per window is not a dense tile: the
 // kernel runs on CUDA cores and is bound by gathering B rows (N * 2 bytes per
-// nonzero) from L2.  One CTA (8 warps) per work unit; the unit's nonzeros
-// (row-major inside the unit) are cut into 8 equal chunks, one per warp.  Each
-// warp keeps 8 B-row loads in flight, accumulates fp32 per row in registers
-// (lane = 4 columns of a 128-column slab), writes rows that lie inside its
+// nonzero) from L2.  One CTA (8 warps) per work unit.  The CTA first stages the
+// unit's sparse operand in shared memory (local row, column resolved through
+// the window's column list, value), then cuts it into 8 equal chunks, one per
+// warp.  Each warp keeps 16 B-row loads in flight, accumulates fp32 per row in
+// registers (lane = 4 columns of a 128-column slab), writes rows that lie inside its
 // chunk straight into a shared-memory tile, and hands the two rows at its
 // chunk's ends to a fix-up that adds them in warp order, so every sum has a
 // fixed order.  Unsplit windows write C from the tile; a split window's units
@@ -264,28 +265,40 @@ __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v)
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// Four consecutive B elements (8 bytes, raw) of one row; lanes past N get zeros.
 template <typename T>
-__device__ __forceinline__ float4 load4(const T* p, int valid) {
-    // four consecutive B elements (8 bytes) as fp32; `valid` lanes of the slab
-    if (valid >= 4) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p));
-        const T* e = reinterpret_cast<const T*>(&raw);
-        return make_float4(to_f<T>(e[0]), to_f<T>(e[1]), to_f<T>(e[2]), to_f<T>(e[3]));
-    }
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid > 0) r.x = to_f<T>(p[0]);
-    if (valid > 1) r.y = to_f<T>(p[1]);
-    if (valid > 2) r.z = to_f<T>(p[2]);
-    return r;
+__device__ __forceinline__ uint2 load_raw4(const T* p, int valid) {
+    if (valid >= 4) return __ldg(reinterpret_cast<const uint2*>(p));
+    uint16_t e[4] = {0, 0, 0, 0};
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+    for (int i = 0; i < valid; ++i) e[i] = q[i];
+    return make_uint2(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16));
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) wcsr_spmm_kernel(const WcsrArgs a) {
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+constexpr int kStage = 1024;  // nonzeros whose metadata is staged in shared memory at once
+constexpr int kBatch = 16;    // B-row loads in flight per warp
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 4) wcsr_spmm_kernel(const WcsrArgs a) {
     extern __shared__ float sm[];
-    // tile[h][kSlab] | bnd[kWarps][2][kSlab] | bnd_row[kWarps][2]
+    // tile[h][kSlab] | bnd[2*kWarps][kSlab] | bnd_row[2*kWarps] | s_col[kStage] | s_val[kStage] | s_row[kStage]
     float* tile = sm;
     float* bnd = tile + a.h * kSlab;
-    int* bnd_row = reinterpret_cast<int*>(bnd + kWarps * 2 * kSlab);
+    int* bnd_row = reinterpret_cast<int*>(bnd + 2 * kWarps * kSlab);
+    int* s_col = bnd_row + 2 * kWarps;
+    float* s_val = reinterpret_cast<float*>(s_col + kStage);
+    signed char* s_row = reinterpret_cast<signed char*>(s_val + kStage);
     __shared__ int s_last;
 
     const int u = blockIdx.x;
@@ -302,8 +315,6 @@ __global__ void __launch_bounds__(kThreads) wcsr_spmm_kernel(const WcsrArgs a) {
     const bool split = units_in_window > 1;
     const int32_t wbase = a.wcol_ptr[w], T_w = a.wcol_ptr[w + 1] - wbase;
     const int32_t nz0 = a.unit_nz_ptr[u], nz1 = a.unit_nz_ptr[u + 1];
-    const int32_t per = (nz1 - nz0 + kWarps - 1) / kWarps;
-    const int32_t c0 = nz0 + warp * per, c1 = (nz1 < c0 + per) ? nz1 : c0 + per;
     const T* val = static_cast<const T*>(a.val);
     const T* B = static_cast<const T*>(a.B);
 
@@ -312,78 +323,80 @@ __global__ void __launch_bounds__(kThreads) wcsr_spmm_kernel(const WcsrArgs a) {
         const int64_t left = a.N - ncol;
         const int valid = left >= 4 ? 4 : (left > 0 ? static_cast<int>(left) : 0);
         for (int i = threadIdx.x; i < a.h * kSlab; i += kThreads) tile[i] = 0.f;
-        if (lane < 2) bnd_row[warp * 2 + lane] = -1;
-        __syncthreads();
 
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int cur = -1;            // current local row
-        bool first_seg = true;   // the current row segment starts this chunk
-        for (int32_t e0 = c0; e0 < c1; e0 += 8) {
-            // lanes 0..7 fetch the metadata of 8 nonzeros, then every lane fetches
-            // its 4 columns of the 8 B rows before any arithmetic
-            int my_r = -1, my_c = 0;
-            float my_v = 0.f;
-            if (lane < 8 && e0 + lane < c1) {
-                const int32_t e = e0 + lane;
+        for (int32_t st0 = nz0; st0 < nz1; st0 += kStage) {
+            const int n_st = (nz1 - st0 < kStage) ? nz1 - st0 : kStage;
+            // stage the sparse operand: local row, resolved column, value
+            for (int i = threadIdx.x; i < n_st; i += kThreads) {
+                const int32_t e = st0 + i;
                 const int lr = a.lrow[e];
-                const int32_t s = a.slot[e];
-                const int32_t c = (s >= 0 && s < T_w) ? a.wcols[wbase + s] : -1;
-                if (lr < nrows && c >= 0 && c < a.K) {
-                    my_r = lr;
-                    my_c = c;
-                    my_v = to_f<T>(val[e]);
-                } else {
-                    atomicOr(a.err, SPMM_DEVERR_INDEX);
+                const int32_t sl = a.slot[e];
+                const int32_t c = (sl >= 0 && sl < T_w) ? a.wcols[wbase + sl] : -1;
+                const bool ok = lr < nrows && c >= 0 && c < a.K;
+                if (!ok) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                s_row[i] = ok ? static_cast<signed char>(lr) : static_cast<signed char>(-1);
+                s_col[i] = ok ? c : 0;
+                s_val[i] = ok ? to_f<T>(val[e]) : 0.f;
+            }
+            if (threadIdx.x < 2 * kWarps) bnd_row[threadIdx.x] = -1;
+            __syncthreads();
+
+            const int per = (n_st + kWarps - 1) / kWarps;
+            const int j_lo = warp * per, j_hi = (n_st < j_lo + per) ? n_st : j_lo + per;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            int cur = -1;
+            bool first_seg = true;
+            for (int j0 = j_lo; j0 < j_hi; j0 += kBatch) {
+                uint2 raw[kBatch];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int j = j0 + b;
+                    const bool live = j < j_hi && s_row[j] >= 0;
+                    raw[b] = live ? load_raw4<T>(B + static_cast<int64_t>(s_col[j]) * a.ldb + ncol, valid)
+                                  : make_uint2(0u, 0u);
                 }
-            }
-            int rr[8];
-            float vv[8];
-            float4 bb[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                rr[j] = __shfl_sync(0xffffffffu, my_r, j);
-                const int cj = __shfl_sync(0xffffffffu, my_c, j);
-                vv[j] = __shfl_sync(0xffffffffu, my_v, j);
-                bb[j] = (rr[j] >= 0) ? load4<T>(B + static_cast<int64_t>(cj) * a.ldb + ncol, valid)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (rr[j] < 0) continue;
-                if (rr[j] != cur) {
-                    if (cur >= 0) {
-                        // a finished segment: the chunk's first row goes to the fix-up,
-                        // any later one lies wholly inside this chunk
-                        float* dst = first_seg ? bnd + (warp * 2) * kSlab : tile + cur * kSlab;
-                        *reinterpret_cast<float4*>(dst + 4 * lane) = acc;
-                        if (first_seg && lane == 0) bnd_row[warp * 2] = cur;
-                        first_seg = false;
+                for (int b = 0; b < kBatch; ++b) {
+                    const int j = j0 + b;
+                    if (j >= j_hi) break;
+                    const int rr = s_row[j];
+                    if (rr < 0) continue;
+                    if (rr != cur) {
+                        if (cur >= 0) {
+                            // a finished segment: the chunk's first row goes to the fix-up,
+                            // any later one lies wholly inside this chunk
+                            float* dst = first_seg ? bnd + (warp * 2) * kSlab : tile + cur * kSlab;
+                            *reinterpret_cast<float4*>(dst + 4 * lane) = acc;
+                            if (first_seg && lane == 0) bnd_row[warp * 2] = cur;
+                            first_seg = false;
+                        }
+                        cur = rr;
+                        acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    cur = rr[j];
-                    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float v = s_val[j];
+                    const float2 lo = unpack2<T>(raw[b].x), hi = unpack2<T>(raw[b].y);
+                    acc.x += v * lo.x;
+                    acc.y += v * lo.y;
+                    acc.z += v * hi.x;
+                    acc.w += v * hi.y;
                 }
-                acc.x += vv[j] * bb[j].x;
-                acc.y += vv[j] * bb[j].y;
-                acc.z += vv[j] * bb[j].z;
-                acc.w += vv[j] * bb[j].w;
             }
-        }
-        if (cur >= 0) {
-            // the chunk's last segment may continue in the next chunk: fix-up slot 1
-            // (slot 0 if it is also the chunk's first segment)
-            const int k = first_seg ? 0 : 1;
-            *reinterpret_cast<float4*>(bnd + (warp * 2 + k) * kSlab + 4 * lane) = acc;
-            if (lane == 0) bnd_row[warp * 2 + k] = cur;
-        }
-        __syncthreads();
-        // fix-up in warp order: thread t owns column t of the slab
-        if (threadIdx.x < kSlab) {
-            for (int k = 0; k < 2 * kWarps; ++k) {
-                const int r = bnd_row[k];
-                if (r >= 0) tile[r * kSlab + threadIdx.x] += bnd[k * kSlab + threadIdx.x];
+            if (cur >= 0) {
+                // the chunk's last segment may continue in the next chunk
+                const int k = first_seg ? 0 : 1;
+                *reinterpret_cast<float4*>(bnd + (warp * 2 + k) * kSlab + 4 * lane) = acc;
+                if (lane == 0) bnd_row[warp * 2 + k] = cur;
             }
+            __syncthreads();
+            // chunk-boundary rows, added in warp order: thread t owns column t of the slab
+            if (threadIdx.x < kSlab) {
+                for (int k = 0; k < 2 * kWarps; ++k) {
+                    const int r = bnd_row[k];
+                    if (r >= 0) tile[r * kSlab + threadIdx.x] += bnd[k * kSlab + threadIdx.x];
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
 
         if (!split) {
             for (int i = threadIdx.x; i < nrows * (kSlab / 4); i += kThreads) {
@@ -546,7 +559,13 @@ spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float*
     a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                          align256(sizeof(int32_t) * static_cast<size_t>(A->n_windows)));
     a.err = dev->err;
-    const int smem = static_cast<int>(sizeof(float) * (A->h * kSlab + kWarps * 2 * kSlab) + sizeof(int) * kWarps * 2);
+    const int smem = static_cast<int>(sizeof(float) * (A->h * kSlab + kWarps * 2 * kSlab) + sizeof(int) * kWarps * 2 +
+                                      kStage * (sizeof(int) + sizeof(float) + 1));
+    const int smem_max = static_cast<int>(sizeof(float) * (kMaxH * kSlab + kWarps * 2 * kSlab) +
+                                          sizeof(int) * kWarps * 2 + kStage * (sizeof(int) + sizeof(float) + 1));
+    const void* kern = A->dtype == SPMM_BF16 ? reinterpret_cast<const void*>(wcsr_spmm_kernel<__nv_bfloat16>)
+                                             : reinterpret_cast<const void*>(wcsr_spmm_kernel<__half>);
+    if (!set_smem_attr_once(kern, smem_max, A->dtype == SPMM_BF16 ? 4 : 5)) return SPMM_ERR_CUDA;
     trace_begin(SPMM_KERNEL_WCSR, s);
     if (A->dtype == SPMM_BF16)
         wcsr_spmm_kernel<__nv_bfloat16><<<static_cast<unsigned>(A->n_units), kThreads, smem, s>>>(a);
