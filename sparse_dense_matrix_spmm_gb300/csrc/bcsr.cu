@@ -96,29 +96,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t total = static_cast<int64_t>(a.n_brows) * a.n_ntiles;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------------- TMA producer
-            int s = 0;
-            uint32_t ph = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            const uint32_t tx = a.x_bytes + static_cast<uint32_t>(a.bh * a.bw * 2);
-            for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const int ntile = static_cast<int>(u / a.n_brows);
-                const int br = static_cast<int>(u % a.n_brows);
-                const int n0 = ntile * kTokens;
-                const int j0 = __ldg(a.row_ptr + br), j1 = __ldg(a.row_ptr + br + 1);
-                for (int j = j0; j < j1; ++j) {
+        // -------------------------------------------------------- TMA producer
+        // The warp reads a unit's block columns in one coalesced load and
+        // prefetches the next unit's row_ptr pair, so index latency stays off the
+        // issue path; lane 0 issues the copies.
+        int s = 0;
+        uint32_t ph = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        const uint32_t tx = a.x_bytes + static_cast<uint32_t>(a.bh * a.bw * 2);
+        int64_t u = blockIdx.x;
+        int j0 = 0, j1 = 0;
+        if (u < total) {
+            const int br = static_cast<int>(u % a.n_brows);
+            j0 = __ldg(a.row_ptr + br);
+            j1 = __ldg(a.row_ptr + br + 1);
+        }
+        for (; u < total && ok; u += gridDim.x) {
+            const int ntile = static_cast<int>(u / a.n_brows);
+            const int n0 = ntile * kTokens;
+            const int cj0 = j0, cj1 = j1;
+            const int64_t un = u + gridDim.x;
+            if (un < total) {  // next unit's block range, in flight while this unit issues
+                const int brn = static_cast<int>(un % a.n_brows);
+                j0 = __ldg(a.row_ptr + brn);
+                j1 = __ldg(a.row_ptr + brn + 1);
+            }
+            for (int jb = cj0; jb < cj1 && ok; jb += 32) {
+                const int cidx = (jb + lane < cj1) ? __ldg(a.col_idx + jb + lane) : 0;
+                const int nb = (cj1 - jb < 32) ? cj1 - jb : 32;
+                for (int t = 0; t < nb; ++t) {
+                    const int kc = __shfl_sync(0xffffffffu, cidx, t) * a.bw;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
-                    const int kc = __ldg(a.col_idx + j) * a.bw;
-                    const uint32_t xs = s0 + s * stage_bytes, ws = xs + a.x_bytes;
-                    mbar_arrive_expect_tx(full_bar(s), tx);
-                    tma_load_2d(ws, &tmW, full_bar(s), 0, j * a.bh);
-                    tma_load_2d(xs, &tmB, full_bar(s), n0, kc);
-                    tma_load_2d(xs + a.x_bytes / 2, &tmB, full_bar(s), n0 + 64, kc);
+                    if (lane == 0) {
+                        const uint32_t xs = s0 + s * stage_bytes, ws = xs + a.x_bytes;
+                        mbar_arrive_expect_tx(full_bar(s), tx);
+                        tma_load_2d(ws, &tmW, full_bar(s), 0, (jb + t) * a.bh);
+                        tma_load_2d(xs, &tmB, full_bar(s), n0, kc);
+                        tma_load_2d(xs + a.x_bytes / 2, &tmB, full_bar(s), n0 + 64, kc);
+                    }
                     ++issued;
                     if (++s == a.stages) {
                         s = 0;
@@ -126,12 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Leave no copy in flight: wait for the last phase armed on each slot.
-            for (int i = 0; i < a.stages && i < issued; ++i) {
-                const int slot = (s - 1 - i + 2 * a.stages) % a.stages;
-                const uint32_t par = (slot < s) ? ph : (ph ^ 1u);
-                mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
-            }
+        }
+        // Leave no copy in flight: wait for the last phase armed on each slot.
+        for (int i = 0; i < a.stages && i < issued; ++i) {
+            const int slot = (s - 1 - i + 2 * a.stages) % a.stages;
+            const uint32_t par = (slot < s) ? ph : (ph ^ 1u);
+            mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -141,14 +160,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             int t = 0;
             bool ok = true;
             const int ksteps = a.bw / 16;
+            auto blocks_of = [&](int64_t uu) {
+                if (uu >= total) return 0;
+                const int brr = static_cast<int>(uu % a.n_brows);
+                return __ldg(a.row_ptr + brr + 1) - __ldg(a.row_ptr + brr);
+            };
+            int nblk_next = blocks_of(blockIdx.x);
             for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
-                const int br = static_cast<int>(u % a.n_brows);
                 const int b = t % a.nacc;
                 const uint32_t aph = static_cast<uint32_t>(t / a.nacc) & 1u;
+                const int nblk = nblk_next;
+                nblk_next = blocks_of(u + gridDim.x);
                 if (!mbar_wait(acce_bar(b), aph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(b * a.bh);
-                const int nblk = __ldg(a.row_ptr + br + 1) - __ldg(a.row_ptr + br);
                 for (int j = 0; j < nblk; ++j) {
                     if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                         ok = false;
@@ -177,14 +202,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         int t = 0;
+        auto blocks_of = [&](int64_t uu) {
+            if (uu >= total) return 0;
+            const int brr = static_cast<int>(uu % a.n_brows);
+            return __ldg(a.row_ptr + brr + 1) - __ldg(a.row_ptr + brr);
+        };
+        int nblk_next = blocks_of(blockIdx.x);
         for (int64_t u = blockIdx.x; u < total; u += gridDim.x, ++t) {
             const int ntile = static_cast<int>(u / a.n_brows);
             const int br = static_cast<int>(u % a.n_brows);
             const int b = t % a.nacc;
             const uint32_t aph = static_cast<uint32_t>(t / a.nacc) & 1u;
+            const int nblk = nblk_next;
+            nblk_next = blocks_of(u + gridDim.x);
             if (!mbar_wait(accf_bar(b), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
             tc_fence_after();
-            const int nblk = __ldg(a.row_ptr + br + 1) - __ldg(a.row_ptr + br);
             const int64_t n = static_cast<int64_t>(ntile) * kTokens + q * 32 + lane;
             const bool live = n < a.N;
             float* crow = a.C + static_cast<int64_t>(br) * a.bh * a.ldc + n;

@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// 16-byte global -> shared copy through L2 (LDGSTS); bytes past `src_bytes`
+// are written as zeros (src_bytes = 0 reads nothing).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
+// barrier's expected count must already include this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

@@ -3,21 +3,23 @@
 // core: tcgen05.mma.sp, kind::f16, fp32 accumulation in TMEM.
 //
 // "Accelerating Sparse DNNs Based on Tiled GEMM" (abstract): tile-wise pruning
-// is applied at the global-memory level (here: TMA tile::gather4 of the kept B
-// rows into shared memory) and the 2:4 pattern executes inside the sparse
-// tensor core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
+// is applied at the global-memory level (here: the kept rows of B are gathered
+// into shared memory) and the 2:4 pattern executes inside the sparse tensor
+// core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
 //
 // Roles (320 threads, one CTA per SM, persistent over 128 x 128 output tiles):
 //   warp 0     producer: per 128-wide dense-K step, TMA loads of the compressed A
 //              tile (128 x 64, K-major, 128B swizzle), its metadata (128 x 16 B)
-//              and the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle;
-//              for TVW one gather4 per 4 kept rows).
+//              and the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle).
+//              For TVW the warp gathers the kept rows itself with 16-byte
+//              cp.async copies into the swizzled layout (many more requests in
+//              flight than TMA gather4 gave); rows past a tile's kept count are
+//              zero-filled by the copy.
 //   warp 1     MMA issuer: four sparse MMAs per stage (M=128, N=128, K=32 dense
 //              each), then tcgen05.commit frees the stage.
 //   warps 2-5  metadata warps (one per TMEM lane quarter): rewrite the stage's
-//              stored metadata into the tensor core's order (below), tcgen05.st it
-//              to TMEM (one 8-column-aligned column per MMA), and zero B rows past
-//              a tile's kept-column count.
+//              stored metadata into the tensor core's order (below) and tcgen05.st
+//              it to TMEM (one 8-column-aligned column per MMA).
 //   warps 6-9  epilogue: tcgen05.ld the accumulator and write C.
 //
 // Metadata order in TMEM (measured on the device for kind::f16, M = 128,
@@ -58,9 +60,14 @@ constexpr uint32_t META_COL = NACC * BN;                    // metadata columns 
 constexpr uint32_t META_STRIDE = 8;                         // one aligned TMEM column per MMA
 constexpr int INT_CHUNK_STEPS = 4;                          // 4 x 128 = 512 dense K per int chunk
 constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + M_BYTES;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16 + 4 * KS;
+
+using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
 
 struct SpArgs {
+    const void* B;            // TVW: gathered with cp.async
+    int64_t ldb;
+    int64_t b_rows;           // TVW: rows of B (kept-column indices must be below it)
     int64_t M, N, K;          // K: dense depth of the 2:4 operand (multiple of 128)
     int32_t n_mtiles, n_ntiles;
     const int32_t* tile_ptr;  // TVW only
@@ -72,6 +79,11 @@ struct SpArgs {
     int* err;
     uint64_t timeout_ns;
 };
+
+// Output tiles are visited N-fastest: the CTAs resident at one time share a few
+// row tiles of A and sweep all of B, which stays resident in L2.
+__device__ __forceinline__ int tile_m(const SpArgs& a, int64_t u) { return static_cast<int>(u / a.n_ntiles); }
+__device__ __forceinline__ int tile_n(const SpArgs& a, int64_t u) { return static_cast<int>(u % a.n_ntiles); }
 
 __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int& kt, bool gather) {
     if (gather) {
@@ -92,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
+    int32_t* s_rows = reinterpret_cast<int32_t*>(tslot + 4);  // TVW: kept rows of the step being issued
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
     // stage s: [A | B chunk 0 | B chunk 1 | stored metadata]
@@ -107,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), GATHER ? 33 : 1);  // TVW: + one cp.async arrival per producer lane
             mbar_init(mready_bar(s), 4);
             mbar_init(empty_bar(s), 1);
         }
@@ -155,22 +168,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // first tile with at least one step
         while (u < total) {
-            nk = tile_steps(a, static_cast<int>(u % a.n_mtiles), kb, kt, GATHER);
+            nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
             if (nk > 0) break;
             u += gridDim.x;
         }
         if (GATHER && u < total) load_rows(kb, kt, 0);
         while (u < total && ok) {
-            const int mt = static_cast<int>(u % a.n_mtiles), nt = static_cast<int>(u / a.n_mtiles);
+            const int mt = tile_m(a, u), nt = tile_n(a, u);
             const int m0 = mt * BM, n0 = nt * BN;
             int32_t r[4] = {rnext[0], rnext[1], rnext[2], rnext[3]};
             const int cur_ks = ks;
+            const int kt_cur = kt;
             // advance to the next step and prefetch its rows
             if (++ks >= nk) {
                 ks = 0;
                 u += gridDim.x;
                 while (u < total) {
-                    nk = tile_steps(a, static_cast<int>(u % a.n_mtiles), kb, kt, GATHER);
+                    nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
                     if (nk > 0) break;
                     u += gridDim.x;
                 }
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
+                mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : TX_BYTES);
                 tma_load_2d(a_s(s), &tmA, full_bar(s), cur_ks * (KS / 2), m0);
                 tma_load_2d(mc_s(s), &tmMeta, full_bar(s), cur_ks * (KS / 8), m0);
                 if (!GATHER) {
@@ -190,12 +204,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (GATHER) {
+                // kept row k of the step -> B row s_rows[k] (-1 past the kept count)
+                const int base = cur_ks * KS;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool in_tile = base + 4 * lane + i < kt_cur;
+                    const bool in_b = r[i] >= 0 && r[i] < a.b_rows;
+                    if (in_tile && !in_b) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                    s_rows[4 * lane + i] = (in_tile && in_b) ? r[i] : -1;
+                }
                 __syncwarp();
-                // lane l brings kept rows 4l..4l+3 of the step (both 64-column chunks);
-                // rows past the tile's kept count re-read its first kept row and are
-                // zeroed in shared memory by the metadata warps.
-                tma_gather4(b_s(s) + lane * 512u, &tmB, full_bar(s), n0, r[0], r[1], r[2], r[3]);
-                tma_gather4(b_s(s) + B_CHUNK + lane * 512u, &tmB, full_bar(s), n0 + 64, r[0], r[1], r[2], r[3]);
+                const T16* Bp = static_cast<const T16*>(a.B);
+                const int gi = lane & 7;
+#pragma unroll 4
+                for (int it = 0; it < 2 * KS / 4; ++it) {
+                    const int cr = 4 * it + (lane >> 3);  // (row, 64-column chunk) pair
+                    const int k = cr >> 1, h = cr & 1;
+                    const int32_t row = s_rows[k];
+                    const int64_t col = static_cast<int64_t>(n0) + 64 * h + 8 * gi;
+                    const int64_t left = a.N - col;
+                    const uint32_t nbytes = (row < 0 || left <= 0) ? 0u : (left >= 8 ? 16u : static_cast<uint32_t>(left) * 2u);
+                    const T16* src = nbytes ? Bp + static_cast<int64_t>(row) * a.ldb + col : Bp;
+                    cp_async16(b_s(s) + h * B_CHUNK + k * 128u + (static_cast<uint32_t>(gi ^ (k & 7)) << 4), src, nbytes);
+                }
+                cp_async_arrive_noinc(full_bar(s));
+                __syncwarp();
             }
             ++issued;
             if (++s == STAGES) {
@@ -216,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const int mt = static_cast<int>(u % a.n_mtiles);
+                const int mt = tile_m(a, u);
                 int kb, kt;
                 const int nk = tile_steps(a, mt, kb, kt, GATHER);
                 const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
@@ -237,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
+                        if (GATHER) fence_proxy_async_smem();  // B rows arrived through cp.async
                         const uint32_t mcol = tmem + META_COL + META_STRIDE * 4u * s;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -265,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
-            const int mt = static_cast<int>(u % a.n_mtiles);
+            const int mt = tile_m(a, u);
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
             const bool row_live = static_cast<int64_t>(mt) * BM + row < a.M;
@@ -285,17 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t o = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
                     tmem_st1(tl + META_STRIDE * (4u * s + i), o);
                 }
-                if (GATHER && (ks + 1) * KS > kt) {
-                    // rows past the kept count must contribute nothing
-                    const int r0 = kt - ks * KS;
-                    uint8_t* bs = smem + s * STAGE_BYTES + A_BYTES;
-                    for (int idx = r0 * 8 + q * 32 + lane; idx < KS * 8; idx += 128) {
-                        const int r = idx / 8, c = idx % 8;
-                        *reinterpret_cast<uint4*>(bs + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(bs + B_CHUNK + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -311,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         int acc_i = 0;
         for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
-            const int mt = static_cast<int>(u % a.n_mtiles), nt = static_cast<int>(u / a.n_mtiles);
+            const int mt = tile_m(a, u), nt = tile_n(a, u);
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
             const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
@@ -515,6 +538,9 @@ spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C
                         static_cast<uint64_t>(ldb) * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
         return SPMM_ERR_CUDA;
     SpArgs a{};
+    a.B = B;
+    a.ldb = ldb;
+    a.b_rows = A->K;
     a.M = A->M;
     a.N = N;
     a.K = A->Kp;
