@@ -259,23 +259,6 @@ struct WcsrArgs {
 };
 
 template <typename T>
-__device__ __forceinline__ float to_f(T v);
-template <>
-__device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
-template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
-
-// Four consecutive B elements (8 bytes, raw) of one row; lanes past N get zeros.
-template <typename T>
-__device__ __forceinline__ uint2 load_raw4(const T* p, int valid) {
-    if (valid >= 4) return __ldg(reinterpret_cast<const uint2*>(p));
-    uint16_t e[4] = {0, 0, 0, 0};
-    const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
-    for (int i = 0; i < valid; ++i) e[i] = q[i];
-    return make_uint2(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16));
-}
-
-template <typename T>
 __device__ __forceinline__ float2 unpack2(uint32_t w);
 template <>
 __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
@@ -286,19 +269,87 @@ __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
 }
 
-constexpr int kStage = 1024;  // nonzeros whose metadata is staged in shared memory at once
+// value bits (low half of a packed word) -> fp32
+template <typename T>
+__device__ __forceinline__ float low_to_f(uint32_t pk);
+template <>
+__device__ __forceinline__ float low_to_f<__half>(uint32_t pk) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(pk & 0xFFFFu)));
+}
+template <>
+__device__ __forceinline__ float low_to_f<__nv_bfloat16>(uint32_t pk) {
+    return __uint_as_float(pk << 16);
+}
+
+constexpr int kStage = 1024;  // nonzeros whose operand is staged in shared memory at once
 constexpr int kBatch = 16;    // B-row loads in flight per warp
+constexpr int kPad = kWarps * kBatch;
+
+// One warp's chunk of staged entries [j_lo, j_hi) (a multiple of kBatch long):
+// gather B rows, accumulate per row, store finished rows in the tile and the
+// chunk's end rows in the fix-up slots.
+template <typename T, bool FULL>
+__device__ __forceinline__ void wcsr_chunk(const T* B, int64_t ldb, int64_t ncol, int valid, const int* s_col,
+                                           const uint32_t* s_pk, int j_lo, int j_hi, float* tile, float* bnd,
+                                           int* bnd_row, int warp, int lane) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int cur = -1;
+    bool first_seg = true;
+    for (int j0 = j_lo; j0 < j_hi; j0 += kBatch) {
+        uint2 raw[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const T* p = B + static_cast<int64_t>(s_col[j0 + b]) * ldb + ncol;
+            if (FULL) {
+                raw[b] = __ldg(reinterpret_cast<const uint2*>(p));
+            } else {
+                const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+                const uint32_t e0 = valid > 0 ? q[0] : 0u, e1 = valid > 1 ? q[1] : 0u;
+                const uint32_t e2 = valid > 2 ? q[2] : 0u, e3 = valid > 3 ? q[3] : 0u;
+                raw[b] = make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const uint32_t pk = s_pk[j0 + b];
+            const int rr = static_cast<int>(pk >> 16);
+            if (rr != cur) {
+                if (cur >= 0) {
+                    // a finished segment: the chunk's first row goes to the fix-up,
+                    // any later one lies wholly inside this chunk
+                    float* dst = first_seg ? bnd + (warp * 2) * kSlab : tile + cur * kSlab;
+                    *reinterpret_cast<float4*>(dst + 4 * lane) = acc;
+                    if (first_seg && lane == 0) bnd_row[warp * 2] = cur;
+                    first_seg = false;
+                }
+                cur = rr;
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float v = low_to_f<T>(pk);
+            const float2 lo = unpack2<T>(raw[b].x), hi = unpack2<T>(raw[b].y);
+            acc.x += v * lo.x;
+            acc.y += v * lo.y;
+            acc.z += v * hi.x;
+            acc.w += v * hi.y;
+        }
+    }
+    if (cur >= 0) {
+        // the chunk's last segment may continue in the next chunk
+        const int k = first_seg ? 0 : 1;
+        *reinterpret_cast<float4*>(bnd + (warp * 2 + k) * kSlab + 4 * lane) = acc;
+        if (lane == 0) bnd_row[warp * 2 + k] = cur;
+    }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 4) wcsr_spmm_kernel(const WcsrArgs a) {
     extern __shared__ float sm[];
-    // tile[h][kSlab] | bnd[2*kWarps][kSlab] | bnd_row[2*kWarps] | s_col[kStage] | s_val[kStage] | s_row[kStage]
+    // tile[h][kSlab] | bnd[2*kWarps][kSlab] | bnd_row[2*kWarps] | s_col[kStage+kPad] | s_pk[kStage+kPad]
     float* tile = sm;
     float* bnd = tile + a.h * kSlab;
     int* bnd_row = reinterpret_cast<int*>(bnd + 2 * kWarps * kSlab);
     int* s_col = bnd_row + 2 * kWarps;
-    float* s_val = reinterpret_cast<float*>(s_col + kStage);
-    signed char* s_row = reinterpret_cast<signed char*>(s_val + kStage);
+    uint32_t* s_pk = reinterpret_cast<uint32_t*>(s_col + kStage + kPad);
     __shared__ int s_last;
 
     const int u = blockIdx.x;
@@ -315,18 +366,21 @@ __global__ void __launch_bounds__(kThreads, 4) wcsr_spmm_kernel(const WcsrArgs a
     const bool split = units_in_window > 1;
     const int32_t wbase = a.wcol_ptr[w], T_w = a.wcol_ptr[w + 1] - wbase;
     const int32_t nz0 = a.unit_nz_ptr[u], nz1 = a.unit_nz_ptr[u + 1];
-    const T* val = static_cast<const T*>(a.val);
+    const uint16_t* val = static_cast<const uint16_t*>(a.val);
     const T* B = static_cast<const T*>(a.B);
 
     for (int64_t n0 = 0; n0 < a.N; n0 += kSlab) {
         const int64_t ncol = n0 + 4 * lane;
         const int64_t left = a.N - ncol;
         const int valid = left >= 4 ? 4 : (left > 0 ? static_cast<int>(left) : 0);
+        const bool full = n0 + kSlab <= a.N;
         for (int i = threadIdx.x; i < a.h * kSlab; i += kThreads) tile[i] = 0.f;
 
         for (int32_t st0 = nz0; st0 < nz1; st0 += kStage) {
             const int n_st = (nz1 - st0 < kStage) ? nz1 - st0 : kStage;
-            // stage the sparse operand: local row, resolved column, value
+            const int per = ((n_st + kWarps - 1) / kWarps + kBatch - 1) / kBatch * kBatch;
+            // stage the sparse operand: resolved column, packed (local row, value);
+            // invalid entries become value 0 on row 0, column 0
             for (int i = threadIdx.x; i < n_st; i += kThreads) {
                 const int32_t e = st0 + i;
                 const int lr = a.lrow[e];
@@ -334,59 +388,23 @@ __global__ void __launch_bounds__(kThreads, 4) wcsr_spmm_kernel(const WcsrArgs a
                 const int32_t c = (sl >= 0 && sl < T_w) ? a.wcols[wbase + sl] : -1;
                 const bool ok = lr < nrows && c >= 0 && c < a.K;
                 if (!ok) atomicOr(a.err, SPMM_DEVERR_INDEX);
-                s_row[i] = ok ? static_cast<signed char>(lr) : static_cast<signed char>(-1);
                 s_col[i] = ok ? c : 0;
-                s_val[i] = ok ? to_f<T>(val[e]) : 0.f;
+                s_pk[i] = ok ? ((static_cast<uint32_t>(lr) << 16) | val[e]) : 0u;
+            }
+            __syncthreads();
+            // pad every chunk to whole batches: value-0 copies of the last entry
+            for (int i = n_st + threadIdx.x; i < kWarps * per; i += kThreads) {
+                s_col[i] = s_col[n_st - 1];
+                s_pk[i] = s_pk[n_st - 1] & 0xFFFF0000u;
             }
             if (threadIdx.x < 2 * kWarps) bnd_row[threadIdx.x] = -1;
             __syncthreads();
 
-            const int per = (n_st + kWarps - 1) / kWarps;
-            const int j_lo = warp * per, j_hi = (n_st < j_lo + per) ? n_st : j_lo + per;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            int cur = -1;
-            bool first_seg = true;
-            for (int j0 = j_lo; j0 < j_hi; j0 += kBatch) {
-                uint2 raw[kBatch];
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    const int j = j0 + b;
-                    const bool live = j < j_hi && s_row[j] >= 0;
-                    raw[b] = live ? load_raw4<T>(B + static_cast<int64_t>(s_col[j]) * a.ldb + ncol, valid)
-                                  : make_uint2(0u, 0u);
-                }
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    const int j = j0 + b;
-                    if (j >= j_hi) break;
-                    const int rr = s_row[j];
-                    if (rr < 0) continue;
-                    if (rr != cur) {
-                        if (cur >= 0) {
-                            // a finished segment: the chunk's first row goes to the fix-up,
-                            // any later one lies wholly inside this chunk
-                            float* dst = first_seg ? bnd + (warp * 2) * kSlab : tile + cur * kSlab;
-                            *reinterpret_cast<float4*>(dst + 4 * lane) = acc;
-                            if (first_seg && lane == 0) bnd_row[warp * 2] = cur;
-                            first_seg = false;
-                        }
-                        cur = rr;
-                        acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    const float v = s_val[j];
-                    const float2 lo = unpack2<T>(raw[b].x), hi = unpack2<T>(raw[b].y);
-                    acc.x += v * lo.x;
-                    acc.y += v * lo.y;
-                    acc.z += v * hi.x;
-                    acc.w += v * hi.y;
-                }
-            }
-            if (cur >= 0) {
-                // the chunk's last segment may continue in the next chunk
-                const int k = first_seg ? 0 : 1;
-                *reinterpret_cast<float4*>(bnd + (warp * 2 + k) * kSlab + 4 * lane) = acc;
-                if (lane == 0) bnd_row[warp * 2 + k] = cur;
-            }
+            const int j_lo = warp * per, j_hi = j_lo + per;
+            if (full)
+                wcsr_chunk<T, true>(B, a.ldb, ncol, valid, s_col, s_pk, j_lo, j_hi, tile, bnd, bnd_row, warp, lane);
+            else
+                wcsr_chunk<T, false>(B, a.ldb, ncol, valid, s_col, s_pk, j_lo, j_hi, tile, bnd, bnd_row, warp, lane);
             __syncthreads();
             // chunk-boundary rows, added in warp order: thread t owns column t of the slab
             if (threadIdx.x < kSlab) {
@@ -560,9 +578,9 @@ spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float*
                                          align256(sizeof(int32_t) * static_cast<size_t>(A->n_windows)));
     a.err = dev->err;
     const int smem = static_cast<int>(sizeof(float) * (A->h * kSlab + kWarps * 2 * kSlab) + sizeof(int) * kWarps * 2 +
-                                      kStage * (sizeof(int) + sizeof(float) + 1));
+                                      (kStage + kPad) * (sizeof(int) + sizeof(uint32_t)));
     const int smem_max = static_cast<int>(sizeof(float) * (kMaxH * kSlab + kWarps * 2 * kSlab) +
-                                          sizeof(int) * kWarps * 2 + kStage * (sizeof(int) + sizeof(float) + 1));
+                                          sizeof(int) * kWarps * 2 + (kStage + kPad) * (sizeof(int) + sizeof(uint32_t)));
     const void* kern = A->dtype == SPMM_BF16 ? reinterpret_cast<const void*>(wcsr_spmm_kernel<__nv_bfloat16>)
                                              : reinterpret_cast<const void*>(wcsr_spmm_kernel<__half>);
     if (!set_smem_attr_once(kern, smem_max, A->dtype == SPMM_BF16 ? 4 : 5)) return SPMM_ERR_CUDA;
