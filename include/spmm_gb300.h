@@ -206,8 +206,8 @@ SPMM_API spmm_status spmm_wcsr(const spmm_wcsr_t *A, const void *B, int64_t ldb,
 SPMM_API spmm_status spmm_24_workspace_size(const spmm_24_t *A, int64_t N, size_t *bytes);
 /* C = A * B with A 2:4 ("Accelerating Sparse DNNs Based on Tiled GEMM": 2:4
  * executed inside the sparse tensor core).  int8: C is int32 and exact (the
- * kernel accumulates 512-wide K chunks in fp32, every partial an integer of
- * magnitude at most 2^22, and sums the chunks in int32).  fp16/bf16: C is fp32.
+ * kernel accumulates 2048-wide K chunks in fp32, every partial an integer of
+ * magnitude below 2^24, and sums the chunks in int32).  fp16/bf16: C is fp32.
  * Needs K % 128 == 0. */
 SPMM_API spmm_status spmm_24(const spmm_24_t *A, const void *B, int64_t ldb, void *C, int64_t ldc, int64_t N,
                              void *workspace, size_t workspace_bytes, spmm_stream_t stream);

@@ -221,19 +221,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool live = n < a.N;
             float* crow = a.C + static_cast<int64_t>(br) * a.bh * a.ldc + n;
             const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * a.bh);
-            for (int c0 = 0; c0 < a.bh; c0 += 16) {
-                uint32_t v[16];
+            // up to 64 columns per TMEM round trip: issue the loads, wait once, store
+            for (int c0 = 0; c0 < a.bh; c0 += 64) {
+                uint32_t v[4][16];
+                const int nq = (a.bh - c0) >= 64 ? 4 : (a.bh - c0) / 16;
                 if (nblk > 0) {
-                    tmem_ld16(tl + c0, v);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        if (g < nq) tmem_ld16(tl + c0 + 16 * g, v[g]);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0u;
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[g][i] = 0u;
                 }
                 if (live) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        __stcs(crow + static_cast<int64_t>(c0 + i) * a.ldc, __uint_as_float(v[i]));
+                    for (int g = 0; g < 4; ++g)
+                        if (g < nq) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                __stcs(crow + static_cast<int64_t>(c0 + 16 * g + i) * a.ldc, __uint_as_float(v[g][i]));
+                        }
                 }
             }
             tc_fence_before();

@@ -10,16 +10,17 @@
 // Roles (320 threads, one CTA per SM, persistent over 128 x 128 output tiles):
 //   warp 0     producer: per 128-wide dense-K step, TMA loads of the compressed A
 //              tile (128 x 64, K-major, 128B swizzle), its metadata (128 x 16 B)
-//              and the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle).
-//              For TVW the warp gathers the kept rows itself with 16-byte
-//              cp.async copies into the swizzled layout (many more requests in
-//              flight than TMA gather4 gave); rows past a tile's kept count are
-//              zero-filled by the copy.
+//              and, for 2:4, the B tile (128 K-rows x 128 columns, MN-major,
+//              128B swizzle).
 //   warp 1     MMA issuer: four sparse MMAs per stage (M=128, N=128, K=32 dense
 //              each), then tcgen05.commit frees the stage.
-//   warps 2-5  metadata warps (one per TMEM lane quarter): rewrite the stage's
-//              stored metadata into the tensor core's order (below) and tcgen05.st
-//              it to TMEM (one 8-column-aligned column per MMA).
+//   warps 2-5  metadata warps (one per TMEM lane quarter): for TVW they first
+//              gather the stage's kept B rows (32 rows each) with 16-byte cp.async
+//              copies into the swizzled tile, zero-filling rows past the tile's kept
+//              count (far more requests in flight than TMA gather4 of 4 x 128-byte
+//              rows gave); then they rewrite the stage's stored metadata into the
+//              tensor core's order (below) and tcgen05.st it to TMEM (one
+//              8-column-aligned column per MMA).
 //   warps 6-9  epilogue: tcgen05.ld the accumulator and write C.
 //
 // Metadata order in TMEM (measured on the device for kind::f16, M = 128,
@@ -33,9 +34,9 @@
 // int8 operands: the tensor core on sm_103a has no integer MMA, so int8 values
 // (exact in fp16) are widened to fp16 in a workspace and multiplied with fp32
 // accumulation.  Every product is an integer of magnitude at most 127*127; the
-// accumulator is drained every 512 dense K (256 products, |partial| <= 2^22,
-// all partial sums exact) and the chunks are summed in int32 by the epilogue,
-// so C is exact.
+// accumulator is drained every 2048 dense K (1024 products, |partial| <=
+// 16 516 096 < 2^24, so every partial sum is an exactly representable integer)
+// and the chunks are summed in int32 by the epilogue, so C is exact.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -58,9 +59,9 @@ constexpr int NACC = 2;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t META_COL = NACC * BN;                    // metadata columns after the accumulators
 constexpr uint32_t META_STRIDE = 8;                         // one aligned TMEM column per MMA
-constexpr int INT_CHUNK_STEPS = 4;                          // 4 x 128 = 512 dense K per int chunk
+constexpr int INT_CHUNK_STEPS = 16;                         // 16 x 128 = 2048 dense K per int chunk
 constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + M_BYTES;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16 + 4 * KS;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
 
 using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
 
@@ -104,7 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
-    int32_t* s_rows = reinterpret_cast<int32_t*>(tslot + 4);  // TVW: kept rows of the step being issued
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
     // stage s: [A | B chunk 0 | B chunk 1 | stored metadata]
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), GATHER ? 33 : 1);  // TVW: + one cp.async arrival per producer lane
+            mbar_init(full_bar(s), GATHER ? 129 : 1);  // TVW: + one cp.async arrival per metadata-warp lane
             mbar_init(mready_bar(s), 4);
             mbar_init(empty_bar(s), 1);
         }
@@ -153,87 +153,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         int64_t issued = 0;
         bool ok = true;
-        // Steps are visited as a flat sequence of (tile, k-step).  For TVW the
-        // kept-row indices of the next step are loaded right after the current
-        // step is issued, so their latency overlaps the wait for a free stage.
-        int64_t u = blockIdx.x;
-        int ks = 0, kb = 0, kt = 0, nk = 0;
-        int32_t rnext[4] = {0, 0, 0, 0};
-        auto load_rows = [&](int kb_, int kt_, int ks_) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int k = ks_ * KS + 4 * lane + i;
-                rnext[i] = __ldg(a.cols + kb_ + (k < kt_ ? k : 0));
-            }
-        };
-        // first tile with at least one step
-        while (u < total) {
-            nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
-            if (nk > 0) break;
-            u += gridDim.x;
-        }
-        if (GATHER && u < total) load_rows(kb, kt, 0);
-        while (u < total && ok) {
+        for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
             const int mt = tile_m(a, u), nt = tile_n(a, u);
             const int m0 = mt * BM, n0 = nt * BN;
-            int32_t r[4] = {rnext[0], rnext[1], rnext[2], rnext[3]};
-            const int cur_ks = ks;
-            const int kt_cur = kt;
-            // advance to the next step and prefetch its rows
-            if (++ks >= nk) {
-                ks = 0;
-                u += gridDim.x;
-                while (u < total) {
-                    nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
-                    if (nk > 0) break;
-                    u += gridDim.x;
+            int kb, kt;
+            const int nk = tile_steps(a, mt, kb, kt, GATHER);
+            for (int ks = 0; ks < nk; ++ks) {
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
                 }
-            }
-            if (GATHER && u < total) load_rows(kb, kt, ks);
-            if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : TX_BYTES);
-                tma_load_2d(a_s(s), &tmA, full_bar(s), cur_ks * (KS / 2), m0);
-                tma_load_2d(mc_s(s), &tmMeta, full_bar(s), cur_ks * (KS / 8), m0);
-                if (!GATHER) {
-                    tma_load_2d(b_s(s), &tmB, full_bar(s), n0, cur_ks * KS);
-                    tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, cur_ks * KS);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : TX_BYTES);
+                    tma_load_2d(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0);
+                    tma_load_2d(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0);
+                    if (!GATHER) {
+                        tma_load_2d(b_s(s), &tmB, full_bar(s), n0, ks * KS);
+                        tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, ks * KS);
+                    }
                 }
-            }
-            if (GATHER) {
-                // kept row k of the step -> B row s_rows[k] (-1 past the kept count)
-                const int base = cur_ks * KS;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const bool in_tile = base + 4 * lane + i < kt_cur;
-                    const bool in_b = r[i] >= 0 && r[i] < a.b_rows;
-                    if (in_tile && !in_b) atomicOr(a.err, SPMM_DEVERR_INDEX);
-                    s_rows[4 * lane + i] = (in_tile && in_b) ? r[i] : -1;
+                ++issued;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
                 }
-                __syncwarp();
-                const T16* Bp = static_cast<const T16*>(a.B);
-                const int gi = lane & 7;
-#pragma unroll 4
-                for (int it = 0; it < 2 * KS / 4; ++it) {
-                    const int cr = 4 * it + (lane >> 3);  // (row, 64-column chunk) pair
-                    const int k = cr >> 1, h = cr & 1;
-                    const int32_t row = s_rows[k];
-                    const int64_t col = static_cast<int64_t>(n0) + 64 * h + 8 * gi;
-                    const int64_t left = a.N - col;
-                    const uint32_t nbytes = (row < 0 || left <= 0) ? 0u : (left >= 8 ? 16u : static_cast<uint32_t>(left) * 2u);
-                    const T16* src = nbytes ? Bp + static_cast<int64_t>(row) * a.ldb + col : Bp;
-                    cp_async16(b_s(s) + h * B_CHUNK + k * 128u + (static_cast<uint32_t>(gi ^ (k & 7)) << 4), src, nbytes);
-                }
-                cp_async_arrive_noinc(full_bar(s));
-                __syncwarp();
-            }
-            ++issued;
-            if (++s == STAGES) {
-                s = 0;
-                ph ^= 1u;
             }
         }
         // Leave no copy in flight: wait for the last phase armed on each slot.
@@ -294,39 +237,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- metadata warps
         const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q+31 of the tile
         const int row = 32 * q + lane;
+        const int gq = warp - 2;  // TVW: this warp gathers kept rows 32gq .. 32gq+31 of each step
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + META_COL;
+        const T16* Bp = static_cast<const T16*>(a.B);
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
-            const int mt = tile_m(a, u);
-            int kb, kt;
-            const int nk = tile_steps(a, mt, kb, kt, GATHER);
-            const bool row_live = static_cast<int64_t>(mt) * BM + row < a.M;
-            for (int ks = 0; ks < nk; ++ks) {
-                if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+        // Steps are visited as a flat sequence of (tile, k-step); for TVW this lane's
+        // kept-row index of the next step is loaded one step ahead.
+        int64_t u = blockIdx.x;
+        int ks = 0, kb = 0, kt = 0, nk = 0;
+        while (u < total) {
+            nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
+            if (nk > 0) break;
+            u += gridDim.x;
+        }
+        auto kept_row = [&](int kb_, int kt_, int ks_) {
+            const int k = ks_ * KS + 32 * gq + lane;
+            return k < kt_ ? __ldg(a.cols + kb_ + k) : -1;
+        };
+        int32_t rnext = (GATHER && u < total) ? kept_row(kb, kt, 0) : -1;
+        while (u < total && ok) {
+            const int mt = tile_m(a, u), nt = tile_n(a, u);
+            const int32_t rcur = rnext;
+            if (++ks >= nk) {
+                ks = 0;
+                u += gridDim.x;
+                while (u < total) {
+                    nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
+                    if (nk > 0) break;
+                    u += gridDim.x;
+                }
+            }
+            if (GATHER && u < total) rnext = kept_row(kb, kt, ks);
+            if (GATHER) {
+                // gather this warp's 32 kept rows of B (two 64-column chunks each) into the
+                // stage's swizzled MN-major tile; rows past the kept count are zero-filled
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* mc = smem + s * STAGE_BYTES + A_BYTES + B_BYTES;
-                uint4 w = *reinterpret_cast<const uint4*>(mc + 16 * row);
-                // rows past M arrive zero-filled; give them the valid (0, 1) pattern
-                if (!row_live) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
-                const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+                const bool in_b = rcur >= 0 && rcur < a.b_rows;
+                if (rcur >= 0 && !in_b) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                const int32_t myrow = in_b ? rcur : -1;
+                const int gi = lane & 7;
+                const int64_t n0 = static_cast<int64_t>(nt) * BN;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t p = __shfl_xor_sync(0xffffffffu, in[i], 8);
-                    const uint32_t o = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
-                    tmem_st1(tl + META_STRIDE * (4u * s + i), o);
+                for (int it = 0; it < 16; ++it) {
+                    const int cr = 4 * it + (lane >> 3);  // (row, chunk) pair within the warp's rows
+                    const int lr = cr >> 1, h = cr & 1;
+                    const int32_t brow = __shfl_sync(0xffffffffu, myrow, lr);
+                    const int k = 32 * gq + lr;
+                    const int64_t col = n0 + 64 * h + 8 * gi;
+                    const int64_t left = a.N - col;
+                    const uint32_t nbytes =
+                        (brow < 0 || left <= 0) ? 0u : (left >= 8 ? 16u : static_cast<uint32_t>(left) * 2u);
+                    const T16* src = nbytes ? Bp + static_cast<int64_t>(brow) * a.ldb + col : Bp;
+                    cp_async16(b_s(s) + h * B_CHUNK + k * 128u + (static_cast<uint32_t>(gi ^ (k & 7)) << 4), src,
+                               nbytes);
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(mready_bar(s));
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                cp_async_arrive_noinc(full_bar(s));
+            }
+            if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                ok = false;
+                break;
+            }
+            const bool row_live = static_cast<int64_t>(mt) * BM + row < a.M;
+            const uint8_t* mc = smem + s * STAGE_BYTES + A_BYTES + B_BYTES;
+            uint4 w = *reinterpret_cast<const uint4*>(mc + 16 * row);
+            // rows past M arrive zero-filled; give them the valid (0, 1) pattern
+            if (!row_live) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+            const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t p = __shfl_xor_sync(0xffffffffu, in[i], 8);
+                const uint32_t o = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
+                tmem_st1(tl + META_STRIDE * (4u * s + i), o);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mready_bar(s));
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
             }
         }
     } else {
@@ -367,11 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 16; ++i) v[i] = 0u;
                     }
                     if constexpr (INT_EXACT) {
-                        // integer-valued fp32 with |x| <= 2^22: x + 1.5 * 2^23 has the bits
-                        // 0x4B400000 + x
+                        // every chunk partial is an integer of magnitude below 2^24, exact in
+                        // fp32; round-to-nearest conversion returns it unchanged
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            run[16 * j + i] += __float_as_int(__uint_as_float(v[i]) + 12582912.0f) - 0x4B400000;
+                        for (int i = 0; i < 16; ++i) run[16 * j + i] += __float2int_rn(__uint_as_float(v[i]));
                     } else if (row_live) {
                         float* cp = static_cast<float*>(a.C) + row * a.ldc + n0 + 16 * j;
                         if (full_n) {
