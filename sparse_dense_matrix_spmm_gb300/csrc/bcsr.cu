@@ -9,8 +9,11 @@
 //               128-column token tile, into a ring of shared-memory stages.
 //   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate) into a
 //               TMEM accumulator, then tcgen05.commit frees the stage.
-//   warps 2-5   epilogue: tcgen05.ld the accumulator, stream fp32 C to HBM while
-//               the next work unit's MMAs run (accumulators are multi-buffered).
+//   warps 2-5   epilogue: tcgen05.ld the accumulator into a double-buffered
+//               shared-memory tile (64 rows x 128 tokens) and write it with TMA
+//               tensor stores while the next work unit's MMAs run (accumulators
+//               are multi-buffered).  Row-scattered 128-byte warp stores reached
+//               only ~5 B/clk per SM; bulk tensor stores keep C at HBM speed.
 //
 // Orientation: the MMA computes C^T for one (token tile, block row) unit,
 //   D[token][r] = sum_j sum_c B[col_idx[j]*bw + c][token] * vals[j][r][c],
@@ -19,6 +22,8 @@
 // is MN-major (tokens contiguous, as B is row-major), the block K-major.
 // Work units are ordered token-tile-major, so CTAs resident at the same time
 // share one token slab of B in L2.
+#include <cstring>
+
 #include "internal.h"
 #include "sm103.cuh"
 
@@ -43,6 +48,7 @@ struct BcsrArgs {
     int32_t nacc;
     uint32_t tmem_cols;
     uint32_t x_bytes;  // per stage: B tile, two 64-token halves of bw rows x 128 B
+    uint32_t cbuf_off; // offset of the two 32 KB C staging buffers (0: store C directly)
     uint32_t w_bytes;  // per stage: block tile (1024-aligned)
     uint32_t idesc;
     uint32_t w_swz;
@@ -53,7 +59,7 @@ struct BcsrArgs {
 
 __global__ void __launch_bounds__(kThreads, 1)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmW,
-                     const BcsrArgs a) {
+                     const __grid_constant__ CUtensorMap tmC, const BcsrArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t stage_bytes = a.x_bytes + a.w_bytes;
@@ -201,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // -------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        int t = 0;
+        const bool elected = (warp == 2 && lane == 0);  // issues the bulk stores
+        int t = 0, chunk = 0;
         auto blocks_of = [&](int64_t uu) {
             if (uu >= total) return 0;
             const int brr = static_cast<int>(uu % a.n_brows);
@@ -221,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool live = n < a.N;
             float* crow = a.C + static_cast<int64_t>(br) * a.bh * a.ldc + n;
             const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * a.bh);
-            // up to 64 columns per TMEM round trip: issue the loads, wait once, store
-            for (int c0 = 0; c0 < a.bh; c0 += 64) {
+            // 64 accumulator columns (C rows) per TMEM round trip
+            for (int c0 = 0; c0 < a.bh; c0 += 64, ++chunk) {
                 uint32_t v[4][16];
                 const int nq = (a.bh - c0) >= 64 ? 4 : (a.bh - c0) / 16;
                 if (nblk > 0) {
@@ -236,7 +243,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[g][i] = 0u;
                 }
-                if (live) {
+                if (c0 + 64 >= a.bh) {  // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(b));
+                }
+                if (a.cbuf_off) {
+                    // stage rows c0 .. c0+63 of the unit as [row][token] and bulk-store them
+                    const uint32_t buf = static_cast<uint32_t>(chunk & 1);
+                    float* st = reinterpret_cast<float*>(smem + a.cbuf_off + buf * 32768u);
+                    if (elected) bulk_wait_read<1>();  // the store that last used `buf` has read it
+                    named_barrier(1, 128);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        if (g < nq) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) st[(16 * g + i) * kTokens + q * 32 + lane] = __uint_as_float(v[g][i]);
+                        }
+                    fence_proxy_async_smem();
+                    named_barrier(1, 128);
+                    if (elected) {
+                        tma_store_2d(&tmC, smem_u32(st), ntile * kTokens, br * a.bh + c0);
+                        bulk_commit();
+                    }
+                } else if (live) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g)
                         if (g < nq) {
@@ -246,10 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(b));
         }
+        if (elected) bulk_wait<0>();  // every bulk store has completed before the CTA exits
     }
 
     tc_fence_before();
@@ -312,19 +340,29 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
     a.err = dev->err;
     a.timeout_ns = kWaitTimeoutNs;
 
+    // C through TMA stores when its rows are 16-byte aligned (box: 128 tokens x 64 rows)
+    CUtensorMap tmC;
+    const bool tma_c = (ldc % 4 == 0) && aligned16(C) && bh % 64 == 0 &&
+                       encode_tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
+                                      static_cast<uint64_t>(A->M), static_cast<uint64_t>(ldc) * 4, kTokens, 64,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!tma_c) std::memset(&tmC, 0, sizeof(tmC));
     const int max_smem = dev->max_smem_optin;
     const uint32_t stage_bytes = a.x_bytes + a.w_bytes;
-    const int fixed = 1024 + 8 * (2 * 8 + 2 * 4 + 1) + 16;
+    const int cbuf = tma_c ? 2 * 32768 : 0;
+    const int fixed = 1024 + 8 * (2 * 8 + 2 * 4 + 1) + 16 + cbuf + (tma_c ? 1024 : 0);  // + staging alignment
     int stages = (max_smem - fixed) / static_cast<int>(stage_bytes);
     stages = stages > 8 ? 8 : stages;
     if (stages < 2) return SPMM_ERR_UNSUPPORTED;
     a.stages = stages;
-    const int smem = 1024 + stages * static_cast<int>(stage_bytes) + 8 * (2 * stages + 2 * a.nacc + 1) + 16;
+    const int bar_bytes = 8 * (2 * stages + 2 * a.nacc + 1) + 16;
+    a.cbuf_off = tma_c ? static_cast<uint32_t>((stages * stage_bytes + bar_bytes + 1023) & ~1023u) : 0u;
+    const int smem = 1024 + (tma_c ? static_cast<int>(a.cbuf_off) + cbuf : stages * static_cast<int>(stage_bytes) + bar_bytes);
     if (!set_smem_attr_once(reinterpret_cast<const void*>(bcsr_spmm_kernel), max_smem, 0)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_brows) * a.n_ntiles;
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_BCSR, stream);
-    bcsr_spmm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmW, a);
+    bcsr_spmm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_BCSR, stream);
     return cuda_status(e);
