@@ -50,11 +50,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on the phase with parity `parity`.  Spins briefly, then checks
-// %globaltimer; after `timeout_ns` it records `code` in the error word and
-// returns false, so the caller can leave its loop instead of hanging.
+// Non-blocking test of the phase with parity `parity` (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on the phase with parity `parity`.  A non-blocking test first
+// (a completed phase costs far less than a try_wait round trip), then try_wait
+// spins, then %globaltimer checks; after `timeout_ns` it records `code` in the
+// error word and returns false, so the caller can leave its loop instead of
+// hanging.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                           int* err, int code) {
+    if (mbar_test_wait(bar, parity)) return true;
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
