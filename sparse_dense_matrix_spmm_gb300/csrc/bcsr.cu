@@ -4,16 +4,21 @@
 // Fig. 4 warp-specialised pipeline) overlaps TMA transfers of B tiles with
 // tensor-core work on every nonzero block.  On sm_103a that becomes:
 //
-//   warp 0      TMA producer: per nonzero block j of a block row, the block
-//               (bh x bw, K-major, swizzled) and the matching bw rows of B for a
-//               128-column token tile, into a ring of shared-memory stages.
-//   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate) into a
-//               TMEM accumulator, then tcgen05.commit frees the stage.
-//   warps 2-5   epilogue: tcgen05.ld the accumulator into a double-buffered
+//   warps 0-1   TMA producers, taking alternate stages of one ring: per nonzero
+//               block j of a block row, the block (bh x bw, K-major, swizzled)
+//               and the matching bw rows of B for a 128-column token tile (one
+//               3-D box holding both 64-token halves when N is a multiple of 64).
+//               One issuing thread moves ~70 B/clk; two keep the ring full.
+//   warp 2      one thread issues tcgen05.mma (kind::f16, fp32 accumulate) into a
+//               TMEM accumulator, then tcgen05.commit frees the stage.  The shared
+//               memory descriptors are built once; per MMA only the stage and K
+//               offsets are added, which keeps the issue loop a few instructions
+//               long (a single thread building two descriptors per MMA cost more
+//               than the N = 64 MMA itself).
+//   warps 3-6   epilogue: tcgen05.ld the accumulator into a double-buffered
 //               shared-memory tile (64 rows x 128 tokens) and write it with TMA
 //               tensor stores while the next work unit's MMAs run (accumulators
-//               are multi-buffered).  Row-scattered 128-byte warp stores reached
-//               only ~5 B/clk per SM; bulk tensor stores keep C at HBM speed.
+//               are multi-buffered).
 //
 // Orientation: the MMA computes C^T for one (token tile, block row) unit,
 //   D[token][r] = sum_j sum_c B[col_idx[j]*bw + c][token] * vals[j][r][c],
@@ -21,7 +26,8 @@
 // and each stored block is one K = bw contraction (bw / 16 MMAs).  The B tile
 // is MN-major (tokens contiguous, as B is row-major), the block K-major.
 // Work units are ordered token-tile-major, so CTAs resident at the same time
-// share one token slab of B in L2.
+// share one token slab of B in L2; every role walks its units with 32-bit
+// increments (no division per unit).
 #include <cstring>
 
 #include "internal.h"
@@ -32,7 +38,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;
+constexpr int kProducers = 2;
+constexpr int kMmaWarp = kProducers;
+constexpr int kEpiWarp0 = kProducers + 1;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kTokens = 128;
 
 struct BcsrArgs {
@@ -44,8 +53,9 @@ struct BcsrArgs {
     int32_t n_brows;
     int32_t n_ntiles;
     int32_t bh, bw;
-    int32_t stages;
+    int32_t stages;    // even: producer p owns the slots s with s % 2 == p
     int32_t nacc;
+    int32_t x3d;       // B tile as one 3-D box (both halves) instead of two 2-D boxes
     uint32_t tmem_cols;
     uint32_t x_bytes;  // per stage: B tile, two 64-token halves of bw rows x 128 B
     uint32_t cbuf_off; // offset of the two 32 KB C staging buffers (0: store C directly)
@@ -57,6 +67,32 @@ struct BcsrArgs {
     uint64_t timeout_ns;
 };
 
+// Units u = start, start + stride, ... as (token tile, block row) with
+// u = nt * n_brows + br, advanced without division.
+struct UnitWalk {
+    int nt, br, step_nt, step_br, n_brows;
+    __device__ __forceinline__ void init(int n_brows_, int start, int stride) {
+        n_brows = n_brows_;
+        nt = start / n_brows;
+        br = start % n_brows;
+        step_nt = stride / n_brows;
+        step_br = stride % n_brows;
+    }
+    __device__ __forceinline__ void next() {
+        br += step_br;
+        nt += step_nt;
+        if (br >= n_brows) {
+            br -= n_brows;
+            ++nt;
+        }
+    }
+};
+
+__device__ __forceinline__ int blocks_in_row(const BcsrArgs& a, int br) {
+    return __ldg(a.row_ptr + br + 1) - __ldg(a.row_ptr + br);
+}
+
+template <int KSTEPS>
 __global__ void __launch_bounds__(kThreads, 1)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmC, const BcsrArgs a) {
@@ -90,8 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmW);
+        if (a.cbuf_off) tma_prefetch_desc(&tmC);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tslot), a.tmem_cols);
         tmem_relinquish();
     }
@@ -99,106 +136,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int64_t total = static_cast<int64_t>(a.n_brows) * a.n_ntiles;
 
-    if (warp == 0) {
-        // -------------------------------------------------------- TMA producer
-        // The warp reads a unit's block columns in one coalesced load and
-        // prefetches the next unit's row_ptr pair, so index latency stays off the
-        // issue path; lane 0 issues the copies.
-        int s = 0;
-        uint32_t ph = 0;
-        int64_t issued = 0;
+    if (warp < kProducers) {
+        // -------------------------------------------------------- TMA producers
+        // Both warps walk every block of every unit; producer p issues the blocks
+        // whose position in that sequence has parity p, into its own slots.  The
+        // warp reads a unit's block columns in one coalesced load and prefetches
+        // the next unit's row_ptr pair; lane 0 issues the copies.
+        const int p = warp;
+        const int own = a.stages / 2;
+        int s = p;          // next own slot
+        uint32_t ph = 0;    // its phase
+        int armed = 0;      // own slots armed so far (saturates at `own`)
+        bool mine = (p == 0);
         bool ok = true;
         const uint32_t tx = a.x_bytes + static_cast<uint32_t>(a.bh * a.bw * 2);
-        int64_t u = blockIdx.x;
+        UnitWalk w;
+        w.init(a.n_brows, blockIdx.x, gridDim.x);
         int j0 = 0, j1 = 0;
-        if (u < total) {
-            const int br = static_cast<int>(u % a.n_brows);
-            j0 = __ldg(a.row_ptr + br);
-            j1 = __ldg(a.row_ptr + br + 1);
+        if (w.nt < a.n_ntiles) {
+            j0 = __ldg(a.row_ptr + w.br);
+            j1 = __ldg(a.row_ptr + w.br + 1);
         }
-        for (; u < total && ok; u += gridDim.x) {
-            const int ntile = static_cast<int>(u / a.n_brows);
-            const int n0 = ntile * kTokens;
+        while (w.nt < a.n_ntiles && ok) {
+            const int n0 = w.nt * kTokens;
             const int cj0 = j0, cj1 = j1;
-            const int64_t un = u + gridDim.x;
-            if (un < total) {  // next unit's block range, in flight while this unit issues
-                const int brn = static_cast<int>(un % a.n_brows);
-                j0 = __ldg(a.row_ptr + brn);
-                j1 = __ldg(a.row_ptr + brn + 1);
+            UnitWalk wn = w;
+            wn.next();
+            if (wn.nt < a.n_ntiles) {  // next unit's block range, in flight while this unit issues
+                j0 = __ldg(a.row_ptr + wn.br);
+                j1 = __ldg(a.row_ptr + wn.br + 1);
             }
             for (int jb = cj0; jb < cj1 && ok; jb += 32) {
                 const int cidx = (jb + lane < cj1) ? __ldg(a.col_idx + jb + lane) : 0;
                 const int nb = (cj1 - jb < 32) ? cj1 - jb : 32;
                 for (int t = 0; t < nb; ++t) {
                     const int kc = __shfl_sync(0xffffffffu, cidx, t) * a.bw;
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
-                        ok = false;
-                        break;
+                    if (mine) {
+                        if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            const uint32_t xs = s0 + static_cast<uint32_t>(s) * stage_bytes, ws = xs + a.x_bytes;
+                            mbar_arrive_expect_tx(full_bar(s), tx);
+                            tma_load_2d(ws, &tmW, full_bar(s), 0, (jb + t) * a.bh);
+                            if (a.x3d) {
+                                tma_load_3d(xs, &tmB, full_bar(s), 0, kc, n0 / 64);
+                            } else {
+                                tma_load_2d(xs, &tmB, full_bar(s), n0, kc);
+                                tma_load_2d(xs + a.x_bytes / 2, &tmB, full_bar(s), n0 + 64, kc);
+                            }
+                        }
+                        if (armed < own) ++armed;
+                        s += 2;
+                        if (s >= a.stages) {
+                            s -= a.stages;
+                            ph ^= 1u;
+                        }
                     }
-                    if (lane == 0) {
-                        const uint32_t xs = s0 + s * stage_bytes, ws = xs + a.x_bytes;
-                        mbar_arrive_expect_tx(full_bar(s), tx);
-                        tma_load_2d(ws, &tmW, full_bar(s), 0, (jb + t) * a.bh);
-                        tma_load_2d(xs, &tmB, full_bar(s), n0, kc);
-                        tma_load_2d(xs + a.x_bytes / 2, &tmB, full_bar(s), n0 + 64, kc);
-                    }
-                    ++issued;
-                    if (++s == a.stages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    mine = !mine;
                 }
             }
+            w = wn;
         }
-        // Leave no copy in flight: wait for the last phase armed on each slot.
-        for (int i = 0; i < a.stages && i < issued; ++i) {
-            const int slot = (s - 1 - i + 2 * a.stages) % a.stages;
-            const uint32_t par = (slot < s) ? ph : (ph ^ 1u);
-            mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        // Leave no copy in flight: wait for the last phase armed on each own slot.
+        for (int i = 0; i < armed; ++i) {
+            int idx = (s - p) / 2 - 1 - i;
+            uint32_t par = ph;
+            if (idx < 0) {
+                idx += own;
+                par ^= 1u;
+            }
+            mbar_wait(full_bar(2 * idx + p), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         if (lane == 0) {
             // ---------------------------------------------------- MMA issuer
-            int s = 0;
-            uint32_t ph = 0;
-            int t = 0;
+            // Descriptor of stage 0 at K offset 0; stage s and K step kk add
+            // s * stage_bytes and kk * (16 rows x 128 B) (B tile) or kk * 32 B
+            // (block), in 16-byte units, to the address field.
+            const uint64_t adesc0 = smem_desc(s0, a.x_bytes / 2, 1024u, SWZ_128B);
+            const uint64_t bdesc0 = smem_desc(s0 + a.x_bytes, 16u, a.w_sbo, a.w_swz);
+            const uint32_t sdesc = stage_bytes >> 4;
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
             bool ok = true;
-            const int ksteps = a.bw / 16;
-            auto blocks_of = [&](int64_t uu) {
-                if (uu >= total) return 0;
-                const int brr = static_cast<int>(uu % a.n_brows);
-                return __ldg(a.row_ptr + brr + 1) - __ldg(a.row_ptr + brr);
-            };
-            int nblk_next = blocks_of(blockIdx.x);
-            for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x, ++t) {
-                const int b = t % a.nacc;
-                const uint32_t aph = static_cast<uint32_t>(t / a.nacc) & 1u;
+            UnitWalk w;
+            w.init(a.n_brows, blockIdx.x, gridDim.x);
+            int nblk_next = w.nt < a.n_ntiles ? blocks_in_row(a, w.br) : 0;
+            while (w.nt < a.n_ntiles && ok) {
+                UnitWalk wn = w;
+                wn.next();
                 const int nblk = nblk_next;
-                nblk_next = blocks_of(u + gridDim.x);
-                if (!mbar_wait(acce_bar(b), aph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
+                nblk_next = wn.nt < a.n_ntiles ? blocks_in_row(a, wn.br) : 0;
+                if (!mbar_wait(acce_bar(acc), aph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
                 tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(b * a.bh);
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * a.bh);
                 for (int j = 0; j < nblk; ++j) {
                     if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xs = s0 + s * stage_bytes, ws = xs + a.x_bytes;
-                    for (int kk = 0; kk < ksteps; ++kk) {
-                        const uint64_t ad = smem_desc(xs + kk * 2048u, a.x_bytes / 2, 1024u, SWZ_128B);
-                        const uint64_t bd = smem_desc(ws + kk * 32u, 16u, a.w_sbo, a.w_swz);
-                        mma_f16(d, ad, bd, a.idesc, (j | kk) != 0);
-                    }
+                    const uint64_t so = static_cast<uint64_t>(static_cast<uint32_t>(s) * sdesc);
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS; ++kk)
+                        mma_f16(d, adesc0 + so + 128u * kk, bdesc0 + so + 2u * kk, a.idesc, (j | kk) != 0 ? 1u : 0u);
                     mma_commit(empty_bar(s));
                     if (++s == a.stages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
-                mma_commit(accf_bar(b));
+                mma_commit(accf_bar(acc));
+                if (++acc == a.nacc) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+                w = wn;
             }
             // Every MMA issued has completed before TMEM is released.
             mma_commit(done_bar);
@@ -207,27 +263,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // -------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const bool elected = (warp == 2 && lane == 0);  // issues the bulk stores
-        int t = 0, chunk = 0;
-        auto blocks_of = [&](int64_t uu) {
-            if (uu >= total) return 0;
-            const int brr = static_cast<int>(uu % a.n_brows);
-            return __ldg(a.row_ptr + brr + 1) - __ldg(a.row_ptr + brr);
-        };
-        int nblk_next = blocks_of(blockIdx.x);
-        for (int64_t u = blockIdx.x; u < total; u += gridDim.x, ++t) {
-            const int ntile = static_cast<int>(u / a.n_brows);
-            const int br = static_cast<int>(u % a.n_brows);
-            const int b = t % a.nacc;
-            const uint32_t aph = static_cast<uint32_t>(t / a.nacc) & 1u;
+        const bool elected = (warp == kEpiWarp0 && lane == 0);  // issues the bulk stores
+        int acc = 0, chunk = 0;
+        uint32_t aph = 0;
+        UnitWalk w;
+        w.init(a.n_brows, blockIdx.x, gridDim.x);
+        int nblk_next = w.nt < a.n_ntiles ? blocks_in_row(a, w.br) : 0;
+        while (w.nt < a.n_ntiles) {
+            UnitWalk wn = w;
+            wn.next();
             const int nblk = nblk_next;
-            nblk_next = blocks_of(u + gridDim.x);
-            if (!mbar_wait(accf_bar(b), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
+            nblk_next = wn.nt < a.n_ntiles ? blocks_in_row(a, wn.br) : 0;
+            if (!mbar_wait(accf_bar(acc), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
             tc_fence_after();
-            const int64_t n = static_cast<int64_t>(ntile) * kTokens + q * 32 + lane;
+            const int64_t n = static_cast<int64_t>(w.nt) * kTokens + q * 32 + lane;
             const bool live = n < a.N;
-            float* crow = a.C + static_cast<int64_t>(br) * a.bh * a.ldc + n;
-            const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * a.bh);
+            float* crow = a.C + static_cast<int64_t>(w.br) * a.bh * a.ldc + n;
+            const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.bh);
             // 64 accumulator columns (C rows) per TMEM round trip
             for (int c0 = 0; c0 < a.bh; c0 += 64, ++chunk) {
                 uint32_t v[4][16];
@@ -246,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (c0 + 64 >= a.bh) {  // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(b));
+                    if (lane == 0) mbar_arrive(acce_bar(acc));
                 }
                 if (a.cbuf_off) {
                     // stage rows c0 .. c0+63 of the unit as [row][token] and bulk-store them
@@ -263,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     named_barrier(1, 128);
                     if (elected) {
-                        tma_store_2d(&tmC, smem_u32(st), ntile * kTokens, br * a.bh + c0);
+                        tma_store_2d(&tmC, smem_u32(st), w.nt * kTokens, w.br * a.bh + c0);
                         bulk_commit();
                     }
                 } else if (live) {
@@ -276,13 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                 }
             }
+            if (++acc == a.nacc) {
+                acc = 0;
+                aph ^= 1u;
+            }
+            w = wn;
         }
         if (elected) bulk_wait<0>();  // every bulk store has completed before the CTA exits
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, a.tmem_cols);
     }
@@ -306,10 +363,24 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
                                              static_cast<size_t>(A->M), stream));
     }
     const int bh = A->bh, bw = A->bw;
+    const int64_t n_brows = A->M / bh, n_ntiles = (N + kTokens - 1) / kTokens;
+    // unit indices and TMA coordinates (tokens, C rows) are 32-bit
+    if (n_brows * n_ntiles >= (int64_t(1) << 31) - dev->sms || n_ntiles * kTokens >= (int64_t(1) << 31) ||
+        A->M >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    // B tile: one 3-D box {64 tokens, bw rows, 2 halves} when whole 64-token
+    // halves tile N (a ragged half would read past the row), else two 2-D boxes.
     CUtensorMap tmB, tmW;
-    if (!encode_tmap_2d(&tmB, half_type(A->dtype), B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
-                        static_cast<uint64_t>(ldb) * 2, 64, static_cast<uint32_t>(bw),
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    bool x3d = false;
+    if (N % 64 == 0) {
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(A->K), static_cast<uint64_t>(N / 64)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2, 128};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(bw), 2};
+        x3d = encode_tmap_3d(&tmB, half_type(A->dtype), B, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!x3d && !encode_tmap_2d(&tmB, half_type(A->dtype), B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+                                static_cast<uint64_t>(ldb) * 2, 64, static_cast<uint32_t>(bw),
+                                CU_TENSOR_MAP_SWIZZLE_128B))
         return SPMM_ERR_CUDA;
     const CUtensorMapSwizzle wswz = bw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : bw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -325,10 +396,11 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
     a.C = C;
     a.ldc = ldc;
     a.N = N;
-    a.n_brows = static_cast<int32_t>(A->M / bh);
-    a.n_ntiles = static_cast<int32_t>((N + kTokens - 1) / kTokens);
+    a.n_brows = static_cast<int32_t>(n_brows);
+    a.n_ntiles = static_cast<int32_t>(n_ntiles);
     a.bh = bh;
     a.bw = bw;
+    a.x3d = x3d ? 1 : 0;
     a.x_bytes = static_cast<uint32_t>(bw) * 256u;
     a.w_bytes = (static_cast<uint32_t>(bh * bw * 2) + 1023u) & ~1023u;
     a.nacc = bh <= 128 ? 4 : 2;
@@ -353,16 +425,25 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
     const int fixed = 1024 + 8 * (2 * 8 + 2 * 4 + 1) + 16 + cbuf + (tma_c ? 1024 : 0);  // + staging alignment
     int stages = (max_smem - fixed) / static_cast<int>(stage_bytes);
     stages = stages > 8 ? 8 : stages;
+    stages &= ~1;  // the two producers own alternate slots
     if (stages < 2) return SPMM_ERR_UNSUPPORTED;
     a.stages = stages;
     const int bar_bytes = 8 * (2 * stages + 2 * a.nacc + 1) + 16;
     a.cbuf_off = tma_c ? static_cast<uint32_t>((stages * stage_bytes + bar_bytes + 1023) & ~1023u) : 0u;
     const int smem = 1024 + (tma_c ? static_cast<int>(a.cbuf_off) + cbuf : stages * static_cast<int>(stage_bytes) + bar_bytes);
-    if (!set_smem_attr_once(reinterpret_cast<const void*>(bcsr_spmm_kernel), max_smem, 0)) return SPMM_ERR_CUDA;
-    const int64_t units = static_cast<int64_t>(a.n_brows) * a.n_ntiles;
+    const void* kern = bw == 64 ? reinterpret_cast<const void*>(bcsr_spmm_kernel<4>)
+                     : bw == 32 ? reinterpret_cast<const void*>(bcsr_spmm_kernel<2>)
+                                : reinterpret_cast<const void*>(bcsr_spmm_kernel<1>);
+    if (!set_smem_attr_once(kern, max_smem, bw == 64 ? 0 : bw == 32 ? 6 : 7)) return SPMM_ERR_CUDA;
+    const int64_t units = n_brows * n_ntiles;
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_BCSR, stream);
-    bcsr_spmm_kernel<<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+    if (bw == 64)
+        bcsr_spmm_kernel<4><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+    else if (bw == 32)
+        bcsr_spmm_kernel<2><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+    else
+        bcsr_spmm_kernel<1><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_BCSR, stream);
     return cuda_status(e);

@@ -28,6 +28,11 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base
                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                     CUtensorMapSwizzle swizzle);
 
+// 3-D tiled tensor map: dims[0] contiguous, byte strides of dims 1 and 2, box
+// of box[0] x box[1] x box[2] elements.  Returns false if the driver rejects it.
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, const uint64_t dims[3],
+                    const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle);
+
 inline spmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
