@@ -7,21 +7,24 @@
 // into shared memory) and the 2:4 pattern executes inside the sparse tensor
 // core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
 //
-// Roles (320 threads, one CTA per SM, persistent over 128 x 128 output tiles):
-//   warp 0     producer: per 128-wide dense-K step, TMA loads of the compressed A
-//              tile (128 x 64, K-major, 128B swizzle), its metadata (128 x 16 B)
-//              and, for 2:4, the B tile (128 K-rows x 128 columns, MN-major,
-//              128B swizzle).
-//   warp 1     MMA issuer: four sparse MMAs per stage (M=128, N=128, K=32 dense
-//              each), then tcgen05.commit frees the stage.
-//   warps 2-5  metadata warps (one per TMEM lane quarter): for TVW they first
+// Roles (352 threads, one CTA per SM, persistent over 128 x 128 output tiles):
+//   warps 0-1  producers, taking alternate stages of one ring: per 128-wide
+//              dense-K step, TMA loads of the compressed A tile (128 x 64,
+//              K-major, 128B swizzle), its metadata (128 x 16 B) and, for 2:4,
+//              the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle; one
+//              3-D box for both 64-column halves when N is a multiple of 64).  A
+//              single issuing thread moves ~70 B/clk, less than a stage needs.
+//   warp 2     MMA issuer: four sparse MMAs per stage (M=128, N=128, K=32 dense
+//              each), then tcgen05.commit frees the stage.  Descriptors are built
+//              once and only offset per stage and K step.
+//   warps 3-6  metadata warps (one per TMEM lane quarter): for TVW they first
 //              gather the stage's kept B rows (32 rows each) with 16-byte cp.async
 //              copies into the swizzled tile, zero-filling rows past the tile's kept
 //              count (far more requests in flight than TMA gather4 of 4 x 128-byte
 //              rows gave); then they rewrite the stage's stored metadata into the
 //              tensor core's order (below) and tcgen05.st it to TMEM (one
 //              8-column-aligned column per MMA).
-//   warps 6-9  epilogue: tcgen05.ld the accumulator and write C.
+//   warps 7-10 epilogue: tcgen05.ld the accumulator and write C.
 //
 // Metadata order in TMEM (measured on the device for kind::f16, M = 128,
 // selector 0): within each 16-row block, TMEM lane l (l < 8) holds in its low
@@ -47,7 +50,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
+constexpr int kProducers = 2;
+constexpr int kMmaWarp = kProducers;
+constexpr int kMetaWarp0 = kProducers + 1;
+constexpr int kEpiWarp0 = kMetaWarp0 + 4;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int BM = 128, BN = 128, KS = 128;                 // KS: dense K per stage
 constexpr uint32_t A_BYTES = BM * (KS / 2) * 2;             // 16 KB
 constexpr uint32_t B_BYTES = KS * BN * 2;                   // 32 KB: two 64-column chunks
@@ -76,6 +83,7 @@ struct SpArgs {
     void* C;
     int64_t ldc;
     uint32_t idesc;
+    int32_t b3d;              // 2:4: B tile as one 3-D box (both halves)
     int32_t vec_ok;           // C rows 16-byte aligned
     int* err;
     uint64_t timeout_ns;
@@ -83,8 +91,9 @@ struct SpArgs {
 
 // Output tiles are visited N-fastest: the CTAs resident at one time share a few
 // row tiles of A and sweep all of B, which stays resident in L2.
-__device__ __forceinline__ int tile_m(const SpArgs& a, int64_t u) { return static_cast<int>(u / a.n_ntiles); }
-__device__ __forceinline__ int tile_n(const SpArgs& a, int64_t u) { return static_cast<int>(u % a.n_ntiles); }
+// Tile indices fit in 32 bits (checked on the host).
+__device__ __forceinline__ int tile_m(const SpArgs& a, int u) { return u / a.n_ntiles; }
+__device__ __forceinline__ int tile_n(const SpArgs& a, int u) { return u % a.n_ntiles; }
 
 __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int& kt, bool gather) {
     if (gather) {
@@ -136,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmMeta);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tslot), TMEM_COLS);
         tmem_relinquish();
     }
@@ -144,21 +153,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int64_t total = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
+    const int total = a.n_mtiles * a.n_ntiles;
     constexpr int CH = INT_EXACT ? INT_CHUNK_STEPS : (1 << 30);
 
-    if (warp == 0) {
-        // -------------------------------------------------------- producer
-        int s = 0;
+    if (warp < kProducers) {
+        // -------------------------------------------------------- producers
+        // Both warps walk every (tile, K step); producer p issues the steps whose
+        // position in that sequence has parity p, into its own slots s % 2 == p.
+        const int p = warp;
+        constexpr int OWN = STAGES / 2;
+        int s = p;
         uint32_t ph = 0;
-        int64_t issued = 0;
+        int armed = 0;
+        bool mine = (p == 0);
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
             const int mt = tile_m(a, u), nt = tile_n(a, u);
             const int m0 = mt * BM, n0 = nt * BN;
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
-            for (int ks = 0; ks < nk; ++ks) {
+            // this producer's steps of the tile: ks = first, first + 2, ...
+            const int first = mine ? 0 : 1;
+            mine = ((nk & 1) == 0) ? mine : !mine;
+            for (int ks = first; ks < nk; ks += 2) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                     ok = false;
                     break;
@@ -168,30 +185,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0);
                     tma_load_2d(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0);
                     if (!GATHER) {
-                        tma_load_2d(b_s(s), &tmB, full_bar(s), n0, ks * KS);
-                        tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, ks * KS);
+                        if (a.b3d) {
+                            tma_load_3d(b_s(s), &tmB, full_bar(s), 0, ks * KS, n0 / 64);
+                        } else {
+                            tma_load_2d(b_s(s), &tmB, full_bar(s), n0, ks * KS);
+                            tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, ks * KS);
+                        }
                     }
                 }
-                ++issued;
-                if (++s == STAGES) {
-                    s = 0;
+                if (armed < OWN) ++armed;
+                s += 2;
+                if (s >= STAGES) {
+                    s -= STAGES;
                     ph ^= 1u;
                 }
             }
         }
-        // Leave no copy in flight: wait for the last phase armed on each slot.
-        for (int i = 0; i < STAGES && i < issued; ++i) {
-            const int slot = (s - 1 - i + 2 * STAGES) % STAGES;
-            const uint32_t par = (slot < s) ? ph : (ph ^ 1u);
-            mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        // Leave no copy in flight: wait for the last phase armed on each own slot.
+        for (int i = 0; i < armed; ++i) {
+            int idx = (s - p) / 2 - 1 - i;
+            uint32_t par = ph;
+            if (idx < 0) {
+                idx += OWN;
+                par ^= 1u;
+            }
+            mbar_wait(full_bar(2 * idx + p), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            // stage 0 descriptors; stage s adds s * STAGE_BYTES, MMA i adds 32 B
+            // (A: 16 stored K elements) or 4 KB (B: 32 K rows), in 16-byte units
+            const uint64_t adesc0 = smem_desc(a_s(0), 16u, 1024u, SWZ_128B);
+            const uint64_t bdesc0 = smem_desc(b_s(0), B_CHUNK, 1024u, SWZ_128B);
             int s = 0, acc_i = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
                 const int mt = tile_m(a, u);
                 int kb, kt;
                 const int nk = tile_steps(a, mt, kb, kt, GATHER);
@@ -215,12 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         if (GATHER) fence_proxy_async_smem();  // B rows arrived through cp.async
                         const uint32_t mcol = tmem + META_COL + META_STRIDE * 4u * s;
+                        const uint64_t so = static_cast<uint64_t>(static_cast<uint32_t>(s) * (STAGE_BYTES >> 4));
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint64_t ad = smem_desc(a_s(s) + 32u * i, 16u, 1024u, SWZ_128B);
-                            const uint64_t bd = smem_desc(b_s(s) + 4096u * i, B_CHUNK, 1024u, SWZ_128B);
-                            mma_sp_f16(d, ad, bd, mcol + META_STRIDE * i, a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
-                        }
+                        for (int i = 0; i < 4; ++i)
+                            mma_sp_f16(d, adesc0 + so + 2u * i, bdesc0 + so + 256u * i, mcol + META_STRIDE * i, a.idesc,
+                                       (ks > k_lo || i > 0) ? 1u : 0u);
                         mma_commit(empty_bar(s));
                         if (++s == STAGES) {
                             s = 0;
@@ -233,11 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(done_bar);
             mbar_wait(done_bar, 0, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
         }
-    } else if (warp < 6) {
+    } else if (warp < kEpiWarp0) {
         // -------------------------------------------------------- metadata warps
         const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q+31 of the tile
         const int row = 32 * q + lane;
-        const int gq = warp - 2;  // TVW: this warp gathers kept rows 32gq .. 32gq+31 of each step
+        const int gq = warp - kMetaWarp0;  // TVW: this warp gathers kept rows 32gq .. 32gq+31 of each step
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + META_COL;
         const T16* Bp = static_cast<const T16*>(a.B);
         int s = 0;
@@ -245,29 +274,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         // Steps are visited as a flat sequence of (tile, k-step); for TVW this lane's
         // kept-row index of the next step is loaded one step ahead.
-        int64_t u = blockIdx.x;
-        int ks = 0, kb = 0, kt = 0, nk = 0;
+        int u = blockIdx.x;
+        int ks = 0, kb = 0, kt = 0, nk = 0, mt = 0, nt = 0;
         while (u < total) {
-            nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
+            mt = tile_m(a, u);
+            nk = tile_steps(a, mt, kb, kt, GATHER);
             if (nk > 0) break;
             u += gridDim.x;
         }
+        nt = u < total ? tile_n(a, u) : 0;
         auto kept_row = [&](int kb_, int kt_, int ks_) {
             const int k = ks_ * KS + 32 * gq + lane;
             return k < kt_ ? __ldg(a.cols + kb_ + k) : -1;
         };
         int32_t rnext = (GATHER && u < total) ? kept_row(kb, kt, 0) : -1;
         while (u < total && ok) {
-            const int mt = tile_m(a, u), nt = tile_n(a, u);
+            const int cmt = mt, cnt = nt;  // this step's tile
             const int32_t rcur = rnext;
             if (++ks >= nk) {
                 ks = 0;
                 u += gridDim.x;
                 while (u < total) {
-                    nk = tile_steps(a, tile_m(a, u), kb, kt, GATHER);
+                    mt = tile_m(a, u);
+                    nk = tile_steps(a, mt, kb, kt, GATHER);
                     if (nk > 0) break;
                     u += gridDim.x;
                 }
+                nt = u < total ? tile_n(a, u) : 0;
             }
             if (GATHER && u < total) rnext = kept_row(kb, kt, ks);
             if (GATHER) {
@@ -281,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rcur >= 0 && !in_b) atomicOr(a.err, SPMM_DEVERR_INDEX);
                 const int32_t myrow = in_b ? rcur : -1;
                 const int gi = lane & 7;
-                const int64_t n0 = static_cast<int64_t>(nt) * BN;
+                const int64_t n0 = static_cast<int64_t>(cnt) * BN;
 #pragma unroll
                 for (int it = 0; it < 16; ++it) {
                     const int cr = 4 * it + (lane >> 3);  // (row, chunk) pair within the warp's rows
@@ -302,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const bool row_live = static_cast<int64_t>(mt) * BM + row < a.M;
+            const bool row_live = static_cast<int64_t>(cmt) * BM + row < a.M;
             const uint8_t* mc = smem + s * STAGE_BYTES + A_BYTES + B_BYTES;
             uint4 w = *reinterpret_cast<const uint4*>(mc + 16 * row);
             // rows past M arrive zero-filled; give them the valid (0, 1) pattern
@@ -327,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- epilogue
         const int q = warp & 3;
         int acc_i = 0;
-        for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const int mt = tile_m(a, u), nt = tile_n(a, u);
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
@@ -405,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -444,6 +477,7 @@ spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const 
     auto kern = sparse_spmm_kernel<GATHER, INT_EXACT>;
     if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), SMEM_BYTES, slot)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
+    if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_SPARSE, stream);
     kern<<<grid, kThreads, SMEM_BYTES, stream>>>(tmA, tmM, tmB, a);
@@ -491,15 +525,25 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
         bld = np;
     }
     CUtensorMap tmA, tmM, tmB;
+    // B tile: one 3-D box {64 columns, 128 K rows, 2 halves} when whole 64-column
+    // halves tile N (a ragged half would read past the row), else two 2-D boxes.
+    bool b3d = false;
+    if (N % 64 == 0) {
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(A->K), static_cast<uint64_t>(N / 64)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(bld) * 2, 128};
+        const uint32_t box[3] = {64, 128, 2};
+        b3d = encode_tmap_3d(&tmB, t, bsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (!encode_tmap_2d(&tmA, t, vals, static_cast<uint64_t>(A->K / 2), static_cast<uint64_t>(A->M),
                         static_cast<uint64_t>(A->K), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->meta, static_cast<uint64_t>(A->K / 8),
                         static_cast<uint64_t>(A->M), static_cast<uint64_t>(A->K / 8), 16, 128,
                         CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tmap_2d(&tmB, t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
-                        static_cast<uint64_t>(bld) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        (!b3d && !encode_tmap_2d(&tmB, t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+                                 static_cast<uint64_t>(bld) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
         return SPMM_ERR_CUDA;
     SpArgs a{};
+    a.b3d = b3d ? 1 : 0;
     a.M = A->M;
     a.N = N;
     a.K = A->K;
