@@ -7,7 +7,8 @@
 // into shared memory) and the 2:4 pattern executes inside the sparse tensor
 // core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
 //
-// Roles (352 threads, one CTA per SM, persistent over 128 x 128 output tiles):
+// Roles (one CTA per SM, persistent over 128 x 128 output tiles; 352 threads for
+// 2:4, 480 for TVW):
 //   warps 0-1  producers, taking alternate stages of one ring: per 128-wide
 //              dense-K step, TMA loads of the compressed A tile (128 x 64,
 //              K-major, 128B swizzle), its metadata (128 x 16 B) and, for 2:4,
@@ -17,14 +18,16 @@
 //   warp 2     MMA issuer: four sparse MMAs per stage (M=128, N=128, K=32 dense
 //              each), then tcgen05.commit frees the stage.  Descriptors are built
 //              once and only offset per stage and K step.
-//   warps 3-6  metadata warps (one per TMEM lane quarter): for TVW they first
-//              gather the stage's kept B rows (32 rows each) with 16-byte cp.async
-//              copies into the swizzled tile, zero-filling rows past the tile's kept
-//              count (far more requests in flight than TMA gather4 of 4 x 128-byte
-//              rows gave); then they rewrite the stage's stored metadata into the
-//              tensor core's order (below) and tcgen05.st it to TMEM (one
-//              8-column-aligned column per MMA).
-//   warps 7-10 epilogue: tcgen05.ld the accumulator and write C.
+//   warps 3-6  metadata warps (one per TMEM lane quarter): they rewrite each
+//              stage's stored metadata into the tensor core's order (below) and
+//              tcgen05.st it to TMEM (one 8-column-aligned column per MMA).  For
+//              TVW, warps 3-10 gather the stage's kept B rows (16 rows each) with
+//              16-byte cp.async copies into the swizzled tile, zero-filling rows
+//              past the tile's kept count, two steps ahead of the metadata rewrite
+//              (far more requests in flight than TMA gather4 of 4 x 128-byte rows
+//              gave; copy issue, not bandwidth, bounds the gather, hence eight
+//              warps).
+//   last four  epilogue: tcgen05.ld the accumulator and write C.
 //
 // Metadata order in TMEM (measured on the device for kind::f16, M = 128,
 // selector 0): within each 16-row block, TMEM lane l (l < 8) holds in its low
@@ -53,8 +56,10 @@ using namespace ptx;
 constexpr int kProducers = 2;
 constexpr int kMmaWarp = kProducers;
 constexpr int kMetaWarp0 = kProducers + 1;
-constexpr int kEpiWarp0 = kMetaWarp0 + 4;
-constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+// TVW runs eight gathering warps (the first four also rewrite metadata); 2:4 runs four.
+__host__ __device__ constexpr int gather_warps(bool gather) { return gather ? 8 : 4; }
+__host__ __device__ constexpr int epi_warp0(bool gather) { return kMetaWarp0 + gather_warps(gather); }
+__host__ __device__ constexpr int threads_for(bool gather) { return 32 * (epi_warp0(gather) + 4); }
 constexpr int BM = 128, BN = 128, KS = 128;                 // KS: dense K per stage
 constexpr uint32_t A_BYTES = BM * (KS / 2) * 2;             // 16 KB
 constexpr uint32_t B_BYTES = KS * BN * 2;                   // 32 KB: two 64-column chunks
@@ -107,7 +112,7 @@ __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int&
 }
 
 template <bool GATHER, bool INT_EXACT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(GATHER), 1)
     sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
                        const __grid_constant__ CUtensorMap tmB, const SpArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -115,6 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr int kGatherWarps = gather_warps(GATHER);
+    constexpr int kEpiWarp0 = epi_warp0(GATHER);
+    constexpr int kRowsPerWarp = KS / kGatherWarps;  // TVW: kept rows each gathering warp copies per step
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
     // stage s: [A | B chunk 0 | B chunk 1 | stored metadata]
     auto a_s = [&](int s) { return s0 + s * STAGE_BYTES; };
@@ -129,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), GATHER ? 129 : 1);  // TVW: + one cp.async arrival per metadata-warp lane
+            mbar_init(full_bar(s), GATHER ? 1 + 32 * kGatherWarps : 1);  // TVW: + one cp.async arrival per gathering lane
             mbar_init(mready_bar(s), 4);
             mbar_init(empty_bar(s), 1);
         }
@@ -266,77 +274,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- metadata warps
         const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q+31 of the tile
         const int row = 32 * q + lane;
-        const int gq = warp - kMetaWarp0;  // TVW: this warp gathers kept rows 32gq .. 32gq+31 of each step
+        const int gq = warp - kMetaWarp0;  // TVW: this warp gathers kept rows kRowsPerWarp * gq + [0, kRowsPerWarp)
+        const bool writes_meta = gq < 4;    // one metadata warp per TMEM lane quarter
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + META_COL;
-        const T16* Bp = static_cast<const T16*>(a.B);
+        bool ok = true;
+        // Walk over the flat sequence of (tile, K step), skipping tiles without steps.
+        struct Walk {
+            int u, ks, nk, kb, kt, mt, nt;
+        };
+        auto seek = [&](Walk& w, int u0) {
+            w.u = u0;
+            w.ks = 0;
+            while (w.u < total) {
+                w.mt = tile_m(a, w.u);
+                w.nk = tile_steps(a, w.mt, w.kb, w.kt, GATHER);
+                if (w.nk > 0) break;
+                w.u += gridDim.x;
+            }
+            w.nt = w.u < total ? tile_n(a, w.u) : 0;
+        };
+        auto advance = [&](Walk& w) {
+            if (++w.ks >= w.nk) seek(w, w.u + gridDim.x);
+        };
+        Walk m;
+        seek(m, blockIdx.x);
         int s = 0;
         uint32_t ph = 0;
-        bool ok = true;
-        // Steps are visited as a flat sequence of (tile, k-step); for TVW this lane's
-        // kept-row index of the next step is loaded one step ahead.
-        int u = blockIdx.x;
-        int ks = 0, kb = 0, kt = 0, nk = 0, mt = 0, nt = 0;
-        while (u < total) {
-            mt = tile_m(a, u);
-            nk = tile_steps(a, mt, kb, kt, GATHER);
-            if (nk > 0) break;
-            u += gridDim.x;
-        }
-        nt = u < total ? tile_n(a, u) : 0;
-        auto kept_row = [&](int kb_, int kt_, int ks_) {
-            const int k = ks_ * KS + 32 * gq + lane;
-            return k < kt_ ? __ldg(a.cols + kb_ + k) : -1;
-        };
-        int32_t rnext = (GATHER && u < total) ? kept_row(kb, kt, 0) : -1;
-        while (u < total && ok) {
-            const int cmt = mt, cnt = nt;  // this step's tile
-            const int32_t rcur = rnext;
-            if (++ks >= nk) {
-                ks = 0;
-                u += gridDim.x;
-                while (u < total) {
-                    mt = tile_m(a, u);
-                    nk = tile_steps(a, mt, kb, kt, GATHER);
-                    if (nk > 0) break;
-                    u += gridDim.x;
-                }
-                nt = u < total ? tile_n(a, u) : 0;
+        // Rewrite the stored metadata of walker m's step into the tensor core's
+        // order and place it in TMEM (one 8-aligned column per MMA).
+        auto meta_step = [&]() -> bool {
+            const int cmt = m.mt;
+            const int slot = s;
+            const uint32_t par = ph;
+            advance(m);
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
             }
-            if (GATHER && u < total) rnext = kept_row(kb, kt, ks);
-            if (GATHER) {
-                // gather this warp's 32 kept rows of B (two 64-column chunks each) into the
-                // stage's swizzled MN-major tile; rows past the kept count are zero-filled
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
-                    ok = false;
-                    break;
-                }
-                const bool in_b = rcur >= 0 && rcur < a.b_rows;
-                if (rcur >= 0 && !in_b) atomicOr(a.err, SPMM_DEVERR_INDEX);
-                const int32_t myrow = in_b ? rcur : -1;
-                const int gi = lane & 7;
-                const int64_t n0 = static_cast<int64_t>(cnt) * BN;
-#pragma unroll
-                for (int it = 0; it < 16; ++it) {
-                    const int cr = 4 * it + (lane >> 3);  // (row, chunk) pair within the warp's rows
-                    const int lr = cr >> 1, h = cr & 1;
-                    const int32_t brow = __shfl_sync(0xffffffffu, myrow, lr);
-                    const int k = 32 * gq + lr;
-                    const int64_t col = n0 + 64 * h + 8 * gi;
-                    const int64_t left = a.N - col;
-                    const uint32_t nbytes =
-                        (brow < 0 || left <= 0) ? 0u : (left >= 8 ? 16u : static_cast<uint32_t>(left) * 2u);
-                    const T16* src = nbytes ? Bp + static_cast<int64_t>(brow) * a.ldb + col : Bp;
-                    cp_async16(b_s(s) + h * B_CHUNK + k * 128u + (static_cast<uint32_t>(gi ^ (k & 7)) << 4), src,
-                               nbytes);
-                }
-                cp_async_arrive_noinc(full_bar(s));
-            }
-            if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
-                ok = false;
-                break;
-            }
+            if (!mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
             const bool row_live = static_cast<int64_t>(cmt) * BM + row < a.M;
-            const uint8_t* mc = smem + s * STAGE_BYTES + A_BYTES + B_BYTES;
+            const uint8_t* mc = smem + slot * STAGE_BYTES + A_BYTES + B_BYTES;
             uint4 w = *reinterpret_cast<const uint4*>(mc + 16 * row);
             // rows past M arrive zero-filled; give them the valid (0, 1) pattern
             if (!row_live) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
@@ -345,16 +322,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) {
                 const uint32_t p = __shfl_xor_sync(0xffffffffu, in[i], 8);
                 const uint32_t o = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
-                tmem_st1(tl + META_STRIDE * (4u * s + i), o);
+                tmem_st1(tl + META_STRIDE * (4u * slot + i), o);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(mready_bar(s));
-            if (++s == STAGES) {
-                s = 0;
-                ph ^= 1u;
+            if (lane == 0) mbar_arrive(mready_bar(slot));
+            return true;
+        };
+        if constexpr (GATHER) {
+            // TVW: these warps also gather the kept rows of B into each stage's
+            // swizzled MN-major tile with 16-byte cp.async copies, GATHER_AHEAD steps
+            // ahead of the metadata rewrite so that several stages of gathers are in
+            // flight (the rewrite of a step waits for that step's copies to land).
+            // Walker g leads m; this lane's kept-row index for g's step is loaded
+            // one step ahead of its use.
+            const T16* Bp = static_cast<const T16*>(a.B);
+            const int gi = lane & 7;                 // 16-byte piece within a 128-byte chunk row
+            const int hi = lane >> 4;                // row parity within an iteration's pair of rows
+            const uint32_t hoff = ((lane >> 3) & 1) * B_CHUNK;
+            Walk g = m;
+            int sg = 0;
+            uint32_t phg = 0;
+            auto kept_row = [&](const Walk& w) {
+                const int k = w.ks * KS + kRowsPerWarp * gq + lane;
+                return (w.u < total && lane < kRowsPerWarp && k < w.kt) ? __ldg(a.cols + w.kb + k) : -1;
+            };
+            int32_t rnext = kept_row(g);
+            auto gather_step = [&]() -> bool {
+                const int32_t rcur = rnext;
+                const int64_t n0 = static_cast<int64_t>(g.nt) * BN;
+                const int slot = sg;
+                const uint32_t par = phg ^ 1u;
+                advance(g);
+                rnext = kept_row(g);
+                if (++sg == STAGES) {
+                    sg = 0;
+                    phg ^= 1u;
+                }
+                if (!mbar_wait(empty_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
+                const bool in_b = rcur >= 0 && rcur < a.b_rows;
+                if (rcur >= 0 && !in_b) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                const int32_t myrow = in_b ? rcur : -1;
+                const int64_t col = n0 + 64 * ((lane >> 3) & 1) + 8 * gi;  // this lane's first column
+                const int64_t left = a.N - col;
+                const uint32_t nb_full = left >= 8 ? 16u : (left > 0 ? static_cast<uint32_t>(left) * 2u : 0u);
+                const uint32_t dst0 = b_s(slot) + hoff;
+#pragma unroll
+                for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+                    const int lr = 2 * it + hi;  // row within the warp's kept rows
+                    const int32_t brow = __shfl_sync(0xffffffffu, myrow, lr);
+                    const int k = kRowsPerWarp * gq + lr;
+                    const uint32_t nbytes = brow < 0 ? 0u : nb_full;
+                    const T16* src = nbytes ? Bp + static_cast<int64_t>(brow) * a.ldb + col : Bp;
+                    cp_async16(dst0 + k * 128u + (static_cast<uint32_t>(gi ^ (k & 7)) << 4), src, nbytes);
+                }
+                cp_async_arrive_noinc(full_bar(slot));
+                return true;
+            };
+            constexpr int GATHER_AHEAD = 2;  // < STAGES: the step a gather waits on is already rewritten
+            if (writes_meta) {
+                for (int i = 0; i < GATHER_AHEAD && ok && g.u < total; ++i) ok = gather_step();
+                while (ok && m.u < total) {
+                    if (g.u < total && !gather_step()) break;
+                    ok = meta_step();
+                }
+            } else {
+                while (ok && g.u < total) ok = gather_step();
             }
+        } else {
+            while (ok && m.u < total) ok = meta_step();
         }
     } else {
         // -------------------------------------------------------- epilogue
@@ -480,7 +517,7 @@ spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const 
     if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_SPARSE, stream);
-    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(tmA, tmM, tmB, a);
+    kern<<<grid, threads_for(GATHER), SMEM_BYTES, stream>>>(tmA, tmM, tmB, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_SPARSE, stream);
     return cuda_status(e);
