@@ -94,11 +94,22 @@ struct SpArgs {
     uint64_t timeout_ns;
 };
 
-// Output tiles are visited N-fastest: the CTAs resident at one time share a few
-// row tiles of A and sweep all of B, which stays resident in L2.
+// Output tiles are visited in groups of kGroupN column tiles, row-tile major
+// inside a group: the CTAs resident at one time share ~152 / kGroupN row tiles
+// of A and the group's column slab of B, which stays in L2 while every row tile
+// passes (A is streamed with an evict-first hint).  Visiting all column tiles of
+// a row tile at once instead needs all of B per wave, and the C writes evict it.
 // Tile indices fit in 32 bits (checked on the host).
-__device__ __forceinline__ int tile_m(const SpArgs& a, int u) { return u / a.n_ntiles; }
-__device__ __forceinline__ int tile_n(const SpArgs& a, int u) { return u % a.n_ntiles; }
+constexpr int kGroupN = 16;
+__device__ __forceinline__ void tile_of(const SpArgs& a, int u, int& mt, int& nt) {
+    const int per_group = a.n_mtiles * kGroupN;
+    const int g = u / per_group;
+    const int r = u - g * per_group;
+    const int rest = a.n_ntiles - g * kGroupN;
+    const int gw = rest < kGroupN ? rest : kGroupN;  // the last group may be narrower
+    mt = r / gw;
+    nt = g * kGroupN + (r - (r / gw) * gw);
+}
 
 __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int& kt, bool gather) {
     if (gather) {
@@ -174,9 +185,11 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
         uint32_t ph = 0;
         int armed = 0;
         bool mine = (p == 0);
+        const uint64_t pol_stream = l2_policy_evict_first();  // A is read once per column group
         bool ok = true;
         for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-            const int mt = tile_m(a, u), nt = tile_n(a, u);
+            int mt, nt;
+            tile_of(a, u, mt, nt);
             const int m0 = mt * BM, n0 = nt * BN;
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
@@ -190,8 +203,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : TX_BYTES);
-                    tma_load_2d(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0);
-                    tma_load_2d(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0);
+                    tma_load_2d_hint(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0, pol_stream);
+                    tma_load_2d_hint(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0, pol_stream);
                     if (!GATHER) {
                         if (a.b3d) {
                             tma_load_3d(b_s(s), &tmB, full_bar(s), 0, ks * KS, n0 / 64);
@@ -230,7 +243,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                const int mt = tile_m(a, u);
+                int mt, nt;
+                tile_of(a, u, mt, nt);  // the MMA issuer needs only the row tile
                 int kb, kt;
                 const int nk = tile_steps(a, mt, kb, kt, GATHER);
                 const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
@@ -286,12 +300,11 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
             w.u = u0;
             w.ks = 0;
             while (w.u < total) {
-                w.mt = tile_m(a, w.u);
+                tile_of(a, w.u, w.mt, w.nt);
                 w.nk = tile_steps(a, w.mt, w.kb, w.kt, GATHER);
                 if (w.nk > 0) break;
                 w.u += gridDim.x;
             }
-            w.nt = w.u < total ? tile_n(a, w.u) : 0;
         };
         auto advance = [&](Walk& w) {
             if (++w.ks >= w.nk) seek(w, w.u + gridDim.x);
@@ -398,7 +411,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
         const int q = warp & 3;
         int acc_i = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const int mt = tile_m(a, u), nt = tile_n(a, u);
+            int mt, nt;
+            tile_of(a, u, mt, nt);
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
             const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
