@@ -495,27 +495,51 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     }
 }
 
-// int8 -> fp16, exact (|v| <= 127).  8 elements per thread; rows of `cols`
-// elements with leading dimensions lds (source) and ldd (destination).
-__global__ void widen_i8_kernel(const int8_t* __restrict__ src, int64_t lds, __half* __restrict__ dst, int64_t ldd,
-                                int64_t rows, int64_t cols) {
-    const int64_t per_row = (cols + 7) / 8;
-    const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (id >= rows * per_row) return;
-    const int64_t r = id / per_row, c = (id % per_row) * 8;
-    const int8_t* sp = src + r * lds + c;
-    __half* dp = dst + r * ldd + c;
-    if (c + 8 <= cols && (reinterpret_cast<uintptr_t>(sp) & 7) == 0 && (reinterpret_cast<uintptr_t>(dp) & 15) == 0) {
-        const int2 w = *reinterpret_cast<const int2*>(sp);
-        const int8_t* b = reinterpret_cast<const int8_t*>(&w);
-        __align__(16) __half h[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = __int2half_rn(b[i]);
-        *reinterpret_cast<uint4*>(dp) = *reinterpret_cast<const uint4*>(h);
+// int8 -> fp16, exact.  Four bytes become four halves without a conversion
+// instruction: flipping the sign bit gives v + 128 in [0, 255]; placed under
+// the fp16 exponent of 1024 (high byte 0x64) each half reads 1024 + v + 128,
+// and subtracting 1152 leaves v.  Every step is exact in fp16 (integers below
+// 2048 are representable).
+__device__ __forceinline__ uint2 widen4(uint32_t w) {
+    const uint32_t b = w ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(b, 0x64646464u, 0x4150);  // halves 0x64 b0, 0x64 b1
+    const uint32_t hi = __byte_perm(b, 0x64646464u, 0x4352);  // halves 0x64 b2, 0x64 b3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+    const __half2 l = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&l), *reinterpret_cast<const uint32_t*>(&h));
+}
+
+// One row-major int8 matrix to widen: rows of `cols` elements, leading
+// dimensions lds (source) and ldd (destination, columns [cols, ldd) zeroed).
+struct WidenJob {
+    const int8_t* src;
+    int64_t lds;
+    __half* dst;
+    int64_t ldd;
+    int64_t rows, cols;
+    int64_t per_row;   // threads per row: ceil(ldd / 16)
+    int64_t threads;   // rows * per_row
+};
+
+// Both operands in one launch; 16 elements (one 16-byte load) per thread.
+__global__ void widen_i8_kernel(const WidenJob j0, const WidenJob j1) {
+    int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const bool first = id < j0.threads;
+    const WidenJob& j = first ? j0 : j1;
+    if (!first) id -= j0.threads;
+    if (id >= j.threads) return;
+    const int64_t r = id / j.per_row, c = (id - r * j.per_row) * 16;
+    const int8_t* sp = j.src + r * j.lds + c;
+    __half* dp = j.dst + r * j.ldd + c;
+    if (c + 16 <= j.cols && (reinterpret_cast<uintptr_t>(sp) & 15) == 0 && (reinterpret_cast<uintptr_t>(dp) & 15) == 0) {
+        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(sp));
+        const uint2 a = widen4(w.x), b = widen4(w.y), e = widen4(w.z), f = widen4(w.w);
+        reinterpret_cast<uint4*>(dp)[0] = make_uint4(a.x, a.y, b.x, b.y);
+        reinterpret_cast<uint4*>(dp)[1] = make_uint4(e.x, e.y, f.x, f.y);
     } else {
-        for (int i = 0; i < 8 && c + i < cols; ++i) dp[i] = __int2half_rn(sp[i]);
-        for (int i = static_cast<int>(cols - c); i < 8 && c + i < ldd; ++i)
-            if (i >= 0) dp[i] = __float2half(0.f);
+        for (int i = 0; i < 16 && c + i < j.ldd; ++i)
+            dp[i] = c + i < j.cols ? __int2half_rn(sp[i]) : __float2half(0.f);
     }
 }
 
@@ -562,12 +586,16 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
         __half* wb = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) +
                                                align256(static_cast<size_t>(A->M) * (A->K / 2) * 2));
         const int64_t np = (N + 7) / 8 * 8;
-        const int64_t na = A->M * ((A->K / 2 + 7) / 8), nb = A->K * (np / 8);
+        auto job = [](const void* src, int64_t lds, __half* dst, int64_t ldd, int64_t rows, int64_t cols) {
+            WidenJob j{static_cast<const int8_t*>(src), lds, dst, ldd, rows, cols, (ldd + 15) / 16, 0};
+            j.threads = rows * j.per_row;
+            return j;
+        };
+        const WidenJob ja = job(A->vals, A->K / 2, wa, A->K / 2, A->M, A->K / 2);
+        const WidenJob jb = job(B, ldb, wb, np, A->K, N);
+        const int64_t threads = ja.threads + jb.threads;
         trace_begin(SPMM_KERNEL_WIDEN, stream);
-        widen_i8_kernel<<<static_cast<unsigned>((na + 255) / 256), 256, 0, stream>>>(
-            static_cast<const int8_t*>(A->vals), A->K / 2, wa, A->K / 2, A->M, A->K / 2);
-        widen_i8_kernel<<<static_cast<unsigned>((nb + 255) / 256), 256, 0, stream>>>(
-            static_cast<const int8_t*>(B), ldb, wb, np, A->K, N);
+        widen_i8_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(ja, jb);
         const cudaError_t e = cudaGetLastError();
         trace_end(SPMM_KERNEL_WIDEN, stream);
         if (e != cudaSuccess) return SPMM_ERR_CUDA;
