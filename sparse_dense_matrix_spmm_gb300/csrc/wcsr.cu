@@ -19,9 +19,11 @@
 // SpMM.  On the synthetic power-law workload the windows are about 6% dense
 // (uniform columns), so the contraction per window is not a dense tile: the
 // kernel runs on CUDA cores and is bound by gathering B rows (N * 2 bytes per
-// nonzero) from L2.  One CTA (8 warps) per work unit.  The CTA first stages the
+// nonzero) from L2, which is latency-bound: throughput is the bytes in flight
+// per SM over the L2 round trip, so occupancy decides it.  One CTA (4 warps,
+// 8 CTAs per SM) per work unit.  The CTA first stages the
 // unit's sparse operand in shared memory (local row, column resolved through
-// the window's column list, value), then cuts it into 8 equal chunks, one per
+// the window's column list, value), then cuts it into equal chunks, one per
 // warp.  Each warp keeps 16 B-row loads in flight, accumulates fp32 per row in
 // registers (lane = 4 columns of a 128-column slab), writes rows that lie inside its
 // chunk straight into a shared-memory tile, and hands the two rows at its
@@ -42,9 +44,10 @@ __device__ int g_wcsr_build_error;  // data-dependent builder errors (SPMM_DEVER
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;   // 8 CTAs per SM: one CTA's staging overlaps the others' gathers
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlab = 128;  // output columns per pass (4 per lane)
+static_assert(kThreads >= kSlab, "the boundary fix-up gives one thread to each slab column");
 constexpr int kMaxH = 64;   // largest window height the SpMM kernel accepts
 
 std::mutex g_mu;
@@ -342,7 +345,7 @@ __device__ __forceinline__ void wcsr_chunk(const T* B, int64_t ldb, int64_t ncol
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 4) wcsr_spmm_kernel(const WcsrArgs a) {
+__global__ void __launch_bounds__(kThreads, 8) wcsr_spmm_kernel(const WcsrArgs a) {
     extern __shared__ float sm[];
     // tile[h][kSlab] | bnd[2*kWarps][kSlab] | bnd_row[2*kWarps] | s_col[kStage+kPad] | s_pk[kStage+kPad]
     float* tile = sm;
