@@ -345,10 +345,348 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// 64-row blocks: the W block is the MMA's A operand (M = 64, K-major) and a
+// 256-token tile of B its B operand (N = 256, MN-major), so one issued MMA does
+// twice the work of the M = 128 tokens x N = 64 orientation above, whose issue
+// cost exceeds its tensor time.  An M = 64 accumulator keeps row m in TMEM lane
+// 32 * (m / 16) + m % 16 (measured on the device), i.e. lanes 0-15 of each lane
+// quarter.  C goes out through 128-byte-swizzled shared tiles and TMA stores.
+constexpr int kWideTokens = 256;
+constexpr int kWideRows = 64;
+constexpr uint32_t kWideCBuf = 2 * kWideRows * 128;  // one staging buffer: 2 boxes of 64 rows x 32 fp32
+
+template <int KSTEPS>
+__global__ void __launch_bounds__(kThreads, 1)
+    bcsr_wide_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmC, const BcsrArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t stage_bytes = a.x_bytes + a.w_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.stages * stage_bytes);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * a.stages + 2 * a.nacc + 1);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (a.stages + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * a.stages + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * a.stages + a.nacc + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * a.stages + 2 * a.nacc);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < a.nacc; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tslot), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp < kProducers) {
+        // ------------------------------------------------ TMA producers (as above)
+        const int p = warp;
+        const int own = a.stages / 2;
+        int s = p;
+        uint32_t ph = 0;
+        int armed = 0;
+        bool mine = (p == 0);
+        bool ok = true;
+        const uint32_t tx = a.x_bytes + static_cast<uint32_t>(kWideRows * a.bw * 2);
+        UnitWalk w;
+        w.init(a.n_brows, blockIdx.x, gridDim.x);
+        int j0 = 0, j1 = 0;
+        if (w.nt < a.n_ntiles) {
+            j0 = __ldg(a.row_ptr + w.br);
+            j1 = __ldg(a.row_ptr + w.br + 1);
+        }
+        while (w.nt < a.n_ntiles && ok) {
+            const int n0 = w.nt * kWideTokens;
+            const int cj0 = j0, cj1 = j1;
+            UnitWalk wn = w;
+            wn.next();
+            if (wn.nt < a.n_ntiles) {
+                j0 = __ldg(a.row_ptr + wn.br);
+                j1 = __ldg(a.row_ptr + wn.br + 1);
+            }
+            for (int jb = cj0; jb < cj1 && ok; jb += 32) {
+                const int cidx = (jb + lane < cj1) ? __ldg(a.col_idx + jb + lane) : 0;
+                const int nb = (cj1 - jb < 32) ? cj1 - jb : 32;
+                for (int t = 0; t < nb; ++t) {
+                    const int kc = __shfl_sync(0xffffffffu, cidx, t) * a.bw;
+                    if (mine) {
+                        if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            const uint32_t xs = s0 + static_cast<uint32_t>(s) * stage_bytes, ws = xs + a.x_bytes;
+                            mbar_arrive_expect_tx(full_bar(s), tx);
+                            tma_load_2d(ws, &tmW, full_bar(s), 0, (jb + t) * kWideRows);
+                            if (a.x3d) {
+                                tma_load_3d(xs, &tmB, full_bar(s), 0, kc, n0 / 64);
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < 4; ++h)
+                                    tma_load_2d(xs + h * (a.x_bytes / 4), &tmB, full_bar(s), n0 + 64 * h, kc);
+                            }
+                        }
+                        if (armed < own) ++armed;
+                        s += 2;
+                        if (s >= a.stages) {
+                            s -= a.stages;
+                            ph ^= 1u;
+                        }
+                    }
+                    mine = !mine;
+                }
+            }
+            w = wn;
+        }
+        for (int i = 0; i < armed; ++i) {
+            int idx = (s - p) / 2 - 1 - i;
+            uint32_t par = ph;
+            if (idx < 0) {
+                idx += own;
+                par ^= 1u;
+            }
+            mbar_wait(full_bar(2 * idx + p), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---------------------------------------------------- MMA issuer
+            // A = block (K-major, +32 B per K step), B = token tile (MN-major,
+            // 64-token chunks bw rows apart, +16 rows x 128 B per K step)
+            const uint64_t bdesc0 = smem_desc(s0, a.x_bytes / 4, 1024u, SWZ_128B);
+            const uint64_t adesc0 = smem_desc(s0 + a.x_bytes, 16u, a.w_sbo, a.w_swz);
+            const uint32_t sdesc = stage_bytes >> 4;
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            UnitWalk w;
+            w.init(a.n_brows, blockIdx.x, gridDim.x);
+            int nblk_next = w.nt < a.n_ntiles ? blocks_in_row(a, w.br) : 0;
+            while (w.nt < a.n_ntiles && ok) {
+                UnitWalk wn = w;
+                wn.next();
+                const int nblk = nblk_next;
+                nblk_next = wn.nt < a.n_ntiles ? blocks_in_row(a, wn.br) : 0;
+                if (!mbar_wait(acce_bar(acc), aph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kWideTokens);
+                for (int j = 0; j < nblk; ++j) {
+                    if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t so = static_cast<uint64_t>(static_cast<uint32_t>(s) * sdesc);
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS; ++kk)
+                        mma_f16(d, adesc0 + so + 2u * kk, bdesc0 + so + 128u * kk, a.idesc, (j | kk) != 0 ? 1u : 0u);
+                    mma_commit(empty_bar(s));
+                    if (++s == a.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                mma_commit(accf_bar(acc));
+                if (++acc == a.nacc) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+                w = wn;
+            }
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        // Warp q reads lane quarter q: block rows 16q .. 16q+15 in lanes 0-15.
+        // 64 tokens per round trip: 4 x 16 columns into registers, then into a
+        // staging buffer of two 128B-swizzled boxes (64 rows x 32 fp32 each),
+        // stored with two TMA stores.  Empty units write zeros.
+        const int q = warp & 3;
+        const int row = 16 * q + lane;  // meaningful for lane < 16
+        const bool elected = (warp == kEpiWarp0 && lane == 0);
+        int acc = 0, chunk = 0;
+        uint32_t aph = 0;
+        UnitWalk w;
+        w.init(a.n_brows, blockIdx.x, gridDim.x);
+        int nblk_next = w.nt < a.n_ntiles ? blocks_in_row(a, w.br) : 0;
+        while (w.nt < a.n_ntiles) {
+            UnitWalk wn = w;
+            wn.next();
+            const int nblk = nblk_next;
+            nblk_next = wn.nt < a.n_ntiles ? blocks_in_row(a, wn.br) : 0;
+            if (!mbar_wait(accf_bar(acc), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
+            tc_fence_after();
+            const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kWideTokens);
+            for (int c0 = 0; c0 < kWideTokens; c0 += 64, ++chunk) {
+                uint32_t v[4][16];
+                if (nblk > 0) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) tmem_ld16(tl + c0 + 16 * g, v[g]);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[g][i] = 0u;
+                }
+                if (c0 + 64 >= kWideTokens) {  // accumulator fully read
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                }
+                const uint32_t buf = a.cbuf_off + static_cast<uint32_t>(chunk & 1) * kWideCBuf;
+                if (elected) bulk_wait_read<1>();  // the store that last used `buf` has read it
+                named_barrier(1, 128);
+                if (lane < 16) {
+                    // box h holds tokens 32h .. 32h+31 of the chunk; row r is 128 B,
+                    // its 16-byte units XOR-swizzled by r % 8
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int h = u >> 3, uu = u & 7;
+                        const uint32_t off = buf + static_cast<uint32_t>(h) * (kWideRows * 128) +
+                                             static_cast<uint32_t>(row) * 128u +
+                                             (static_cast<uint32_t>(uu ^ (row & 7)) << 4);
+                        float4 val = make_float4(__uint_as_float(v[u >> 2][4 * (u & 3)]),
+                                                 __uint_as_float(v[u >> 2][4 * (u & 3) + 1]),
+                                                 __uint_as_float(v[u >> 2][4 * (u & 3) + 2]),
+                                                 __uint_as_float(v[u >> 2][4 * (u & 3) + 3]));
+                        *reinterpret_cast<float4*>(smem + off) = val;
+                    }
+                }
+                fence_proxy_async_smem();
+                named_barrier(1, 128);
+                if (elected) {
+                    const int tok = w.nt * kWideTokens + c0;
+                    tma_store_2d(&tmC, s0 + buf, tok, w.br * kWideRows);
+                    tma_store_2d(&tmC, s0 + buf + kWideRows * 128, tok + 32, w.br * kWideRows);
+                    bulk_commit();
+                }
+            }
+            if (++acc == a.nacc) {
+                acc = 0;
+                aph ^= 1u;
+            }
+            w = wn;
+        }
+        if (elected) bulk_wait<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
 uint32_t pow2_at_least(uint32_t x) {
     uint32_t p = 32;
     while (p < x) p <<= 1;
     return p;
+}
+
+spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                             cudaStream_t stream, const DeviceInfo* dev) {
+    const int bw = A->bw;
+    const int64_t n_brows = A->M / kWideRows, n_ntiles = (N + kWideTokens - 1) / kWideTokens;
+    if (n_brows * n_ntiles >= (int64_t(1) << 31) - dev->sms || n_ntiles * kWideTokens >= (int64_t(1) << 31) ||
+        A->M >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    // B tile: one 3-D box {64 tokens, bw rows, 4 chunks} when whole 64-token
+    // chunks tile N (a ragged chunk would read past the row), else four 2-D boxes.
+    CUtensorMap tmB, tmW, tmC;
+    bool x3d = false;
+    if (N % 64 == 0) {
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(A->K), static_cast<uint64_t>(N / 64)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2, 128};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(bw), 4};
+        x3d = encode_tmap_3d(&tmB, half_type(A->dtype), B, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!x3d && !encode_tmap_2d(&tmB, half_type(A->dtype), B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+                                static_cast<uint64_t>(ldb) * 2, 64, static_cast<uint32_t>(bw),
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPMM_ERR_CUDA;
+    const CUtensorMapSwizzle wswz = bw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : bw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!encode_tmap_2d(&tmW, half_type(A->dtype), A->vals, static_cast<uint64_t>(bw),
+                        static_cast<uint64_t>(A->nnzb) * kWideRows, static_cast<uint64_t>(bw) * 2,
+                        static_cast<uint32_t>(bw), kWideRows, wswz) ||
+        !encode_tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(ldc) * 4, 32, kWideRows,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPMM_ERR_CUDA;
+    BcsrArgs a{};
+    a.row_ptr = A->row_ptr;
+    a.col_idx = A->col_idx;
+    a.C = C;
+    a.ldc = ldc;
+    a.N = N;
+    a.n_brows = static_cast<int32_t>(n_brows);
+    a.n_ntiles = static_cast<int32_t>(n_ntiles);
+    a.bh = kWideRows;
+    a.bw = bw;
+    a.x3d = x3d ? 1 : 0;
+    a.x_bytes = static_cast<uint32_t>(bw) * 512u;  // 4 chunks of bw rows x 128 B
+    a.w_bytes = (static_cast<uint32_t>(kWideRows * bw * 2) + 1023u) & ~1023u;
+    a.nacc = 2;
+    a.tmem_cols = 2 * kWideTokens;
+    a.idesc = idesc_f16(kWideRows, kWideTokens, A->dtype == SPMM_BF16, /*a_mn_major=*/false, /*b_mn_major=*/true,
+                        /*sparse=*/false);
+    a.w_swz = bw == 64 ? SWZ_128B : bw == 32 ? SWZ_64B : SWZ_32B;
+    a.w_sbo = 8u * static_cast<uint32_t>(bw) * 2u;
+    a.err = dev->err;
+    a.timeout_ns = kWaitTimeoutNs;
+    const int max_smem = dev->max_smem_optin;
+    const uint32_t stage_bytes = a.x_bytes + a.w_bytes;
+    const int cbuf = 2 * static_cast<int>(kWideCBuf);
+    const int fixed = 1024 + 8 * (2 * 8 + 2 * 2 + 1) + 16 + cbuf + 1024;  // + staging alignment
+    int stages = (max_smem - fixed) / static_cast<int>(stage_bytes);
+    stages = stages > 8 ? 8 : stages;
+    stages &= ~1;
+    if (stages < 2) return SPMM_ERR_UNSUPPORTED;
+    a.stages = stages;
+    const int bar_bytes = 8 * (2 * stages + 2 * a.nacc + 1) + 16;
+    a.cbuf_off = static_cast<uint32_t>((stages * stage_bytes + bar_bytes + 1023) & ~1023u);
+    const int smem = 1024 + static_cast<int>(a.cbuf_off) + cbuf;
+    const void* kern = bw == 64 ? reinterpret_cast<const void*>(bcsr_wide_kernel<4>)
+                     : bw == 32 ? reinterpret_cast<const void*>(bcsr_wide_kernel<2>)
+                                : reinterpret_cast<const void*>(bcsr_wide_kernel<1>);
+    if (!set_smem_attr_once(kern, max_smem, bw == 64 ? 8 : bw == 32 ? 9 : 10)) return SPMM_ERR_CUDA;
+    const int64_t units = n_brows * n_ntiles;
+    const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
+    trace_begin(SPMM_KERNEL_BCSR, stream);
+    if (bw == 64)
+        bcsr_wide_kernel<4><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+    else if (bw == 32)
+        bcsr_wide_kernel<2><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+    else
+        bcsr_wide_kernel<1><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_BCSR, stream);
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -389,6 +727,9 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
                         static_cast<uint64_t>(A->nnzb) * bh, static_cast<uint64_t>(bw) * 2,
                         static_cast<uint32_t>(bw), static_cast<uint32_t>(bh), wswz))
         return SPMM_ERR_CUDA;
+
+    // 64-row blocks with TMA-storable C: the wide kernel (M = 64 blocks x N = 256 tokens)
+    if (bh == kWideRows && (ldc % 4 == 0) && aligned16(C)) return launch_bcsr_wide(A, B, ldb, C, ldc, N, stream, dev);
 
     BcsrArgs a{};
     a.row_ptr = A->row_ptr;

@@ -38,6 +38,10 @@ def test_bcsr_tiny_config():
     (384, 256, 300, 128, 16, 0.5, "bf16"),    # tall blocks, narrow K
     (512, 256, 64, 256, 64, 0.5, "f16"),      # bh = 256 (two accumulators)
     (128, 1024, 1000, 16, 64, 0.05, "bf16"),  # very sparse: empty block rows
+    # 64-row blocks run the 64 x 256-token kernel:
+    (512, 256, 640, 64, 32, 0.3, "f16"),      # bw = 32, whole 64-token chunks, 2.5 token tiles
+    (256, 256, 300, 64, 16, 0.4, "bf16"),     # bw = 16, ragged chunk (per-chunk loads)
+    (1024, 512, 512, 64, 64, 0.02, "bf16"),   # very sparse: empty block rows write zeros
 ])
 def test_bcsr_shapes(M, K, N, bh, bw, frac, dtype):
     nb = (M // bh) * (K // bw)
@@ -84,3 +88,22 @@ def test_bcsr_llm_full_size_sampled_columns():
     got = C[:, torch.from_numpy(cols).cuda()].cpu().numpy()
     del C
     assert_close(got, oracle.bcsr_spmm(O, p["B"], cols=cols), "bcsr_llm slice")
+
+
+def test_bcsr_64_row_blocks_padded_strides():
+    """64-row blocks with padded B and C rows (the 64 x 256-token kernel): the
+    padding columns of C stay untouched."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.bcsr_problem(384, 256, 320, 64, 64, 8, seed=11)
+    A = dev_half(p["A"], "bf16")
+    Bpad = torch.zeros((256, 336), dtype=torch.bfloat16, device="cuda")
+    Bpad[:, :320] = dev_half(p["B"], "bf16")
+    F = spmm.build_bcsr(A, 64, 64)
+    Cpad = torch.full((384, 324), -1.0, device="cuda")
+    out = spmm.spmm_bcsr(F, Bpad[:, :320], Cpad[:, :320])
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    O = oracle.bcsr_build(p["A"], 64, 64, "bf16")
+    assert_close(out.cpu().numpy(), oracle.bcsr_spmm(O, p["B"]), "64-row blocks, padded")
+    assert (Cpad[:, 320:] == -1.0).all().item()
