@@ -38,8 +38,8 @@ def test_bcsr_tiny_config():
     (384, 256, 300, 128, 16, 0.5, "bf16"),    # tall blocks, narrow K
     (512, 256, 64, 256, 64, 0.5, "f16"),      # bh = 256 (two accumulators)
     (128, 1024, 1000, 16, 64, 0.05, "bf16"),  # very sparse: empty block rows
-    # 64-row blocks run the 64 x 256-token kernel:
-    (512, 256, 640, 64, 32, 0.3, "f16"),      # bw = 32, whole 64-token chunks, 2.5 token tiles
+    # 64-row blocks run the 64-row x 192-token kernel:
+    (512, 256, 640, 64, 32, 0.3, "f16"),      # bw = 32, whole 64-token chunks, 3.3 token tiles
     (256, 256, 300, 64, 16, 0.4, "bf16"),     # bw = 16, ragged chunk (per-chunk loads)
     (1024, 512, 512, 64, 64, 0.02, "bf16"),   # very sparse: empty block rows write zeros
 ])
@@ -91,7 +91,7 @@ def test_bcsr_llm_full_size_sampled_columns():
 
 
 def test_bcsr_64_row_blocks_padded_strides():
-    """64-row blocks with padded B and C rows (the 64 x 256-token kernel): the
+    """64-row blocks with padded B and C rows (the 64-row x 192-token kernel): the
     padding columns of C stay untouched."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
