@@ -158,6 +158,13 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// Close the group of this thread's cp.async copies issued since the last commit.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Arrive on `bar` once this thread's earlier cp.async copies have landed; the
 // barrier's expected count must already include this arrival.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -73,7 +73,12 @@ constexpr uint32_t META_COL = NACC * BN;                    // metadata columns 
 constexpr uint32_t META_STRIDE = 8;                         // one aligned TMEM column per MMA
 constexpr int INT_CHUNK_STEPS = 16;                         // 16 x 128 = 2048 dense K per int chunk
 constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + M_BYTES;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+// 2:4: the metadata warps copy their rows' metadata with cp.async into a ring of
+// META_RING tile steps, META_AHEAD steps ahead (the TMA unit moved 128 separate
+// 16-byte rows per stage for it, ~6% of the kernel's time).
+constexpr int META_RING = 8, META_AHEAD = 6;
+constexpr uint32_t RING_OFF = STAGES * STAGE_BYTES;
+constexpr int SMEM_BYTES = 1024 + RING_OFF + META_RING * M_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
 
 using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
 
@@ -85,6 +90,8 @@ struct SpArgs {
     int32_t n_mtiles, n_ntiles;
     const int32_t* tile_ptr;  // TVW only
     const int32_t* cols;      // TVW only
+    const uint8_t* meta;      // 2:4: stored metadata, ldm bytes per row
+    int64_t ldm;
     void* C;
     int64_t ldc;
     uint32_t idesc;
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                        const __grid_constant__ CUtensorMap tmB, const SpArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + META_RING * M_BYTES);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int kGatherWarps = gather_warps(GATHER);
@@ -202,9 +209,9 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : TX_BYTES);
+                    mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : A_BYTES + B_BYTES);
                     tma_load_2d_hint(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0, pol_stream);
-                    tma_load_2d_hint(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0, pol_stream);
+                    if (GATHER) tma_load_2d_hint(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0, pol_stream);
                     if (!GATHER) {
                         if (a.b3d) {
                             tma_load_3d(b_s(s), &tmB, full_bar(s), 0, ks * KS, n0 / 64);
@@ -315,6 +322,24 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
         uint32_t ph = 0;
         // Rewrite the stored metadata of walker m's step into the tensor core's
         // order and place it in TMEM (one 8-aligned column per MMA).
+        // 2:4: walker f runs META_AHEAD steps ahead of m and copies this thread's
+        // row of metadata for its step into ring slot (step % META_RING); the
+        // thread later reads back only what it copied itself.
+        Walk f = m;
+        int f_step = 0;
+        auto meta_copy = [&]() {
+            const int64_t grow = static_cast<int64_t>(f.mt) * BM + row;
+            const bool live = f.u < total && grow < a.M;
+            const uint8_t* src = live ? a.meta + grow * a.ldm + static_cast<int64_t>(f.ks) * (KS / 8) : a.meta;
+            cp_async16(s0 + RING_OFF + static_cast<uint32_t>(f_step % META_RING) * M_BYTES + 16u * row, src,
+                       live ? 16u : 0u);
+            cp_async_commit();
+            ++f_step;
+            if (f.u < total) advance(f);
+        };
+        int m_step = 0;
+        if (!GATHER)
+            for (int i = 0; i < META_AHEAD; ++i) meta_copy();
         auto meta_step = [&]() -> bool {
             const int cmt = m.mt;
             const int slot = s;
@@ -324,10 +349,20 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                 s = 0;
                 ph ^= 1u;
             }
-            if (!mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
             const bool row_live = static_cast<int64_t>(cmt) * BM + row < a.M;
-            const uint8_t* mc = smem + slot * STAGE_BYTES + A_BYTES + B_BYTES;
-            uint4 w = *reinterpret_cast<const uint4*>(mc + 16 * row);
+            uint4 w;
+            if (GATHER) {
+                if (!mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
+                const uint8_t* mc = smem + slot * STAGE_BYTES + A_BYTES + B_BYTES;
+                w = *reinterpret_cast<const uint4*>(mc + 16 * row);
+            } else {
+                cp_async_wait<META_AHEAD - 1>();  // this thread's copy for this step has landed
+                w = *reinterpret_cast<const uint4*>(smem + RING_OFF + (m_step % META_RING) * M_BYTES + 16 * row);
+                ++m_step;
+                meta_copy();
+                // the MMAs that read this slot's metadata columns last time are done
+                if (!mbar_wait(empty_bar(slot), par ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
+            }
             // rows past M arrive zero-filled; give them the valid (0, 1) pattern
             if (!row_live) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
             const uint32_t in[4] = {w.x, w.y, w.z, w.w};
@@ -405,6 +440,7 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
             }
         } else {
             while (ok && m.u < total) ok = meta_step();
+            cp_async_wait<0>();  // no copy into shared memory outstanding at exit
         }
     } else {
         // -------------------------------------------------------- epilogue
@@ -632,6 +668,8 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
     a.ldc = ldc;
     a.idesc = idesc_f16(128, BN, A->dtype == SPMM_BF16, false, true, true, 0);
     a.vec_ok = (ldc % 4 == 0) && aligned16(C);
+    a.meta = static_cast<const uint8_t*>(A->meta);
+    a.ldm = A->K / 8;
     a.err = dev->err;
     a.timeout_ns = kWaitTimeoutNs;
     if (i8) return launch_sparse<false, true>(tmA, tmM, tmB, a, stream, 2);
