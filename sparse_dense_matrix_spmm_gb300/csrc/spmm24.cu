@@ -72,7 +72,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t META_COL = NACC * BN;                    // metadata columns after the accumulators
 constexpr uint32_t META_STRIDE = 8;                         // one aligned TMEM column per MMA
 constexpr int INT_CHUNK_STEPS = 16;                         // 16 x 128 = 2048 dense K per int chunk
-constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + M_BYTES;
 // 2:4: the metadata warps copy their rows' metadata with cp.async into a ring of
 // META_RING tile steps, META_AHEAD steps ahead (the TMA unit moved 128 separate
 // 16-byte rows per stage for it, ~6% of the kernel's time).
