@@ -153,6 +153,13 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (no completion to wait on); p and
+// bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 // 16-byte global -> shared copy through L2 (LDGSTS); bytes past `src_bytes`
 // are written as zeros (src_bytes = 0 reads nothing).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {

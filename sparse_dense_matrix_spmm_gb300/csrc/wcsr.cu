@@ -18,25 +18,32 @@
 //
 // SpMM.  On the synthetic power-law workload the windows are about 6% dense
 // (uniform columns), so the contraction per window is not a dense tile: the
-// kernel runs on CUDA cores and is bound by gathering B rows (N * 2 bytes per
-// nonzero) from L2, which is latency-bound: throughput is the bytes in flight
-// per SM over the L2 round trip, so occupancy decides it.  One CTA (4 warps,
-// 8 CTAs per SM) per work unit.  The CTA first stages the
-// unit's sparse operand in shared memory (local row, column resolved through
-// the window's column list, value), then cuts it into equal chunks, one per
-// warp.  Each warp keeps 16 B-row loads in flight, accumulates fp32 per row in
-// registers (lane = 4 columns of a 128-column slab), writes rows that lie inside its
-// chunk straight into a shared-memory tile, and hands the two rows at its
-// chunk's ends to a fix-up that adds them in warp order, so every sum has a
-// fixed order.  Unsplit windows write C from the tile; a split window's units
-// write partial tiles to the workspace, and the last unit to finish (ticket
-// counter) sums them in unit order and resets the counter.
+// kernel runs on CUDA cores.  Each nonzero gathers one B row (N * 2 bytes) from
+// L2; with one CTA per work unit the kernel is bound by instruction issue and
+// by the chain of dependent loads per unit (unit header, window header and
+// nonzeros, column list, B rows), so occupancy (8 CTAs of 4 warps per SM) and
+// instructions per nonzero decide its rate.  The CTA stages the unit's sparse
+// operand in shared memory as {column, local row | value} (all of a thread's
+// slots requested before any column is resolved), then cuts it into eight
+// contiguous streams, one per half-warp.  The 16 lanes of a half read one B
+// row per load (8 columns, 16 bytes, each), accumulate with one mixed-precision
+// FMA per element (16-bit operands, fp32 accumulator; the same result as
+// converting both and using fmaf), write rows that lie inside the stream into
+// a shared-memory tile, and hand the two rows at the stream's ends to a fix-up
+// that adds them in stream order, so every sum has a fixed order.  Rows never
+// decrease along a stream, so a batch whose last entry is on the current row
+// needs no per-entry row test.  Unsplit windows write C from the tile; a split
+// window's units write partial tiles to the workspace, and the last unit to
+// finish (ticket counter) sums them in unit order, with several loads in
+// flight per thread, and resets the counter.  The first wave of CTAs prefetches
+// the format arrays and B into L2 with bulk prefetches.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
 #include <mutex>
 
 #include "internal.h"
+#include "sm103.cuh"
 
 namespace spmm {
 
@@ -44,9 +51,10 @@ __device__ int g_wcsr_build_error;  // data-dependent builder errors (SPMM_DEVER
 
 namespace {
 
-constexpr int kWarps = 4;   // 8 CTAs per SM: one CTA's staging overlaps the others' gathers
+constexpr int kWarps = 4;     // several CTAs per SM: one CTA's staging overlaps the others' gathers
+constexpr int kMinBlocks = 8; // resident CTAs per SM the register budget is sized for (64 registers)
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlab = 128;  // output columns per pass (4 per lane)
+constexpr int kSlab = 128;    // output columns per pass (8 per lane of a half-warp)
 static_assert(kThreads >= kSlab, "the boundary fix-up gives one thread to each slab column");
 constexpr int kMaxH = 64;   // largest window height the SpMM kernel accepts
 
@@ -241,6 +249,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* a, int64_t n) {
 }
 
 // ---------------------------------------------------------------- SpMM
+constexpr int kPfArrays = 10;
+
 struct WcsrArgs {
     const int32_t* wcol_ptr;
     const int32_t* wcols;
@@ -256,110 +266,216 @@ struct WcsrArgs {
     int64_t ldc;
     int64_t M, K, N;
     int32_t h;
+    int32_t b_vec;    // B rows can be read as 16-byte pieces (16-byte aligned base, ldb % 8 == 0, K * ldb < 2^31)
+    int32_t c_vec;    // C and the partials can be written as float4 (aligned base, ldc % 4 == 0, N % 4 == 0)
     float* partial;   // [n_units][h][N]
     int32_t* ticket;  // [n_windows]
     int* err;
+    // L2 warm-up: the first pf_ctas CTAs each prefetch their share of these
+    // arrays (format arrays and B), so later index and B-row loads hit L2
+    // instead of paying an HBM round trip each.
+    const void* pf_ptr[kPfArrays];
+    int64_t pf_bytes[kPfArrays];
+    int32_t pf_n, pf_ctas;
 };
 
+constexpr int kStage = 1024;                   // nonzeros whose operand is staged in shared memory at once
+constexpr int kPerThread = kStage / kThreads;  // staged entries per thread
+constexpr int kBatch = 4;                      // entries per half-warp batch: 4 B-row loads in flight per half
+constexpr int kStreams = 2 * kWarps;           // one stream of staged entries per half-warp
+constexpr int kBnd = 2 * kStreams;             // fix-up slots: first and last row of every stream
+static_assert(kStage % kThreads == 0, "staging gives every thread the same number of entries");
+
+// acc[i] += v * x_i for the eight 16-bit values x_0..x_7 packed in r, with v the
+// low 16 bits of pk: one mixed-precision FMA per element (the 16-bit product is
+// exact in fp32, so this equals converting both operands and using fmaf).
 template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t w);
+__device__ __forceinline__ void fma8(float (&acc)[8], uint32_t pk, const uint4& r);
+#define SPMM_WCSR_FMA8(TY)                                                                                  \
+    asm("{\n\t.reg .b16 v, t, x0, x1, x2, x3, x4, x5, x6, x7;\n\t"                                          \
+        "mov.b32 {v, t}, %8;\n\t"                                                                          \
+        "mov.b32 {x0, x1}, %9;\n\tmov.b32 {x2, x3}, %10;\n\tmov.b32 {x4, x5}, %11;\n\tmov.b32 {x6, x7}, %12;\n\t" \
+        "fma.rn.f32." TY " %0, v, x0, %0;\n\tfma.rn.f32." TY " %1, v, x1, %1;\n\t"                          \
+        "fma.rn.f32." TY " %2, v, x2, %2;\n\tfma.rn.f32." TY " %3, v, x3, %3;\n\t"                          \
+        "fma.rn.f32." TY " %4, v, x4, %4;\n\tfma.rn.f32." TY " %5, v, x5, %5;\n\t"                          \
+        "fma.rn.f32." TY " %6, v, x6, %6;\n\tfma.rn.f32." TY " %7, v, x7, %7;\n\t}"                         \
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]), \
+          "+f"(acc[7])                                                                                      \
+        : "r"(pk), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w))
 template <>
-__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+__device__ __forceinline__ void fma8<__half>(float (&acc)[8], uint32_t pk, const uint4& r) {
+    SPMM_WCSR_FMA8("f16");
 }
 template <>
-__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+__device__ __forceinline__ void fma8<__nv_bfloat16>(float (&acc)[8], uint32_t pk, const uint4& r) {
+    SPMM_WCSR_FMA8("bf16");
+}
+#undef SPMM_WCSR_FMA8
+
+__device__ __forceinline__ void store8(float* dst, const float (&acc)[8]) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-// value bits (low half of a packed word) -> fp32
-template <typename T>
-__device__ __forceinline__ float low_to_f(uint32_t pk);
-template <>
-__device__ __forceinline__ float low_to_f<__half>(uint32_t pk) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(pk & 0xFFFFu)));
-}
-template <>
-__device__ __forceinline__ float low_to_f<__nv_bfloat16>(uint32_t pk) {
-    return __uint_as_float(pk << 16);
-}
-
-constexpr int kStage = 1024;  // nonzeros whose operand is staged in shared memory at once
-constexpr int kBatch = 16;    // B-row loads in flight per warp
-constexpr int kPad = kWarps * kBatch;
-
-// One warp's chunk of staged entries [j_lo, j_hi) (a multiple of kBatch long):
-// gather B rows, accumulate per row, store finished rows in the tile and the
-// chunk's end rows in the fix-up slots.
+// This lane's 8 columns of B row `col` (16 bytes).  FULL: one vector load, with
+// Bv = B as 16-byte pieces already offset to this lane's columns and ldv = ldb / 8
+// (the host guarantees K * ldb < 2^31, so the offset fits 32 bits).  Otherwise
+// element loads of the `valid` columns at B + col * ldb + ncol.
 template <typename T, bool FULL>
-__device__ __forceinline__ void wcsr_chunk(const T* B, int64_t ldb, int64_t ncol, int valid, const int* s_col,
-                                           const uint32_t* s_pk, int j_lo, int j_hi, float* tile, float* bnd,
-                                           int* bnd_row, int warp, int lane) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+__device__ __forceinline__ uint4 load_b8(const uint4* Bv, uint32_t ldv, const T* B, int64_t ldb, int64_t ncol,
+                                         int valid, int col) {
+    if (FULL) return __ldg(Bv + static_cast<uint32_t>(col) * ldv);
+    const uint16_t* q = reinterpret_cast<const uint16_t*>(B + static_cast<int64_t>(col) * ldb + ncol);
+    uint32_t e[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) e[t] = t < valid ? static_cast<uint32_t>(q[t]) : 0u;
+    return make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+}
+
+// One half-warp's stream of staged entries [j_lo, j_end): the 16 lanes of the
+// half read 128 columns of one B row per load (8 columns, 16 bytes, per lane),
+// BATCH loads in flight (fewer on the element-wise path for ragged or unaligned
+// B), and accumulate fp32 per row in registers.  A row finished inside the
+// stream goes straight into the tile; the stream's first and last rows, which
+// may continue in the neighbouring streams, go to the stream's two fix-up
+// slots.  Entries are {column, local row << 16 | value bits}; rows change
+// rarely, so the change test is a warp vote around a rarely taken branch.
+template <typename T, bool FULL, int BATCH = FULL ? kBatch : 4>
+__device__ __forceinline__ void wcsr_stream(const T* B, int64_t ldb, int64_t ncol, int valid, const int2* s_ent,
+                                            int j_lo, int j_end, float* tile, float* bnd, int* bnd_row, int stream,
+                                            int hl) {
+    const uint4* Bv = reinterpret_cast<const uint4*>(B) + (FULL ? ncol / 8 : 0);
+    const uint32_t ldv = static_cast<uint32_t>(ldb / 8);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
     int cur = -1;
     bool first_seg = true;
-    for (int j0 = j_lo; j0 < j_hi; j0 += kBatch) {
-        uint2 raw[kBatch];
+    for (int j0 = j_lo;; j0 += BATCH) {
+        if (!__any_sync(0xffffffffu, j0 < j_end)) break;
+        uint4 raw[BATCH];
+        uint32_t pk[BATCH];
+        if (__all_sync(0xffffffffu, j0 + BATCH <= j_end)) {
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const T* p = B + static_cast<int64_t>(s_col[j0 + b]) * ldb + ncol;
-            if (FULL) {
-                raw[b] = __ldg(reinterpret_cast<const uint2*>(p));
-            } else {
-                const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
-                const uint32_t e0 = valid > 0 ? q[0] : 0u, e1 = valid > 1 ? q[1] : 0u;
-                const uint32_t e2 = valid > 2 ? q[2] : 0u, e3 = valid > 3 ? q[3] : 0u;
-                raw[b] = make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
+            for (int b = 0; b < BATCH; ++b) {
+                const int2 e = s_ent[j0 + b];
+                pk[b] = static_cast<uint32_t>(e.y);
+                raw[b] = load_b8<T, FULL>(Bv, ldv, B, ldb, ncol, valid, e.x);
+            }
+        } else {
+            // past the stream's end: value 0 on the stream's last row (adds nothing,
+            // and rows stay non-decreasing through the batch)
+            const uint32_t tail = j0 < j_end ? (static_cast<uint32_t>(s_ent[j_end - 1].y) & 0xFFFF0000u)
+                                             : static_cast<uint32_t>(cur) << 16;
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const bool live = j0 + b < j_end;
+                const int2 e = live ? s_ent[j0 + b] : make_int2(0, static_cast<int>(tail));
+                pk[b] = static_cast<uint32_t>(e.y);
+                raw[b] = live ? load_b8<T, FULL>(Bv, ldv, B, ldb, ncol, valid, e.x) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        // Rows never decrease along a stream: if the batch's last entry is still on
+        // the current row, so is every entry of the batch.
+        if (__all_sync(0xffffffffu, (static_cast<int>(pk[BATCH - 1]) >> 16) == cur)) {
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const uint32_t pk = s_pk[j0 + b];
-            const int rr = static_cast<int>(pk >> 16);
-            if (rr != cur) {
-                if (cur >= 0) {
-                    // a finished segment: the chunk's first row goes to the fix-up,
-                    // any later one lies wholly inside this chunk
-                    float* dst = first_seg ? bnd + (warp * 2) * kSlab : tile + cur * kSlab;
-                    *reinterpret_cast<float4*>(dst + 4 * lane) = acc;
-                    if (first_seg && lane == 0) bnd_row[warp * 2] = cur;
-                    first_seg = false;
+            for (int b = 0; b < BATCH; ++b) fma8<T>(acc, pk[b], raw[b]);
+            continue;
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int rr = static_cast<int>(pk[b]) >> 16;
+            if (__any_sync(0xffffffffu, rr != cur)) {
+                if (rr != cur) {
+                    if (cur >= 0) {
+                        // a finished segment: the stream's first row goes to its fix-up
+                        // slot, any later one lies wholly inside this stream
+                        float* dst = first_seg ? bnd + (2 * stream) * kSlab : tile + cur * kSlab;
+                        store8(dst + 8 * hl, acc);
+                        if (first_seg && hl == 0) bnd_row[2 * stream] = cur;
+                        first_seg = false;
+                    }
+                    cur = rr;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
                 }
-                cur = rr;
-                acc = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            const float v = low_to_f<T>(pk);
-            const float2 lo = unpack2<T>(raw[b].x), hi = unpack2<T>(raw[b].y);
-            acc.x += v * lo.x;
-            acc.y += v * lo.y;
-            acc.z += v * hi.x;
-            acc.w += v * hi.y;
+            fma8<T>(acc, pk[b], raw[b]);
         }
     }
     if (cur >= 0) {
-        // the chunk's last segment may continue in the next chunk
+        // the stream's last segment may continue in the next stream
         const int k = first_seg ? 0 : 1;
-        *reinterpret_cast<float4*>(bnd + (warp * 2 + k) * kSlab + 4 * lane) = acc;
-        if (lane == 0) bnd_row[warp * 2 + k] = cur;
+        store8(bnd + (2 * stream + k) * kSlab + 8 * hl, acc);
+        if (hl == 0) bnd_row[2 * stream + k] = cur;
+    }
+}
+
+// Stage entries [st0, st0 + n_st) of the nonzero arrays (at most COUNT per
+// thread) as {column, local row << 16 | value bits}; invalid entries become value
+// 0 on row 0, column 0 and are reported.  All of a thread's slots are requested
+// before any column is resolved through the window's column list.
+template <int COUNT>
+__device__ __forceinline__ void stage_entries(const WcsrArgs& a, int32_t st0, int n_st, int32_t wbase, int32_t T_w,
+                                              int nrows, int2* s_ent, int tid) {
+    const uint16_t* val = static_cast<const uint16_t*>(a.val);
+    uint32_t lr[COUNT], v[COUNT];
+    int32_t sl[COUNT], c[COUNT];
+#pragma unroll
+    for (int k = 0; k < COUNT; ++k) {
+        const int i = tid + k * kThreads;
+        lr[k] = 0u;
+        sl[k] = -1;
+        v[k] = 0u;
+        if (i < n_st) {
+            lr[k] = a.lrow[st0 + i];
+            sl[k] = a.slot[st0 + i];
+            v[k] = val[st0 + i];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < COUNT; ++k) c[k] = (sl[k] >= 0 && sl[k] < T_w) ? a.wcols[wbase + sl[k]] : -1;
+#pragma unroll
+    for (int k = 0; k < COUNT; ++k) {
+        const int i = tid + k * kThreads;
+        if (i < n_st) {
+            const bool ok = static_cast<int>(lr[k]) < nrows && c[k] >= 0 && c[k] < a.K;
+            if (!ok) atomicOr(a.err, SPMM_DEVERR_INDEX);
+            s_ent[i] = ok ? make_int2(c[k], static_cast<int>((lr[k] << 16) | v[k])) : make_int2(0, 0);
+        }
     }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 8) wcsr_spmm_kernel(const WcsrArgs a) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) wcsr_spmm_kernel(const WcsrArgs a) {
     extern __shared__ float sm[];
-    // tile[h][kSlab] | bnd[2*kWarps][kSlab] | bnd_row[2*kWarps] | s_col[kStage+kPad] | s_pk[kStage+kPad]
+    // tile[h][kSlab] | bnd[kBnd][kSlab] | s_ent[kStage] | bnd_row[kBnd]
     float* tile = sm;
     float* bnd = tile + a.h * kSlab;
-    int* bnd_row = reinterpret_cast<int*>(bnd + 2 * kWarps * kSlab);
-    int* s_col = bnd_row + 2 * kWarps;
-    uint32_t* s_pk = reinterpret_cast<uint32_t*>(s_col + kStage + kPad);
+    int2* s_ent = reinterpret_cast<int2*>(bnd + kBnd * kSlab);
+    int* bnd_row = reinterpret_cast<int*>(s_ent + kStage);
     __shared__ int s_last;
 
     const int u = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = lane >> 4, hl = lane & 15;
+    const int stream = 2 * warp + half;
+    if (u < a.pf_ctas && tid < a.pf_n) {
+        // this CTA's share of array `tid`, shrunk to 16-byte boundaries inside it
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.pf_ptr[tid]);
+        const int64_t n = a.pf_bytes[tid];
+        const uintptr_t lo = (b0 + n * u / a.pf_ctas + 15) & ~uintptr_t(15);
+        uintptr_t hi = (b0 + n * (u + 1) / a.pf_ctas) & ~uintptr_t(15);
+        const uintptr_t end = (b0 + n) & ~uintptr_t(15);
+        if (hi > end) hi = end;
+        for (uintptr_t x = lo; x < hi; x += 65536u)
+            ptx::bulk_prefetch_l2(reinterpret_cast<const void*>(x), static_cast<uint32_t>(hi - x < 65536u ? hi - x : 65536u));
+    }
     const int w = a.unit_win[u];
+    const int32_t nz0 = a.unit_nz_ptr[u], nz1 = a.unit_nz_ptr[u + 1];
+    const T* B = static_cast<const T*>(a.B);
     if (w < 0 || static_cast<int64_t>(w) * a.h >= a.M) {  // malformed unit list: skip the unit
-        if (threadIdx.x == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);
+        if (tid == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);
         return;
     }
     const int64_t r0 = static_cast<int64_t>(w) * a.h;
@@ -368,64 +484,53 @@ __global__ void __launch_bounds__(kThreads, 8) wcsr_spmm_kernel(const WcsrArgs a
     const int units_in_window = a.unit_ptr[w + 1] - a.unit_ptr[w];
     const bool split = units_in_window > 1;
     const int32_t wbase = a.wcol_ptr[w], T_w = a.wcol_ptr[w + 1] - wbase;
-    const int32_t nz0 = a.unit_nz_ptr[u], nz1 = a.unit_nz_ptr[u + 1];
-    const uint16_t* val = static_cast<const uint16_t*>(a.val);
-    const T* B = static_cast<const T*>(a.B);
+    const bool one_stage = nz1 - nz0 <= kStage;
+    const bool full_vec = a.b_vec != 0;
 
     for (int64_t n0 = 0; n0 < a.N; n0 += kSlab) {
-        const int64_t ncol = n0 + 4 * lane;
+        const int64_t ncol = n0 + 8 * hl;
         const int64_t left = a.N - ncol;
-        const int valid = left >= 4 ? 4 : (left > 0 ? static_cast<int>(left) : 0);
-        const bool full = n0 + kSlab <= a.N;
-        for (int i = threadIdx.x; i < a.h * kSlab; i += kThreads) tile[i] = 0.f;
+        const int valid = left >= 8 ? 8 : (left > 0 ? static_cast<int>(left) : 0);
+        const bool full = full_vec && n0 + kSlab <= a.N;
+        for (int i = tid; i < a.h * (kSlab / 4); i += kThreads)
+            reinterpret_cast<float4*>(tile)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 
         for (int32_t st0 = nz0; st0 < nz1; st0 += kStage) {
             const int n_st = (nz1 - st0 < kStage) ? nz1 - st0 : kStage;
-            const int per = ((n_st + kWarps - 1) / kWarps + kBatch - 1) / kBatch * kBatch;
-            // stage the sparse operand: resolved column, packed (local row, value);
-            // invalid entries become value 0 on row 0, column 0
-            for (int i = threadIdx.x; i < n_st; i += kThreads) {
-                const int32_t e = st0 + i;
-                const int lr = a.lrow[e];
-                const int32_t sl = a.slot[e];
-                const int32_t c = (sl >= 0 && sl < T_w) ? a.wcols[wbase + sl] : -1;
-                const bool ok = lr < nrows && c >= 0 && c < a.K;
-                if (!ok) atomicOr(a.err, SPMM_DEVERR_INDEX);
-                s_col[i] = ok ? c : 0;
-                s_pk[i] = ok ? ((static_cast<uint32_t>(lr) << 16) | val[e]) : 0u;
+            if (!(one_stage && n0 > 0)) {
+                // stage the sparse operand: resolved column, packed (local row, value)
+                if (n_st <= 2 * kThreads)
+                    stage_entries<2>(a, st0, n_st, wbase, T_w, nrows, s_ent, tid);
+                else
+                    stage_entries<kPerThread>(a, st0, n_st, wbase, T_w, nrows, s_ent, tid);
             }
-            __syncthreads();
-            // pad every chunk to whole batches: value-0 copies of the last entry
-            for (int i = n_st + threadIdx.x; i < kWarps * per; i += kThreads) {
-                s_col[i] = s_col[n_st - 1];
-                s_pk[i] = s_pk[n_st - 1] & 0xFFFF0000u;
-            }
-            if (threadIdx.x < 2 * kWarps) bnd_row[threadIdx.x] = -1;
+            if (tid < kBnd) bnd_row[tid] = -1;
             __syncthreads();
 
-            const int j_lo = warp * per, j_hi = j_lo + per;
+            // whole batches per stream, so at most one stream ends in a partial batch
+            const int per = ((n_st + kStreams - 1) / kStreams + kBatch - 1) / kBatch * kBatch;
+            const int j_lo = stream * per;
+            const int j_end = min(n_st, j_lo + per);
             if (full)
-                wcsr_chunk<T, true>(B, a.ldb, ncol, valid, s_col, s_pk, j_lo, j_hi, tile, bnd, bnd_row, warp, lane);
+                wcsr_stream<T, true>(B, a.ldb, ncol, valid, s_ent, j_lo, j_end, tile, bnd, bnd_row, stream, hl);
             else
-                wcsr_chunk<T, false>(B, a.ldb, ncol, valid, s_col, s_pk, j_lo, j_hi, tile, bnd, bnd_row, warp, lane);
+                wcsr_stream<T, false>(B, a.ldb, ncol, valid, s_ent, j_lo, j_end, tile, bnd, bnd_row, stream, hl);
             __syncthreads();
-            // chunk-boundary rows, added in warp order: thread t owns column t of the slab
-            if (threadIdx.x < kSlab) {
-                for (int k = 0; k < 2 * kWarps; ++k) {
-                    const int r = bnd_row[k];
-                    if (r >= 0) tile[r * kSlab + threadIdx.x] += bnd[k * kSlab + threadIdx.x];
-                }
+            // stream-boundary rows, added in stream order: thread t owns column t of the slab
+            for (int k = 0; k < kBnd; ++k) {
+                const int r = bnd_row[k];
+                if (r >= 0) tile[r * kSlab + tid] += bnd[k * kSlab + tid];
             }
             __syncthreads();
         }
 
         if (!split) {
-            for (int i = threadIdx.x; i < nrows * (kSlab / 4); i += kThreads) {
+            for (int i = tid; i < nrows * (kSlab / 4); i += kThreads) {
                 const int r = i / (kSlab / 4), q = i % (kSlab / 4);
                 const int64_t col = n0 + 4 * q;
                 const float4 v = *reinterpret_cast<const float4*>(tile + r * kSlab + 4 * q);
                 float* cp = a.C + (r0 + r) * a.ldc + col;
-                if (col + 4 <= a.N && (reinterpret_cast<uintptr_t>(cp) & 15) == 0) {
+                if (col + 4 <= a.N && a.c_vec) {
                     __stcs(reinterpret_cast<float4*>(cp), v);
                 } else {
                     const float e[4] = {v.x, v.y, v.z, v.w};
@@ -434,9 +539,17 @@ __global__ void __launch_bounds__(kThreads, 8) wcsr_spmm_kernel(const WcsrArgs a
             }
         } else {
             float* part = a.partial + static_cast<int64_t>(u) * a.h * a.N;
-            for (int i = threadIdx.x; i < nrows * kSlab; i += kThreads) {
-                const int r = i / kSlab, q = i % kSlab;
-                if (n0 + q < a.N) __stcg(part + static_cast<int64_t>(r) * a.N + n0 + q, tile[i]);
+            for (int i = tid; i < nrows * (kSlab / 4); i += kThreads) {
+                const int r = i / (kSlab / 4), q = i % (kSlab / 4);
+                const int64_t col = n0 + 4 * q;
+                const float4 v = *reinterpret_cast<const float4*>(tile + r * kSlab + 4 * q);
+                float* pp = part + static_cast<int64_t>(r) * a.N + col;
+                if (col + 4 <= a.N && a.c_vec) {
+                    __stcg(reinterpret_cast<float4*>(pp), v);
+                } else {
+                    const float e[4] = {v.x, v.y, v.z, v.w};
+                    for (int t = 0; t < 4 && col + t < a.N; ++t) __stcg(pp + t, e[t]);
+                }
             }
         }
         __syncthreads();
@@ -446,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 8) wcsr_spmm_kernel(const WcsrArgs a
     // last unit of the window to finish sums the partials in unit order
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         const int t = atomicAdd(a.ticket + w, 1);
         s_last = (t == units_in_window - 1);
     }
@@ -454,14 +567,56 @@ __global__ void __launch_bounds__(kThreads, 8) wcsr_spmm_kernel(const WcsrArgs a
     if (!s_last) return;
     __threadfence();
     const int u0 = a.unit_ptr[w];
-    for (int64_t i = threadIdx.x; i < static_cast<int64_t>(nrows) * a.N; i += kThreads) {
-        const int64_t r = i / a.N, c = i % a.N;
-        float s = 0.f;
-        for (int k = 0; k < units_in_window; ++k)
-            s += __ldcg(a.partial + (static_cast<int64_t>(u0 + k) * a.h + r) * a.N + c);
-        a.C[(r0 + r) * a.ldc + c] = s;
+    const int U = units_in_window;
+    if (a.c_vec) {
+        // four float4 positions per thread per pass, units two at a time: eight
+        // independent loads in flight, summed in unit order
+        const int64_t nv = static_cast<int64_t>(nrows) * a.N / 4;
+        const int64_t stride_u = static_cast<int64_t>(a.h) * a.N / 4;  // float4s per unit partial
+        const float4* pv = reinterpret_cast<const float4*>(a.partial) + static_cast<int64_t>(u0) * stride_u;
+        for (int64_t i0 = tid; i0 < nv; i0 += 4 * kThreads) {
+            float4 s[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k0 = 0; k0 < U; k0 += 2) {
+                float4 x[4][2];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int64_t i = i0 + q * kThreads;
+                        x[q][kk] = (k0 + kk < U && i < nv) ? __ldcg(pv + (k0 + kk) * stride_u + i)
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        if (k0 + kk < U) {
+                            s[q].x += x[q][kk].x;
+                            s[q].y += x[q][kk].y;
+                            s[q].z += x[q][kk].z;
+                            s[q].w += x[q][kk].w;
+                        }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t i = i0 + q * kThreads;
+                if (i < nv) {
+                    const int64_t r = (4 * i) / a.N, c = (4 * i) % a.N;
+                    *reinterpret_cast<float4*>(a.C + (r0 + r) * a.ldc + c) = s[q];
+                }
+            }
+        }
+    } else {
+        for (int64_t i = tid; i < static_cast<int64_t>(nrows) * a.N; i += kThreads) {
+            const int64_t r = i / a.N, c = i % a.N;
+            float s = 0.f;
+            for (int k = 0; k < U; ++k) s += __ldcg(a.partial + (static_cast<int64_t>(u0 + k) * a.h + r) * a.N + c);
+            a.C[(r0 + r) * a.ldc + c] = s;
+        }
     }
-    if (threadIdx.x == 0) a.ticket[w] = 0;  // ready for the next call
+    if (tid == 0) a.ticket[w] = 0;  // ready for the next call
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -580,10 +735,36 @@ spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float*
     a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                          align256(sizeof(int32_t) * static_cast<size_t>(A->n_windows)));
     a.err = dev->err;
-    const int smem = static_cast<int>(sizeof(float) * (A->h * kSlab + kWarps * 2 * kSlab) + sizeof(int) * kWarps * 2 +
-                                      (kStage + kPad) * (sizeof(int) + sizeof(uint32_t)));
-    const int smem_max = static_cast<int>(sizeof(float) * (kMaxH * kSlab + kWarps * 2 * kSlab) +
-                                          sizeof(int) * kWarps * 2 + (kStage + kPad) * (sizeof(int) + sizeof(uint32_t)));
+    {
+        // L2 warm-up set: the format arrays, and B when its rows are not much wider than N
+        int n = 0;
+        auto add = [&](const void* p, int64_t bytes) {
+            if (p && bytes >= 16 && n < kPfArrays) {
+                a.pf_ptr[n] = p;
+                a.pf_bytes[n] = bytes;
+                ++n;
+            }
+        };
+        add(A->unit_win, 4 * A->n_units);
+        add(A->unit_nz_ptr, 4 * (A->n_units + 1));
+        add(A->unit_ptr, 4 * (A->n_windows + 1));
+        add(A->wcol_ptr, 4 * (A->n_windows + 1));
+        add(A->lrow, A->nnz);
+        add(A->slot, 4 * A->nnz);
+        add(A->val, 2 * A->nnz);
+        add(A->wcols, 4 * A->n_wcols);
+        if (ldb <= 2 * N && A->K * ldb * 2 <= (int64_t(64) << 20)) add(B, A->K * ldb * 2);
+        a.pf_n = n;
+        const int64_t wave = static_cast<int64_t>(dev->sms) * kMinBlocks;
+        a.pf_ctas = static_cast<int32_t>(A->n_units < wave ? A->n_units : wave);
+    }
+    a.b_vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 8 == 0) && (A->K * ldb < (int64_t(1) << 31));
+    a.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (N % 4 == 0);
+    auto smem_for = [](int h) {
+        return static_cast<int>(sizeof(float) * (h * kSlab + kBnd * kSlab) + sizeof(int2) * kStage +
+                                sizeof(int) * kBnd);
+    };
+    const int smem = smem_for(A->h), smem_max = smem_for(kMaxH);
     const void* kern = A->dtype == SPMM_BF16 ? reinterpret_cast<const void*>(wcsr_spmm_kernel<__nv_bfloat16>)
                                              : reinterpret_cast<const void*>(wcsr_spmm_kernel<__half>);
     if (!set_smem_attr_once(kern, smem_max, A->dtype == SPMM_BF16 ? 4 : 5)) return SPMM_ERR_CUDA;
