@@ -351,17 +351,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 1.5x the work of the M = 128 tokens x N = 64 orientation above, whose issue
 // cost exceeds its tensor time.  An M = 64 accumulator keeps row m in TMEM lane
 // 32 * (m / 16) + m % 16 (measured on the device), i.e. lanes 0-15 of each lane
-// quarter.  C goes out through 128-byte-swizzled shared tiles and TMA stores.
-// 192 tokens (not 256): a 32 KB stage leaves room for six stages beside the C
-// staging buffers, which outweighs the slightly lower N = 192 MMA efficiency
-// (1.65 vs 1.71 ms on the 18944 x 3584 x 65536 workload).
+// quarter.
+//
+// Roles (12 warps): warps 0-2 are TMA producers, producer p filling the stages
+// s with s % 3 == p (a TMA copy of 128-byte rows moves ~25 B/clk per issuing
+// thread, so a 32 KB stage needs several issuers to keep up with its ~420 clk
+// of MMAs); warp 3 issues the MMAs; warps 4-11 are the epilogue, two per TMEM
+// lane quarter.  The epilogue cuts a unit's 192 tokens into six 32-token boxes:
+// warp e takes boxes (e / 4), (e / 4) + 2, ..., reads its 16 rows x 32 columns
+// from TMEM, writes them 128-byte swizzled into its own double-buffered 2 KB
+// staging tile and stores it with its own TMA store, so no epilogue warp waits
+// for another.  192 tokens (not 256): a 32 KB stage leaves room for six stages
+// beside the C staging tiles.
 constexpr int kWideTokens = 192;
-constexpr int kWideChunks = kWideTokens / 64;  // 64-token chunks per tile (128-byte swizzle rows)
+constexpr int kWideChunks = kWideTokens / 64;  // 64-token chunks per B tile (128-byte swizzle rows)
 constexpr int kWideRows = 64;
-constexpr uint32_t kWideCBuf = 2 * kWideRows * 128;  // one staging buffer: 2 boxes of 64 rows x 32 fp32
+constexpr int kWideProducers = 3;
+constexpr int kWideMmaWarp = kWideProducers;
+constexpr int kWideEpi0 = kWideProducers + 1;
+constexpr int kWideEpiWarps = 8;
+constexpr int kWideThreads = 32 * (kWideEpi0 + kWideEpiWarps);
+constexpr int kWideBoxTokens = 32;                                  // one 128-byte swizzle row of fp32
+constexpr int kWideBoxes = kWideTokens / kWideBoxTokens;            // per unit
+constexpr uint32_t kWideBoxBytes = 16u * kWideBoxTokens * 4u;       // 16 rows x 32 fp32 = 2 KB
+constexpr uint32_t kWideCStage = kWideEpiWarps * 2u * kWideBoxBytes;  // all epilogue warps, double-buffered
+static_assert(kWideEpiWarps % 4 == 0 && kWideBoxes % (kWideEpiWarps / 4) == 0, "boxes split evenly over warp sets");
 
 template <int KSTEPS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, 1)
     bcsr_wide_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmC, const BcsrArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -385,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < a.nacc; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), kWideEpiWarps);
         }
         mbar_init(done_bar, 1);
         fence_mbar_init();
@@ -395,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmC);
     }
-    if (warp == kMmaWarp) {
+    if (warp == kWideMmaWarp) {
         tmem_alloc(smem_u32(tslot), a.tmem_cols);
         tmem_relinquish();
     }
@@ -404,16 +421,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp < kProducers) {
-        // ------------------------------------------------ TMA producers (as above)
+    if (warp < kWideProducers) {
+        // ------------------------------------------------ TMA producers
+        // Every producer walks every block of every unit; producer p issues the
+        // blocks whose position in that sequence is p modulo kWideProducers, into
+        // its own slots s = p, p + kWideProducers, ... (stages is a multiple).
         const int p = warp;
-        const int own = a.stages / 2;
+        const int own = a.stages / kWideProducers;
         int s = p;
         uint32_t ph = 0;
         int armed = 0;
-        bool mine = (p == 0);
+        int turn = 0;  // position of the next block in the sequence, modulo kWideProducers
         bool ok = true;
         const uint32_t tx = a.x_bytes + static_cast<uint32_t>(kWideRows * a.bw * 2);
+        const uint64_t pol_keep = l2_policy_evict_last();
         UnitWalk w;
         w.init(a.n_brows, blockIdx.x, gridDim.x);
         int j0 = 0, j1 = 0;
@@ -435,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = (cj1 - jb < 32) ? cj1 - jb : 32;
                 for (int t = 0; t < nb; ++t) {
                     const int kc = __shfl_sync(0xffffffffu, cidx, t) * a.bw;
-                    if (mine) {
+                    if (turn == p) {
                         if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                             ok = false;
                             break;
@@ -444,36 +465,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t xs = s0 + static_cast<uint32_t>(s) * stage_bytes, ws = xs + a.x_bytes;
                             mbar_arrive_expect_tx(full_bar(s), tx);
                             tma_load_2d(ws, &tmW, full_bar(s), 0, (jb + t) * kWideRows);
+                            // B tiles are re-read by every block row with a block in this
+                            // column while the C stream passes through L2: keep them there
                             if (a.x3d) {
-                                tma_load_3d(xs, &tmB, full_bar(s), 0, kc, n0 / 64);
+                                tma_load_3d_hint(xs, &tmB, full_bar(s), 0, kc, n0 / 64, pol_keep);
                             } else {
 #pragma unroll
                                 for (int h = 0; h < kWideChunks; ++h)
-                                    tma_load_2d(xs + h * (a.x_bytes / kWideChunks), &tmB, full_bar(s), n0 + 64 * h, kc);
+                                    tma_load_2d_hint(xs + h * (a.x_bytes / kWideChunks), &tmB, full_bar(s), n0 + 64 * h,
+                                                     kc, pol_keep);
                             }
                         }
                         if (armed < own) ++armed;
-                        s += 2;
+                        s += kWideProducers;
                         if (s >= a.stages) {
                             s -= a.stages;
                             ph ^= 1u;
                         }
                     }
-                    mine = !mine;
+                    turn = (turn + 1 == kWideProducers) ? 0 : turn + 1;
                 }
             }
             w = wn;
         }
+        // Leave no copy in flight: wait for the last phase armed on each own slot.
         for (int i = 0; i < armed; ++i) {
-            int idx = (s - p) / 2 - 1 - i;
+            int idx = (s - p) / kWideProducers - 1 - i;
             uint32_t par = ph;
             if (idx < 0) {
                 idx += own;
                 par ^= 1u;
             }
-            mbar_wait(full_bar(2 * idx + p), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+            mbar_wait(full_bar(kWideProducers * idx + p), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kWideMmaWarp) {
         if (lane == 0) {
             // ---------------------------------------------------- MMA issuer
             // A = block (K-major, +32 B per K step), B = token tile (MN-major,
@@ -523,14 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------------- epilogue
-        // Warp q reads lane quarter q: block rows 16q .. 16q+15 in lanes 0-15.
-        // 64 tokens per round trip: 4 x 16 columns into registers, then into a
-        // staging buffer of two 128B-swizzled boxes (64 rows x 32 fp32 each),
-        // stored with two TMA stores.  Empty units write zeros.
+        // Warp e (0..7) reads TMEM lane quarter q = warp % 4, i.e. block rows
+        // 16q .. 16q+15 in lanes 0-15, for the boxes e / 4, e / 4 + 2, ... of
+        // every unit.  Empty units write zeros.
+        const int e = warp - kWideEpi0;
         const int q = warp & 3;
-        const int row = 16 * q + lane;  // meaningful for lane < 16
-        const bool elected = (warp == kEpiWarp0 && lane == 0);
-        int acc = 0, chunk = 0;
+        const int first_box = e >> 2;
+        constexpr int kStep = kWideEpiWarps / 4;
+        const uint32_t stage0 = s0 + a.cbuf_off + static_cast<uint32_t>(e) * 2u * kWideBoxBytes;
+        int acc = 0, k = 0;
         uint32_t aph = 0;
         UnitWalk w;
         w.init(a.n_brows, blockIdx.x, gridDim.x);
@@ -543,48 +569,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(accf_bar(acc), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) break;
             tc_fence_after();
             const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kWideTokens);
-            for (int c0 = 0; c0 < kWideTokens; c0 += 64, ++chunk) {
-                uint32_t v[4][16];
-                if (nblk > 0) {
+            // all of this warp's boxes of the unit in one TMEM round trip
+            constexpr int kMine = kWideBoxes / kStep;
+            uint32_t v[kMine][2][16];
+            if (nblk > 0) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) tmem_ld16(tl + c0 + 16 * g, v[g]);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[g][i] = 0u;
+                for (int m = 0; m < kMine; ++m) {
+                    tmem_ld16(tl + kWideBoxTokens * (first_box + kStep * m), v[m][0]);
+                    tmem_ld16(tl + kWideBoxTokens * (first_box + kStep * m) + 16, v[m][1]);
                 }
-                if (c0 + 64 >= kWideTokens) {  // accumulator fully read
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(acc));
-                }
-                const uint32_t buf = a.cbuf_off + static_cast<uint32_t>(chunk & 1) * kWideCBuf;
-                if (elected) bulk_wait_read<1>();  // the store that last used `buf` has read it
-                named_barrier(1, 128);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int m = 0; m < kMine; ++m)
+#pragma unroll
+                    for (int g = 0; g < 2; ++g)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[m][g][i] = 0u;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));  // this warp's share of the accumulator is read
+#pragma unroll
+            for (int m = 0; m < kMine; ++m, ++k) {
+                const int bx = first_box + kStep * m;
+                const uint32_t buf = stage0 + static_cast<uint32_t>(k & 1) * kWideBoxBytes;
+                if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
+                __syncwarp();
                 if (lane < 16) {
-                    // box h holds tokens 32h .. 32h+31 of the chunk; row r is 128 B,
-                    // its 16-byte units XOR-swizzled by r % 8
+                    // row `lane` of the box is 128 B, its 16-byte units XOR-swizzled by lane % 8
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int h = u >> 3, uu = u & 7;
-                        const uint32_t off = buf + static_cast<uint32_t>(h) * (kWideRows * 128) +
-                                             static_cast<uint32_t>(row) * 128u +
-                                             (static_cast<uint32_t>(uu ^ (row & 7)) << 4);
-                        float4 val = make_float4(__uint_as_float(v[u >> 2][4 * (u & 3)]),
-                                                 __uint_as_float(v[u >> 2][4 * (u & 3) + 1]),
-                                                 __uint_as_float(v[u >> 2][4 * (u & 3) + 2]),
-                                                 __uint_as_float(v[u >> 2][4 * (u & 3) + 3]));
-                        *reinterpret_cast<float4*>(smem + off) = val;
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t off = buf + static_cast<uint32_t>(lane) * 128u +
+                                             (static_cast<uint32_t>(u ^ (lane & 7)) << 4);
+                        const uint32_t* src = &v[m][u >> 2][4 * (u & 3)];
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(off), "r"(src[0]), "r"(src[1]),
+                                     "r"(src[2]), "r"(src[3])
+                                     : "memory");
                     }
                 }
                 fence_proxy_async_smem();
-                named_barrier(1, 128);
-                if (elected) {
-                    const int tok = w.nt * kWideTokens + c0;
-                    tma_store_2d(&tmC, s0 + buf, tok, w.br * kWideRows);
-                    tma_store_2d(&tmC, s0 + buf + kWideRows * 128, tok + 32, w.br * kWideRows);
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmC, buf, w.nt * kWideTokens + kWideBoxTokens * bx, w.br * kWideRows + 16 * q);
                     bulk_commit();
                 }
             }
@@ -594,12 +621,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             w = wn;
         }
-        if (elected) bulk_wait<0>();
+        if (lane == 0) bulk_wait<0>();  // this warp's stores have completed before the CTA exits
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kWideMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, a.tmem_cols);
     }
@@ -639,7 +666,7 @@ spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, f
                         static_cast<uint64_t>(A->nnzb) * kWideRows, static_cast<uint64_t>(bw) * 2,
                         static_cast<uint32_t>(bw), kWideRows, wswz) ||
         !encode_tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
-                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(ldc) * 4, 32, kWideRows,
+                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(ldc) * 4, kWideBoxTokens, 16,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return SPMM_ERR_CUDA;
     BcsrArgs a{};
@@ -665,12 +692,12 @@ spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, f
     a.timeout_ns = kWaitTimeoutNs;
     const int max_smem = dev->max_smem_optin;
     const uint32_t stage_bytes = a.x_bytes + a.w_bytes;
-    const int cbuf = 2 * static_cast<int>(kWideCBuf);
-    const int fixed = 1024 + 8 * (2 * 8 + 2 * 2 + 1) + 16 + cbuf + 1024;  // + staging alignment
+    const int cbuf = static_cast<int>(kWideCStage);
+    const int fixed = 1024 + 8 * (2 * 9 + 2 * 2 + 1) + 16 + cbuf + 1024;  // + staging alignment
     int stages = (max_smem - fixed) / static_cast<int>(stage_bytes);
-    stages = stages > 8 ? 8 : stages;
-    stages &= ~1;
-    if (stages < 2) return SPMM_ERR_UNSUPPORTED;
+    stages = stages > 9 ? 9 : stages;
+    stages -= stages % kWideProducers;  // every producer owns the same number of slots
+    if (stages < kWideProducers) return SPMM_ERR_UNSUPPORTED;
     a.stages = stages;
     const int bar_bytes = 8 * (2 * stages + 2 * a.nacc + 1) + 16;
     a.cbuf_off = static_cast<uint32_t>((stages * stage_bytes + bar_bytes + 1023) & ~1023u);
@@ -683,11 +710,11 @@ spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, f
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_BCSR, stream);
     if (bw == 64)
-        bcsr_wide_kernel<4><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+        bcsr_wide_kernel<4><<<grid, kWideThreads, smem, stream>>>(tmB, tmW, tmC, a);
     else if (bw == 32)
-        bcsr_wide_kernel<2><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+        bcsr_wide_kernel<2><<<grid, kWideThreads, smem, stream>>>(tmB, tmW, tmC, a);
     else
-        bcsr_wide_kernel<1><<<grid, kThreads, smem, stream>>>(tmB, tmW, tmC, a);
+        bcsr_wide_kernel<1><<<grid, kWideThreads, smem, stream>>>(tmB, tmW, tmC, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_BCSR, stream);
     return cuda_status(e);
