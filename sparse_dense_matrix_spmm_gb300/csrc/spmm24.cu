@@ -8,25 +8,24 @@
 // core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
 //
 // Roles (one CTA per SM, persistent over 128 x 128 output tiles; 352 threads for
-// 2:4, 480 for TVW):
+// 2:4, 608 for TVW):
 //   warps 0-1  producers, taking alternate stages of one ring: per 128-wide
 //              dense-K step, TMA loads of the compressed A tile (128 x 64,
-//              K-major, 128B swizzle), its metadata (128 x 16 B) and, for 2:4,
-//              the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle; one
-//              3-D box for both 64-column halves when N is a multiple of 64).  A
-//              single issuing thread moves ~70 B/clk, less than a stage needs.
+//              K-major, 128B swizzle), for TVW its metadata (128 x 16 B) and, for
+//              2:4, the B tile (128 K-rows x 128 columns, MN-major, 128B swizzle;
+//              one 3-D box for both 64-column halves when N is a multiple of 64).
+//              A single issuing thread moves ~70 B/clk, less than a stage needs.
 //   warp 2     MMA issuer: four sparse MMAs per stage (M=128, N=128, K=32 dense
 //              each), then tcgen05.commit frees the stage.  Descriptors are built
 //              once and only offset per stage and K step.
 //   warps 3-6  metadata warps (one per TMEM lane quarter): they rewrite each
 //              stage's stored metadata into the tensor core's order (below) and
-//              tcgen05.st it to TMEM (one 8-column-aligned column per MMA).  For
-//              TVW, warps 3-10 gather the stage's kept B rows (16 rows each) with
+//              tcgen05.st it to TMEM (one 8-column-aligned column per MMA).
+//   TVW only, warps 7-14: gather the stage's kept B rows (16 rows each) with
 //              16-byte cp.async copies into the swizzled tile, zero-filling rows
-//              past the tile's kept count, two steps ahead of the metadata rewrite
-//              (far more requests in flight than TMA gather4 of 4 x 128-byte rows
-//              gave; copy issue, not bandwidth, bounds the gather, hence eight
-//              warps).
+//              past the tile's kept count, as soon as the stage is released (far
+//              more requests in flight than TMA gather4 of 4 x 128-byte rows gave;
+//              copy issue, not bandwidth, bounds the gather, hence eight warps).
 //   last four  epilogue: tcgen05.ld the accumulator and write C.
 //
 // Metadata order in TMEM (measured on the device for kind::f16, M = 128,
@@ -56,9 +55,13 @@ using namespace ptx;
 constexpr int kProducers = 2;
 constexpr int kMmaWarp = kProducers;
 constexpr int kMetaWarp0 = kProducers + 1;
-// TVW runs eight gathering warps (the first four also rewrite metadata); 2:4 runs four.
-__host__ __device__ constexpr int gather_warps(bool gather) { return gather ? 8 : 4; }
-__host__ __device__ constexpr int epi_warp0(bool gather) { return kMetaWarp0 + gather_warps(gather); }
+// Four metadata warps (one per TMEM lane quarter); TVW adds eight warps that
+// gather the kept B rows.  The metadata warps do not gather: a gathering warp
+// waits for the stage it fills to be released, and a metadata rewrite held up
+// behind that wait left the MMAs waiting for their metadata.
+constexpr int kMetaWarps = 4;
+__host__ __device__ constexpr int gather_warps(bool gather) { return gather ? 8 : 0; }
+__host__ __device__ constexpr int epi_warp0(bool gather) { return kMetaWarp0 + kMetaWarps + gather_warps(gather); }
 __host__ __device__ constexpr int threads_for(bool gather) { return 32 * (epi_warp0(gather) + 4); }
 constexpr int BM = 128, BN = 128, KS = 128;                 // KS: dense K per stage
 constexpr uint32_t A_BYTES = BM * (KS / 2) * 2;             // 16 KB
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int kGatherWarps = gather_warps(GATHER);
     constexpr int kEpiWarp0 = epi_warp0(GATHER);
-    constexpr int kRowsPerWarp = KS / kGatherWarps;  // TVW: kept rows each gathering warp copies per step
+    constexpr int kRowsPerWarp = KS / (GATHER ? kGatherWarps : 1);  // TVW: kept rows each gathering warp copies per step
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
     // stage s: [A | B chunk 0 | B chunk 1 | stored metadata]
     auto a_s = [&](int s) { return s0 + s * STAGE_BYTES; };
@@ -294,8 +297,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
         // -------------------------------------------------------- metadata warps
         const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q+31 of the tile
         const int row = 32 * q + lane;
-        const int gq = warp - kMetaWarp0;  // TVW: this warp gathers kept rows kRowsPerWarp * gq + [0, kRowsPerWarp)
-        const bool writes_meta = gq < 4;    // one metadata warp per TMEM lane quarter
+        const int gq = warp - kMetaWarp0 - kMetaWarps;  // TVW gathering warp: kept rows kRowsPerWarp * gq + [0, kRowsPerWarp)
+        const bool writes_meta = gq < 0;                // one metadata warp per TMEM lane quarter
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + META_COL;
         bool ok = true;
         // Walk over the flat sequence of (tile, K step), skipping tiles without steps.
@@ -378,12 +381,11 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
             return true;
         };
         if constexpr (GATHER) {
-            // TVW: these warps also gather the kept rows of B into each stage's
-            // swizzled MN-major tile with 16-byte cp.async copies, GATHER_AHEAD steps
-            // ahead of the metadata rewrite so that several stages of gathers are in
-            // flight (the rewrite of a step waits for that step's copies to land).
-            // Walker g leads m; this lane's kept-row index for g's step is loaded
-            // one step ahead of its use.
+            // TVW: eight warps gather the kept rows of B into each stage's swizzled
+            // MN-major tile with 16-byte cp.async copies, as soon as the stage is
+            // released; the metadata warps rewrite a step once its copies (and the
+            // A tile) have landed.  This lane's kept-row index for walker g's step is
+            // loaded one step ahead of its use.
             const T16* Bp = static_cast<const T16*>(a.B);
             const int gi = lane & 7;                 // 16-byte piece within a 128-byte chunk row
             const int hi = lane >> 4;                // row parity within an iteration's pair of rows
@@ -427,13 +429,8 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                 cp_async_arrive_noinc(full_bar(slot));
                 return true;
             };
-            constexpr int GATHER_AHEAD = 2;  // < STAGES: the step a gather waits on is already rewritten
             if (writes_meta) {
-                for (int i = 0; i < GATHER_AHEAD && ok && g.u < total; ++i) ok = gather_step();
-                while (ok && m.u < total) {
-                    if (g.u < total && !gather_step()) break;
-                    ok = meta_step();
-                }
+                while (ok && m.u < total) ok = meta_step();
             } else {
                 while (ok && g.u < total) ok = gather_step();
             }
