@@ -60,7 +60,7 @@ def source_sha(*rel):
 KERNEL_SOURCES = {
     "sparse_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/spmm24.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "bcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/bcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
-    "wcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu",),
+    "wcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
 }
 
 
