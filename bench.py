@@ -256,23 +256,62 @@ def run_headline(args, ws, rank, local, peaks, flush_buf):
     rl["kernel_ms"] = round(t_kernel * 1e3, 4)
     rl["widen_ms"] = round(ms_wd / max(n_wd, 1), 4)
 
-    # end to end through the public API: pinned host B in, int32 C out, every step
+    # End to end through the public API: every step copies B in from pinned host
+    # memory and the int32 C out to pinned host memory.  Consecutive steps overlap
+    # on three streams (copy in / compute / copy out) with double-buffered device
+    # and host buffers, as a serving loop would run them.  The per-step footprint
+    # (B, widened operands, C: ~340 MB) is larger than L2, so no flush is needed.
     Bh = torch.from_numpy(p["B"]).pin_memory()
-    Ch = torch.empty((M, N), dtype=torch.int32).pin_memory()
-    Bd = torch.empty_like(B)
+    Chs = [torch.empty((M, N), dtype=torch.int32).pin_memory() for _ in range(2)]
+    Bds = [torch.empty_like(B) for _ in range(2)]
+    Cds = [Cd, torch.empty_like(Cd)]
+    s_cmp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        Bd.copy_(Bh, non_blocking=True)
-        spmm.spmm_24(F, Bd, Cd, wsp)
-        Ch.copy_(Cd, non_blocking=True)
+    def e2e_run(n):
+        for i in range(n):
+            j = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_cmp[j])  # step i-2 is done reading Bds[j]
+            with torch.cuda.stream(s_in):
+                Bds[j].copy_(Bh, non_blocking=True)
+                ev_in[j].record(s_in)
+            s_cmp.wait_event(ev_in[j])
+            if i >= 2:
+                s_cmp.wait_event(ev_out[j])  # step i-2's C has left Cds[j]
+            spmm.spmm_24(F, Bds[j], Cds[j], wsp)
+            ev_cmp[j].record(s_cmp)
+            s_out.wait_event(ev_cmp[j])
+            with torch.cuda.stream(s_out):
+                Chs[j].copy_(Cds[j], non_blocking=True)
+                ev_out[j].record(s_out)
+        s_cmp.wait_event(ev_out[(n - 1) % 2])
+        s_cmp.wait_event(ev_in[(n - 1) % 2])
 
     n_e2e = max(3, min(args.steps, 10))
-    e2e_ms = timed_steps(e2e_step, n_e2e, 2, flush_buf, ws)
-    e2e_ms = max_over_ranks(e2e_ms, ws, "cuda")
+    e2e_run(2)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(s_cmp)
+    s_in.wait_stream(s_cmp)
+    s_out.wait_stream(s_cmp)
+    e2e_run(n_e2e)
+    e_end.record(s_cmp)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), ws, "cuda")
     e2e = {"value": round(whole_job_tflops(ws, flops, n_e2e, e2e_ms), 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(Bh.numel() * Bh.element_size()),
-           "d2h_bytes_per_step": int(Ch.numel() * Ch.element_size()),
-           "ms_per_step": round(e2e_ms / n_e2e, 4)}
+           "d2h_bytes_per_step": int(Chs[0].numel() * Chs[0].element_size()),
+           "ms_per_step": round(e2e_ms / n_e2e, 4),
+           "overlap": "copy in, compute and copy out of consecutive steps on three streams",
+           "l2": "per-step footprint larger than L2, not flushed",
+           "result_matches_device": bool(torch.equal(Chs[(n_e2e - 1) % 2], Cd.cpu()))}
     launches = (n_sp + n_wd) * ws  # the sparse kernel and one widening launch per call
     return {"value": value, "ms_step": ms_step, "roofline": rl, "clocks": clocks, "e2e": e2e,
             "build_ms": build_ms, "launches": launches, "M": M, "K": K, "N": N, "nnz": nnz, "problem": p}
