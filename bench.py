@@ -366,6 +366,31 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             spmm.spmm_tvw(F, Bx, Cd)
+    elif c["kind"] == "24f":
+        # the same recipe as the host generator, drawn on the device (the bench checks no values):
+        # per 4-group one of the 6 position pairs, N(0,1) fp16 values; B N(0,1) fp16
+        M, K = c["M"], c["K"]
+        pat = torch.tensor([0b0011, 0b0101, 0b1001, 0b0110, 0b1010, 0b1100], device="cuda")
+        sel = pat[torch.randint(0, 6, (M, K // 4), generator=g, device="cuda")]
+        bit = torch.arange(4, device="cuda")
+        keep = ((sel[:, :, None] >> bit) & 1).bool().reshape(M, K)
+        A = torch.randn((M, K), generator=g, device="cuda").to(torch.float16) * keep
+        del sel, keep
+        Bx = torch.randn((K, c["N"]), generator=g, device="cuda").to(torch.float16)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        F = spmm.spmm_compress_24(A)
+        torch.cuda.synchronize()
+        build_ms = (time.perf_counter() - t0) * 1e3
+        del A
+        Cd = torch.empty((M, c["N"]), dtype=torch.float32, device="cuda")
+        wsp = torch.empty(max(1, spmm.spmm_24_workspace_size(F, c["N"])), dtype=torch.uint8, device="cuda")
+        nnz = M * K // 2
+        alg = nnz * 2 + M * K // 8 + K * c["N"] * 2 + M * c["N"] * 4
+        kern, kid = "sparse_spmm_kernel", spmm._lib.KERNEL_SPARSE
+
+        def step():
+            spmm.spmm_24(F, Bx, Cd, wsp)
     elif c["kind"] == "wcsr":
         p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
         dt = torch.float16
@@ -484,7 +509,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other formats")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, bcsr_tiny) and print its result; "
+                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, mask24_f16, bcsr_tiny) and print its result; "
                          "for profiling runs, not the benchmark line")
     ap.add_argument("--n", type=int, default=0, help="with --only: override the workload's N")
     args = ap.parse_args()
@@ -516,7 +541,7 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "bcsr_tiny"):
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "bcsr_tiny"):
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden

@@ -34,7 +34,7 @@ import numpy as np
 BF16, F16, I8 = "bf16", "f16", "i8"
 
 __all__ = [
-    "BF16", "F16", "I8", "round_f32_to_bf16_bits", "normal_bits",
+    "BF16", "F16", "I8", "round_f32_to_bf16_bits", "normal_bits", "mask24_float_problem",
     "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem",
     "CONFIGS", "config_problem",
 ]
@@ -99,6 +99,25 @@ def mask24_problem(M: int, K: int, N: int, seed: int) -> dict:
         A[np.broadcast_to(rows, cols.shape), cols] = v
     B = rng.integers(-127, 128, size=(K, N), dtype=np.int16).astype(np.int8)
     return {"A": A, "B": B, "M": M, "K": K, "N": N, "dtype": I8}
+
+
+def mask24_float_problem(M: int, K: int, N: int, seed: int, dtype: str = F16) -> dict:
+    """16-bit A keeping 2 of every 4 consecutive K-entries (positions uniform over the
+    6 pairs, values N(0,1); a kept value may round to zero), B (K x N) N(0,1); all as
+    raw bits."""
+    assert K % 4 == 0
+    rng = np.random.default_rng(seed)
+    pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)], dtype=np.int64)
+    G = K // 4
+    A = normal_bits(rng, (M, K), dtype)
+    keep = np.zeros((M, K), dtype=bool)
+    sel = pairs[rng.integers(0, 6, size=(M, G))]                      # (M, G, 2)
+    cols = sel + (np.arange(G, dtype=np.int64) * 4)[None, :, None]
+    rows = np.broadcast_to(np.arange(M, dtype=np.int64)[:, None, None], cols.shape)
+    keep[rows, cols] = True
+    A[~keep] = 0
+    B = normal_bits(rng, (K, N), dtype)
+    return {"A": A, "B": B, "M": M, "K": K, "N": N, "dtype": dtype}
 
 
 def _unique_sorted_rows(rng, lengths: np.ndarray, K: int):
@@ -174,6 +193,7 @@ CONFIGS = {
     "bcsr_tiny": dict(kind="bcsr", M=256, K=256, N=64, bh=16, bw=16, nnzb=64, seed=1,
                       dtype=BF16, std=1.0),
     "mask24_int8": dict(kind="24", M=8192, K=8192, N=4096, seed=2),
+    "mask24_f16": dict(kind="24f", M=8192, K=8192, N=4096, seed=6, dtype=F16),
     "wcsr_lognormal": dict(kind="wcsr", M=65536, K=65536, N=128, seed=3, mean=16.0,
                            sigma=1.5, clip=4096, dtype=F16),
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
@@ -192,6 +212,8 @@ def config_problem(name: str, **overrides) -> dict:
                             c.get("dtype", BF16), c.get("std", 1.0))
     if kind == "24":
         return mask24_problem(c["M"], c["K"], c["N"], c["seed"])
+    if kind == "24f":
+        return mask24_float_problem(c["M"], c["K"], c["N"], c["seed"], c.get("dtype", F16))
     if kind == "wcsr":
         return csr_lognormal_problem(c["M"], c["K"], c["N"], c["seed"], c.get("mean", 16.0),
                                      c.get("sigma", 1.5), c.get("clip", 4096), c.get("dtype", F16))

@@ -95,3 +95,18 @@ def test_24_int8_full_size_sampled_rows():
     got = C[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.int64)
     ref = np.concatenate([oracle.spmm24(O, p["B"], rows=(int(r), int(r) + 1)) for r in rows])
     assert np.array_equal(got, ref)
+
+
+def test_24_f16_full_size_sampled_rows():
+    """A 8192 x 8192 fp16 2:4 (N(0,1) values), B 8192 x 4096 fp16, C fp32: three
+    seeded 128-row tiles (one of them the last) against the oracle."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.config_problem("mask24_f16")
+    F, O = _compress(p, "f16")
+    C = spmm.spmm_24(F, dev_half(p["B"], "f16"))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    rng = np.random.default_rng(61)
+    for r0 in sorted(set([int(t) * 128 for t in rng.choice(p["M"] // 128 - 1, 2, replace=False)] + [p["M"] - 128])):
+        assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.spmm24(O, p["B"], rows=(r0, r0 + 128)), f"2:4 f16 rows {r0}..")

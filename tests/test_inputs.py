@@ -41,3 +41,11 @@ def test_tvw_problem_structure():
         assert not (rows[:, outside] & 0x7FFF).any()
         g = (rows[:, kc] & 0x7FFF).reshape(128, 64, 4) != 0
         assert np.all(g.sum(axis=2) == 2)
+
+
+def test_mask24_float_problem_two_kept_per_group():
+    p = gen.mask24_float_problem(32, 128, 4, seed=6)
+    nz = (p["A"] & 0x7FFF).reshape(32, 32, 4) != 0
+    assert np.all(nz.sum(axis=2) <= 2) and nz.sum() >= 32 * 32 * 2 - 2
+    q = gen.mask24_float_problem(32, 128, 4, seed=6)
+    assert np.array_equal(p["A"], q["A"]) and np.array_equal(p["B"], q["B"])
