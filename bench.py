@@ -391,6 +391,19 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             spmm.spmm_24(F, Bx, Cd, wsp)
+    elif c["kind"] == "prune24":
+        # magnitude pruning of a dense fp16 N(0,1) matrix into 2:4 (a builder: HBM-bound)
+        M, K = c["M"], c["K"]
+        A = torch.randn((M, K), generator=g, device="cuda").to(torch.float16)
+        build_ms = 0.0
+        nnz = M * K // 2
+        flops = 0.0
+        alg = M * K * 2 + nnz * 2 + M * K // 8
+        kern, kid = "prune24_kernel", spmm._lib.KERNEL_PRUNE
+        out = {}
+
+        def step():
+            out["F"] = spmm.spmm_prune_24(A)
     elif c["kind"] == "wcsr":
         p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
         dt = torch.float16
@@ -413,7 +426,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
             spmm.spmm_wcsr(F, Bx, Cd, wsp)
     else:
         raise ValueError(name)
-    flops = 2.0 * nnz * c["N"]
+    flops = 2.0 * nnz * c["N"] if c["kind"] != "prune24" else 0.0
     spmm.trace_enable(True)
     for _ in range(args.warmup):
         step()
@@ -424,7 +437,8 @@ def run_extra(name, args, ws, peaks, flush_buf):
     spmm.trace_enable(False)
     total_ms = max_over_ranks(total_ms, ws, "cuda")
     t_kernel = ms / max(n, 1) / 1e3
-    rl = roofline(flops, alg, t_kernel, peaks, traffic=measured_traffic(kern, name))
+    rl = roofline(flops, alg, t_kernel, peaks, prefer="hbm" if c["kind"] == "prune24" else None,
+                  traffic=measured_traffic(kern, name))
     rl["kernel"] = kern
     rl["kernel_ms"] = round(t_kernel * 1e3, 4)
     t_step = total_ms / steps / 1e3
@@ -509,7 +523,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other formats")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, mask24_f16, bcsr_tiny) and print its result; "
+                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, mask24_f16, prune24_f16, bcsr_tiny) and print its result; "
                          "for profiling runs, not the benchmark line")
     ap.add_argument("--n", type=int, default=0, help="with --only: override the workload's N")
     args = ap.parse_args()
@@ -541,7 +555,7 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "bcsr_tiny"):
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "prune24_f16", "bcsr_tiny"):
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden

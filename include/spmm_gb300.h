@@ -177,6 +177,7 @@ SPMM_API spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t st
 #define SPMM_KERNEL_SPARSE 2  /* tcgen05.mma.sp SpMM (2:4 and tile-vector-wise)    */
 #define SPMM_KERNEL_WIDEN 3   /* int8 -> fp16 operand widening (int8 2:4)          */
 #define SPMM_KERNEL_WCSR 4    /* row-window SpMM                                   */
+#define SPMM_KERNEL_PRUNE 5   /* dense -> 2:4 magnitude pruning                    */
 /* Turns tracing on (clearing earlier records) or off. */
 SPMM_API spmm_status spmm_trace_enable(int32_t on);
 /* Synchronises the traced events and reports launches and total milliseconds
@@ -269,6 +270,19 @@ SPMM_API spmm_status spmm_build_wcsr_fill(const spmm_csr_t *A, int32_t h, int32_
  * two nonzeros in a group -> SPMM_ERR_FORMAT.  Synchronises `stream`. */
 SPMM_API spmm_status spmm_compress_24(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
                                       void *vals, uint8_t *meta, spmm_stream_t stream);
+
+/* Magnitude pruning into 2:4 ("Accelerating Sparse DNNs Based on Tiled GEMM",
+ * abstract: pruning into the 2:4 pattern of the sparse tensor core): dense
+ * (M x K, row pitch ld elements, device memory) -> vals[M][K/2] + meta[M][K/8]
+ * in the layout of spmm_compress_24 (caller-allocated device arrays).  In every
+ * group of 4 consecutive K entries the two of largest magnitude are kept, ties
+ * going to the lower index; magnitude is |v| for int8 and the bit pattern
+ * without its sign for bf16/fp16 (so NaN ranks above every number).  The result
+ * equals spmm_compress_24 of the matrix with the other two entries zeroed.
+ * K % 8 == 0 (else SPMM_ERR_SHAPE); never fails on data.  Asynchronous on
+ * `stream`. */
+SPMM_API spmm_status spmm_prune_24(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
+                                   void *vals, uint8_t *meta, spmm_stream_t stream);
 
 /* dense (M x K) + kept columns -> TVW vals[M][Kp/2] + meta[M][Kp/8].
  * tile_ptr/cols are device arrays (tile_ptr has n_tiles + 1 entries).  Kept

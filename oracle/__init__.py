@@ -77,6 +77,8 @@ def lib():
         L.orc_compress24.restype = I32
         L.orc_compress24.argtypes = [P, I64, I64, I64, I32, P, P]
         L.orc_densify24.argtypes = [I64, I64, I32, P, P, P]
+        L.orc_prune24.restype = I32
+        L.orc_prune24.argtypes = [P, I64, I64, I64, I32, P, P]
         L.orc_spmm24_f64.argtypes = [I64, I64, I32, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_spmm24_i64.argtypes = [I64, I64, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_tvw_build.restype = I32
@@ -246,6 +248,19 @@ def compress24(A, dtype):
     rc = lib().orc_compress24(_p(A), M, K, K, DTYPES[dtype], _p(vals), _p(meta))
     if rc:
         raise OracleError(f"compress24 error {rc}")
+    return {"M": M, "K": K, "dtype": dtype, "vals": vals, "meta": meta}
+
+
+def prune24(A, dtype):
+    """Magnitude pruning of a dense matrix into the 2:4 format (the two largest
+    magnitudes of every 4-group, ties to the lower index)."""
+    A = _c(A, _edt(dtype))
+    M, K = A.shape
+    vals = np.zeros((M, K // 2), dtype=_edt(dtype))
+    meta = np.zeros((M, (K + 7) // 8), dtype=np.uint8)
+    rc = lib().orc_prune24(_p(A), M, K, K, DTYPES[dtype], _p(vals), _p(meta))
+    if rc:
+        raise OracleError(f"prune24 error {rc}")
     return {"M": M, "K": K, "dtype": dtype, "vals": vals, "meta": meta}
 
 

@@ -390,6 +390,46 @@ int orc_compress24(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, v
     return ORC_OK;
 }
 
+/* Magnitude of element idx as an unsigned key that orders by |a|: |v| for int8
+ * (0..128); for bf16/fp16 the bit pattern without its sign bit, which orders
+ * finite values and infinities by magnitude and puts NaN above every number. */
+static unsigned mag_key(const void *p, int64_t idx, int dtype) {
+    if (dtype == ORC_I8) {
+        int v = ((const int8_t *)p)[idx];
+        return (unsigned)(v < 0 ? -v : v);
+    }
+    return ((const uint16_t *)p)[idx] & 0x7FFFu;
+}
+
+/* Magnitude pruning into 2:4 ("Accelerating Sparse DNNs Based on Tiled GEMM",
+ * abstract: pruning into the sparse tensor core's 2:4 pattern).  Reading: in
+ * every group of 4 consecutive K entries keep the two of largest magnitude,
+ * ties going to the lower index; store them in ascending index order with the
+ * nibble idx0 | idx1 << 2, exactly as the 2:4 format stores a group. */
+int orc_prune24(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, void *vals, uint8_t *meta) {
+    if (K % 4) return ORC_ERR_SHAPE;
+    int64_t G = K / 4, lm = (K + 7) / 8;
+    for (int64_t i = 0; i < M; i++) {
+        for (int64_t j = 0; j < lm; j++) meta[i * lm + j] = 0;
+        for (int64_t g = 0; g < G; g++) {
+            int64_t base = i * ld + 4 * g;
+            int first = 0; /* largest key, lowest index among equals */
+            for (int q = 1; q < 4; q++)
+                if (mag_key(A, base + q, dtype) > mag_key(A, base + first, dtype)) first = q;
+            int second = -1; /* largest of the other three, lowest index among equals */
+            for (int q = 0; q < 4; q++) {
+                if (q == first) continue;
+                if (second < 0 || mag_key(A, base + q, dtype) > mag_key(A, base + second, dtype)) second = q;
+            }
+            int i0 = first < second ? first : second, i1 = first < second ? second : first;
+            copy_elem(vals, i * (K / 2) + 2 * g, A, base + i0, dtype);
+            copy_elem(vals, i * (K / 2) + 2 * g + 1, A, base + i1, dtype);
+            meta[i * lm + g / 2] |= (uint8_t)((i0 | (i1 << 2)) << (4 * (g % 2)));
+        }
+    }
+    return ORC_OK;
+}
+
 void orc_densify24(int64_t M, int64_t K, int dtype, const void *vals, const uint8_t *meta, void *D) {
     int64_t G = K / 4, lm = (K + 7) / 8;
     memset(D, 0, (size_t)(M * K * esize(dtype)));

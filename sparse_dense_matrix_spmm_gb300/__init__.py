@@ -25,7 +25,7 @@ from . import _lib
 from ._lib import SpmmError
 
 __all__ = ["BCSR", "Mat24", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bcsr", "spmm_build_bcsr_count",
-           "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_24", "spmm_24_workspace_size",
+           "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_prune_24", "spmm_24", "spmm_24_workspace_size",
            "spmm_build_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
            "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
@@ -223,6 +223,17 @@ def spmm_compress_24(dense: torch.Tensor, stream=None) -> Mat24:
     vals = torch.empty((M, K // 2), dtype=dense.dtype, device=dense.device)
     meta = torch.empty((M, K // 8), dtype=torch.uint8, device=dense.device)
     _lib.call("spmm_compress_24", _ptr(dense), M, K, dense.stride(0), _code(dense.dtype), _ptr(vals),
+              _ptr(meta), _stream(stream))
+    return Mat24(M, K, dense.dtype, vals, meta)
+
+
+def spmm_prune_24(dense: torch.Tensor, stream=None) -> Mat24:
+    """Magnitude-prune a dense (M x K) matrix into 2:4 (two largest |a| per group of 4)."""
+    _check_dev(dense)
+    M, K = dense.shape
+    vals = torch.empty((M, K // 2), dtype=dense.dtype, device=dense.device)
+    meta = torch.empty((M, K // 8), dtype=torch.uint8, device=dense.device)
+    _lib.call("spmm_prune_24", _ptr(dense), M, K, dense.stride(0), _code(dense.dtype), _ptr(vals),
               _ptr(meta), _stream(stream))
     return Mat24(M, K, dense.dtype, vals, meta)
 

@@ -274,6 +274,14 @@ spmm_status spmm_compress_24(const void* dense, int64_t M, int64_t K, int64_t ld
     return run_compress24(dense, M, K, ld, dtype, vals, meta, reinterpret_cast<cudaStream_t>(stream));
 }
 
+spmm_status spmm_prune_24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
+                          uint8_t* meta, spmm_stream_t stream) {
+    if (M > 0 && K > 0 && (!dense || !vals || !meta)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (M < 0 || K < 0 || K % 8 || ld < K) return SPMM_ERR_SHAPE;
+    return run_prune24(dense, M, K, ld, dtype, vals, meta, reinterpret_cast<cudaStream_t>(stream));
+}
+
 spmm_status spmm_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
                            const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
                            uint8_t* meta, spmm_stream_t stream) {

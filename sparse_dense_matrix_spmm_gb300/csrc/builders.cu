@@ -152,6 +152,50 @@ __global__ void bcsr_fill_kernel(const T* dense, int64_t ld, int bh, int bw, int
 }
 
 // ---------------------------------------------------------------- 2:4
+// Eight consecutive elements (two 4-groups) as one 16-byte (16-bit types) or
+// 8-byte (int8) access when `vec` (base and pitch aligned), else element-wise;
+// four stored values likewise as one 8- or 4-byte store.
+template <typename T>
+__device__ __forceinline__ void load8(const T* src, bool vec, T (&v)[8]) {
+    if (vec) {
+        if constexpr (sizeof(T) == 2) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = static_cast<T>(u[i] & 0xFFFFu);
+                v[2 * i + 1] = static_cast<T>(u[i] >> 16);
+            }
+        } else {
+            const uint2 w = *reinterpret_cast<const uint2*>(src);
+            const uint32_t u[2] = {w.x, w.y};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = static_cast<T>((u[i / 4] >> (8 * (i % 4))) & 0xFFu);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = src[i];
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, bool vec, const T (&v)[4]) {
+    if (vec) {
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t lo = static_cast<uint16_t>(v[0]) | (static_cast<uint32_t>(static_cast<uint16_t>(v[1])) << 16);
+            const uint32_t hi = static_cast<uint16_t>(v[2]) | (static_cast<uint32_t>(static_cast<uint16_t>(v[3])) << 16);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+        } else {
+            uint32_t w = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w |= static_cast<uint32_t>(static_cast<uint8_t>(v[i])) << (8 * i);
+            *reinterpret_cast<uint32_t*>(dst) = w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = v[i];
+    }
+}
+
 // Keep the nonzero positions of a 4-group, padded with the lowest-index zero
 // positions; nibble = idx0 | idx1 << 2.  Returns false on > 2 nonzeros.
 __device__ __forceinline__ bool pick2(unsigned mask, int& i0, int& i1) {
@@ -165,35 +209,86 @@ __device__ __forceinline__ bool pick2(unsigned mask, int& i0, int& i1) {
 
 // One thread per (row, meta byte) = 2 groups = 8 dense columns.
 template <typename T>
-__global__ void compress24_kernel(const T* dense, int64_t M, int64_t K, int64_t ld, T* vals, uint8_t* meta,
-                                  int* err) {
+__global__ void compress24_kernel(const T* __restrict__ dense, int64_t M, int64_t K, int64_t ld,
+                                  T* __restrict__ vals, uint8_t* __restrict__ meta, int vec, int* err) {
+    // grid: x over the row's meta bytes, y over rows (strided when M exceeds the grid)
     const int64_t nb = K / 8;
-    const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (id >= M * nb) return;
-    const int64_t i = id / nb, j = id % nb;
-    const T* src = dense + i * ld + 8 * j;
-    T* dst = vals + i * (K / 2) + 4 * j;
-    uint8_t byte = 0;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= nb) return;
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        T x[8], out[4];
+        load8<T>(dense + i * ld + 8 * j, vec != 0, x);
+        uint8_t byte = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        unsigned mask = 0;
-        T v[4];
+        for (int h = 0; h < 2; ++h) {
+            unsigned mask = 0;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            v[p] = src[4 * h + p];
-            if (nz<T>(v[p])) mask |= 1u << p;
+            for (int p = 0; p < 4; ++p)
+                if (nz<T>(x[4 * h + p])) mask |= 1u << p;
+            int i0 = 0, i1 = 1;
+            if (!pick2(mask, i0, i1)) {
+                atomicOr(err, SPMM_DEVERR_FORMAT);
+                i0 = 0;
+                i1 = 1;
+            }
+            out[2 * h] = x[4 * h + i0];
+            out[2 * h + 1] = x[4 * h + i1];
+            byte |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
         }
-        int i0 = 0, i1 = 1;
-        if (!pick2(mask, i0, i1)) {
-            atomicOr(err, SPMM_DEVERR_FORMAT);
-            i0 = 0;
-            i1 = 1;
-        }
-        dst[2 * h] = v[i0];
-        dst[2 * h + 1] = v[i1];
-        byte |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
+        store4<T>(vals + i * (K / 2) + 4 * j, vec != 0, out);
+        meta[i * nb + j] = byte;
     }
-    meta[i * nb + j] = byte;
+}
+
+// Magnitude pruning into 2:4 ("Accelerating Sparse DNNs Based on Tiled GEMM",
+// abstract: pruning into the sparse tensor core's 2:4 pattern): per 4-group the
+// two entries of largest magnitude, ties to the lower index, stored in
+// ascending index order.  The magnitude key is |v| for int8 and the bits
+// without the sign for bf16/fp16 (orders |a|; NaN above every number).
+template <typename T>
+__device__ __forceinline__ unsigned mag_key(T v);
+template <>
+__device__ __forceinline__ unsigned mag_key<int8_t>(int8_t v) {
+    return static_cast<unsigned>(v < 0 ? -static_cast<int>(v) : static_cast<int>(v));
+}
+template <>
+__device__ __forceinline__ unsigned mag_key<uint16_t>(uint16_t v) {
+    return v & 0x7FFFu;
+}
+
+// One thread per (row, meta byte) = 2 groups = 8 dense columns.
+template <typename T>
+__global__ void prune24_kernel(const T* __restrict__ dense, int64_t M, int64_t K, int64_t ld, T* __restrict__ vals,
+                               uint8_t* __restrict__ meta, int vec) {
+    // grid: x over the row's meta bytes, y over rows (strided when M exceeds the grid)
+    const int64_t nb = K / 8;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= nb) return;
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        T x[8], out[4];
+        load8<T>(dense + i * ld + 8 * j, vec != 0, x);
+        uint8_t byte = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            unsigned key[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) key[p] = mag_key<T>(x[4 * h + p]);
+            int first = 0;  // largest key, lowest index among equals
+#pragma unroll
+            for (int p = 1; p < 4; ++p)
+                if (key[p] > key[first]) first = p;
+            int second = first == 0 ? 1 : 0;  // largest of the other three, lowest index among equals
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                if (p != first && p > second && key[p] > key[second]) second = p;
+            const int i0 = min(first, second), i1 = max(first, second);
+            out[2 * h] = x[4 * h + i0];
+            out[2 * h + 1] = x[4 * h + i1];
+            byte |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
+        }
+        store4<T>(vals + i * (K / 2) + 4 * j, vec != 0, out);
+        meta[i * nb + j] = byte;
+    }
 }
 
 // ---------------------------------------------------------------- TVW
@@ -329,16 +424,39 @@ spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, 
     spmm_status st = build_begin(e, s);
     if (st != SPMM_OK) return st;
     const int64_t n = M * (K / 8);
+    const int64_t es = dtype == SPMM_I8 ? 1 : 2;  // 8 elements: 16 (or 8) bytes per access
+    const int vec = (reinterpret_cast<uintptr_t>(dense) % (8 * es) == 0) && ((ld * es) % (8 * es) == 0) &&
+                    (reinterpret_cast<uintptr_t>(vals) % (4 * es) == 0);
+    const dim3 grid(static_cast<unsigned>((K / 8 + 255) / 256), static_cast<unsigned>(M < 65535 ? (M > 0 ? M : 1) : 65535));
     if (n > 0) {
-        const int64_t blocks = (n + 255) / 256;
         if (dtype == SPMM_I8)
-            compress24_kernel<int8_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-                static_cast<const int8_t*>(dense), M, K, ld, static_cast<int8_t*>(vals), meta, e);
+            compress24_kernel<int8_t><<<grid, 256, 0, s>>>(
+                static_cast<const int8_t*>(dense), M, K, ld, static_cast<int8_t*>(vals), meta, vec, e);
         else
-            compress24_kernel<uint16_t><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-                static_cast<const uint16_t*>(dense), M, K, ld, static_cast<uint16_t*>(vals), meta, e);
+            compress24_kernel<uint16_t><<<grid, 256, 0, s>>>(
+                static_cast<const uint16_t*>(dense), M, K, ld, static_cast<uint16_t*>(vals), meta, vec, e);
     }
     return build_end(e, s);
+}
+
+spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
+                        uint8_t* meta, cudaStream_t s) {
+    const int64_t n = M * (K / 8);
+    const int64_t es = dtype == SPMM_I8 ? 1 : 2;  // 8 elements: 16 (or 8) bytes per access
+    const int vec = (reinterpret_cast<uintptr_t>(dense) % (8 * es) == 0) && ((ld * es) % (8 * es) == 0) &&
+                    (reinterpret_cast<uintptr_t>(vals) % (4 * es) == 0);
+    const dim3 grid(static_cast<unsigned>((K / 8 + 255) / 256), static_cast<unsigned>(M < 65535 ? (M > 0 ? M : 1) : 65535));
+    if (n > 0) {
+        trace_begin(SPMM_KERNEL_PRUNE, s);
+        if (dtype == SPMM_I8)
+            prune24_kernel<int8_t><<<grid, 256, 0, s>>>(
+                static_cast<const int8_t*>(dense), M, K, ld, static_cast<int8_t*>(vals), meta, vec);
+        else
+            prune24_kernel<uint16_t><<<grid, 256, 0, s>>>(
+                static_cast<const uint16_t*>(dense), M, K, ld, static_cast<uint16_t*>(vals), meta, vec);
+        trace_end(SPMM_KERNEL_PRUNE, s);
+    }
+    return cuda_status(cudaGetLastError());
 }
 
 spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,

@@ -74,6 +74,8 @@ spmm_status run_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, i
                           const int32_t* row_ptr, int32_t* col_idx, void* vals, cudaStream_t s);
 spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
                            uint8_t* meta, cudaStream_t s);
+spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
+                        uint8_t* meta, cudaStream_t stream);
 spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
                           uint8_t* meta, cudaStream_t s);

@@ -194,6 +194,7 @@ CONFIGS = {
                       dtype=BF16, std=1.0),
     "mask24_int8": dict(kind="24", M=8192, K=8192, N=4096, seed=2),
     "mask24_f16": dict(kind="24f", M=8192, K=8192, N=4096, seed=6, dtype=F16),
+    "prune24_f16": dict(kind="prune24", M=8192, K=8192, N=0, seed=7, dtype=F16),
     "wcsr_lognormal": dict(kind="wcsr", M=65536, K=65536, N=128, seed=3, mean=16.0,
                            sigma=1.5, clip=4096, dtype=F16),
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
@@ -220,4 +221,8 @@ def config_problem(name: str, **overrides) -> dict:
     if kind == "tvw":
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))
+    if kind == "prune24":  # a dense matrix to prune into 2:4
+        rng = np.random.default_rng(c["seed"])
+        return {"A": normal_bits(rng, (c["M"], c["K"]), c.get("dtype", F16)), "M": c["M"], "K": c["K"],
+                "dtype": c.get("dtype", F16)}
     raise ValueError(kind)

@@ -110,3 +110,41 @@ def test_24_f16_full_size_sampled_rows():
     rng = np.random.default_rng(61)
     for r0 in sorted(set([int(t) * 128 for t in rng.choice(p["M"] // 128 - 1, 2, replace=False)] + [p["M"] - 128])):
         assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.spmm24(O, p["B"], rows=(r0, r0 + 128)), f"2:4 f16 rows {r0}..")
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16"])
+@pytest.mark.parametrize("M,K", [(64, 256), (37, 1024)])
+def test_24_prune_bit_exact_and_spmm(dtype, M, K):
+    """Magnitude pruning on the GPU equals the oracle's bit for bit (ties, signed
+    zeros, int8 -128, NaN and infinities included), and the pruned operand
+    multiplies like any 2:4 operand (rows without NaN or infinities compared)."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    rng = np.random.default_rng(M + K)
+    if dtype == "i8":
+        A = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+        small = rng.random((M, K)) < 0.3                            # many equal magnitudes
+        A[small] = rng.integers(-2, 3, size=int(small.sum())).astype(np.int8)
+        A[0, :4] = [-128, 127, -128, 5]
+    else:
+        A = gen.normal_bits(rng, (M, K), dtype)
+        A[rng.random((M, K)) < 0.15] = 0
+        A[rng.random((M, K)) < 0.05] = 0x8000                       # -0.0
+        one, nan, inf = (0x3C00, 0x7E00, 0x7C00) if dtype == "f16" else (0x3F80, 0x7FC0, 0x7F80)
+        A[0, :8] = [nan, inf, one, one, one | 0x8000, one, one, 0]  # NaN above inf; equal magnitudes
+    Ad = dev(A) if dtype == "i8" else dev_half(A, dtype)
+    F = spmm.spmm_prune_24(Ad)
+    O = oracle.prune24(A, dtype)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(F.vals), O["vals"])
+    assert np.array_equal(F.meta.cpu().numpy(), O["meta"])
+    if dtype == "i8":
+        B = rng.integers(-127, 128, size=(K, 96)).astype(np.int8)
+        C = spmm.spmm_24(F, dev(B))
+        torch.cuda.synchronize()
+        assert np.array_equal(C.cpu().numpy(), oracle.spmm24(O, B))
+    else:
+        B = gen.normal_bits(rng, (K, 96), dtype)
+        C = spmm.spmm_24(F, padded_b(B, dtype))
+        torch.cuda.synchronize()
+        assert_close(C[1:].cpu().numpy(), oracle.spmm24(O, B, rows=(1, M)), f"pruned 2:4 {dtype}")

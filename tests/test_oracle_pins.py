@@ -291,3 +291,75 @@ def test_wcsr_windows_with_repeated_columns():
         assert F["n_wcols"] < p["row_ptr"][-1]
         np.testing.assert_allclose(oracle.wcsr_spmm(F, p["B"]), _csr_dense(p) @ bits_to_f64(p["B"], "f16"),
                                    rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- 2:4 magnitude pruning
+def _prune_keys(A, dtype):
+    if dtype == "i8":
+        return np.abs(A.astype(np.int64))
+    return (A.astype(np.int64) & 0x7FFF)
+
+
+def test_prune24_hand_worked_groups():
+    """Worked by hand: ties go to the lower index; -128 outranks 127; NaN outranks inf."""
+    A = np.array([[3, -3, 3, 1, 0, 0, 0, 0, -128, 127, 5, -128, 0, 9, 0, -9]], dtype=np.int8)
+    F = oracle.prune24(A, "i8")
+    assert F["vals"].tolist() == [[3, -3, 0, 0, -128, -128, 9, -9]]
+    # groups: (0,1) -> 0x4, (0,1) -> 0x4 | (0,3) -> 0xC, (1,3) -> 0xD
+    assert F["meta"].tolist() == [[0x44, 0xDC]]
+    h = np.array([[0x7E00, 0x7C00, 0x8000, 0x3C00, 0x8000, 0x0000, 0x0000, 0x0000]], dtype=np.uint16)
+    Fh = oracle.prune24(h, "f16")
+    assert Fh["vals"].tolist() == [[0x7E00, 0x7C00, 0x8000, 0x0000]]
+    assert Fh["meta"].tolist() == [[0x44]]
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16"])
+def test_prune24_keeps_the_largest_magnitudes(dtype):
+    """Properties any correct magnitude pruning has: exactly two positions per group,
+    kept values copied bit for bit, every dropped magnitude at most the smaller kept
+    one (and on a tie the dropped index is the higher), the kept pair's magnitude sum
+    the largest over all six pairs."""
+    rng = np.random.default_rng(11)
+    M, K = 24, 64
+    if dtype == "i8":
+        A = rng.integers(-4, 5, size=(M, K)).astype(np.int8)        # small range: many ties
+    else:
+        A = gen.normal_bits(rng, (M, K), dtype)
+        A[rng.random((M, K)) < 0.3] = 0
+        A[rng.random((M, K)) < 0.1] ^= 0x8000                       # sign flips keep magnitudes
+    F = oracle.prune24(A, dtype)
+    D = oracle.densify24(F)
+    keys = _prune_keys(A, dtype).reshape(M, K // 4, 4)
+    nib = np.stack([F["meta"] & 15, F["meta"] >> 4], axis=2).reshape(M, K // 4)
+    i0, i1 = nib & 3, nib >> 2
+    assert np.all(i0 < i1)
+    g = np.arange(K // 4)
+    for r in range(M):
+        kept = np.zeros((K // 4, 4), dtype=bool)
+        kept[g, i0[r]] = True
+        kept[g, i1[r]] = True
+        dense_row = A[r].reshape(K // 4, 4)
+        assert np.array_equal(D[r].reshape(K // 4, 4)[kept], dense_row[kept])
+        assert not (D[r].reshape(K // 4, 4)[~kept].astype(np.int64) & (0xFF if dtype == "i8" else 0xFFFF)).any()
+        kr = keys[r]
+        kmin = np.minimum(kr[g, i0[r]], kr[g, i1[r]])
+        lo_of_min = np.where(kr[g, i0[r]] <= kr[g, i1[r]], np.where(kr[g, i0[r]] == kr[g, i1[r]], i1[r], i0[r]), i1[r])
+        for q in range(4):
+            dropped = ~kept[:, q]
+            assert np.all(kr[dropped, q] <= kmin[dropped])
+            tie = dropped & (kr[:, q] == kmin)
+            assert np.all(q > lo_of_min[tie])
+        pair_sums = np.stack([kr[:, a] + kr[:, b] for a in range(4) for b in range(a + 1, 4)], axis=1)
+        assert np.all(kr[g, i0[r]] + kr[g, i1[r]] == pair_sums.max(axis=1))
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16"])
+def test_prune24_of_a_24_matrix_is_its_compression(dtype):
+    """A matrix that already has at most two nonzeros per group loses nothing: pruning
+    equals plain 2:4 compression (padding with the lowest zero positions)."""
+    if dtype == "i8":
+        A = gen.mask24_problem(32, 256, 1, seed=4)["A"]
+    else:
+        A = gen.mask24_float_problem(32, 256, 1, seed=4)["A"]
+    P, Cq = oracle.prune24(A, dtype), oracle.compress24(A, dtype)
+    assert np.array_equal(P["vals"], Cq["vals"]) and np.array_equal(P["meta"], Cq["meta"])
