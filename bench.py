@@ -404,6 +404,23 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             out["F"] = spmm.spmm_prune_24(A)
+    elif c["kind"] == "prunetvw":
+        # magnitude pruning of a dense fp16 N(0,1) matrix into TVW (given kept columns; a builder)
+        M, K, tr, keep = c["M"], c["K"], c["tile_rows"], c["keep"]
+        A = torch.randn((M, K), generator=g, device="cuda").to(torch.float16)
+        rng = np.random.default_rng(int(c["seed"]))
+        n_t = -(-M // tr)
+        cl = torch.from_numpy(np.concatenate([np.sort(rng.choice(K, keep, replace=False)) for _ in range(n_t)])
+                              .astype(np.int32)).cuda()
+        tp = torch.arange(0, n_t * keep + 1, keep, dtype=torch.int32, device="cuda")
+        build_ms = 0.0
+        nnz = M * keep // 2
+        alg = M * keep * 2 + n_t * keep * 4 + nnz * 2 + M * keep // 8
+        kern, kid = "tvw_build_kernel", None
+        out = {}
+
+        def step():
+            out["F"] = spmm.spmm_prune_tvw(A, tr, tp, cl, Kp=keep)
     elif c["kind"] == "wcsr":
         p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
         dt = torch.float16
@@ -426,18 +443,21 @@ def run_extra(name, args, ws, peaks, flush_buf):
             spmm.spmm_wcsr(F, Bx, Cd, wsp)
     else:
         raise ValueError(name)
-    flops = 2.0 * nnz * c["N"] if c["kind"] != "prune24" else 0.0
+    builder = c["kind"] in ("prune24", "prunetvw")
+    flops = 0.0 if builder else 2.0 * nnz * c["N"]
     spmm.trace_enable(True)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     spmm.trace_enable(True)
     total_ms = timed_steps(step, steps, 0, flush_buf, ws)
-    n, ms = spmm.trace_read(kid)
+    # untraced builder: a check and a build kernel per call
+    n, ms = spmm.trace_read(kid) if kid is not None else (2 * steps, 0.0)
     spmm.trace_enable(False)
     total_ms = max_over_ranks(total_ms, ws, "cuda")
-    t_kernel = ms / max(n, 1) / 1e3
-    rl = roofline(flops, alg, t_kernel, peaks, prefer="hbm" if c["kind"] == "prune24" else None,
+    # a builder without a traced kernel id (it synchronises inside): time the whole call
+    t_kernel = ms / max(n, 1) / 1e3 if kid is not None else total_ms / steps / 1e3
+    rl = roofline(flops, alg, t_kernel, peaks, prefer="hbm" if builder else None,
                   traffic=measured_traffic(kern, name))
     rl["kernel"] = kern
     rl["kernel_ms"] = round(t_kernel * 1e3, 4)
@@ -523,7 +543,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other formats")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, mask24_f16, prune24_f16, bcsr_tiny) and print its result; "
+                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, mask24_f16, prune24_f16, prune_tvw_f16, bcsr_tiny) "
+                         "and print its result; "
                          "for profiling runs, not the benchmark line")
     ap.add_argument("--n", type=int, default=0, help="with --only: override the workload's N")
     args = ap.parse_args()
@@ -555,7 +576,7 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "prune24_f16", "bcsr_tiny"):
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "prune24_f16", "prune_tvw_f16", "bcsr_tiny"):
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden

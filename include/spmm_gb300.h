@@ -293,6 +293,17 @@ SPMM_API spmm_status spmm_build_tvw(const void *dense, int64_t M, int64_t K, int
                                     int32_t tile_rows, const int32_t *tile_ptr, const int32_t *cols,
                                     int64_t n_tiles, int64_t Kp, void *vals, uint8_t *meta, spmm_stream_t stream);
 
+/* Magnitude pruning into TVW ("Accelerating Sparse DNNs Based on Tiled GEMM",
+ * abstract: tile-wise pattern with 2:4 inside): arguments, layout and output
+ * as spmm_build_tvw, but entries outside a tile's kept columns are dropped and
+ * each group of 4 consecutive kept columns keeps its two largest magnitudes
+ * (ties to the lower index; magnitude as for spmm_prune_24).  The kept columns
+ * are still checked (ascending, inside [0, K)) -> SPMM_ERR_FORMAT; the matrix
+ * values never cause an error.  Synchronises `stream`. */
+SPMM_API spmm_status spmm_prune_tvw(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
+                                    int32_t tile_rows, const int32_t *tile_ptr, const int32_t *cols, int64_t n_tiles,
+                                    int64_t Kp, void *vals, uint8_t *meta, spmm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

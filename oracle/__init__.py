@@ -79,6 +79,8 @@ def lib():
         L.orc_densify24.argtypes = [I64, I64, I32, P, P, P]
         L.orc_prune24.restype = I32
         L.orc_prune24.argtypes = [P, I64, I64, I64, I32, P, P]
+        L.orc_prune_tvw.restype = I32
+        L.orc_prune_tvw.argtypes = [P, I64, I64, I64, I32, I32, P, P, I64, P, P]
         L.orc_spmm24_f64.argtypes = [I64, I64, I32, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_spmm24_i64.argtypes = [I64, I64, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_tvw_build.restype = I32
@@ -303,6 +305,26 @@ def tvw_build(A, tile_rows, tile_ptr, cols, dtype, Kp=None):
                              _p(vals), _p(meta))
     if rc:
         raise OracleError(f"tvw error {rc}")
+    return {"M": M, "K": K, "dtype": dtype, "tile_rows": tile_rows, "tile_ptr": tile_ptr,
+            "cols": cols, "Kp": Kp, "vals": vals, "meta": meta}
+
+
+def prune_tvw(A, tile_rows, tile_ptr, cols, dtype, Kp=None):
+    """Magnitude pruning into TVW: entries outside each tile's kept columns dropped,
+    2:4 by magnitude inside (ties to the lower index)."""
+    A = _c(A, _edt(dtype))
+    M, K = A.shape
+    tile_ptr = _c(tile_ptr, np.int32)
+    cols = _c(cols, np.int32)
+    kt_max = int(np.max(np.diff(tile_ptr))) if tile_ptr.shape[0] > 1 else 0
+    if Kp is None:
+        Kp = max(8, -(-kt_max // 8) * 8)
+    vals = np.zeros((M, Kp // 2), dtype=_edt(dtype))
+    meta = np.zeros((M, Kp // 8), dtype=np.uint8)
+    rc = lib().orc_prune_tvw(_p(A), M, K, K, DTYPES[dtype], tile_rows, _p(tile_ptr), _p(cols), Kp,
+                             _p(vals), _p(meta))
+    if rc:
+        raise OracleError(f"prune_tvw error {rc}")
     return {"M": M, "K": K, "dtype": dtype, "tile_rows": tile_rows, "tile_ptr": tile_ptr,
             "cols": cols, "Kp": Kp, "vals": vals, "meta": meta}
 

@@ -430,6 +430,55 @@ int orc_prune24(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, void
     return ORC_OK;
 }
 
+/* Magnitude pruning into the tile-vector-wise format ("Accelerating Sparse DNNs
+ * Based on Tiled GEMM", abstract: tile-wise column selection, 2:4 inside).
+ * The kept columns of each row tile are an input (ascending, inside [0, K));
+ * entries outside them are dropped, and each group of 4 consecutive kept
+ * columns keeps its two largest magnitudes (ties to the lower index), as in
+ * orc_prune24.  Groups past a tile's kept count are padding: value 0, nibble
+ * (0, 1). */
+int orc_prune_tvw(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, int tile_rows,
+                  const int32_t *tile_ptr, const int32_t *cols, int64_t Kp, void *vals, uint8_t *meta) {
+    if (tile_rows <= 0 || Kp % 8) return ORC_ERR_SHAPE;
+    int64_t nt = (M + tile_rows - 1) / tile_rows, lm = Kp / 8;
+    for (int64_t t = 0; t < nt; t++) {
+        int64_t kb = tile_ptr[t], Kt = tile_ptr[t + 1] - kb;
+        if (Kt < 0 || Kt % 4 || Kt > Kp) return ORC_ERR_SHAPE;
+        for (int64_t q = 0; q < Kt; q++) {
+            if (cols[kb + q] < 0 || cols[kb + q] >= K) return ORC_ERR_FORMAT;
+            if (q && cols[kb + q] <= cols[kb + q - 1]) return ORC_ERR_FORMAT;
+        }
+        int64_t rb = t * tile_rows, re = rb + tile_rows < M ? rb + tile_rows : M;
+        for (int64_t i = rb; i < re; i++) {
+            for (int64_t j = 0; j < lm; j++) meta[i * lm + j] = 0;
+            for (int64_t g = 0; g < Kp / 4; g++) {
+                int i0 = 0, i1 = 1;
+                if (4 * g < Kt) {
+                    int64_t at[4];
+                    for (int p = 0; p < 4; p++) at[p] = i * ld + cols[kb + 4 * g + p];
+                    int first = 0;
+                    for (int q = 1; q < 4; q++)
+                        if (mag_key(A, at[q], dtype) > mag_key(A, at[first], dtype)) first = q;
+                    int second = -1;
+                    for (int q = 0; q < 4; q++) {
+                        if (q == first) continue;
+                        if (second < 0 || mag_key(A, at[q], dtype) > mag_key(A, at[second], dtype)) second = q;
+                    }
+                    i0 = first < second ? first : second;
+                    i1 = first < second ? second : first;
+                    copy_elem(vals, i * (Kp / 2) + 2 * g, A, at[i0], dtype);
+                    copy_elem(vals, i * (Kp / 2) + 2 * g + 1, A, at[i1], dtype);
+                } else {
+                    zero_elem(vals, i * (Kp / 2) + 2 * g, dtype);
+                    zero_elem(vals, i * (Kp / 2) + 2 * g + 1, dtype);
+                }
+                meta[i * lm + g / 2] |= (uint8_t)((i0 | (i1 << 2)) << (4 * (g % 2)));
+            }
+        }
+    }
+    return ORC_OK;
+}
+
 void orc_densify24(int64_t M, int64_t K, int dtype, const void *vals, const uint8_t *meta, void *D) {
     int64_t G = K / 4, lm = (K + 7) / 8;
     memset(D, 0, (size_t)(M * K * esize(dtype)));

@@ -26,7 +26,7 @@ from ._lib import SpmmError
 
 __all__ = ["BCSR", "Mat24", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bcsr", "spmm_build_bcsr_count",
            "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_prune_24", "spmm_24", "spmm_24_workspace_size",
-           "spmm_build_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
+           "spmm_build_tvw", "spmm_prune_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
            "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
 
@@ -272,6 +272,23 @@ def spmm_build_tvw(dense: torch.Tensor, tile_rows: int, tile_ptr: torch.Tensor, 
     vals = torch.empty((M, Kp // 2), dtype=dense.dtype, device=dense.device)
     meta = torch.empty((M, Kp // 8), dtype=torch.uint8, device=dense.device)
     _lib.call("spmm_build_tvw", _ptr(dense), M, K, dense.stride(0), _code(dense.dtype), tile_rows, _ptr(tile_ptr),
+              _ptr(cols), n_tiles, Kp, _ptr(vals), _ptr(meta), _stream(stream))
+    return TVW(M, K, tile_rows, dense.dtype, n_tiles, Kp, tile_ptr, cols, vals, meta)
+
+
+
+def spmm_prune_tvw(dense: torch.Tensor, tile_rows: int, tile_ptr: torch.Tensor, cols: torch.Tensor,
+                   Kp: Optional[int] = None, stream=None) -> TVW:
+    """Magnitude-prune a dense matrix into TVW (kept columns given; 2:4 by magnitude inside)."""
+    _check_dev(dense, tile_ptr, cols)
+    M, K = dense.shape
+    n_tiles = (M + tile_rows - 1) // tile_rows
+    if Kp is None:
+        kt = int((tile_ptr[1:] - tile_ptr[:-1]).max().item()) if n_tiles else 0
+        Kp = max(128, -(-kt // 128) * 128)
+    vals = torch.empty((M, Kp // 2), dtype=dense.dtype, device=dense.device)
+    meta = torch.empty((M, Kp // 8), dtype=torch.uint8, device=dense.device)
+    _lib.call("spmm_prune_tvw", _ptr(dense), M, K, dense.stride(0), _code(dense.dtype), tile_rows, _ptr(tile_ptr),
               _ptr(cols), n_tiles, Kp, _ptr(vals), _ptr(meta), _stream(stream))
     return TVW(M, K, tile_rows, dense.dtype, n_tiles, Kp, tile_ptr, cols, vals, meta)
 

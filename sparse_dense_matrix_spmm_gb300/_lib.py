@@ -71,6 +71,7 @@ SIGNATURES = {
     "spmm_compress_24": (I32, [P, I64, I64, I64, I32, P, P, P]),
     "spmm_prune_24": (I32, [P, I64, I64, I64, I32, P, P, P]),
     "spmm_build_tvw": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, I64, P, P, P]),
+    "spmm_prune_tvw": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, I64, P, P, P]),
 }
 
 _lib = None

@@ -282,9 +282,9 @@ spmm_status spmm_prune_24(const void* dense, int64_t M, int64_t K, int64_t ld, i
     return run_prune24(dense, M, K, ld, dtype, vals, meta, reinterpret_cast<cudaStream_t>(stream));
 }
 
-spmm_status spmm_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
-                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
-                           uint8_t* meta, spmm_stream_t stream) {
+static spmm_status tvw_build_checked(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
+                                     int32_t tile_rows, const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles,
+                                     int64_t Kp, void* vals, uint8_t* meta, bool prune, spmm_stream_t stream) {
     if (M > 0 && (!dense || !tile_ptr || !vals || !meta)) return SPMM_ERR_NULL;
     if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
     if (M < 0 || K < 0 || ld < K || tile_rows <= 0 || Kp < 0 || Kp % 8) return SPMM_ERR_SHAPE;
@@ -303,7 +303,21 @@ spmm_status spmm_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, 
         if (kt < 0 || kt % 4 || kt > Kp) return SPMM_ERR_FORMAT;
     }
     if (tp[n_tiles] > 0 && !cols) return SPMM_ERR_NULL;
-    return run_build_tvw(dense, M, K, ld, dtype, tile_rows, tile_ptr, cols, n_tiles, Kp, vals, meta, s);
+    return run_build_tvw(dense, M, K, ld, dtype, tile_rows, tile_ptr, cols, n_tiles, Kp, vals, meta, prune, s);
+}
+
+spmm_status spmm_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
+                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
+                           uint8_t* meta, spmm_stream_t stream) {
+    return tvw_build_checked(dense, M, K, ld, dtype, tile_rows, tile_ptr, cols, n_tiles, Kp, vals, meta, false,
+                             stream);
+}
+
+spmm_status spmm_prune_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
+                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
+                           uint8_t* meta, spmm_stream_t stream) {
+    return tvw_build_checked(dense, M, K, ld, dtype, tile_rows, tile_ptr, cols, n_tiles, Kp, vals, meta, true,
+                             stream);
 }
 
 static spmm_status check_csr(const spmm_csr_t* A, int32_t h, int32_t S) {

@@ -256,6 +256,20 @@ __device__ __forceinline__ unsigned mag_key<uint16_t>(uint16_t v) {
     return v & 0x7FFFu;
 }
 
+// The two positions of largest key (lowest index among equals), ascending.
+__device__ __forceinline__ void top2(const unsigned (&key)[4], int& i0, int& i1) {
+    int first = 0;
+#pragma unroll
+    for (int p = 1; p < 4; ++p)
+        if (key[p] > key[first]) first = p;
+    int second = first == 0 ? 1 : 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        if (p != first && p > second && key[p] > key[second]) second = p;
+    i0 = min(first, second);
+    i1 = max(first, second);
+}
+
 // One thread per (row, meta byte) = 2 groups = 8 dense columns.
 template <typename T>
 __global__ void prune24_kernel(const T* __restrict__ dense, int64_t M, int64_t K, int64_t ld, T* __restrict__ vals,
@@ -273,15 +287,8 @@ __global__ void prune24_kernel(const T* __restrict__ dense, int64_t M, int64_t K
             unsigned key[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) key[p] = mag_key<T>(x[4 * h + p]);
-            int first = 0;  // largest key, lowest index among equals
-#pragma unroll
-            for (int p = 1; p < 4; ++p)
-                if (key[p] > key[first]) first = p;
-            int second = first == 0 ? 1 : 0;  // largest of the other three, lowest index among equals
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-                if (p != first && p > second && key[p] > key[second]) second = p;
-            const int i0 = min(first, second), i1 = max(first, second);
+            int i0, i1;
+            top2(key, i0, i1);
             out[2 * h] = x[4 * h + i0];
             out[2 * h + 1] = x[4 * h + i1];
             byte |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
@@ -306,7 +313,10 @@ __global__ void tvw_check_cols_kernel(const int32_t* tile_ptr, const int32_t* co
 
 // One CTA per row.  Every nonzero of the row must sit in a kept column; then
 // each group of 4 kept columns is compressed to 2:4.
-template <typename T>
+// PRUNE (magnitude pruning into TVW): entries outside the kept columns are
+// dropped instead of rejected, and each group of 4 kept columns keeps its two
+// largest magnitudes instead of requiring at most two nonzeros.
+template <typename T, bool PRUNE>
 __global__ void tvw_build_kernel(const T* dense, int64_t M, int64_t K, int64_t ld, int tile_rows,
                                  const int32_t* tile_ptr, const int32_t* cols, int64_t Kp, T* vals, uint8_t* meta,
                                  int* err) {
@@ -315,16 +325,18 @@ __global__ void tvw_build_kernel(const T* dense, int64_t M, int64_t K, int64_t l
     const int64_t t = i / tile_rows;
     const int32_t kb = tile_ptr[t], Kt = tile_ptr[t + 1] - kb;
     const T* row = dense + i * ld;
-    int32_t all = 0, kept = 0;
-    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) all += nz<T>(row[k]);
-    for (int32_t q = threadIdx.x; q < Kt; q += blockDim.x) {
-        const int32_t c = cols[kb + q];
-        if (c >= 0 && c < K) kept += nz<T>(row[c]);
+    if (!PRUNE) {
+        int32_t all = 0, kept = 0;
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) all += nz<T>(row[k]);
+        for (int32_t q = threadIdx.x; q < Kt; q += blockDim.x) {
+            const int32_t c = cols[kb + q];
+            if (c >= 0 && c < K) kept += nz<T>(row[c]);
+        }
+        int32_t tall = 0, tkept = 0;
+        block_exclusive_scan(all, &tall, sh);
+        block_exclusive_scan(kept, &tkept, sh);
+        if (threadIdx.x == 0 && tall != tkept) atomicOr(err, SPMM_DEVERR_FORMAT);
     }
-    int32_t tall = 0, tkept = 0;
-    block_exclusive_scan(all, &tall, sh);
-    block_exclusive_scan(kept, &tkept, sh);
-    if (threadIdx.x == 0 && tall != tkept) atomicOr(err, SPMM_DEVERR_FORMAT);
     const int64_t nb = Kp / 8;
     for (int64_t j = threadIdx.x; j < nb; j += blockDim.x) {
         uint8_t byte = 0;
@@ -334,14 +346,17 @@ __global__ void tvw_build_kernel(const T* dense, int64_t M, int64_t K, int64_t l
             int i0 = 0, i1 = 1;
             if (4 * g < Kt) {
                 T v[4];
-                unsigned mask = 0;
+                unsigned mask = 0, key[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     const int32_t c = cols[kb + 4 * g + p];
                     v[p] = (c >= 0 && c < K) ? row[c] : T(0);
                     if (nz<T>(v[p])) mask |= 1u << p;
+                    key[p] = mag_key<T>(v[p]);
                 }
-                if (!pick2(mask, i0, i1)) {
+                if (PRUNE) {
+                    top2(key, i0, i1);
+                } else if (!pick2(mask, i0, i1)) {
                     atomicOr(err, SPMM_DEVERR_FORMAT);
                     i0 = 0;
                     i1 = 1;
@@ -461,7 +476,7 @@ spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int
 
 spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
-                          uint8_t* meta, cudaStream_t s) {
+                          uint8_t* meta, bool prune, cudaStream_t s) {
     std::lock_guard<std::mutex> lock(g_build_mu);
     int* e = build_err_ptr();
     if (!e) return SPMM_ERR_CUDA;
@@ -470,14 +485,19 @@ spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, i
     if (n_tiles > 0)
         tvw_check_cols_kernel<<<static_cast<unsigned>(n_tiles), 256, 0, s>>>(tile_ptr, cols, n_tiles, K, e);
     if (M > 0) {
+        auto run = [&](auto tag, const auto* d, auto* v) {
+            using T = decltype(tag);
+            if (prune)
+                tvw_build_kernel<T, true><<<static_cast<unsigned>(M), 256, 0, s>>>(d, M, K, ld, tile_rows, tile_ptr,
+                                                                                    cols, Kp, v, meta, e);
+            else
+                tvw_build_kernel<T, false><<<static_cast<unsigned>(M), 256, 0, s>>>(d, M, K, ld, tile_rows, tile_ptr,
+                                                                                     cols, Kp, v, meta, e);
+        };
         if (dtype == SPMM_I8)
-            tvw_build_kernel<int8_t><<<static_cast<unsigned>(M), 256, 0, s>>>(
-                static_cast<const int8_t*>(dense), M, K, ld, tile_rows, tile_ptr, cols, Kp,
-                static_cast<int8_t*>(vals), meta, e);
+            run(int8_t{}, static_cast<const int8_t*>(dense), static_cast<int8_t*>(vals));
         else
-            tvw_build_kernel<uint16_t><<<static_cast<unsigned>(M), 256, 0, s>>>(
-                static_cast<const uint16_t*>(dense), M, K, ld, tile_rows, tile_ptr, cols, Kp,
-                static_cast<uint16_t*>(vals), meta, e);
+            run(uint16_t{}, static_cast<const uint16_t*>(dense), static_cast<uint16_t*>(vals));
     }
     return build_end(e, s);
 }

@@ -78,6 +78,6 @@ spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int
                         uint8_t* meta, cudaStream_t stream);
 spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
-                          uint8_t* meta, cudaStream_t s);
+                          uint8_t* meta, bool prune, cudaStream_t s);
 
 }  // namespace spmm

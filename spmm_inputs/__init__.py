@@ -195,6 +195,7 @@ CONFIGS = {
     "mask24_int8": dict(kind="24", M=8192, K=8192, N=4096, seed=2),
     "mask24_f16": dict(kind="24f", M=8192, K=8192, N=4096, seed=6, dtype=F16),
     "prune24_f16": dict(kind="prune24", M=8192, K=8192, N=0, seed=7, dtype=F16),
+    "prune_tvw_f16": dict(kind="prunetvw", M=4096, K=4096, N=0, tile_rows=128, keep=2048, seed=8, dtype=F16),
     "wcsr_lognormal": dict(kind="wcsr", M=65536, K=65536, N=128, seed=3, mean=16.0,
                            sigma=1.5, clip=4096, dtype=F16),
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
@@ -221,7 +222,7 @@ def config_problem(name: str, **overrides) -> dict:
     if kind == "tvw":
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))
-    if kind == "prune24":  # a dense matrix to prune into 2:4
+    if kind in ("prune24", "prunetvw"):  # a dense matrix to prune (into 2:4, or into TVW given kept columns)
         rng = np.random.default_rng(c["seed"])
         return {"A": normal_bits(rng, (c["M"], c["K"]), c.get("dtype", F16)), "M": c["M"], "K": c["K"],
                 "dtype": c.get("dtype", F16)}

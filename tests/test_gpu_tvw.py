@@ -65,3 +65,29 @@ def test_tvw_full_size_sampled_rows():
     got = C[torch.from_numpy(rows).cuda()].cpu().numpy()
     ref = np.concatenate([oracle.tvw_spmm(O, p["B"], rows=(int(r), int(r) + 1)) for r in rows])
     assert_close(got, ref, "tvw full-size rows")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tvw_prune_bit_exact_and_spmm(dtype):
+    """Magnitude pruning of a dense matrix into TVW on the GPU equals the oracle's bit
+    for bit (ragged kept counts, an empty tile), and the pruned operand multiplies
+    within tolerance."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    rng = np.random.default_rng(17)
+    M, K, N = 300, 640, 136
+    A = gen.normal_bits(rng, (M, K), dtype)
+    A[rng.random((M, K)) < 0.1] = 0
+    counts = [256, 100, 0]
+    cols = np.concatenate([np.sort(rng.choice(K, c, replace=False)) for c in counts]).astype(np.int32)
+    tp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    F = spmm.spmm_prune_tvw(dev_half(A, dtype), 128, dev(tp), dev(cols), Kp=256)
+    O = oracle.prune_tvw(A, 128, tp, cols, dtype, Kp=256)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(F.vals), O["vals"])
+    assert np.array_equal(F.meta.cpu().numpy(), O["meta"])
+    B = gen.normal_bits(rng, (K, N), dtype)
+    C = spmm.spmm_tvw(F, padded_b(B, dtype))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert_close(C.cpu().numpy(), oracle.tvw_spmm(O, B), f"pruned tvw {dtype}")

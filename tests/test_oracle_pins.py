@@ -363,3 +363,36 @@ def test_prune24_of_a_24_matrix_is_its_compression(dtype):
         A = gen.mask24_float_problem(32, 256, 1, seed=4)["A"]
     P, Cq = oracle.prune24(A, dtype), oracle.compress24(A, dtype)
     assert np.array_equal(P["vals"], Cq["vals"]) and np.array_equal(P["meta"], Cq["meta"])
+
+
+def _kept_cols(rng, M, K, tile_rows, keep):
+    n_tiles = -(-M // tile_rows)
+    cols = np.concatenate([np.sort(rng.choice(K, keep, replace=False)) for _ in range(n_tiles)]).astype(np.int32)
+    return np.arange(0, n_tiles * keep + 1, keep, dtype=np.int32), cols
+
+
+@pytest.mark.parametrize("dtype", ["i8", "bf16"])
+def test_prune_tvw_is_prune24_on_the_gathered_columns(dtype):
+    """Pruning into TVW equals 2:4 pruning of each tile's kept columns gathered into a
+    dense block, and drops everything outside them."""
+    rng = np.random.default_rng(5)
+    M, K, tr, keep = 40, 96, 16, 32
+    A = rng.integers(-5, 6, size=(M, K)).astype(np.int8) if dtype == "i8" else gen.normal_bits(rng, (M, K), dtype)
+    tp, cols = _kept_cols(rng, M, K, tr, keep)
+    F = oracle.prune_tvw(A, tr, tp, cols, dtype, Kp=keep)
+    for t in range(len(tp) - 1):
+        kc = cols[tp[t]:tp[t + 1]]
+        rows = slice(t * tr, min(M, (t + 1) * tr))
+        P = oracle.prune24(np.ascontiguousarray(A[rows][:, kc]), dtype)
+        assert np.array_equal(F["vals"][rows], P["vals"]) and np.array_equal(F["meta"][rows], P["meta"])
+    D = oracle.tvw_densify(F)
+    for t in range(len(tp) - 1):
+        outside = np.setdiff1d(np.arange(K), cols[tp[t]:tp[t + 1]])
+        assert not (D[t * tr:(t + 1) * tr][:, outside].astype(np.int64) & 0xFFFF).any()
+
+
+def test_prune_tvw_of_a_tvw_matrix_is_its_build():
+    p = gen.tvw_problem(256, 512, 8, tile_rows=128, keep=256, seed=9)
+    P = oracle.prune_tvw(p["A"], 128, p["tile_ptr"], p["cols"], "f16")
+    B = oracle.tvw_build(p["A"], 128, p["tile_ptr"], p["cols"], "f16")
+    assert np.array_equal(P["vals"], B["vals"]) and np.array_equal(P["meta"], B["meta"])
