@@ -81,6 +81,10 @@ def lib():
         L.orc_prune24.argtypes = [P, I64, I64, I64, I32, P, P]
         L.orc_prune_tvw.restype = I32
         L.orc_prune_tvw.argtypes = [P, I64, I64, I64, I32, I32, P, P, I64, P, P]
+        L.orc_slide_src.restype = I64
+        L.orc_slide_src.argtypes = [I64, I64, I32]
+        L.orc_slide_decompose.restype = I32
+        L.orc_slide_decompose.argtypes = [P, I64, I64, I64, I32, I32, P]
         L.orc_spmm24_f64.argtypes = [I64, I64, I32, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_spmm24_i64.argtypes = [I64, I64, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_tvw_build.restype = I32
@@ -288,6 +292,49 @@ def spmm24(F, B, rows=None, cols=None):
         lib().orc_spmm24_f64(F["M"], F["K"], DTYPES[F["dtype"]], _p(H["vals"]), _p(H["meta"]),
                              _p(B), B.shape[1], r0, r1, _p(colarr), ncols, _p(out))
     return out
+
+
+# ------------------------------------------------------------------ (2n-2):2n
+def slide_lifted_k(K, n):
+    """Lifted depth K' = 4 (n - 1) K / 2n: n - 1 windows of 4 per group of 2n."""
+    return 4 * (n - 1) * (K // (2 * n))
+
+
+def slide_src(K, n):
+    """Original column (= row of B) read by every lifted column, window-plane order."""
+    return np.array([lib().orc_slide_src(q, K, n) for q in range(slide_lifted_k(K, n))], dtype=np.int64)
+
+
+def slide_decompose(A, n, dtype):
+    """Dense (2n-2):2n matrix -> dense lifted matrix (M x K'), each nonzero in
+    exactly one window and every window 2:4."""
+    A = _c(A, _edt(dtype))
+    M, K = A.shape
+    L = np.zeros((M, slide_lifted_k(K, n)), dtype=_edt(dtype))
+    rc = lib().orc_slide_decompose(_p(A), M, K, K, DTYPES[dtype], n, _p(L))
+    if rc:
+        raise OracleError(f"slide_decompose error {rc}")
+    return L
+
+
+def slide_build(A, n, dtype):
+    """(2n-2):2n -> the lifted operand in the 2:4 format: vals[M][K'/2] and
+    meta[M][K'/8], as compress24 of the lifted matrix.  "K" is the original depth."""
+    M, K = np.shape(A)
+    F = compress24(slide_decompose(A, n, dtype), dtype)
+    return {"M": M, "K": K, "n": n, "dtype": dtype, "vals": F["vals"], "meta": F["meta"]}
+
+
+def slide_lift_b(B, K, n):
+    """Activation lifting: lifted row q of B is original row slide_src(K, n)[q]."""
+    return np.ascontiguousarray(np.asarray(B)[slide_src(K, n)])
+
+
+def slide_spmm(F, B, rows=None, cols=None):
+    """C = A_lifted * lift(B), through the 2:4 SpMM of the lifted operand."""
+    Kl = slide_lifted_k(F["K"], F["n"])
+    G = {"M": F["M"], "K": Kl, "dtype": F["dtype"], "vals": F["vals"], "meta": F["meta"]}
+    return spmm24(G, slide_lift_b(B, F["K"], F["n"]), rows, cols)
 
 
 # ------------------------------------------------------------------ TVW

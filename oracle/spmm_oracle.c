@@ -479,6 +479,67 @@ int orc_prune_tvw(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, in
     return ORC_OK;
 }
 
+/* ================================================================== (2n-2):2n
+ * "SlideSparse" (abstract): a (2n-2):2n block is rewritten as n-1 overlapping
+ * 2:4 windows and the activations are rearranged to match.  Group g of a row
+ * is columns 2n g .. 2n g + 2n - 1 (at most 2n - 2 nonzero); window j of the
+ * group (0 <= j < n - 1) covers the group's positions 2j .. 2j + 3, i.e. the
+ * pairs j and j + 1, so pair 0 and pair n - 1 lie in one window each and every
+ * other pair in two.
+ *
+ * Lifted order (a reading; the pages fix none): with G = K / 2n groups, the
+ * lifted operand has K' = 4 (n - 1) G columns, window j of group g occupying
+ * lifted columns 4 (j G + g) .. 4 (j G + g) + 3 ("window planes": all groups'
+ * window 0, then all groups' window 1, ...).  Lifted column 4 (j G + g) + p
+ * therefore reads original column 2n g + 2j + p; the same map lifts B's rows.
+ *
+ * Assignment of the nonzeros to windows (a reading; the pages state only that
+ * the decomposition is exact): windows are filled in order j = 0, 1, ...;
+ * window j first takes every nonzero of pair j that window j - 1 left (no later
+ * window covers them), then the nonzeros of pair j + 1 in ascending position
+ * while it holds fewer than two.  This earliest-deadline order places every
+ * nonzero whenever the group has at most 2n - 2 of them (pairs a..b reach
+ * windows a-1..b, which hold at least as many entries as the pairs unless the
+ * range is the whole group).  Each window then holds at most two nonzeros, so
+ * the lifted matrix is 2:4 and compresses with the ordinary 2:4 rule. */
+
+/* Original column of lifted column q (window planes). */
+static int64_t slide_src(int64_t q, int64_t G, int n) {
+    int64_t w = q / 4, p = q % 4, j = w / G, g = w % G;
+    return 2 * n * g + 2 * j + p;
+}
+
+int64_t orc_slide_src(int64_t q, int64_t K, int n) { return slide_src(q, K / (2 * n), n); }
+
+/* dense A (M x K, leading dim ld) -> dense lifted L (M x K', leading dim K'),
+ * every nonzero of A placed in exactly one window, zeros elsewhere. */
+int orc_slide_decompose(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, int n, void *L) {
+    if (n < 2 || n > 32 || K % (2 * n)) return ORC_ERR_SHAPE;
+    int64_t G = K / (2 * n), Kl = 4 * (n - 1) * G;
+    for (int64_t i = 0; i < M; i++) {
+        for (int64_t q = 0; q < Kl; q++) zero_elem(L, i * Kl + q, dtype);
+        for (int64_t g = 0; g < G; g++) {
+            int64_t base = i * ld + 2 * n * g;
+            int nzc = 0, placed[64] = {0};
+            for (int t = 0; t < 2 * n; t++) nzc += !is_zero(A, base + t, dtype);
+            if (nzc > 2 * n - 2) return ORC_ERR_FORMAT;
+            for (int j = 0; j < n - 1; j++) {
+                int held = 0;
+                for (int t = 2 * j; t < 2 * j + 4; t++) {
+                    if (placed[t] || is_zero(A, base + t, dtype)) continue;
+                    if (held == 2) break; /* only pair j + 1 can be left for window j + 1 */
+                    placed[t] = 1;
+                    held++;
+                    copy_elem(L, i * Kl + 4 * (j * G + g) + (t - 2 * j), A, base + t, dtype);
+                }
+            }
+            for (int t = 0; t < 2 * n; t++)
+                if (!placed[t] && !is_zero(A, base + t, dtype)) return ORC_ERR_FORMAT;
+        }
+    }
+    return ORC_OK;
+}
+
 void orc_densify24(int64_t M, int64_t K, int dtype, const void *vals, const uint8_t *meta, void *D) {
     int64_t G = K / 4, lm = (K + 7) / 8;
     memset(D, 0, (size_t)(M * K * esize(dtype)));

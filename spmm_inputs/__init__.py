@@ -35,7 +35,7 @@ BF16, F16, I8 = "bf16", "f16", "i8"
 
 __all__ = [
     "BF16", "F16", "I8", "round_f32_to_bf16_bits", "normal_bits", "mask24_float_problem",
-    "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem",
+    "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem", "slide_problem",
     "CONFIGS", "config_problem",
 ]
 
@@ -120,6 +120,34 @@ def mask24_float_problem(M: int, K: int, N: int, seed: int, dtype: str = F16) ->
     return {"A": A, "B": B, "M": M, "K": K, "N": N, "dtype": dtype}
 
 
+def slide_problem(M: int, K: int, N: int, n: int, seed: int, dtype: str = F16) -> dict:
+    """(2n-2):2n A: in every group of 2n consecutive K-entries two positions, uniform
+    over the pairs, are zero and the other 2n - 2 hold values (int8: nonzero, sign
+    and magnitude uniform; 16-bit: N(0,1), which may round to zero); B (K x N) of the
+    same type.  n = 4 is the 6:8 pattern (25% of the weights pruned)."""
+    assert n >= 2 and K % (2 * n) == 0
+    rng = np.random.default_rng(seed)
+    G = K // (2 * n)
+    if dtype == I8:
+        mag = rng.integers(1, 128, size=(M, K), dtype=np.int16)
+        sgn = rng.integers(0, 2, size=(M, K), dtype=np.int16) * 2 - 1
+        A = (mag * sgn).astype(np.int8)
+        B = rng.integers(-127, 128, size=(K, N), dtype=np.int16).astype(np.int8)
+    else:
+        A = normal_bits(rng, (M, K), dtype)
+        B = None
+    # two distinct zero positions per group: first uniform on 2n, second uniform on the rest
+    z0 = rng.integers(0, 2 * n, size=(M, G))
+    z1 = (z0 + 1 + rng.integers(0, 2 * n - 1, size=(M, G))) % (2 * n)
+    base = (np.arange(G, dtype=np.int64) * 2 * n)[None, :]
+    rows = np.broadcast_to(np.arange(M, dtype=np.int64)[:, None], (M, G))
+    A[rows, base + z0] = 0
+    A[rows, base + z1] = 0
+    if B is None:
+        B = normal_bits(rng, (K, N), dtype)
+    return {"A": A, "B": B, "M": M, "K": K, "N": N, "n": n, "dtype": dtype}
+
+
 def _unique_sorted_rows(rng, lengths: np.ndarray, K: int):
     """Per row, ``lengths[r]`` distinct columns uniform on [0, K), ascending."""
     M = lengths.shape[0]
@@ -201,6 +229,8 @@ CONFIGS = {
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
                      dtype=BF16, std=0.02),
     "tvw": dict(kind="tvw", M=4096, K=4096, N=4096, tile_rows=128, keep=2048, seed=5, dtype=F16),
+    # 6:8 on a Qwen2.5-7B-sized FFN projection (18944 x 3584), 8192 tokens
+    "slide68_f16": dict(kind="slide", M=18944, K=3584, N=8192, n=4, seed=9, dtype=F16),
 }
 
 
@@ -222,6 +252,8 @@ def config_problem(name: str, **overrides) -> dict:
     if kind == "tvw":
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))
+    if kind == "slide":
+        return slide_problem(c["M"], c["K"], c["N"], c["n"], c["seed"], c.get("dtype", F16))
     if kind in ("prune24", "prunetvw"):  # a dense matrix to prune (into 2:4, or into TVW given kept columns)
         rng = np.random.default_rng(c["seed"])
         return {"A": normal_bits(rng, (c["M"], c["K"]), c.get("dtype", F16)), "M": c["M"], "K": c["K"],

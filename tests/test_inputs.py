@@ -49,3 +49,14 @@ def test_mask24_float_problem_two_kept_per_group():
     assert np.all(nz.sum(axis=2) <= 2) and nz.sum() >= 32 * 32 * 2 - 2
     q = gen.mask24_float_problem(32, 128, 4, seed=6)
     assert np.array_equal(p["A"], q["A"]) and np.array_equal(p["B"], q["B"])
+
+
+def test_slide_problem_two_zeros_per_group():
+    for n, dtype in ((4, gen.I8), (3, gen.I8), (4, gen.F16)):
+        p = gen.slide_problem(12, 16 * n, 5, n, seed=3, dtype=dtype)
+        nz = (p["A"].reshape(12, 8, 2 * n) != 0).sum(axis=2)
+        assert nz.max() <= 2 * n - 2
+        if dtype == gen.I8:
+            assert np.all(nz == 2 * n - 2)
+        q = gen.slide_problem(12, 16 * n, 5, n, seed=3, dtype=dtype)
+        assert np.array_equal(p["A"], q["A"]) and np.array_equal(p["B"], q["B"])

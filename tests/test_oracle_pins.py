@@ -396,3 +396,96 @@ def test_prune_tvw_of_a_tvw_matrix_is_its_build():
     P = oracle.prune_tvw(p["A"], 128, p["tile_ptr"], p["cols"], "f16")
     B = oracle.tvw_build(p["A"], 128, p["tile_ptr"], p["cols"], "f16")
     assert np.array_equal(P["vals"], B["vals"]) and np.array_equal(P["meta"], B["meta"])
+
+
+# ---------------------------------------------------------------- (2n-2):2n sliding windows
+def _fold_back(L, K, n):
+    """Sum every lifted column into the original column it reads (numpy, int64/f64)."""
+    src = oracle.slide_src(K, n)
+    out = np.zeros((L.shape[0], K), dtype=L.dtype)
+    np.add.at(out, (slice(None), src), L)
+    return out
+
+
+def test_slide_golden():
+    g = golden("slide68_int8_2x16.json")
+    A, B = np.array(g["A"], np.int8), np.array(g["B"], np.int8)
+    assert oracle.slide_src(16, g["n"]).tolist() == g["src"]
+    assert oracle.slide_decompose(A, g["n"], "i8").tolist() == g["L"]
+    F = oracle.slide_build(A, g["n"], "i8")
+    assert F["vals"].tolist() == g["vals"] and F["meta"].tolist() == g["meta"]
+    assert oracle.slide_spmm(F, B).tolist() == g["C"]
+
+
+def test_slide_window_map_covers_pairs():
+    """Window j of group g reads the group's columns 2j .. 2j+3: pairs 0 and n-1 are
+    read once, every inner pair twice (by windows j-1 and j), nothing else."""
+    for n in (2, 3, 4, 5, 8):
+        K = 2 * n * 3
+        src = oracle.slide_src(K, n)
+        assert src.shape[0] == 4 * (n - 1) * 3
+        counts = np.bincount(src, minlength=K).reshape(3, n, 2)
+        assert np.all(counts[:, 0] == 1) and np.all(counts[:, n - 1] == 1)
+        assert np.all(counts[:, 1:n - 1] == 2)
+        w = src.reshape(-1, 4)
+        assert np.all(np.diff(w, axis=1) == 1) and np.all(w[:, 0] % 2 == 0)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5])
+def test_slide_decompose_exhaustive_masks(n):
+    """Every mask of at most 2n-2 nonzeros in a 2n-group decomposes: each window
+    holds at most two nonzeros, and the lifted matrix folds back onto A exactly
+    (every nonzero lands in exactly one window)."""
+    import itertools
+    masks = [m for k in range(2 * n - 1) for m in itertools.combinations(range(2 * n), k)]
+    rng = np.random.default_rng(n)
+    A = np.zeros((len(masks), 4 * n), np.int8)            # two groups per row
+    for r, m in enumerate(masks):
+        for h in range(2):
+            for t in m:
+                A[r, 2 * n * h + t] = rng.integers(1, 128) * rng.choice([-1, 1])
+        A[r, 2 * n:] = np.roll(A[r, 2 * n:], r % (2 * n))  # second group: another mask
+    L = oracle.slide_decompose(A, n, "i8")
+    assert np.all((L.reshape(len(masks), -1, 4) != 0).sum(axis=2) <= 2)
+    assert np.array_equal(_fold_back(L.astype(np.int64), 4 * n, n), A.astype(np.int64))
+    assert np.count_nonzero(L) == np.count_nonzero(A)
+
+
+def test_slide_int8_exact_vs_int64_gemm():
+    """C = A B exactly (int64), whatever the decomposition, for 6:8 and 4:6."""
+    for n in (4, 3):
+        p = gen.slide_problem(40, 32 * n, 19, n, seed=12, dtype=gen.I8)
+        F = oracle.slide_build(p["A"], n, "i8")
+        assert np.array_equal(oracle.slide_spmm(F, p["B"]),
+                              p["A"].astype(np.int64) @ p["B"].astype(np.int64))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_slide_float_vs_dense_gemm(dtype):
+    p = gen.slide_problem(24, 64, 7, 4, seed=13, dtype=dtype)
+    F = oracle.slide_build(p["A"], 4, dtype)
+    ref = bits_to_f64(p["A"], dtype) @ bits_to_f64(p["B"], dtype)
+    np.testing.assert_allclose(oracle.slide_spmm(F, p["B"]), ref, rtol=1e-12, atol=1e-12)
+    # the lifted values are the original bit patterns (or +0 padding)
+    L = oracle.slide_decompose(p["A"], 4, dtype)
+    assert np.array_equal(_fold_back(L.astype(np.int64), 64, 4), p["A"].astype(np.int64) * (p["A"] & 0x7FFF != 0))
+
+
+def test_slide_n2_is_24_and_ratio():
+    """n = 2 is plain 2:4 (one window per group, the identity map); for 6:8 the
+    tensor-core depth is K (n-1)/n, the N/(N-1) = 4/3 bound the abstract states."""
+    p = gen.mask24_problem(16, 64, 3, seed=14)
+    F, G = oracle.slide_build(p["A"], 2, "i8"), oracle.compress24(p["A"], "i8")
+    assert np.array_equal(F["vals"], G["vals"]) and np.array_equal(F["meta"], G["meta"])
+    assert oracle.slide_src(64, 2).tolist() == list(range(64))
+    for K in (64, 3584, 8192):
+        assert K / (oracle.slide_lifted_k(K, 4) // 2) == 4 / 3
+
+
+def test_slide_errors():
+    A = np.zeros((2, 16), np.int8)
+    A[1, 8:15] = 3                                        # 7 nonzeros in a 6:8 group
+    with pytest.raises(oracle.OracleError):
+        oracle.slide_decompose(A, 4, "i8")
+    with pytest.raises(oracle.OracleError):
+        oracle.slide_decompose(np.zeros((2, 12), np.int8), 4, "i8")   # K % 8 != 0
