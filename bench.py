@@ -7,8 +7,9 @@ one spmm_24 call with A (already compressed) and B resident in HBM; the L2 is
 flushed (256 MiB written) before every timed step.  Metric: effective
 TFLOP/s = 2 * nnz * N / time.
 
-The same line carries, per other format (BCSR LLM-shaped, tile-vector-wise,
-row-window CSR, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
+The same line carries, per other workload (BCSR LLM-shaped, tile-vector-wise,
+row-window CSR, fp16 2:4, 6:8 through overlapping 2:4 windows, the two pruning
+builders, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -328,6 +329,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
     steps = max(3, min(args.steps, 10))
     g = torch.Generator(device="cuda")
     g.manual_seed(int(c["seed"]))
+    extra_fields = {}
     if c["kind"] == "bcsr":
         p = gen.bcsr_problem(c["M"], c["K"], 8, c["bh"], c["bw"], c["nnzb"], c["seed"], c["dtype"], c["std"])
         dt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float16
@@ -391,6 +393,42 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             spmm.spmm_24(F, Bx, Cd, wsp)
+    elif c["kind"] == "slide":
+        # (2n-2):2n, the same recipe as the host generator drawn on the device: per group of 2n
+        # two distinct zero positions, N(0,1) fp16 values elsewhere; B N(0,1) fp16
+        M, K, n = c["M"], c["K"], c["n"]
+        grp = 2 * n
+        z0 = torch.randint(0, grp, (M, K // grp), generator=g, device="cuda")
+        z1 = (z0 + 1 + torch.randint(0, grp - 1, (M, K // grp), generator=g, device="cuda")) % grp
+        pos = torch.arange(grp, device="cuda")
+        keep = ((pos != z0[..., None]) & (pos != z1[..., None])).reshape(M, K)
+        A = torch.randn((M, K), generator=g, device="cuda").to(torch.float16) * keep
+        del z0, z1, keep
+        Bx = torch.randn((K, c["N"]), generator=g, device="cuda").to(torch.float16)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        F = spmm.spmm_build_slide(A, n)
+        torch.cuda.synchronize()
+        build_ms = (time.perf_counter() - t0) * 1e3
+        # context: the dense fp16 GEMM (cuBLAS, fp16 out) of the same M x K x N on the unpruned shape
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for _ in range(3):
+            torch.mm(A, Bx)
+        ev[0].record()
+        for _ in range(5):
+            torch.mm(A, Bx)
+        ev[1].record()
+        torch.cuda.synchronize()
+        extra_fields["dense_cublas_fp16_ms"] = round(ev[0].elapsed_time(ev[1]) / 5, 4)
+        del A
+        Kl = F.K_lifted
+        Cd = torch.empty((M, c["N"]), dtype=torch.float32, device="cuda")
+        nnz = M * Kl // 2                      # = M K (n-1)/n stored nonzeros of the (2n-2):2n operand
+        alg = nnz * 2 + M * Kl // 8 + K * c["N"] * 2 + M * c["N"] * 4
+        kern, kid = "sparse_spmm_kernel", spmm._lib.KERNEL_SPARSE
+
+        def step():
+            spmm.spmm_slide(F, Bx, Cd)
     elif c["kind"] == "prune24":
         # magnitude pruning of a dense fp16 N(0,1) matrix into 2:4 (a builder: HBM-bound)
         M, K = c["M"], c["K"]
@@ -464,7 +502,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
     t_step = total_ms / steps / 1e3
     return {"workload": name, "ms_per_step": round(t_step * 1e3, 4),
             "tflops": round(ws * flops / t_step / 1e12, 3), "gbs": round(alg / t_step / 1e9, 1),
-            "nnz": int(nnz), "build_ms": round(build_ms, 2), "roofline": rl, "launches": n}
+            "nnz": int(nnz), "build_ms": round(build_ms, 2), "roofline": rl, "launches": n, **extra_fields}
 
 
 # ------------------------------------------------------------------ CPU oracle legs
@@ -576,7 +614,8 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "prune24_f16", "prune_tvw_f16", "bcsr_tiny"):
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "slide68_f16", "prune24_f16", "prune_tvw_f16",
+                     "bcsr_tiny"):
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden

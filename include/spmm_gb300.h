@@ -138,6 +138,23 @@ typedef struct {
     uint8_t *meta;
 } spmm_24_t;
 
+/* (2n-2):2n sparsity run as 2:4 ("SlideSparse", abstract: sliding window
+ * decomposition of a (2n-2):2n block into n-1 overlapping 2:4 windows, with
+ * the activations lifted to match).  Group g of a row is columns
+ * 2n g .. 2n g + 2n - 1; its window j (j < n - 1) covers the group's columns
+ * 2j .. 2j + 3.  With G = K / 2n groups the lifted depth is K' = 4 (n-1) G, and
+ * window j of group g is 2:4 group j G + g of the lifted row ("window
+ * planes"), so lifted column 4 (j G + g) + p is original column
+ * 2n g + 2j + p.  vals[M][K'/2] and meta[M][K'/8] store the lifted rows in the
+ * layout of spmm_24_t.  2 <= n <= 8; K is the original depth. */
+typedef struct {
+    int64_t M, K;
+    int32_t n;
+    int32_t dtype; /* SPMM_I8 (-> int32 C), SPMM_F16 or SPMM_BF16 (-> fp32 C) */
+    void *vals;
+    uint8_t *meta;
+} spmm_slide_t;
+
 /* Tile-vector-wise ("Accelerating Sparse DNNs Based on Tiled GEMM",
  * abstract).  Rows form tiles of tile_rows rows; tile t keeps the ascending
  * columns cols[tile_ptr[t] .. tile_ptr[t+1]) (Kt entries, Kt % 4 == 0); each
@@ -233,6 +250,19 @@ SPMM_API spmm_status spmm_24(const spmm_24_t *A, const void *B, int64_t ldb, voi
 SPMM_API spmm_status spmm_24_noalloc(const spmm_24_t *A, const void *B, int64_t ldb, void *C, int64_t ldc,
                                      int64_t N, spmm_stream_t stream);
 
+/* Workspace bytes spmm_slide needs (int8: the lifted values and B widened to
+ * fp16; 0 for fp16/bf16). */
+SPMM_API spmm_status spmm_slide_workspace_size(const spmm_slide_t *A, int64_t N, size_t *bytes);
+/* C = A * B with A a lifted (2n-2):2n operand ("SlideSparse", abstract): the
+ * 2:4 sparse tensor-core SpMM over the lifted depth K', B (K x N, the original
+ * rows) read through window-plane tensor maps, so that B is lifted on its way
+ * into shared memory and never written out.  Arithmetic, C types and the int8
+ * exactness are those of spmm_24.  Needs K % (64 n) == 0 (each 128-deep lifted
+ * K step within one window plane), else SPMM_ERR_SHAPE; n outside [2, 8] ->
+ * SPMM_ERR_SHAPE. */
+SPMM_API spmm_status spmm_slide(const spmm_slide_t *A, const void *B, int64_t ldb, void *C, int64_t ldc, int64_t N,
+                                void *workspace, size_t workspace_bytes, spmm_stream_t stream);
+
 /* C = A * B with A tile-vector-wise ("Accelerating Sparse DNNs Based on Tiled
  * GEMM": tile-wise column selection at global-memory level, 2:4 in the sparse
  * tensor core).  Each tile gathers its kept rows of B.  fp32 C. */
@@ -303,6 +333,21 @@ SPMM_API spmm_status spmm_build_tvw(const void *dense, int64_t M, int64_t K, int
 SPMM_API spmm_status spmm_prune_tvw(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
                                     int32_t tile_rows, const int32_t *tile_ptr, const int32_t *cols, int64_t n_tiles,
                                     int64_t Kp, void *vals, uint8_t *meta, spmm_stream_t stream);
+
+/* dense (M x K, row pitch ld elements, device memory, at most 2n-2 nonzeros in
+ * every group of 2n consecutive K entries) -> the lifted operand of
+ * spmm_slide_t ("SlideSparse", abstract): vals[M][K'/2] + meta[M][K'/8] in
+ * caller-allocated device arrays, K' = 2 K (n-1) / n.  Windows of a group are
+ * filled in order j = 0, 1, ...: each first takes the nonzeros of its lower pair
+ * that the previous window left (no later window covers them), then those of
+ * its upper pair in ascending order while it holds fewer than two.  This places
+ * every nonzero of a group with at most 2n-2 of them in exactly one window; a
+ * window with fewer than two nonzeros is padded with its lowest other
+ * positions, value +0.  Values are copied bit for bit.  2 <= n <= 8 and
+ * K % (4 n) == 0 (else SPMM_ERR_SHAPE); a group with more than 2n-2 nonzeros ->
+ * SPMM_ERR_FORMAT.  Synchronises `stream`. */
+SPMM_API spmm_status spmm_build_slide(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
+                                      void *vals, uint8_t *meta, spmm_stream_t stream);
 
 #ifdef __cplusplus
 }

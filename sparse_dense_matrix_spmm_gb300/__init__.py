@@ -9,6 +9,7 @@ library raises.
 Format containers hold device tensors:
   BCSR(M, K, bh, bw, nnzb, dtype, row_ptr, col_idx, vals)
   Mat24(M, K, dtype, vals, meta)
+  Slide(M, K, n, dtype, vals, meta)   ((2n-2):2n lifted into 2:4 windows)
   TVW(M, K, tile_rows, dtype, n_tiles, Kp, tile_ptr, cols, vals, meta)
   CSR(M, K, nnz, dtype, row_ptr, col, val)
   WCSR(...)  (see include/spmm_gb300.h for the field meanings)
@@ -24,10 +25,11 @@ import torch
 from . import _lib
 from ._lib import SpmmError
 
-__all__ = ["BCSR", "Mat24", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bcsr", "spmm_build_bcsr_count",
+__all__ = ["BCSR", "Mat24", "Slide", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bcsr", "spmm_build_bcsr_count",
            "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_prune_24", "spmm_24", "spmm_24_workspace_size",
            "spmm_build_tvw", "spmm_prune_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
+           "spmm_build_slide", "spmm_slide", "spmm_slide_workspace_size",
            "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
 
 _DT = {torch.bfloat16: _lib.SPMM_BF16, torch.float16: _lib.SPMM_F16, torch.int8: _lib.SPMM_I8}
@@ -86,6 +88,25 @@ class Mat24:
 
     def c(self) -> _lib.T24:
         return _lib.T24(self.M, self.K, _code(self.dtype), _ptr(self.vals), _ptr(self.meta))
+
+
+@dataclass
+class Slide:
+    """(2n-2):2n operand lifted into n - 1 overlapping 2:4 windows per group of 2n
+    (window planes); K is the original depth, vals/meta span K' = 2 K (n-1) / n."""
+    M: int
+    K: int
+    n: int
+    dtype: torch.dtype
+    vals: torch.Tensor
+    meta: torch.Tensor
+
+    @property
+    def K_lifted(self) -> int:
+        return 4 * (self.n - 1) * (self.K // (2 * self.n))
+
+    def c(self) -> _lib.SlideT:
+        return _lib.SlideT(self.M, self.K, self.n, _code(self.dtype), _ptr(self.vals), _ptr(self.meta))
 
 
 @dataclass
@@ -256,6 +277,43 @@ def spmm_24(A: Mat24, B: torch.Tensor, C_: Optional[torch.Tensor] = None,
         workspace = torch.empty(need, dtype=torch.uint8, device=B.device)
     a = A.c()
     _lib.call("spmm_24", C.byref(a), _ptr(B), B.stride(0), _ptr(out), out.stride(0), N, _ptr(workspace),
+              0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+    return out
+
+
+# ------------------------------------------------------------------ (2n-2):2n
+def spmm_build_slide(dense: torch.Tensor, n: int, stream=None) -> Slide:
+    """Decompose a dense (2n-2):2n matrix into its lifted 2:4 operand (n - 1
+    overlapping windows per group of 2n, window-plane order)."""
+    _check_dev(dense)
+    M, K = dense.shape
+    Kl = 4 * (n - 1) * (K // (2 * n)) if n > 0 else 0
+    vals = torch.empty((M, Kl // 2), dtype=dense.dtype, device=dense.device)
+    meta = torch.empty((M, Kl // 8), dtype=torch.uint8, device=dense.device)
+    _lib.call("spmm_build_slide", _ptr(dense), M, K, dense.stride(0), _code(dense.dtype), n, _ptr(vals),
+              _ptr(meta), _stream(stream))
+    return Slide(M, K, n, dense.dtype, vals, meta)
+
+
+def spmm_slide_workspace_size(A: Slide, N: int) -> int:
+    n = C.c_size_t(0)
+    a = A.c()
+    _lib.call("spmm_slide_workspace_size", C.byref(a), N, C.byref(n))
+    return n.value
+
+
+def spmm_slide(A: Slide, B: torch.Tensor, C_: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """C = A @ B for a lifted (2n-2):2n operand; B holds the original K rows."""
+    _check_dev(B, C_, workspace)
+    N = B.shape[1]
+    odt = torch.int32 if A.dtype == torch.int8 else torch.float32
+    out = _out(C_, A.M, N, odt, B.device)
+    need = spmm_slide_workspace_size(A, N)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=B.device)
+    a = A.c()
+    _lib.call("spmm_slide", C.byref(a), _ptr(B), B.stride(0), _ptr(out), out.stride(0), N, _ptr(workspace),
               0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
     return out
 

@@ -43,6 +43,10 @@ class T24(C.Structure):
     _fields_ = [("M", I64), ("K", I64), ("dtype", I32), ("vals", P), ("meta", P)]
 
 
+class SlideT(C.Structure):
+    _fields_ = [("M", I64), ("K", I64), ("n", I32), ("dtype", I32), ("vals", P), ("meta", P)]
+
+
 class TvwT(C.Structure):
     _fields_ = [("M", I64), ("K", I64), ("tile_rows", I32), ("dtype", I32), ("n_tiles", I64), ("Kp", I64),
                 ("tile_ptr", P), ("cols", P), ("vals", P), ("meta", P)]
@@ -63,6 +67,8 @@ SIGNATURES = {
     "spmm_24": (I32, [C.POINTER(T24), P, I64, P, I64, I64, P, SZ, P]),
     "spmm_24_noalloc": (I32, [C.POINTER(T24), P, I64, P, I64, I64, P]),
     "spmm_tvw": (I32, [C.POINTER(TvwT), P, I64, P, I64, I64, P]),
+    "spmm_slide_workspace_size": (I32, [C.POINTER(SlideT), I64, C.POINTER(SZ)]),
+    "spmm_slide": (I32, [C.POINTER(SlideT), P, I64, P, I64, I64, P, SZ, P]),
     "spmm_build_bcsr_count": (I32, [P, I64, I64, I64, I32, I32, I32, P, C.POINTER(I64), P]),
     "spmm_build_bcsr_fill": (I32, [P, I64, I64, I64, I32, I32, I32, P, P, P, P]),
     "spmm_build_wcsr_workspace_size": (I32, [C.POINTER(CsrT), I32, C.POINTER(SZ)]),
@@ -72,6 +78,7 @@ SIGNATURES = {
     "spmm_prune_24": (I32, [P, I64, I64, I64, I32, P, P, P]),
     "spmm_build_tvw": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, I64, P, P, P]),
     "spmm_prune_tvw": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, I64, P, P, P]),
+    "spmm_build_slide": (I32, [P, I64, I64, I64, I32, I32, P, P, P]),
 }
 
 _lib = None

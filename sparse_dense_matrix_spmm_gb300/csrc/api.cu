@@ -156,6 +156,19 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType type, const void* base, const uint64_t dims[4],
+                    const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    cuuint64_t st[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    std::memset(map, 0, sizeof(*map));
+    return f(map, type, 4, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace spmm
 
 using namespace spmm;
@@ -320,6 +333,14 @@ spmm_status spmm_prune_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, 
                              stream);
 }
 
+spmm_status spmm_build_slide(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
+                             void* vals, uint8_t* meta, spmm_stream_t stream) {
+    if (M > 0 && K > 0 && (!dense || !vals || !meta)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (M < 0 || K < 0 || ld < K || n < 2 || n > 8 || K % (4 * n)) return SPMM_ERR_SHAPE;
+    return run_build_slide(dense, M, K, ld, dtype, n, vals, meta, reinterpret_cast<cudaStream_t>(stream));
+}
+
 static spmm_status check_csr(const spmm_csr_t* A, int32_t h, int32_t S) {
     if (!A) return SPMM_ERR_NULL;
     if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
@@ -428,6 +449,36 @@ spmm_status spmm_24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int
     const size_t need = spmm24_workspace_bytes(A, N);
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SPMM_ERR_WORKSPACE;
     return launch_spmm24(A, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static spmm_status check_slide(const spmm_slide_t* A, int64_t N) {
+    if (!A) return SPMM_ERR_NULL;
+    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || N < 0 || A->n < 2 || A->n > 8) return SPMM_ERR_SHAPE;
+    if (A->K % (64 * A->n)) return SPMM_ERR_SHAPE;
+    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    return SPMM_OK;
+}
+
+spmm_status spmm_slide_workspace_size(const spmm_slide_t* A, int64_t N, size_t* bytes) {
+    if (!bytes) return SPMM_ERR_NULL;
+    spmm_status st = check_slide(A, N);
+    if (st != SPMM_OK) return st;
+    *bytes = slide_workspace_bytes(A, N);
+    return SPMM_OK;
+}
+
+spmm_status spmm_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
+                       void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
+    spmm_status st = check_slide(A, N);
+    if (st != SPMM_OK) return st;
+    if (!B || !C || (A->M > 0 && (!A->vals || !A->meta))) return SPMM_ERR_NULL;
+    if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
+    if (A->dtype != SPMM_I8 && ((ldb * 2) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
+    const size_t need = slide_workspace_bytes(A, N);
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SPMM_ERR_WORKSPACE;
+    return launch_slide(A, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 spmm_status spmm_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,

@@ -1,4 +1,5 @@
-// builders.cu -- GPU format builders: dense -> BCSR, dense -> 2:4, dense -> TVW.
+// builders.cu -- GPU format builders: dense -> BCSR, dense -> 2:4, dense -> TVW,
+// (2n-2):2n -> lifted 2:4 windows.
 //
 // Every builder is bit-exact with respect to its format definition: stored
 // values are copied bit for bit, and the order of stored items comes from
@@ -298,6 +299,103 @@ __global__ void prune24_kernel(const T* __restrict__ dense, int64_t M, int64_t K
     }
 }
 
+// ---------------------------------------------------------------- (2n-2):2n
+// Four consecutive elements as one 8-byte (16-bit types) or 4-byte (int8) load
+// when `vec`, else element-wise.
+template <typename T>
+__device__ __forceinline__ void load4(const T* src, bool vec, T* v) {
+    if (vec) {
+        if constexpr (sizeof(T) == 2) {
+            const uint2 w = *reinterpret_cast<const uint2*>(src);
+            v[0] = static_cast<T>(w.x & 0xFFFFu);
+            v[1] = static_cast<T>(w.x >> 16);
+            v[2] = static_cast<T>(w.y & 0xFFFFu);
+            v[3] = static_cast<T>(w.y >> 16);
+        } else {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = static_cast<T>((w >> (8 * i)) & 0xFFu);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = src[i];
+    }
+}
+
+// y[i] for a runtime i < 4 by selects, keeping y in registers.
+template <typename T>
+__device__ __forceinline__ T sel4(const T* y, int i) {
+    T r = y[0];
+    r = i == 1 ? y[1] : r;
+    r = i == 2 ? y[2] : r;
+    r = i == 3 ? y[3] : r;
+    return r;
+}
+
+// (2n-2):2n -> n-1 overlapping 2:4 windows per group ("SlideSparse", abstract:
+// sliding window decomposition).  Window j of group g covers the group's
+// positions 2j .. 2j+3 and is stored as 2:4 group j G + g of the lifted row
+// (window planes: every group's window 0, then every group's window 1, ...).
+// Windows are filled in order j = 0, 1, ...: first the nonzeros of pair j that
+// window j-1 left, then those of pair j+1 while the window holds fewer than
+// two; this places every nonzero of a group with at most 2n-2 of them.  A
+// window's stored pair is its nonzero positions padded with its lowest other
+// positions (value +0).  One thread per (row, two groups): groups 2q and 2q+1
+// share metadata byte (j G) / 2 + q of every plane j, so each thread writes
+// whole bytes.  `vec`: bit 0 = vector loads, bit 1 = vector stores.
+template <typename T, int NN>
+__global__ void slide_build_kernel(const T* __restrict__ dense, int64_t M, int64_t G, int64_t ld,
+                                   T* __restrict__ vals, uint8_t* __restrict__ meta, int vec, int* err) {
+    constexpr int W = NN - 1;  // windows per group
+    const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (q >= G / 2) return;
+    const int64_t lv = 2 * W * G;  // stored values per row: K' / 2
+    const int64_t lm = W * G / 2;  // metadata bytes per row: K' / 8
+    for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
+        T x[4 * NN];
+#pragma unroll
+        for (int c = 0; c < NN; ++c) load4<T>(dense + i * ld + 4 * NN * q + 4 * c, (vec & 1) != 0, x + 4 * c);
+        uint8_t byte[W];
+        T out[W][4];
+#pragma unroll
+        for (int j = 0; j < W; ++j) byte[j] = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const T* y = x + 2 * NN * h;
+            unsigned mask = 0;
+#pragma unroll
+            for (int p = 0; p < 2 * NN; ++p)
+                if (nz<T>(y[p])) mask |= 1u << p;
+            unsigned placed = 0;
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                unsigned keep = 0;
+                int held = 0;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int pos = 2 * j + t;
+                    if ((((mask & ~placed) >> pos) & 1u) && held < 2) {
+                        placed |= 1u << pos;
+                        keep |= 1u << t;
+                        ++held;
+                    }
+                }
+                int i0 = 0, i1 = 1;
+                pick2(keep, i0, i1);  // keep holds at most two positions
+                out[j][2 * h] = ((keep >> i0) & 1u) ? sel4<T>(y + 2 * j, i0) : T(0);
+                out[j][2 * h + 1] = ((keep >> i1) & 1u) ? sel4<T>(y + 2 * j, i1) : T(0);
+                byte[j] |= static_cast<uint8_t>((i0 | (i1 << 2)) << (4 * h));
+            }
+            if (__popc(mask) > 2 * NN - 2 || (mask & ~placed) != 0) atomicOr(err, SPMM_DEVERR_FORMAT);
+        }
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            store4<T>(vals + i * lv + 2 * (j * G + 2 * q), (vec & 2) != 0, out[j]);
+            meta[i * lm + (j * G) / 2 + q] = byte[j];
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TVW
 // Kept columns of every tile must be ascending and inside [0, K).
 __global__ void tvw_check_cols_kernel(const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t K,
@@ -493,6 +591,39 @@ spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, i
             else
                 tvw_build_kernel<T, false><<<static_cast<unsigned>(M), 256, 0, s>>>(d, M, K, ld, tile_rows, tile_ptr,
                                                                                      cols, Kp, v, meta, e);
+        };
+        if (dtype == SPMM_I8)
+            run(int8_t{}, static_cast<const int8_t*>(dense), static_cast<int8_t*>(vals));
+        else
+            run(uint16_t{}, static_cast<const uint16_t*>(dense), static_cast<uint16_t*>(vals));
+    }
+    return build_end(e, s);
+}
+
+spmm_status run_build_slide(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
+                            void* vals, uint8_t* meta, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_build_mu);
+    int* e = build_err_ptr();
+    if (!e) return SPMM_ERR_CUDA;
+    spmm_status st = build_begin(e, s);
+    if (st != SPMM_OK) return st;
+    const int64_t G = K / (2 * n);
+    const int64_t es = dtype == SPMM_I8 ? 1 : 2;
+    const int vec = ((reinterpret_cast<uintptr_t>(dense) % (4 * es) == 0 && ld % 4 == 0) ? 1 : 0) |
+                    (reinterpret_cast<uintptr_t>(vals) % (4 * es) == 0 ? 2 : 0);
+    if (M > 0 && G > 0) {
+        const dim3 grid(static_cast<unsigned>((G / 2 + 127) / 128), static_cast<unsigned>(M < 65535 ? M : 65535));
+        auto run = [&](auto tag, const auto* d, auto* v) {
+            using T = decltype(tag);
+            switch (n) {
+                case 2: slide_build_kernel<T, 2><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+                case 3: slide_build_kernel<T, 3><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+                case 4: slide_build_kernel<T, 4><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+                case 5: slide_build_kernel<T, 5><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+                case 6: slide_build_kernel<T, 6><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+                case 7: slide_build_kernel<T, 7><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+                default: slide_build_kernel<T, 8><<<grid, 128, 0, s>>>(d, M, G, ld, v, meta, vec, e); break;
+            }
         };
         if (dtype == SPMM_I8)
             run(int8_t{}, static_cast<const int8_t*>(dense), static_cast<int8_t*>(vals));

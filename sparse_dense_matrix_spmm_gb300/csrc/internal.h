@@ -33,6 +33,10 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base
 bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType type, const void* base, const uint64_t dims[3],
                     const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle);
 
+// 4-D tiled tensor map: dims[0] contiguous, byte strides of dims 1-3.
+bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType type, const void* base, const uint64_t dims[4],
+                    const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle);
+
 inline spmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -56,6 +60,9 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
 size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N);
 spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
                           void* ws, cudaStream_t stream);
+size_t slide_workspace_bytes(const spmm_slide_t* A, int64_t N);
+spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
+                         void* ws, cudaStream_t stream);
 spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
                        cudaStream_t stream);
 
@@ -79,5 +86,7 @@ spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int
 spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t tile_rows,
                           const int32_t* tile_ptr, const int32_t* cols, int64_t n_tiles, int64_t Kp, void* vals,
                           uint8_t* meta, bool prune, cudaStream_t s);
+spmm_status run_build_slide(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
+                            void* vals, uint8_t* meta, cudaStream_t s);
 
 }  // namespace spmm

@@ -44,6 +44,8 @@
 // and the chunks are summed in int32 by the epilogue, so C is exact.
 #include <cuda_fp16.h>
 
+#include <cstring>
+
 #include "internal.h"
 #include "sm103.cuh"
 
@@ -84,6 +86,18 @@ constexpr int SMEM_BYTES = 1024 + RING_OFF + META_RING * M_BYTES + 8 * (3 * STAG
 
 using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
 
+// B's tensor maps.  2:4 and TVW use one.  A (2n-2):2n operand lifted into
+// window planes ("SlideSparse", abstract: activations rearranged to match the
+// windows) uses one per plane j: rows 2j + p + 2n g of B, viewed as the 4-D box
+// {64 columns, 4 rows p, 32 groups g, 2 column halves}, so one load lands the
+// 128 lifted rows of a K step (32 windows of one plane) in the same swizzled
+// order as a plain 128-row tile, and TMA performs the lifting.
+constexpr int kMaxPlanes = 7;  // (2n-2):2n with n <= 8
+template <int P>
+struct BMaps {
+    CUtensorMap m[P];
+};
+
 struct SpArgs {
     const void* B;            // TVW: gathered with cp.async
     int64_t ldb;
@@ -97,7 +111,9 @@ struct SpArgs {
     void* C;
     int64_t ldc;
     uint32_t idesc;
-    int32_t b3d;              // 2:4: B tile as one 3-D box (both halves)
+    int32_t b3d;              // 2:4: B tile as one 3-D box (both halves); lifted: one 4-D box
+    int32_t planes;           // B tensor maps in use (1, or n - 1 window planes)
+    int32_t plane_groups;     // lifted: windows per plane (groups G, a multiple of 32)
     int32_t vec_ok;           // C rows 16-byte aligned
     int* err;
     uint64_t timeout_ns;
@@ -131,10 +147,10 @@ __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int&
     return static_cast<int>(a.K / KS);
 }
 
-template <bool GATHER, bool INT_EXACT>
+template <bool GATHER, bool INT_EXACT, int PLANES>
 __global__ void __launch_bounds__(threads_for(GATHER), 1)
     sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
-                       const __grid_constant__ CUtensorMap tmB, const SpArgs a) {
+                       const __grid_constant__ BMaps<PLANES> tmB, const SpArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + META_RING * M_BYTES);
@@ -171,7 +187,9 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmMeta);
-        tma_prefetch_desc(&tmB);
+#pragma unroll
+        for (int p = 0; p < PLANES; ++p)
+            if (p < a.planes) tma_prefetch_desc(&tmB.m[p]);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tslot), TMEM_COLS);
@@ -214,12 +232,25 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                     mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : A_BYTES + B_BYTES);
                     tma_load_2d_hint(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0, pol_stream);
                     if (GATHER) tma_load_2d_hint(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0, pol_stream);
-                    if (!GATHER) {
+                    if constexpr (!GATHER && PLANES > 1) {
+                        // lifted rows ks KS .. ks KS + 127: windows w0 .. w0 + 31 of plane j
+                        const int w0 = ks * (KS / 4);
+                        int j = w0 / a.plane_groups;
+                        j = j < PLANES ? j : PLANES - 1;
+                        const int g0 = w0 - j * a.plane_groups;
+                        const CUtensorMap* bm = &tmB.m[j];
                         if (a.b3d) {
-                            tma_load_3d(b_s(s), &tmB, full_bar(s), 0, ks * KS, n0 / 64);
+                            tma_load_4d(b_s(s), bm, full_bar(s), 0, 0, g0, n0 / 64);
                         } else {
-                            tma_load_2d(b_s(s), &tmB, full_bar(s), n0, ks * KS);
-                            tma_load_2d(b_s(s) + B_CHUNK, &tmB, full_bar(s), n0 + 64, ks * KS);
+                            tma_load_3d(b_s(s), bm, full_bar(s), n0, 0, g0);
+                            tma_load_3d(b_s(s) + B_CHUNK, bm, full_bar(s), n0 + 64, 0, g0);
+                        }
+                    } else if constexpr (!GATHER) {
+                        if (a.b3d) {
+                            tma_load_3d(b_s(s), &tmB.m[0], full_bar(s), 0, ks * KS, n0 / 64);
+                        } else {
+                            tma_load_2d(b_s(s), &tmB.m[0], full_bar(s), n0, ks * KS);
+                            tma_load_2d(b_s(s) + B_CHUNK, &tmB.m[0], full_bar(s), n0 + 64, ks * KS);
                         }
                     }
                 }
@@ -575,13 +606,13 @@ __global__ void widen_i8_kernel(const WidenJob j0, const WidenJob j1) {
     }
 }
 
-template <bool GATHER, bool INT_EXACT>
-spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const CUtensorMap& tmB, const SpArgs& a,
+template <bool GATHER, bool INT_EXACT, int PLANES>
+spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const BMaps<PLANES>& tmB, const SpArgs& a,
                           cudaStream_t stream, int slot) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
     if (dev->max_smem_optin < SMEM_BYTES) return SPMM_ERR_UNSUPPORTED;
-    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT>;
+    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES>;
     if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), SMEM_BYTES, slot)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
     if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
@@ -595,12 +626,73 @@ spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// int8 operands: the stored values (rows x kv) and B (kb rows x N) widened to
+// fp16 in the workspace, B with pitch np = N rounded up to 8.
+size_t widen_bytes(int64_t rows, int64_t kv, int64_t kb, int64_t N) {
+    const int64_t np = (N + 7) / 8 * 8;
+    return align256(static_cast<size_t>(rows) * kv * 2) + align256(static_cast<size_t>(kb) * np * 2);
+}
+
+spmm_status widen_operands(const void* vals, int64_t rows, int64_t kv, const void* B, int64_t ldb, int64_t kb,
+                           int64_t N, void* ws, cudaStream_t stream, const void** vals16, const void** b16,
+                           int64_t* ld16) {
+    __half* wa = static_cast<__half*>(ws);
+    __half* wb = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(rows) * kv * 2));
+    const int64_t np = (N + 7) / 8 * 8;
+    auto job = [](const void* src, int64_t lds, __half* dst, int64_t ldd, int64_t r, int64_t cols) {
+        WidenJob j{static_cast<const int8_t*>(src), lds, dst, ldd, r, cols, (ldd + 15) / 16, 0};
+        j.threads = r * j.per_row;
+        return j;
+    };
+    const WidenJob ja = job(vals, kv, wa, kv, rows, kv);
+    const WidenJob jb = job(B, ldb, wb, np, kb, N);
+    const int64_t threads = ja.threads + jb.threads;
+    trace_begin(SPMM_KERNEL_WIDEN, stream);
+    widen_i8_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(ja, jb);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_WIDEN, stream);
+    if (e != cudaSuccess) return SPMM_ERR_CUDA;
+    *vals16 = wa;
+    *b16 = wb;
+    *ld16 = np;
+    return SPMM_OK;
+}
+
+// Maps of the stored values (M x K/2, 128 x 64 boxes) and metadata (M x K/8)
+// of a 2:4 operand of dense depth K.
+bool encode_a_maps(CUtensorMapDataType t, const void* vals, const uint8_t* meta, int64_t M, int64_t K,
+                   CUtensorMap* tmA, CUtensorMap* tmM) {
+    return encode_tmap_2d(tmA, t, vals, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
+                          static_cast<uint64_t>(K), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tmap_2d(tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, meta, static_cast<uint64_t>(K / 8),
+                          static_cast<uint64_t>(M), static_cast<uint64_t>(K / 8), 16, 128,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+SpArgs dense_b_args(const DeviceInfo* dev, int64_t M, int64_t K, int64_t N, int32_t dtype, const uint8_t* meta,
+                    void* C, int64_t ldc) {
+    SpArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.n_mtiles = static_cast<int32_t>((M + BM - 1) / BM);
+    a.n_ntiles = static_cast<int32_t>((N + BN - 1) / BN);
+    a.C = C;
+    a.ldc = ldc;
+    a.idesc = idesc_f16(128, BN, dtype == SPMM_BF16, false, true, true, 0);
+    a.vec_ok = (ldc % 4 == 0) && aligned16(C);
+    a.meta = meta;
+    a.ldm = K / 8;
+    a.planes = 1;
+    a.err = dev->err;
+    a.timeout_ns = kWaitTimeoutNs;
+    return a;
+}
+
 }  // namespace
 
 size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N) {
-    if (A->dtype != SPMM_I8) return 0;
-    const int64_t np = (N + 7) / 8 * 8;
-    return align256(static_cast<size_t>(A->M) * (A->K / 2) * 2) + align256(static_cast<size_t>(A->K) * np * 2);
+    return A->dtype == SPMM_I8 ? widen_bytes(A->M, A->K / 2, A->K, N) : 0;
 }
 
 spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
@@ -614,28 +706,11 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
     int64_t bld = ldb;
     const CUtensorMapDataType t = i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : half_type(A->dtype);
     if (i8) {
-        __half* wa = static_cast<__half*>(ws);
-        __half* wb = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) +
-                                               align256(static_cast<size_t>(A->M) * (A->K / 2) * 2));
-        const int64_t np = (N + 7) / 8 * 8;
-        auto job = [](const void* src, int64_t lds, __half* dst, int64_t ldd, int64_t rows, int64_t cols) {
-            WidenJob j{static_cast<const int8_t*>(src), lds, dst, ldd, rows, cols, (ldd + 15) / 16, 0};
-            j.threads = rows * j.per_row;
-            return j;
-        };
-        const WidenJob ja = job(A->vals, A->K / 2, wa, A->K / 2, A->M, A->K / 2);
-        const WidenJob jb = job(B, ldb, wb, np, A->K, N);
-        const int64_t threads = ja.threads + jb.threads;
-        trace_begin(SPMM_KERNEL_WIDEN, stream);
-        widen_i8_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(ja, jb);
-        const cudaError_t e = cudaGetLastError();
-        trace_end(SPMM_KERNEL_WIDEN, stream);
-        if (e != cudaSuccess) return SPMM_ERR_CUDA;
-        vals = wa;
-        bsrc = wb;
-        bld = np;
+        const spmm_status st = widen_operands(A->vals, A->M, A->K / 2, B, ldb, A->K, N, ws, stream, &vals, &bsrc, &bld);
+        if (st != SPMM_OK) return st;
     }
-    CUtensorMap tmA, tmM, tmB;
+    CUtensorMap tmA, tmM;
+    BMaps<1> tmB;
     // B tile: one 3-D box {64 columns, 128 K rows, 2 halves} when whole 64-column
     // halves tile N (a ragged half would read past the row), else two 2-D boxes.
     bool b3d = false;
@@ -643,33 +718,69 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
         const uint64_t dims[3] = {64, static_cast<uint64_t>(A->K), static_cast<uint64_t>(N / 64)};
         const uint64_t strides[2] = {static_cast<uint64_t>(bld) * 2, 128};
         const uint32_t box[3] = {64, 128, 2};
-        b3d = encode_tmap_3d(&tmB, t, bsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        b3d = encode_tmap_3d(&tmB.m[0], t, bsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     }
-    if (!encode_tmap_2d(&tmA, t, vals, static_cast<uint64_t>(A->K / 2), static_cast<uint64_t>(A->M),
-                        static_cast<uint64_t>(A->K), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->meta, static_cast<uint64_t>(A->K / 8),
-                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(A->K / 8), 16, 128,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        (!b3d && !encode_tmap_2d(&tmB, t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+    if (!encode_a_maps(t, vals, A->meta, A->M, A->K, &tmA, &tmM) ||
+        (!b3d && !encode_tmap_2d(&tmB.m[0], t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
                                  static_cast<uint64_t>(bld) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
         return SPMM_ERR_CUDA;
-    SpArgs a{};
+    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc);
     a.b3d = b3d ? 1 : 0;
-    a.M = A->M;
-    a.N = N;
-    a.K = A->K;
-    a.n_mtiles = static_cast<int32_t>((A->M + BM - 1) / BM);
-    a.n_ntiles = static_cast<int32_t>((N + BN - 1) / BN);
-    a.C = C;
-    a.ldc = ldc;
-    a.idesc = idesc_f16(128, BN, A->dtype == SPMM_BF16, false, true, true, 0);
-    a.vec_ok = (ldc % 4 == 0) && aligned16(C);
-    a.meta = static_cast<const uint8_t*>(A->meta);
-    a.ldm = A->K / 8;
-    a.err = dev->err;
-    a.timeout_ns = kWaitTimeoutNs;
-    if (i8) return launch_sparse<false, true>(tmA, tmM, tmB, a, stream, 2);
-    return launch_sparse<false, false>(tmA, tmM, tmB, a, stream, 1);
+    if (i8) return launch_sparse<false, true, 1>(tmA, tmM, tmB, a, stream, 2);
+    return launch_sparse<false, false, 1>(tmA, tmM, tmB, a, stream, 1);
+}
+
+size_t slide_workspace_bytes(const spmm_slide_t* A, int64_t N) {
+    const int64_t Kl = 4 * (A->n - 1) * (A->K / (2 * A->n));
+    return A->dtype == SPMM_I8 ? widen_bytes(A->M, Kl / 2, A->K, N) : 0;
+}
+
+spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
+                         void* ws, cudaStream_t stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (A->M == 0 || N == 0) return SPMM_OK;
+    const int n = A->n;
+    const int64_t G = A->K / (2 * n), Kl = 4 * (n - 1) * G;
+    const bool i8 = A->dtype == SPMM_I8;
+    const void* vals = A->vals;
+    const void* bsrc = B;
+    int64_t bld = ldb;
+    const CUtensorMapDataType t = i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : half_type(A->dtype);
+    if (i8) {
+        const spmm_status st = widen_operands(A->vals, A->M, Kl / 2, B, ldb, A->K, N, ws, stream, &vals, &bsrc, &bld);
+        if (st != SPMM_OK) return st;
+    }
+    CUtensorMap tmA, tmM;
+    BMaps<kMaxPlanes> tmB;
+    std::memset(&tmB, 0, sizeof(tmB));
+    // Plane j: rows 2j + p + 2n g of B (p < 4, g < G).  Whole 64-column halves:
+    // one 4-D box {64, 4, 32, 2}; otherwise two 3-D boxes {64, 4, 32}, one per half.
+    const bool b4d = N % 64 == 0;
+    const uint64_t row = static_cast<uint64_t>(bld) * 2;
+    for (int j = 0; j < n - 1; ++j) {
+        const void* base = static_cast<const uint8_t*>(bsrc) + 2 * j * row;
+        bool ok;
+        if (b4d) {
+            const uint64_t dims[4] = {64, 4, static_cast<uint64_t>(G), static_cast<uint64_t>(N / 64)};
+            const uint64_t strides[3] = {row, 2 * n * row, 128};
+            const uint32_t box[4] = {64, 4, 32, 2};
+            ok = encode_tmap_4d(&tmB.m[j], t, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            const uint64_t dims[3] = {static_cast<uint64_t>(N), 4, static_cast<uint64_t>(G)};
+            const uint64_t strides[2] = {row, 2 * n * row};
+            const uint32_t box[3] = {64, 4, 32};
+            ok = encode_tmap_3d(&tmB.m[j], t, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        if (!ok) return SPMM_ERR_CUDA;
+    }
+    if (!encode_a_maps(t, vals, A->meta, A->M, Kl, &tmA, &tmM)) return SPMM_ERR_CUDA;
+    SpArgs a = dense_b_args(dev, A->M, Kl, N, A->dtype, A->meta, C, ldc);
+    a.b3d = b4d ? 1 : 0;
+    a.planes = n - 1;
+    a.plane_groups = static_cast<int32_t>(G);
+    if (i8) return launch_sparse<false, true, kMaxPlanes>(tmA, tmM, tmB, a, stream, 12);
+    return launch_sparse<false, false, kMaxPlanes>(tmA, tmM, tmB, a, stream, 11);
 }
 
 spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
@@ -678,13 +789,10 @@ spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C
     if (!dev) return SPMM_ERR_CUDA;
     if (A->M == 0 || N == 0) return SPMM_OK;
     const CUtensorMapDataType t = half_type(A->dtype);
-    CUtensorMap tmA, tmM, tmB;
-    if (!encode_tmap_2d(&tmA, t, A->vals, static_cast<uint64_t>(A->Kp / 2), static_cast<uint64_t>(A->M),
-                        static_cast<uint64_t>(A->Kp), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tmM, CU_TENSOR_MAP_DATA_TYPE_UINT8, A->meta, static_cast<uint64_t>(A->Kp / 8),
-                        static_cast<uint64_t>(A->M), static_cast<uint64_t>(A->Kp / 8), 16, 128,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tmap_2d(&tmB, t, B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+    CUtensorMap tmA, tmM;
+    BMaps<1> tmB;
+    if (!encode_a_maps(t, A->vals, A->meta, A->M, A->Kp, &tmA, &tmM) ||
+        !encode_tmap_2d(&tmB.m[0], t, B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
                         static_cast<uint64_t>(ldb) * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
         return SPMM_ERR_CUDA;
     SpArgs a{};
@@ -702,9 +810,10 @@ spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C
     a.ldc = ldc;
     a.idesc = idesc_f16(128, BN, A->dtype == SPMM_BF16, false, true, true, 0);
     a.vec_ok = (ldc % 4 == 0) && aligned16(C);
+    a.planes = 1;
     a.err = dev->err;
     a.timeout_ns = kWaitTimeoutNs;
-    return launch_sparse<true, false>(tmA, tmM, tmB, a, stream, 3);
+    return launch_sparse<true, false, 1>(tmA, tmM, tmB, a, stream, 3);
 }
 
 }  // namespace spmm

@@ -56,6 +56,7 @@ def test_struct_layouts_match_c():
     assert ctypes.sizeof(_lib.T24) == 8 * 2 + 8 + 8 * 2
     assert ctypes.sizeof(_lib.TvwT) == 8 * 2 + 4 * 2 + 8 * 2 + 8 * 4
     assert ctypes.sizeof(_lib.WcsrT) == 8 * 3 + 4 * 3 + 4 + 8 * 3 + 8 * 9
+    assert ctypes.sizeof(_lib.SlideT) == 8 * 2 + 4 * 2 + 8 * 2
 
 
 def test_host_validation_rejects_bad_arguments_before_launch():
@@ -72,3 +73,10 @@ def test_host_validation_rejects_bad_arguments_before_launch():
     assert L.spmm_bcsr(ctypes.byref(c), 16, 64, 16, 64, 64, None) == 3
     # K % 8 for the 2:4 compressor -> SPMM_ERR_SHAPE
     assert L.spmm_compress_24(16, 4, 12, 12, 2, 16, 16, None) == 2
+    # (2n-2):2n: n outside [2, 8], K not a multiple of 64 n (SpMM) or 4 n (builder) -> SPMM_ERR_SHAPE
+    sl = _lib.SlideT(128, 256, 1, 1, 16, 16)
+    assert L.spmm_slide(ctypes.byref(sl), 16, 64, 16, 64, 64, None, 0, None) == 2
+    sl = _lib.SlideT(128, 320, 4, 1, 16, 16)
+    assert L.spmm_slide(ctypes.byref(sl), 16, 64, 16, 64, 64, None, 0, None) == 2
+    assert L.spmm_build_slide(16, 4, 40, 40, 1, 4, 16, 16, None) == 2
+    assert L.spmm_build_slide(16, 4, 64, 64, 1, 9, 16, 16, None) == 2
