@@ -85,6 +85,9 @@ def lib():
         L.orc_slide_src.argtypes = [I64, I64, I32]
         L.orc_slide_decompose.restype = I32
         L.orc_slide_decompose.argtypes = [P, I64, I64, I64, I32, I32, P]
+        L.orc_rcm.restype = I32
+        L.orc_rcm.argtypes = [I64, P, P, P]
+        L.orc_permute_sym.argtypes = [I64, I64, I32, P, P, P]
         L.orc_spmm24_f64.argtypes = [I64, I64, I32, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_spmm24_i64.argtypes = [I64, I64, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_tvw_build.restype = I32
@@ -394,3 +397,47 @@ def tvw_spmm(F, B, rows=None, cols=None):
                        F["Kp"], _p(H["vals"]), _p(H["meta"]), _p(B), B.shape[1], r0, r1,
                        _p(colarr), ncols, _p(out))
     return out
+
+
+# ------------------------------------------------------------------ permutation before BCSR
+def rcm(n, row_ptr, col):
+    """Reverse Cuthill-McKee order of the symmetrised pattern: perm[i] is the
+    original index placed at position i."""
+    row_ptr = _c(row_ptr, np.int32)
+    col = _c(col, np.int32)
+    perm = np.zeros(n, dtype=np.int32)
+    rc = lib().orc_rcm(n, _p(row_ptr), _p(col), _p(perm))
+    if rc:
+        raise OracleError(f"rcm error {rc}")
+    return perm
+
+
+def rcm_dense(A):
+    """RCM of the stored (nonzero) pattern of a dense square matrix of any encoding."""
+    A = np.asarray(A)
+    nz = (A & 0x7FFF) != 0 if A.dtype == np.uint16 else A != 0
+    n = A.shape[0]
+    row_ptr = np.concatenate([[0], np.cumsum(nz.sum(axis=1))]).astype(np.int32)
+    col = np.nonzero(nz)[1].astype(np.int32)
+    return rcm(n, row_ptr, col)
+
+
+def permute_sym(A, perm, dtype):
+    """A'[i][j] = A[perm[i]][perm[j]]."""
+    A = _c(A, _edt(dtype))
+    n = A.shape[0]
+    out = np.zeros((n, n), dtype=_edt(dtype))
+    lib().orc_permute_sym(n, A.shape[1], DTYPES[dtype], _p(A), _p(_c(perm, np.int32)), _p(out))
+    return out
+
+
+def bcsr_spmm_permuted(F, perm, B, rows=None, cols=None):
+    """C = P^T (A' (P B)) for the BCSR F of A' = P A P^T: B's rows gathered by
+    perm, the BCSR product, then C' row i written to row perm[i]."""
+    perm = np.asarray(perm)
+    Cp = bcsr_spmm(F, np.ascontiguousarray(np.asarray(B)[perm]), cols=cols)
+    C = np.empty_like(Cp)
+    C[perm] = Cp
+    if rows is not None:
+        C = C[rows[0]:rows[1]]
+    return C

@@ -686,3 +686,74 @@ void orc_tvw_spmm(int64_t M, int dtype, int tile_rows, const int32_t *tile_ptr, 
         }
     }
 }
+
+/* ================================================================== permutation
+ * "SMaT" (abstract): the sparse matrix is permuted to minimise the number of
+ * nonzero blocks before the block-sparse multiply; the method's reference list
+ * cites Cuthill and McKee, "Reducing the bandwidth of sparse symmetric
+ * matrices".  Reading (the pages name no algorithm): symmetric Reverse
+ * Cuthill-McKee on the pattern of A + A^T of a square A (i ~ j iff i != j and
+ * A[i][j] or A[j][i] is stored), applied to rows and columns alike:
+ * A' = P A P^T with A'[i][j] = A[perm[i]][perm[j]].
+ *   degree(i) = number of distinct neighbours of i;
+ *   while nodes remain: start at the unvisited node of least degree (lowest
+ *   index on ties) and run a breadth-first search in which every dequeued node
+ *   appends its unvisited neighbours in ascending (degree, index) order;
+ *   perm = the visiting order reversed. */
+static const int32_t *rcm_deg;
+static int rcm_cmp(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    if (rcm_deg[x] != rcm_deg[y]) return rcm_deg[x] < rcm_deg[y] ? -1 : 1;
+    return (x > y) - (x < y);
+}
+
+int orc_rcm(int64_t n, const int32_t *row_ptr, const int32_t *col, int32_t *perm) {
+    if (n <= 0) return ORC_OK;
+    /* dense boolean adjacency of the symmetrised pattern (test sizes only) */
+    uint8_t *adj = calloc((size_t)(n * n), 1);
+    int32_t *deg = calloc((size_t)n, sizeof(int32_t));
+    int32_t *order = malloc(sizeof(int32_t) * (size_t)n);
+    int32_t *nb = malloc(sizeof(int32_t) * (size_t)n);
+    uint8_t *seen = calloc((size_t)n, 1);
+    if (!adj || !deg || !order || !nb || !seen) return ORC_ERR_SHAPE;
+    for (int64_t i = 0; i < n; i++)
+        for (int32_t e = row_ptr[i]; e < row_ptr[i + 1]; e++) {
+            int64_t j = col[e];
+            if (j < 0 || j >= n) return ORC_ERR_FORMAT;
+            if (j != i) adj[i * n + j] = adj[j * n + i] = 1;
+        }
+    for (int64_t i = 0; i < n; i++)
+        for (int64_t j = 0; j < n; j++) deg[i] += adj[i * n + j];
+    rcm_deg = deg;
+    int64_t head = 0, tail = 0;
+    while (tail < n) {
+        int64_t s = -1;
+        for (int64_t i = 0; i < n; i++)
+            if (!seen[i] && (s < 0 || deg[i] < deg[s])) s = i;
+        seen[s] = 1;
+        order[tail++] = (int32_t)s;
+        while (head < tail) {
+            int64_t v = order[head++], m = 0;
+            for (int64_t j = 0; j < n; j++)
+                if (adj[v * n + j] && !seen[j]) nb[m++] = (int32_t)j;
+            qsort(nb, (size_t)m, sizeof(int32_t), rcm_cmp);
+            for (int64_t t = 0; t < m; t++) {
+                seen[nb[t]] = 1;
+                order[tail++] = nb[t];
+            }
+        }
+    }
+    for (int64_t i = 0; i < n; i++) perm[i] = order[n - 1 - i];
+    free(adj);
+    free(deg);
+    free(order);
+    free(nb);
+    free(seen);
+    return ORC_OK;
+}
+
+/* A'[i][j] = A[perm[i]][perm[j]] (n x n, leading dims ld / n). */
+void orc_permute_sym(int64_t n, int64_t ld, int dtype, const void *A, const int32_t *perm, void *out) {
+    for (int64_t i = 0; i < n; i++)
+        for (int64_t j = 0; j < n; j++) copy_elem(out, i * n + j, A, perm[i] * ld + perm[j], dtype);
+}

@@ -35,7 +35,7 @@ BF16, F16, I8 = "bf16", "f16", "i8"
 
 __all__ = [
     "BF16", "F16", "I8", "round_f32_to_bf16_bits", "normal_bits", "mask24_float_problem",
-    "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem", "slide_problem",
+    "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem", "slide_problem", "banded_scrambled_problem",
     "CONFIGS", "config_problem",
 ]
 
@@ -148,6 +148,25 @@ def slide_problem(M: int, K: int, N: int, n: int, seed: int, dtype: str = F16) -
     return {"A": A, "B": B, "M": M, "K": K, "N": N, "n": n, "dtype": dtype}
 
 
+def banded_scrambled_problem(n: int, w: int, N: int, seed: int, dtype: str = F16) -> dict:
+    """A square band matrix (A[i][j] stored iff |i - j| <= w, values N(0,1); int8: nonzero
+    uniform +-{1..127}) with its rows and columns scrambled by one uniform random
+    permutation q (A = Q Band Q^T, i.e. A[i][j] = Band[q[i]][q[j]]); B (n x N)."""
+    rng = np.random.default_rng(seed)
+    q = rng.permutation(n)
+    i = np.arange(n)
+    band = np.abs(i[:, None] - i[None, :]) <= w
+    if dtype == I8:
+        v = (rng.integers(1, 128, size=(n, n)) * (rng.integers(0, 2, size=(n, n)) * 2 - 1)).astype(np.int8)
+        B = rng.integers(-127, 128, size=(n, N), dtype=np.int16).astype(np.int8)
+    else:
+        v = normal_bits(rng, (n, n), dtype)
+        B = normal_bits(rng, (n, N), dtype)
+    v[~band] = 0
+    A = np.ascontiguousarray(v[np.ix_(q, q)])
+    return {"A": A, "B": B, "M": n, "K": n, "N": N, "w": w, "q": q, "dtype": dtype}
+
+
 def _unique_sorted_rows(rng, lengths: np.ndarray, K: int):
     """Per row, ``lengths[r]`` distinct columns uniform on [0, K), ascending."""
     M = lengths.shape[0]
@@ -229,6 +248,8 @@ CONFIGS = {
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
                      dtype=BF16, std=0.02),
     "tvw": dict(kind="tvw", M=4096, K=4096, N=4096, tile_rows=128, keep=2048, seed=5, dtype=F16),
+    # a scrambled band (half-width 48) before and after RCM, 64 x 64 blocks
+    "bcsr_rcm": dict(kind="rcm", M=16384, K=16384, N=2048, w=48, bh=64, bw=64, seed=10, dtype=F16),
     # 6:8 on a Qwen2.5-7B-sized FFN projection (18944 x 3584), 8192 tokens
     "slide68_f16": dict(kind="slide", M=18944, K=3584, N=8192, n=4, seed=9, dtype=F16),
 }
@@ -252,6 +273,8 @@ def config_problem(name: str, **overrides) -> dict:
     if kind == "tvw":
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))
+    if kind == "rcm":
+        return banded_scrambled_problem(c["M"], c["w"], c["N"], c["seed"], c.get("dtype", F16))
     if kind == "slide":
         return slide_problem(c["M"], c["K"], c["N"], c["n"], c["seed"], c.get("dtype", F16))
     if kind in ("prune24", "prunetvw"):  # a dense matrix to prune (into 2:4, or into TVW given kept columns)

@@ -60,3 +60,11 @@ def test_slide_problem_two_zeros_per_group():
             assert np.all(nz == 2 * n - 2)
         q = gen.slide_problem(12, 16 * n, 5, n, seed=3, dtype=dtype)
         assert np.array_equal(p["A"], q["A"]) and np.array_equal(p["B"], q["B"])
+
+
+def test_banded_scrambled_problem_is_a_permuted_band():
+    p = gen.banded_scrambled_problem(64, 3, 5, seed=4, dtype=gen.I8)
+    inv = np.argsort(p["q"])
+    band = p["A"][np.ix_(inv, inv)]
+    i = np.arange(64)
+    assert np.all((band != 0) == (np.abs(i[:, None] - i[None, :]) <= 3))

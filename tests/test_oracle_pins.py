@@ -489,3 +489,69 @@ def test_slide_errors():
         oracle.slide_decompose(A, 4, "i8")
     with pytest.raises(oracle.OracleError):
         oracle.slide_decompose(np.zeros((2, 12), np.int8), 4, "i8")   # K % 8 != 0
+
+
+# ---------------------------------------------------------------- permutation before BCSR (RCM)
+def _bandwidth(A):
+    r, c = np.nonzero(np.asarray(A) != 0)
+    return int(np.max(np.abs(r - c))) if r.size else 0
+
+
+def test_rcm_golden():
+    g = golden("rcm_int8_7.json")
+    A, B = np.array(g["A"], np.int8), np.array(g["B"], np.int8)
+    perm = oracle.rcm_dense(A)
+    assert perm.tolist() == g["perm"]
+    F = oracle.bcsr_build(oracle.permute_sym(A, perm, "i8"), 1, 1, "i8")
+    assert oracle.bcsr_spmm_permuted(F, perm, B).tolist() == g["C"]
+
+
+def test_rcm_scrambled_path_and_band():
+    """A scrambled path comes back as a path (bandwidth 1, a closed form of the
+    breadth-first order from an end); a scrambled band of half-width w comes back
+    within bandwidth 2w, every breadth-first level of a band being w wide."""
+    rng = np.random.default_rng(3)
+    n = 50
+    q = rng.permutation(n)
+    A = np.zeros((n, n), np.int8)
+    for t in range(n - 1):
+        A[q[t], q[t + 1]] = 1
+    perm = oracle.rcm_dense(A)
+    assert sorted(perm.tolist()) == list(range(n))
+    assert _bandwidth(A[np.ix_(perm, perm)] | A[np.ix_(perm, perm)].T) == 1
+    for w in (2, 5):
+        p = gen.banded_scrambled_problem(96, w, 1, seed=w, dtype="i8")
+        assert _bandwidth(p["A"]) > 4 * w
+        perm = oracle.rcm_dense(p["A"])
+        assert _bandwidth(p["A"][np.ix_(perm, perm)]) <= 2 * w
+
+
+def test_rcm_components_isolated_nodes_and_asymmetric_pattern():
+    rng = np.random.default_rng(5)
+    n = 40
+    A = (rng.random((n, n)) < 0.04).astype(np.int8)       # asymmetric, several components
+    A[7, :] = 0
+    A[:, 7] = 0                                            # an isolated node
+    perm = oracle.rcm_dense(A)
+    assert sorted(perm.tolist()) == list(range(n))
+    # the order is the one of A + A^T: symmetrising the pattern changes nothing
+    assert np.array_equal(oracle.rcm_dense(A | A.T), perm)
+
+
+def test_permute_sym_and_permuted_spmm_equal_the_plain_product():
+    """A' = P A P^T entrywise as numpy indexing gives it; gathering B, multiplying the
+    BCSR of A' and scattering C equals A B (int8 exactly, bf16 to 1e-12)."""
+    p = gen.banded_scrambled_problem(64, 3, 9, seed=8, dtype="i8")
+    perm = oracle.rcm_dense(p["A"])
+    Ap = oracle.permute_sym(p["A"], perm, "i8")
+    assert np.array_equal(Ap, p["A"][np.ix_(perm, perm)])
+    F = oracle.bcsr_build(Ap, 16, 16, "i8")
+    G = oracle.bcsr_build(p["A"], 16, 16, "i8")
+    assert F["nnzb"] <= 10 and G["nnzb"] >= 14             # the band's 4 + 2 * 3 blocks vs (nearly) all 16
+    C = oracle.bcsr_spmm_permuted(F, perm, p["B"])
+    assert np.array_equal(C, p["A"].astype(np.int64) @ p["B"].astype(np.int64))
+    q = gen.banded_scrambled_problem(64, 3, 9, seed=8, dtype="bf16")
+    perm = oracle.rcm_dense(q["A"])
+    F = oracle.bcsr_build(oracle.permute_sym(q["A"], perm, "bf16"), 16, 16, "bf16")
+    np.testing.assert_allclose(oracle.bcsr_spmm_permuted(F, perm, q["B"]),
+                               bits_to_f64(q["A"], "bf16") @ bits_to_f64(q["B"], "bf16"), rtol=1e-12, atol=1e-12)
