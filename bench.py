@@ -8,8 +8,8 @@ flushed (256 MiB written) before every timed step.  Metric: effective
 TFLOP/s = 2 * nnz * N / time.
 
 The same line carries, per other workload (BCSR LLM-shaped, tile-vector-wise,
-row-window CSR, fp16 2:4, 6:8 through overlapping 2:4 windows, the two pruning
-builders, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
+row-window CSR, fp16 2:4, 6:8 through overlapping 2:4 windows, a scrambled band
+multiplied after Reverse Cuthill-McKee, the two pruning builders, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -393,6 +393,50 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             spmm.spmm_24(F, Bx, Cd, wsp)
+    elif c["kind"] == "rcm":
+        # a scrambled band: RCM (host) on its pattern, P A P^T and its BCSR on the device; the step is
+        # the permuted product (B gathered, BCSR, C scattered); context: BCSR of the scrambled matrix as is
+        p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
+        n, bh = c["M"], c["bh"]
+        nzm = (p["A"] & 0x7FFF) != 0
+        row_ptr = np.concatenate([[0], np.cumsum(nzm.sum(axis=1))]).astype(np.int32)
+        col = np.nonzero(nzm)[1].astype(np.int32)
+        del nzm
+        t0 = time.perf_counter()
+        perm = spmm.rcm_order(n, row_ptr, col)
+        extra_fields["rcm_host_ms"] = round((time.perf_counter() - t0) * 1e3, 2)
+        A = to_dev(p["A"], torch.float16)
+        Bx = to_dev(p["B"], torch.float16)
+        permd = perm.cuda()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        F = spmm.build_bcsr(spmm.spmm_permute_sym(A, permd), bh, c["bw"])
+        torch.cuda.synchronize()
+        build_ms = (time.perf_counter() - t0) * 1e3
+        Cd = torch.empty((n, c["N"]), dtype=torch.float32, device="cuda")
+        wsp = torch.empty(spmm.spmm_bcsr_permuted_workspace_size(F, c["N"]), dtype=torch.uint8, device="cuda")
+        # context: the scrambled matrix's own BCSR and product
+        G = spmm.build_bcsr(A, bh, c["bw"])
+        del A
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for _ in range(2):
+            spmm.spmm_bcsr(G, Bx, Cd)
+        ev[0].record()
+        for _ in range(3):
+            spmm.spmm_bcsr(G, Bx, Cd)
+        ev[1].record()
+        torch.cuda.synchronize()
+        extra_fields.update({"nnzb_scrambled": int(G.nnzb), "nnzb_permuted": int(F.nnzb),
+                             "unpermuted_bcsr_ms": round(ev[0].elapsed_time(ev[1]) / 3, 4)})
+        del G
+        torch.cuda.empty_cache()
+        nnz = F.nnzb * bh * c["bw"]
+        # the BCSR kernel's own bytes: A' blocks + indices, B' read once, C' written once
+        alg = nnz * 2 + F.nnzb * 4 + (n // bh + 1) * 4 + n * c["N"] * 2 + n * c["N"] * 4
+        kern, kid = "bcsr_spmm_kernel", spmm._lib.KERNEL_BCSR
+
+        def step():
+            spmm.spmm_bcsr_permuted(F, permd, Bx, Cd, wsp)
     elif c["kind"] == "slide":
         # (2n-2):2n, the same recipe as the host generator drawn on the device: per group of 2n
         # two distinct zero positions, N(0,1) fp16 values elsewhere; B N(0,1) fp16
@@ -491,6 +535,10 @@ def run_extra(name, args, ws, peaks, flush_buf):
     total_ms = timed_steps(step, steps, 0, flush_buf, ws)
     # untraced builder: a check and a build kernel per call
     n, ms = spmm.trace_read(kid) if kid is not None else (2 * steps, 0.0)
+    if c["kind"] == "rcm":  # the row gather and scatter around each BCSR launch
+        n_p, ms_p = spmm.trace_read(spmm._lib.KERNEL_PERMUTE)
+        extra_fields["permute_kernels_ms_per_step"] = round(ms_p / steps, 4)
+        extra_fields["permute_launches"] = int(n_p)
     spmm.trace_enable(False)
     total_ms = max_over_ranks(total_ms, ws, "cuda")
     # a builder without a traced kernel id (it synchronises inside): time the whole call
@@ -614,8 +662,8 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "slide68_f16", "prune24_f16", "prune_tvw_f16",
-                     "bcsr_tiny"):
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "slide68_f16", "bcsr_rcm", "prune24_f16",
+                     "prune_tvw_f16", "bcsr_tiny"):
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden

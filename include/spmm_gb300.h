@@ -195,6 +195,7 @@ SPMM_API spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t st
 #define SPMM_KERNEL_WIDEN 3   /* int8 -> fp16 operand widening (int8 2:4)          */
 #define SPMM_KERNEL_WCSR 4    /* row-window SpMM                                   */
 #define SPMM_KERNEL_PRUNE 5   /* dense -> 2:4 magnitude pruning                    */
+#define SPMM_KERNEL_PERMUTE 6 /* row gather / scatter (permuted BCSR product)      */
 /* Turns tracing on (clearing earlier records) or off. */
 SPMM_API spmm_status spmm_trace_enable(int32_t on);
 /* Synchronises the traced events and reports launches and total milliseconds
@@ -348,6 +349,53 @@ SPMM_API spmm_status spmm_prune_tvw(const void *dense, int64_t M, int64_t K, int
  * SPMM_ERR_FORMAT.  Synchronises `stream`. */
 SPMM_API spmm_status spmm_build_slide(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
                                       void *vals, uint8_t *meta, spmm_stream_t stream);
+
+/* ---------------------------------------------------------------- permutation
+ * Permuting a square sparse matrix to cut its nonzero blocks before the
+ * block-sparse multiply ("SMaT", abstract).  The permutation is Reverse
+ * Cuthill-McKee (Cuthill and McKee, "Reducing the bandwidth of sparse
+ * symmetric matrices", cited by that page), applied to rows and columns alike:
+ * A' = P A P^T with A'[i][j] = A[perm[i]][perm[j]], and C = A B = P^T A' (P B). */
+
+/* Reverse Cuthill-McKee order of an n x n CSR pattern, on the HOST: row_ptr
+ * [n + 1], col [row_ptr[n]] and perm [n] are host arrays (values are not
+ * needed).  The graph is the pattern of A + A^T without the diagonal.  While
+ * nodes remain unvisited, a breadth-first search starts at the unvisited node
+ * of least degree (lowest index on ties) and every dequeued node appends its
+ * unvisited neighbours in ascending (degree, index) order; perm is the
+ * visiting order reversed (perm[i] = original index at position i).  Column
+ * order within a row and duplicate entries do not matter.  row_ptr not
+ * starting at 0 or decreasing, or a column outside [0, n) -> SPMM_ERR_FORMAT.
+ * Runs on the host because each step of the search depends on the order of
+ * every earlier one; O(nnz log nnz), once per matrix. */
+SPMM_API spmm_status spmm_rcm_order(int64_t n, const int32_t *row_ptr, const int32_t *col, int32_t *perm);
+
+/* out[i][j] = dense[perm[i]][perm[j]] for an n x n dense matrix (device
+ * arrays; row pitches ld and ldo elements; any dtype).  perm must be a
+ * permutation of [0, n); an entry outside the range sets SPMM_DEVERR_INDEX and
+ * writes 0.  Asynchronous on `stream`. */
+SPMM_API spmm_status spmm_permute_sym(const void *dense, int64_t n, int64_t ld, int32_t dtype, const int32_t *perm,
+                                      void *out, int64_t ldo, spmm_stream_t stream);
+
+/* Row permutation of a rows x cols matrix of elem_bytes-byte elements (1, 2
+ * or 4; device arrays, pitches lds / ldd in elements): gather (scatter = 0)
+ * dst row i <- src row perm[i]; scatter (scatter = 1) dst row perm[i] <- src
+ * row i.  perm entries outside [0, rows) set SPMM_DEVERR_INDEX and that row is
+ * skipped.  src and dst must not overlap.  Asynchronous on `stream`. */
+SPMM_API spmm_status spmm_permute_rows(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows,
+                                       int64_t cols, int32_t elem_bytes, const int32_t *perm, int32_t scatter,
+                                       spmm_stream_t stream);
+
+/* Workspace bytes spmm_bcsr_permuted needs: B' (K x N, pitch N rounded up to
+ * 8) and C' (M x N fp32, pitch N rounded up to 4). */
+SPMM_API spmm_status spmm_bcsr_permuted_workspace_size(const spmm_bcsr_t *A, int64_t N, size_t *bytes);
+/* C = A B for A given as the BCSR A' of P A P^T (square, M == K) and its
+ * permutation perm (device, n entries): B' = P B (row gather), C' = A' B'
+ * (spmm_bcsr), C = P^T C' (row scatter).  Arguments and types as spmm_bcsr;
+ * M != K -> SPMM_ERR_SHAPE. */
+SPMM_API spmm_status spmm_bcsr_permuted(const spmm_bcsr_t *A, const int32_t *perm, const void *B, int64_t ldb,
+                                        float *C, int64_t ldc, int64_t N, void *workspace, size_t workspace_bytes,
+                                        spmm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -30,6 +30,7 @@ __all__ = ["BCSR", "Mat24", "Slide", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bc
            "spmm_build_tvw", "spmm_prune_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
            "spmm_build_slide", "spmm_slide", "spmm_slide_workspace_size",
+           "rcm_order", "spmm_permute_sym", "spmm_permute_rows", "spmm_bcsr_permuted", "spmm_bcsr_permuted_workspace_size",
            "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
 
 _DT = {torch.bfloat16: _lib.SPMM_BF16, torch.float16: _lib.SPMM_F16, torch.int8: _lib.SPMM_I8}
@@ -234,6 +235,62 @@ def spmm_bcsr(A: BCSR, B: torch.Tensor, C_: Optional[torch.Tensor] = None, strea
     out = _out(C_, A.M, N, torch.float32, B.device)
     a = A.c()
     _lib.call("spmm_bcsr", C.byref(a), _ptr(B), B.stride(0), _ptr(out), out.stride(0), N, _stream(stream))
+    return out
+
+
+# ------------------------------------------------------------------ permutation before BCSR
+def rcm_order(n: int, row_ptr, col) -> torch.Tensor:
+    """Reverse Cuthill-McKee order (host) of an n x n CSR pattern given as host
+    arrays (numpy or CPU tensors); returns perm as a CPU int32 tensor."""
+    rp = torch.as_tensor(row_ptr, dtype=torch.int32).contiguous()
+    cl = torch.as_tensor(col, dtype=torch.int32).contiguous()
+    if rp.is_cuda or cl.is_cuda:
+        raise ValueError("rcm_order takes host arrays")
+    perm = torch.empty(n, dtype=torch.int32)
+    _lib.call("spmm_rcm_order", n, _ptr(rp), _ptr(cl), _ptr(perm))
+    return perm
+
+
+def spmm_permute_sym(dense: torch.Tensor, perm: torch.Tensor, stream=None) -> torch.Tensor:
+    """out[i][j] = dense[perm[i]][perm[j]] (P A P^T) on the device."""
+    _check_dev(dense, perm)
+    n = dense.shape[0]
+    out = torch.empty((n, n), dtype=dense.dtype, device=dense.device)
+    _lib.call("spmm_permute_sym", _ptr(dense), n, dense.stride(0), _code(dense.dtype), _ptr(perm), _ptr(out),
+              out.stride(0), _stream(stream))
+    return out
+
+
+def spmm_permute_rows(src: torch.Tensor, perm: torch.Tensor, scatter: bool = False,
+                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Row gather (out[i] = src[perm[i]]) or scatter (out[perm[i]] = src[i])."""
+    _check_dev(src, perm, out)
+    rows, cols = src.shape
+    if out is None:
+        out = torch.empty_like(src)
+    _lib.call("spmm_permute_rows", _ptr(src), src.stride(0), _ptr(out), out.stride(0), rows, cols,
+              src.element_size(), _ptr(perm), 1 if scatter else 0, _stream(stream))
+    return out
+
+
+def spmm_bcsr_permuted_workspace_size(A: BCSR, N: int) -> int:
+    n = C.c_size_t(0)
+    a = A.c()
+    _lib.call("spmm_bcsr_permuted_workspace_size", C.byref(a), N, C.byref(n))
+    return n.value
+
+
+def spmm_bcsr_permuted(A: BCSR, perm: torch.Tensor, B: torch.Tensor, C_: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """C = A B where A is given as the BCSR of P A P^T and perm (device int32)."""
+    _check_dev(perm, B, C_, workspace)
+    N = B.shape[1]
+    out = _out(C_, A.M, N, torch.float32, B.device)
+    if workspace is None:
+        workspace = torch.empty(spmm_bcsr_permuted_workspace_size(A, N), dtype=torch.uint8, device=B.device)
+    a = A.c()
+    _lib.call("spmm_bcsr_permuted", C.byref(a), _ptr(perm), _ptr(B), B.stride(0), _ptr(out), out.stride(0), N,
+              _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
 

@@ -242,19 +242,79 @@ spmm_status spmm_trace_read(int32_t kernel, int64_t* launches, double* total_ms)
     return SPMM_OK;
 }
 
-spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
-                      spmm_stream_t stream) {
-    if (!A || !B || !C) return SPMM_ERR_NULL;
+static spmm_status check_bcsr(const spmm_bcsr_t* A, int64_t N) {
+    if (!A) return SPMM_ERR_NULL;
     if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
     if (A->M < 0 || A->K <= 0 || N < 0 || A->bh <= 0 || A->bw <= 0 || A->nnzb < 0) return SPMM_ERR_SHAPE;
     if (A->M % A->bh || A->K % A->bw) return SPMM_ERR_SHAPE;
-    if (ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B) || (A->nnzb > 0 && !aligned16(A->vals)))
-        return SPMM_ERR_SHAPE;
+    if (A->nnzb > 0 && !aligned16(A->vals)) return SPMM_ERR_SHAPE;
     if (A->nnzb > 0 && (!A->row_ptr || !A->col_idx || !A->vals)) return SPMM_ERR_NULL;
     if (A->bh % 16 || A->bh > 256 || (A->bw != 16 && A->bw != 32 && A->bw != 64)) return SPMM_ERR_UNSUPPORTED;
     if (A->nnzb * A->bh >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
         return SPMM_ERR_UNSUPPORTED;
+    return SPMM_OK;
+}
+
+spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                      spmm_stream_t stream) {
+    if (!A || !B || !C) return SPMM_ERR_NULL;
+    const spmm_status st = check_bcsr(A, N);
+    if (st != SPMM_OK) return st;
+    if (ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B)) return SPMM_ERR_SHAPE;
     return launch_bcsr(A, B, ldb, C, ldc, N, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- permutation
+
+spmm_status spmm_rcm_order(int64_t n, const int32_t* row_ptr, const int32_t* col, int32_t* perm) {
+    if (n < 0) return SPMM_ERR_SHAPE;
+    if (n == 0) return SPMM_OK;
+    if (!row_ptr || !perm || (row_ptr[n] > 0 && !col)) return SPMM_ERR_NULL;
+    if (n >= (int64_t(1) << 31)) return SPMM_ERR_UNSUPPORTED;
+    return rcm_order_host(n, row_ptr, col, perm);
+}
+
+spmm_status spmm_permute_sym(const void* dense, int64_t n, int64_t ld, int32_t dtype, const int32_t* perm, void* out,
+                             int64_t ldo, spmm_stream_t stream) {
+    if (n > 0 && (!dense || !perm || !out)) return SPMM_ERR_NULL;
+    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (n < 0 || ld < n || ldo < n) return SPMM_ERR_SHAPE;
+    if (n >= (int64_t(1) << 31)) return SPMM_ERR_UNSUPPORTED;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    return run_permute_sym(dense, n, ld, dtype, perm, out, ldo, dev->err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_permute_rows(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows, int64_t cols,
+                              int32_t elem_bytes, const int32_t* perm, int32_t scatter, spmm_stream_t stream) {
+    if (rows > 0 && cols > 0 && (!src || !dst || !perm)) return SPMM_ERR_NULL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return SPMM_ERR_DTYPE;
+    if (rows < 0 || cols < 0 || lds < cols || ldd < cols) return SPMM_ERR_SHAPE;
+    if (rows >= (int64_t(1) << 31)) return SPMM_ERR_UNSUPPORTED;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    return run_permute_rows(src, lds, dst, ldd, rows, cols, elem_bytes, perm, scatter != 0, dev->err,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_bcsr_permuted_workspace_size(const spmm_bcsr_t* A, int64_t N, size_t* bytes) {
+    if (!bytes) return SPMM_ERR_NULL;
+    const spmm_status st = check_bcsr(A, N);
+    if (st != SPMM_OK) return st;
+    *bytes = bcsr_permuted_ws_bytes(A, N);
+    return SPMM_OK;
+}
+
+spmm_status spmm_bcsr_permuted(const spmm_bcsr_t* A, const int32_t* perm, const void* B, int64_t ldb, float* C,
+                               int64_t ldc, int64_t N, void* workspace, size_t workspace_bytes,
+                               spmm_stream_t stream) {
+    if (!A || !B || !C || (A->M > 0 && !perm)) return SPMM_ERR_NULL;
+    const spmm_status st = check_bcsr(A, N);
+    if (st != SPMM_OK) return st;
+    if (A->M != A->K || ldb < N || ldc < N) return SPMM_ERR_SHAPE;
+    if (!workspace || workspace_bytes < bcsr_permuted_ws_bytes(A, N) || !aligned16(workspace))
+        return SPMM_ERR_WORKSPACE;
+    return launch_bcsr_permuted(A, perm, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- builders

@@ -89,4 +89,13 @@ spmm_status run_build_tvw(const void* dense, int64_t M, int64_t K, int64_t ld, i
 spmm_status run_build_slide(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
                             void* vals, uint8_t* meta, cudaStream_t s);
 
+spmm_status rcm_order_host(int64_t n, const int32_t* row_ptr, const int32_t* col, int32_t* perm);
+spmm_status run_permute_rows(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows, int64_t cols,
+                             int32_t elem_bytes, const int32_t* perm, bool scatter, int* err, cudaStream_t s);
+spmm_status run_permute_sym(const void* dense, int64_t n, int64_t ld, int32_t dtype, const int32_t* perm, void* out,
+                            int64_t ldo, int* err, cudaStream_t s);
+size_t bcsr_permuted_ws_bytes(const spmm_bcsr_t* A, int64_t N);
+spmm_status launch_bcsr_permuted(const spmm_bcsr_t* A, const int32_t* perm, const void* B, int64_t ldb, float* C,
+                                 int64_t ldc, int64_t N, void* ws, cudaStream_t s);
+
 }  // namespace spmm

@@ -80,3 +80,37 @@ def test_host_validation_rejects_bad_arguments_before_launch():
     assert L.spmm_slide(ctypes.byref(sl), 16, 64, 16, 64, 64, None, 0, None) == 2
     assert L.spmm_build_slide(16, 4, 40, 40, 1, 4, 16, 16, None) == 2
     assert L.spmm_build_slide(16, 4, 64, 64, 1, 9, 16, 16, None) == 2
+    # permutation: M != K for the permuted product -> SPMM_ERR_SHAPE; bad CSR for RCM -> SPMM_ERR_FORMAT
+    rect = _lib.BcsrT(128, 256, 16, 16, 0, 1, 16, 16, 16)
+    assert L.spmm_bcsr_permuted(ctypes.byref(rect), 16, 16, 64, 16, 64, 64, 16, 1 << 30, None) == 2
+    rp = (ctypes.c_int32 * 3)(0, 1, 2)
+    col = (ctypes.c_int32 * 2)(0, 5)                      # column 5 outside [0, 2)
+    perm = (ctypes.c_int32 * 2)()
+    assert L.spmm_rcm_order(2, rp, col, perm) == 4
+    assert L.spmm_permute_rows(16, 4, 16, 4, 4, 4, 3, 16, 0, None) == 3   # 3-byte elements -> SPMM_ERR_DTYPE
+
+
+def test_host_rcm_equals_the_oracle():
+    """The library's host RCM and the oracle's (written separately) give the same order."""
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    import numpy as np
+    import oracle
+    import spmm_inputs as gen
+    L = _lib.load()
+    rng = np.random.default_rng(9)
+    for n, dens in ((1, 0.5), (7, 0.2), (60, 0.05), (150, 0.02)):
+        A = (rng.random((n, n)) < dens).astype(np.int8)
+        A[n // 2, :] = 0                                   # isolated or nearly isolated nodes
+        rp = np.concatenate([[0], np.cumsum((A != 0).sum(axis=1))]).astype(np.int32)
+        col = np.nonzero(A)[1].astype(np.int32)
+        perm = np.zeros(n, np.int32)
+        assert L.spmm_rcm_order(n, rp.ctypes.data_as(ctypes.c_void_p), col.ctypes.data_as(ctypes.c_void_p),
+                                perm.ctypes.data_as(ctypes.c_void_p)) == 0
+        assert np.array_equal(perm, oracle.rcm(n, rp, col))
+    p = gen.banded_scrambled_problem(300, 4, 1, seed=2, dtype="i8")
+    rp = np.concatenate([[0], np.cumsum((p["A"] != 0).sum(axis=1))]).astype(np.int32)
+    col = np.nonzero(p["A"])[1].astype(np.int32)
+    perm = np.zeros(300, np.int32)
+    L.spmm_rcm_order(300, rp.ctypes.data_as(ctypes.c_void_p), col.ctypes.data_as(ctypes.c_void_p),
+                     perm.ctypes.data_as(ctypes.c_void_p))
+    assert np.array_equal(perm, oracle.rcm_dense(p["A"]))
