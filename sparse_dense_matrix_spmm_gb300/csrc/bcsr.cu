@@ -63,6 +63,7 @@ struct BcsrArgs {
     uint32_t idesc;
     uint32_t w_swz;
     uint32_t w_sbo;
+    const int32_t* row_perm;  // wide kernel: C row row_perm[r] receives row r (nullptr: C row r)
     int* err;
     uint64_t timeout_ns;
 };
@@ -608,11 +609,46 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                                      : "memory");
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmC, buf, w.nt * kWideTokens + kWideBoxTokens * bx, w.br * kWideRows + 16 * q);
-                    bulk_commit();
+                if (a.row_perm == nullptr) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, w.nt * kWideTokens + kWideBoxTokens * bx, w.br * kWideRows + 16 * q);
+                        bulk_commit();
+                    }
+                } else {
+                    // rows scattered to C row row_perm[r]: the warp reads the staged box
+                    // back four rows at a time (eight lanes x 16 B per row), so every
+                    // row leaves as one contiguous 128-byte segment
+                    __syncwarp();
+                    const int64_t tok0 = static_cast<int64_t>(w.nt) * kWideTokens + kWideBoxTokens * bx;
+                    const int u = lane & 7;
+                    const int64_t col = tok0 + 4 * u;
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int r = 4 * it + (lane >> 3);
+                        const int32_t dst = __ldg(a.row_perm + w.br * kWideRows + 16 * q + r);
+                        uint32_t x0, x1, x2, x3;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                     : "r"(buf + static_cast<uint32_t>(r) * 128u +
+                                           (static_cast<uint32_t>(u ^ (r & 7)) << 4))
+                                     : "memory");
+                        if (dst < 0 || dst >= a.n_brows * kWideRows) {
+                            if (u == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                            continue;
+                        }
+                        float* cp = a.C + static_cast<int64_t>(dst) * a.ldc + col;
+                        const float4 f = make_float4(__uint_as_float(x0), __uint_as_float(x1), __uint_as_float(x2),
+                                                     __uint_as_float(x3));
+                        if (col + 4 <= a.N) {
+                            __stcs(reinterpret_cast<float4*>(cp), f);
+                        } else {
+                            const float e4[4] = {f.x, f.y, f.z, f.w};
+                            for (int t = 0; t < 4 && col + t < a.N; ++t) cp[t] = e4[t];
+                        }
+                    }
+                    __syncwarp();  // the box is read before this buffer is written again
                 }
             }
             if (++acc == a.nacc) {
@@ -639,7 +675,7 @@ uint32_t pow2_at_least(uint32_t x) {
 }
 
 spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
-                             cudaStream_t stream, const DeviceInfo* dev) {
+                             cudaStream_t stream, const DeviceInfo* dev, const int32_t* row_perm) {
     const int bw = A->bw;
     const int64_t n_brows = A->M / kWideRows, n_ntiles = (N + kWideTokens - 1) / kWideTokens;
     if (n_brows * n_ntiles >= (int64_t(1) << 31) - dev->sms || n_ntiles * kWideTokens >= (int64_t(1) << 31) ||
@@ -684,6 +720,7 @@ spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, f
     a.w_bytes = (static_cast<uint32_t>(kWideRows * bw * 2) + 1023u) & ~1023u;
     a.nacc = 2;
     a.tmem_cols = pow2_at_least(2 * kWideTokens);
+    a.row_perm = row_perm;
     a.idesc = idesc_f16(kWideRows, kWideTokens, A->dtype == SPMM_BF16, /*a_mn_major=*/false, /*b_mn_major=*/true,
                         /*sparse=*/false);
     a.w_swz = bw == 64 ? SWZ_128B : bw == 32 ? SWZ_64B : SWZ_32B;
@@ -723,7 +760,7 @@ spmm_status launch_bcsr_wide(const spmm_bcsr_t* A, const void* B, int64_t ldb, f
 }  // namespace
 
 spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const int32_t* row_perm) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
     if (A->M == 0 || N == 0) return SPMM_OK;
@@ -760,7 +797,9 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
         return SPMM_ERR_CUDA;
 
     // 64-row blocks with TMA-storable C: the wide kernel (M = 64 block rows x N = 192 tokens)
-    if (bh == kWideRows && (ldc % 4 == 0) && aligned16(C)) return launch_bcsr_wide(A, B, ldb, C, ldc, N, stream, dev);
+    if (bh == kWideRows && (ldc % 4 == 0) && aligned16(C))
+        return launch_bcsr_wide(A, B, ldb, C, ldc, N, stream, dev, row_perm);
+    if (row_perm) return SPMM_ERR_UNSUPPORTED;  // scattered C rows: the wide kernel only
 
     BcsrArgs a{};
     a.row_ptr = A->row_ptr;

@@ -54,8 +54,10 @@ bool set_smem_attr_once(const void* kernel, int bytes, int slot);
 
 // Kernel launchers implemented in the per-format translation units.  Arguments
 // are already validated by the C-ABI layer.
+// row_perm (device, M entries): C row row_perm[r] receives row r; only for
+// 64-row blocks with 16-byte aligned C rows (else SPMM_ERR_UNSUPPORTED).
 spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const int32_t* row_perm = nullptr);
 
 size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N);
 spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,

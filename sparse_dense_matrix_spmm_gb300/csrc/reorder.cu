@@ -10,7 +10,8 @@
 //   spmm_permute_sym     A' = P A P^T on the device (dense, any 8/16-bit type)
 //   spmm_permute_rows    row gather / scatter on the device (1, 2 or 4-byte elements)
 //   spmm_bcsr_permuted   C = P^T (A' (P B)): gather B's rows, the BCSR kernel on
-//                        A', scatter C's rows
+//                        A', scatter C's rows (inside the BCSR epilogue for
+//                        64-row blocks, else as a second pass)
 #include <algorithm>
 #include <vector>
 
@@ -168,6 +169,9 @@ spmm_status launch_bcsr_permuted(const spmm_bcsr_t* A, const int32_t* perm, cons
     float* Cp = reinterpret_cast<float*>(w + ((static_cast<size_t>(A->K) * nb * 2 + 255) & ~size_t(255)));
     spmm_status st = run_permute_rows(B, ldb, Bp, nb, A->K, N, 2, perm, false, dev->err, s);
     if (st != SPMM_OK) return st;
+    // 64-row blocks and 16-byte aligned C rows: the BCSR epilogue writes each row
+    // straight to C row perm[r]; otherwise C' is scattered by a second pass
+    if (A->bh == 64 && ldc % 4 == 0 && aligned16(C) && A->nnzb > 0) return launch_bcsr(A, Bp, nb, C, ldc, N, s, perm);
     st = launch_bcsr(A, Bp, nb, Cp, nc, N, s);
     if (st != SPMM_OK) return st;
     return run_permute_rows(Cp, nc, C, ldc, A->M, N, 4, perm, true, dev->err, s);

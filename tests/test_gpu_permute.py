@@ -92,3 +92,27 @@ def test_bcsr_permuted_full_size_sampled_rows():
     rows = np.sort(np.random.default_rng(31).choice(n, size=64, replace=False))
     ref = bits_to_f64(p["A"][rows], "f16") @ bits_to_f64(p["B"], "f16")
     assert_close(C[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, "permuted full size")
+
+
+@pytest.mark.parametrize("N", [130, 256])
+def test_bcsr_permuted_fused_scatter_equals_two_pass(N):
+    """64-row blocks with 16-byte aligned C rows take the epilogue scatter; an
+    unaligned C pitch takes the gather / BCSR / scatter passes.  Both run the same
+    products, so their results agree bit for bit (ragged N included)."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    n = 512
+    p = gen.banded_scrambled_problem(n, 10, N, seed=N, dtype="f16")
+    perm = spmm.rcm_order(n, *_pattern(p["A"]))
+    F = spmm.build_bcsr(spmm.spmm_permute_sym(dev_half(p["A"], "f16"), perm.cuda()), 64, 64)
+    B = padded_b(p["B"], "f16")
+    pitch4 = -(-N // 4) * 4
+    C1 = torch.full((n, pitch4), float("nan"), device="cuda")[:, :N]       # ldc % 4 == 0: fused
+    C2 = torch.full((n, pitch4 + 1), float("nan"), device="cuda")[:, :N]   # ldc % 4 != 0: two passes
+    spmm.spmm_bcsr_permuted(F, perm.cuda(), B, C1)
+    spmm.spmm_bcsr_permuted(F, perm.cuda(), B, C2)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    a, b = C1.cpu().numpy(), C2.cpu().numpy()
+    assert not np.isnan(a).any() and np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert_close(a, bits_to_f64(p["A"], "f16") @ bits_to_f64(p["B"], "f16"), "fused scatter")
