@@ -9,6 +9,9 @@
  *         consecutive K entries kept           Tiled GEMM", abstract)
  *   TVW   tile-vector-wise: per row tile a   ("Accelerating Sparse DNNs Based on
  *         kept column set, 2:4 inside it       Tiled GEMM", abstract)
+ * and two routes onto them: (2n-2):2n lifted into overlapping 2:4 windows
+ * ("SlideSparse", abstract) and a Reverse Cuthill-McKee permutation before
+ * BCSR ("SMaT", abstract).
  *
  * Conventions shared by every entry point
  *   - All matrix pointers are DEVICE pointers owned by the caller.  The library
@@ -17,7 +20,9 @@
  *     *_workspace_size() query returns.
  *   - B is K x N row-major with leading dimension ldb (elements); C is M x N
  *     row-major with leading dimension ldc.  Every element of C[0:M, 0:N] is
- *     written (rows without stored entries get 0).
+ *     written (rows without stored entries get 0).  When M or N is 0 there is
+ *     nothing to write: B and C may then be null and the call returns SPMM_OK
+ *     without launching.
  *   - Floating-point inputs are bf16 or fp16 with fp32 accumulation and fp32 C;
  *     int8 2:4 accumulates exactly and writes int32 C.
  *   - Every call validates its scalar arguments on the host first and returns a

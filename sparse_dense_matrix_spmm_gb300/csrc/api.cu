@@ -257,7 +257,8 @@ static spmm_status check_bcsr(const spmm_bcsr_t* A, int64_t N) {
 
 spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
                       spmm_stream_t stream) {
-    if (!A || !B || !C) return SPMM_ERR_NULL;
+    if (!A) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;  // an empty C needs no buffers
     const spmm_status st = check_bcsr(A, N);
     if (st != SPMM_OK) return st;
     if (ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B)) return SPMM_ERR_SHAPE;
@@ -308,7 +309,8 @@ spmm_status spmm_bcsr_permuted_workspace_size(const spmm_bcsr_t* A, int64_t N, s
 spmm_status spmm_bcsr_permuted(const spmm_bcsr_t* A, const int32_t* perm, const void* B, int64_t ldb, float* C,
                                int64_t ldc, int64_t N, void* workspace, size_t workspace_bytes,
                                spmm_stream_t stream) {
-    if (!A || !B || !C || (A->M > 0 && !perm)) return SPMM_ERR_NULL;
+    if (!A) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C || !perm)) return SPMM_ERR_NULL;
     const spmm_status st = check_bcsr(A, N);
     if (st != SPMM_OK) return st;
     if (A->M != A->K || ldb < N || ldc < N) return SPMM_ERR_SHAPE;
@@ -472,7 +474,7 @@ spmm_status spmm_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C
                       void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
     spmm_status st = check_wcsr(A);
     if (st != SPMM_OK) return st;
-    if (!B || !C) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
     if (N < 0 || ldb < N || ldc < N || (ldb * 2) % 16 || !aligned16(B)) return SPMM_ERR_SHAPE;
     if (A->M > 0 && (!A->wcol_ptr || !A->unit_ptr || !A->unit_win || !A->unit_nz_ptr)) return SPMM_ERR_NULL;
     if (A->nnz > 0 && (!A->wcols || !A->lrow || !A->slot || !A->val)) return SPMM_ERR_NULL;
@@ -503,7 +505,8 @@ spmm_status spmm_24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int
                     void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
     spmm_status st = check_24(A, N);
     if (st != SPMM_OK) return st;
-    if (!B || !C || (A->M > 0 && (!A->vals || !A->meta))) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
+    if (A->M > 0 && (!A->vals || !A->meta)) return SPMM_ERR_NULL;
     if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
     if (A->dtype != SPMM_I8 && ((ldb * 2) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
     const size_t need = spmm24_workspace_bytes(A, N);
@@ -533,7 +536,8 @@ spmm_status spmm_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void* 
                        void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
     spmm_status st = check_slide(A, N);
     if (st != SPMM_OK) return st;
-    if (!B || !C || (A->M > 0 && (!A->vals || !A->meta))) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
+    if (A->M > 0 && (!A->vals || !A->meta)) return SPMM_ERR_NULL;
     if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
     if (A->dtype != SPMM_I8 && ((ldb * 2) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
     const size_t need = slide_workspace_bytes(A, N);
@@ -543,7 +547,8 @@ spmm_status spmm_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void* 
 
 spmm_status spmm_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
                      spmm_stream_t stream) {
-    if (!A || !B || !C) return SPMM_ERR_NULL;
+    if (!A) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
     if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
     if (A->M < 0 || A->K <= 0 || N < 0 || A->Kp < 0 || A->tile_rows <= 0) return SPMM_ERR_SHAPE;
     if (A->n_tiles != (A->M + A->tile_rows - 1) / A->tile_rows) return SPMM_ERR_SHAPE;

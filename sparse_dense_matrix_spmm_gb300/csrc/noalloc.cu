@@ -50,7 +50,8 @@ using namespace spmm;
 
 extern "C" spmm_status spmm_24_noalloc(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc,
                                        int64_t N, spmm_stream_t stream) {
-    if (!A || !B || !C) return SPMM_ERR_NULL;
+    if (!A) return SPMM_ERR_NULL;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
     if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
     if (A->M < 0 || A->K <= 0 || N < 0 || A->K % 128) return SPMM_ERR_SHAPE;
     if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))

@@ -116,3 +116,23 @@ def test_bcsr_permuted_fused_scatter_equals_two_pass(N):
     a, b = C1.cpu().numpy(), C2.cpu().numpy()
     assert not np.isnan(a).any() and np.array_equal(a.view(np.uint32), b.view(np.uint32))
     assert_close(a, bits_to_f64(p["A"], "f16") @ bits_to_f64(p["B"], "f16"), "fused scatter")
+
+
+def test_permuted_degenerate_inputs():
+    """An empty pattern: RCM visits every isolated node in index order, so perm is
+    the reversed identity; the product (no blocks) is all zeros; N = 0 is a no-op."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    n = 128
+    perm = spmm.rcm_order(n, np.zeros(n + 1, np.int32), np.zeros(0, np.int32))
+    assert perm.tolist() == list(range(n - 1, -1, -1))
+    assert np.array_equal(perm.numpy(), oracle.rcm(n, np.zeros(n + 1, np.int32), np.zeros(0, np.int32)))
+    F = spmm.build_bcsr(torch.zeros((n, n), dtype=torch.float16, device="cuda"), 64, 64)
+    assert F.nnzb == 0
+    C = torch.full((n, 64), float("nan"), device="cuda")
+    spmm.spmm_bcsr_permuted(F, perm.cuda(), torch.ones((n, 64), dtype=torch.float16, device="cuda"), C)
+    torch.cuda.synchronize()
+    assert not C.cpu().numpy().any()
+    assert spmm.spmm_bcsr_permuted(F, perm.cuda(), torch.zeros((n, 0), dtype=torch.float16, device="cuda")).shape == (n, 0)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0

@@ -112,3 +112,22 @@ def test_slide_f16_full_size_sampled_tiles():
     for r0 in sorted(set([int(t) * 128 for t in rng.choice(M // 128 - 1, 2, replace=False)] + [M - 128])):
         assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.slide_spmm(O, p["B"], rows=(r0, r0 + 128)),
                      f"6:8 f16 rows {r0}..")
+
+
+def test_slide_degenerate_inputs():
+    """An all-zero operand (every window padded with (0, 1) and +0) multiplies to
+    zeros; empty M or N returns without work."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    A = np.zeros((64, 512), np.int8)
+    F, O = _build(A, 4, "i8")
+    assert np.all(O["meta"] == 0x44) and not O["vals"].any()
+    B = np.ones((512, 40), np.int8)
+    C = spmm.spmm_slide(F, dev(B))
+    torch.cuda.synchronize()
+    assert not C.cpu().numpy().any()
+    assert spmm.spmm_slide(F, torch.zeros((512, 0), dtype=torch.int8, device="cuda")).shape == (64, 0)
+    E = spmm.spmm_build_slide(torch.zeros((0, 512), dtype=torch.float16, device="cuda"), 4)
+    assert spmm.spmm_slide(E, torch.zeros((512, 16), dtype=torch.float16, device="cuda")).shape == (0, 16)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
