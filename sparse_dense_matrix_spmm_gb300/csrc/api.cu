@@ -314,8 +314,8 @@ spmm_status spmm_bcsr_permuted(const spmm_bcsr_t* A, const int32_t* perm, const 
     const spmm_status st = check_bcsr(A, N);
     if (st != SPMM_OK) return st;
     if (A->M != A->K || ldb < N || ldc < N) return SPMM_ERR_SHAPE;
-    if (!workspace || workspace_bytes < bcsr_permuted_ws_bytes(A, N) || !aligned16(workspace))
-        return SPMM_ERR_WORKSPACE;
+    const size_t need = bcsr_permuted_ws_bytes(A, N);
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SPMM_ERR_WORKSPACE;
     return launch_bcsr_permuted(A, perm, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 

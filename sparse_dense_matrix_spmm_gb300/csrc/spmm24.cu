@@ -54,35 +54,58 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kProducers = 2;
-constexpr int kMmaWarp = kProducers;
-constexpr int kMetaWarp0 = kProducers + 1;
 // Four metadata warps (one per TMEM lane quarter); TVW adds eight warps that
 // gather the kept B rows.  The metadata warps do not gather: a gathering warp
 // waits for the stage it fills to be released, and a metadata rewrite held up
 // behind that wait left the MMAs waiting for their metadata.
 constexpr int kMetaWarps = 4;
 __host__ __device__ constexpr int gather_warps(bool gather) { return gather ? 8 : 0; }
-__host__ __device__ constexpr int epi_warp0(bool gather) { return kMetaWarp0 + kMetaWarps + gather_warps(gather); }
-__host__ __device__ constexpr int threads_for(bool gather) { return 32 * (epi_warp0(gather) + 4); }
-constexpr int BM = 128, BN = 128, KS = 128;                 // KS: dense K per stage
+constexpr int BM = 128, KS = 128;                           // KS: dense K per stage
 constexpr uint32_t A_BYTES = BM * (KS / 2) * 2;             // 16 KB
-constexpr uint32_t B_BYTES = KS * BN * 2;                   // 32 KB: two 64-column chunks
-constexpr uint32_t B_CHUNK = KS * 128;                      // 16 KB
+constexpr uint32_t B_CHUNK = KS * 128;                      // 16 KB: 128 K rows of one 64-column chunk
 constexpr uint32_t M_BYTES = BM * (KS / 8);                 // 2 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + M_BYTES;  // 50 KB, 1024-aligned
-constexpr int STAGES = 4;
 constexpr int NACC = 2;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t META_COL = NACC * BN;                    // metadata columns after the accumulators
 constexpr uint32_t META_STRIDE = 8;                         // one aligned TMEM column per MMA
 constexpr int INT_CHUNK_STEPS = 16;                         // 16 x 128 = 2048 dense K per int chunk
 // 2:4: the metadata warps copy their rows' metadata with cp.async into a ring of
 // META_RING tile steps, META_AHEAD steps ahead (the TMA unit moved 128 separate
 // 16-byte rows per stage for it, ~6% of the kernel's time).
 constexpr int META_RING = 8, META_AHEAD = 6;
-constexpr uint32_t RING_OFF = STAGES * STAGE_BYTES;
-constexpr int SMEM_BYTES = 1024 + RING_OFF + META_RING * M_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+
+// Output tile width.  BN = 128: four 50 KB stages, two producer warps (TVW, the
+// int8 path, whose exact epilogue keeps BN int32 sums per thread, and N <= 128).
+// BN = 192: N = 192 sparse MMAs, which do about a quarter more useful work per
+// tensor-core cycle than N = 128 (measured), in three 66 KB stages with one
+// producer warp per stage; fp16/bf16 2:4 and lifted operands, where the count
+// of tile waves favours it (wide_tile).  Producer p fills
+// the steps at positions t with t % PRODUCERS == p into slot t % STAGES, so each
+// slot has one producer.
+template <int BN_>
+struct Tile {
+    static constexpr int BN = BN_;
+    static constexpr int CHUNKS = BN_ / 64;  // 64-column B chunks (128-byte swizzle rows)
+    static constexpr uint32_t B_BYTES = KS * BN_ * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + M_BYTES;  // 1024-aligned
+    static constexpr int STAGES = BN_ == 128 ? 4 : 3;
+    static constexpr int PRODUCERS = BN_ == 128 ? 2 : 3;
+    static constexpr int MMA_WARP = PRODUCERS;
+    static constexpr int META_WARP0 = PRODUCERS + 1;
+    static constexpr uint32_t META_COL = NACC * BN_;  // metadata columns after the accumulators
+    static constexpr uint32_t RING_OFF = STAGES * STAGE_BYTES;
+    static constexpr int SMEM = 1024 + RING_OFF + META_RING * M_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+    __host__ __device__ static constexpr int epi_warp0(bool gather) {
+        return META_WARP0 + kMetaWarps + gather_warps(gather);
+    }
+    __host__ __device__ static constexpr int threads(bool gather) { return 32 * (epi_warp0(gather) + 4); }
+};
+static_assert(Tile<128>::STAGES % Tile<128>::PRODUCERS == 0 && Tile<192>::STAGES % Tile<192>::PRODUCERS == 0,
+              "every slot belongs to one producer");
+static_assert(Tile<192>::META_COL + META_STRIDE * 4 * Tile<192>::STAGES <= TMEM_COLS &&
+                  Tile<128>::META_COL + META_STRIDE * 4 * Tile<128>::STAGES <= TMEM_COLS,
+              "accumulators and metadata fit in TMEM");
+static_assert(Tile<192>::SMEM <= 232448 && Tile<128>::SMEM <= 232448, "shared memory per block");
+static_assert(Tile<192>::STAGE_BYTES % 1024 == 0 && Tile<128>::STAGE_BYTES % 1024 == 0, "swizzle alignment");
 
 using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
 
@@ -147,20 +170,27 @@ __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int&
     return static_cast<int>(a.K / KS);
 }
 
-template <bool GATHER, bool INT_EXACT, int PLANES>
-__global__ void __launch_bounds__(threads_for(GATHER), 1)
+template <bool GATHER, bool INT_EXACT, int PLANES, int BNT>
+__global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
     sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
                        const __grid_constant__ BMaps<PLANES> tmB, const SpArgs a) {
+    using Cfg = Tile<BNT>;
+    static_assert(!INT_EXACT || BNT == 128, "the int8 epilogue keeps 128 sums per thread");
+    static_assert(!GATHER || BNT == 128, "TVW gathers two 64-column chunks");
+    constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, kProducers = Cfg::PRODUCERS;
+    constexpr int kMmaWarp = Cfg::MMA_WARP, kMetaWarp0 = Cfg::META_WARP0;
+    constexpr uint32_t B_BYTES = Cfg::B_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES, RING_OFF = Cfg::RING_OFF;
+    constexpr uint32_t META_COL = Cfg::META_COL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + META_RING * M_BYTES);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int kGatherWarps = gather_warps(GATHER);
-    constexpr int kEpiWarp0 = epi_warp0(GATHER);
+    constexpr int kEpiWarp0 = Cfg::epi_warp0(GATHER);
     constexpr int kRowsPerWarp = KS / (GATHER ? kGatherWarps : 1);  // TVW: kept rows each gathering warp copies per step
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
-    // stage s: [A | B chunk 0 | B chunk 1 | stored metadata]
+    // stage s: [A | B chunks 0 .. BN/64 - 1 | stored metadata]
     auto a_s = [&](int s) { return s0 + s * STAGE_BYTES; };
     auto b_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES; };
     auto mc_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES + B_BYTES; };
@@ -204,14 +234,12 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
 
     if (warp < kProducers) {
         // -------------------------------------------------------- producers
-        // Both warps walk every (tile, K step); producer p issues the steps whose
-        // position in that sequence has parity p, into its own slots s % 2 == p.
+        // Every producer walks every (tile, K step); producer p issues the steps
+        // at positions t of that sequence with t % kProducers == p, into slot
+        // t % STAGES (STAGES is a multiple of kProducers, so the slot is its own).
         const int p = warp;
-        constexpr int OWN = STAGES / 2;
-        int s = p;
-        uint32_t ph = 0;
-        int armed = 0;
-        bool mine = (p == 0);
+        constexpr int OWN = STAGES / kProducers;
+        int t = 0, t_last = -1, armed = 0;
         const uint64_t pol_stream = l2_policy_evict_first();  // A is read once per column group
         bool ok = true;
         for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -220,10 +248,11 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
             const int m0 = mt * BM, n0 = nt * BN;
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER);
-            // this producer's steps of the tile: ks = first, first + 2, ...
-            const int first = mine ? 0 : 1;
-            mine = ((nk & 1) == 0) ? mine : !mine;
-            for (int ks = first; ks < nk; ks += 2) {
+            // this producer's steps of the tile: t + ks = p (mod kProducers)
+            for (int ks = (p - t % kProducers + kProducers) % kProducers; ks < nk; ks += kProducers) {
+                const int tt = t + ks;
+                const int s = tt % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(tt / STAGES) & 1u;
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                     ok = false;
                     break;
@@ -242,35 +271,31 @@ __global__ void __launch_bounds__(threads_for(GATHER), 1)
                         if (a.b3d) {
                             tma_load_4d(b_s(s), bm, full_bar(s), 0, 0, g0, n0 / 64);
                         } else {
-                            tma_load_3d(b_s(s), bm, full_bar(s), n0, 0, g0);
-                            tma_load_3d(b_s(s) + B_CHUNK, bm, full_bar(s), n0 + 64, 0, g0);
+#pragma unroll
+                            for (int h = 0; h < Cfg::CHUNKS; ++h)
+                                tma_load_3d(b_s(s) + h * B_CHUNK, bm, full_bar(s), n0 + 64 * h, 0, g0);
                         }
                     } else if constexpr (!GATHER) {
                         if (a.b3d) {
                             tma_load_3d(b_s(s), &tmB.m[0], full_bar(s), 0, ks * KS, n0 / 64);
                         } else {
-                            tma_load_2d(b_s(s), &tmB.m[0], full_bar(s), n0, ks * KS);
-                            tma_load_2d(b_s(s) + B_CHUNK, &tmB.m[0], full_bar(s), n0 + 64, ks * KS);
+#pragma unroll
+                            for (int h = 0; h < Cfg::CHUNKS; ++h)
+                                tma_load_2d(b_s(s) + h * B_CHUNK, &tmB.m[0], full_bar(s), n0 + 64 * h, ks * KS);
                         }
                     }
                 }
-                if (armed < OWN) ++armed;
-                s += 2;
-                if (s >= STAGES) {
-                    s -= STAGES;
-                    ph ^= 1u;
-                }
+                ++armed;
+                t_last = tt;
             }
+            t += nk;
         }
-        // Leave no copy in flight: wait for the last phase armed on each own slot.
-        for (int i = 0; i < armed; ++i) {
-            int idx = (s - p) / 2 - 1 - i;
-            uint32_t par = ph;
-            if (idx < 0) {
-                idx += OWN;
-                par ^= 1u;
-            }
-            mbar_wait(full_bar(2 * idx + p), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        // Leave no copy in flight: wait for the last phase armed on each own slot
+        // (no other producer arms these slots, so their phases cannot run ahead).
+        for (int i = 0; i < OWN && i < armed; ++i) {
+            const int tt = t_last - i * kProducers;
+            mbar_wait(full_bar(tt % STAGES), static_cast<uint32_t>(tt / STAGES) & 1u, a.timeout_ns, a.err,
+                      SPMM_DEVERR_TIMEOUT);
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------- MMA issuer
@@ -606,19 +631,20 @@ __global__ void widen_i8_kernel(const WidenJob j0, const WidenJob j1) {
     }
 }
 
-template <bool GATHER, bool INT_EXACT, int PLANES>
+template <bool GATHER, bool INT_EXACT, int PLANES, int BNT>
 spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const BMaps<PLANES>& tmB, const SpArgs& a,
                           cudaStream_t stream, int slot) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
-    if (dev->max_smem_optin < SMEM_BYTES) return SPMM_ERR_UNSUPPORTED;
-    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES>;
-    if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), SMEM_BYTES, slot)) return SPMM_ERR_CUDA;
+    constexpr int kSmem = Tile<BNT>::SMEM;
+    if (dev->max_smem_optin < kSmem) return SPMM_ERR_UNSUPPORTED;
+    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES, BNT>;
+    if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem, slot)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
     if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_SPARSE, stream);
-    kern<<<grid, threads_for(GATHER), SMEM_BYTES, stream>>>(tmA, tmM, tmB, a);
+    kern<<<grid, Tile<BNT>::threads(GATHER), kSmem, stream>>>(tmA, tmM, tmB, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_SPARSE, stream);
     return cuda_status(e);
@@ -669,17 +695,30 @@ bool encode_a_maps(CUtensorMapDataType t, const void* vals, const uint8_t* meta,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// 192-column tiles for fp16/bf16 operands when they take fewer tile-times
+// than 128-column ones.  Persistent CTAs run ceil(tiles / SMs) waves, and a
+// 192-column tile costs about 1.44 times a 128-column one (measured: the
+// three-stage ring, not the wider MMA, sets its pace), so the count of waves
+// decides.  int8 keeps 128 (its exact epilogue holds 128 int32 sums per thread).
+bool wide_tile(bool i8, int64_t M, int64_t N, int sms) {
+    if (i8 || N <= 128) return false;
+    const int64_t mt = (M + BM - 1) / BM;
+    const int64_t w128 = (mt * ((N + 127) / 128) + sms - 1) / sms;
+    const int64_t w192 = (mt * ((N + 191) / 192) + sms - 1) / sms;
+    return w192 * 144 < w128 * 100;
+}
+
 SpArgs dense_b_args(const DeviceInfo* dev, int64_t M, int64_t K, int64_t N, int32_t dtype, const uint8_t* meta,
-                    void* C, int64_t ldc) {
+                    void* C, int64_t ldc, int bn) {
     SpArgs a{};
     a.M = M;
     a.N = N;
     a.K = K;
     a.n_mtiles = static_cast<int32_t>((M + BM - 1) / BM);
-    a.n_ntiles = static_cast<int32_t>((N + BN - 1) / BN);
+    a.n_ntiles = static_cast<int32_t>((N + bn - 1) / bn);
     a.C = C;
     a.ldc = ldc;
-    a.idesc = idesc_f16(128, BN, dtype == SPMM_BF16, false, true, true, 0);
+    a.idesc = idesc_f16(128, bn, dtype == SPMM_BF16, false, true, true, 0);
     a.vec_ok = (ldc % 4 == 0) && aligned16(C);
     a.meta = meta;
     a.ldm = K / 8;
@@ -711,23 +750,26 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
     }
     CUtensorMap tmA, tmM;
     BMaps<1> tmB;
-    // B tile: one 3-D box {64 columns, 128 K rows, 2 halves} when whole 64-column
-    // halves tile N (a ragged half would read past the row), else two 2-D boxes.
+    const int bn = wide_tile(i8, A->M, N, dev->sms) ? 192 : 128;
+    // B tile: one 3-D box {64 columns, 128 K rows, bn / 64 chunks} when whole
+    // 64-column chunks tile N (a ragged chunk would read past the row), else one
+    // 2-D box per chunk.
     bool b3d = false;
     if (N % 64 == 0) {
         const uint64_t dims[3] = {64, static_cast<uint64_t>(A->K), static_cast<uint64_t>(N / 64)};
         const uint64_t strides[2] = {static_cast<uint64_t>(bld) * 2, 128};
-        const uint32_t box[3] = {64, 128, 2};
+        const uint32_t box[3] = {64, 128, static_cast<uint32_t>(bn / 64)};
         b3d = encode_tmap_3d(&tmB.m[0], t, bsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     }
     if (!encode_a_maps(t, vals, A->meta, A->M, A->K, &tmA, &tmM) ||
         (!b3d && !encode_tmap_2d(&tmB.m[0], t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
                                  static_cast<uint64_t>(bld) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
         return SPMM_ERR_CUDA;
-    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc);
+    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, bn);
     a.b3d = b3d ? 1 : 0;
-    if (i8) return launch_sparse<false, true, 1>(tmA, tmM, tmB, a, stream, 2);
-    return launch_sparse<false, false, 1>(tmA, tmM, tmB, a, stream, 1);
+    if (i8) return launch_sparse<false, true, 1, 128>(tmA, tmM, tmB, a, stream, 2);
+    if (bn == 192) return launch_sparse<false, false, 1, 192>(tmA, tmM, tmB, a, stream, 13);
+    return launch_sparse<false, false, 1, 128>(tmA, tmM, tmB, a, stream, 1);
 }
 
 size_t slide_workspace_bytes(const spmm_slide_t* A, int64_t N) {
@@ -754,8 +796,9 @@ spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void
     CUtensorMap tmA, tmM;
     BMaps<kMaxPlanes> tmB;
     std::memset(&tmB, 0, sizeof(tmB));
-    // Plane j: rows 2j + p + 2n g of B (p < 4, g < G).  Whole 64-column halves:
-    // one 4-D box {64, 4, 32, 2}; otherwise two 3-D boxes {64, 4, 32}, one per half.
+    // Plane j: rows 2j + p + 2n g of B (p < 4, g < G).  Whole 64-column chunks:
+    // one 4-D box {64, 4, 32, bn / 64}; otherwise one 3-D box {64, 4, 32} per chunk.
+    const int bn = wide_tile(i8, A->M, N, dev->sms) ? 192 : 128;
     const bool b4d = N % 64 == 0;
     const uint64_t row = static_cast<uint64_t>(bld) * 2;
     for (int j = 0; j < n - 1; ++j) {
@@ -764,7 +807,7 @@ spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void
         if (b4d) {
             const uint64_t dims[4] = {64, 4, static_cast<uint64_t>(G), static_cast<uint64_t>(N / 64)};
             const uint64_t strides[3] = {row, 2 * n * row, 128};
-            const uint32_t box[4] = {64, 4, 32, 2};
+            const uint32_t box[4] = {64, 4, 32, static_cast<uint32_t>(bn / 64)};
             ok = encode_tmap_4d(&tmB.m[j], t, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         } else {
             const uint64_t dims[3] = {static_cast<uint64_t>(N), 4, static_cast<uint64_t>(G)};
@@ -775,12 +818,13 @@ spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void
         if (!ok) return SPMM_ERR_CUDA;
     }
     if (!encode_a_maps(t, vals, A->meta, A->M, Kl, &tmA, &tmM)) return SPMM_ERR_CUDA;
-    SpArgs a = dense_b_args(dev, A->M, Kl, N, A->dtype, A->meta, C, ldc);
+    SpArgs a = dense_b_args(dev, A->M, Kl, N, A->dtype, A->meta, C, ldc, bn);
     a.b3d = b4d ? 1 : 0;
     a.planes = n - 1;
     a.plane_groups = static_cast<int32_t>(G);
-    if (i8) return launch_sparse<false, true, kMaxPlanes>(tmA, tmM, tmB, a, stream, 12);
-    return launch_sparse<false, false, kMaxPlanes>(tmA, tmM, tmB, a, stream, 11);
+    if (i8) return launch_sparse<false, true, kMaxPlanes, 128>(tmA, tmM, tmB, a, stream, 12);
+    if (bn == 192) return launch_sparse<false, false, kMaxPlanes, 192>(tmA, tmM, tmB, a, stream, 14);
+    return launch_sparse<false, false, kMaxPlanes, 128>(tmA, tmM, tmB, a, stream, 11);
 }
 
 spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
@@ -803,17 +847,17 @@ spmm_status launch_tvw(const spmm_tvw_t* A, const void* B, int64_t ldb, float* C
     a.N = N;
     a.K = A->Kp;
     a.n_mtiles = static_cast<int32_t>(A->n_tiles);
-    a.n_ntiles = static_cast<int32_t>((N + BN - 1) / BN);
+    a.n_ntiles = static_cast<int32_t>((N + 127) / 128);
     a.tile_ptr = A->tile_ptr;
     a.cols = A->cols;
     a.C = C;
     a.ldc = ldc;
-    a.idesc = idesc_f16(128, BN, A->dtype == SPMM_BF16, false, true, true, 0);
+    a.idesc = idesc_f16(128, 128, A->dtype == SPMM_BF16, false, true, true, 0);
     a.vec_ok = (ldc % 4 == 0) && aligned16(C);
     a.planes = 1;
     a.err = dev->err;
     a.timeout_ns = kWaitTimeoutNs;
-    return launch_sparse<true, false, 1>(tmA, tmM, tmB, a, stream, 3);
+    return launch_sparse<true, false, 1, 128>(tmA, tmM, tmB, a, stream, 3);
 }
 
 }  // namespace spmm

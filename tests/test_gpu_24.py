@@ -148,3 +148,27 @@ def test_24_prune_bit_exact_and_spmm(dtype, M, K):
         C = spmm.spmm_24(F, padded_b(B, dtype))
         torch.cuda.synchronize()
         assert_close(C[1:].cpu().numpy(), oracle.spmm24(O, B, rows=(1, M)), f"pruned 2:4 {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [384, 380])
+def test_24_float_192_column_tiles(dtype, N):
+    """M = 128 x (SM count) and N of three 128-column tiles: two waves of
+    192-column tiles beat three of 128-column ones, so the kernel runs its
+    192-column configuration (3-D B boxes at N = 384, per-chunk 2-D boxes and a
+    ragged last chunk at N = 380).  Three 128-row tiles are checked."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, K = 128 * sms, 256
+    rng = np.random.default_rng(N + len(dtype))
+    mask = gen.mask24_problem(M, K, 1, seed=3)["A"] != 0
+    Abits = gen.normal_bits(rng, (M, K), dtype)
+    Abits[~mask] = 0
+    Bbits = gen.normal_bits(rng, (K, N), dtype)
+    F, O = _compress({"A": Abits}, dtype)
+    C = spmm.spmm_24(F, padded_b(Bbits, dtype))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    for r0 in (0, 128 * (sms // 2), M - 128):
+        assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.spmm24(O, Bbits, rows=(r0, r0 + 128)), f"2:4 {dtype} wide {r0}")

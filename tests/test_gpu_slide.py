@@ -131,3 +131,23 @@ def test_slide_degenerate_inputs():
     assert spmm.spmm_slide(E, torch.zeros((512, 16), dtype=torch.float16, device="cuda")).shape == (0, 16)
     torch.cuda.synchronize()
     assert spmm.last_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype,N", [("f16", 384), ("bf16", 380)])
+def test_slide_192_column_tiles(dtype, N):
+    """The lifted product in the 192-column configuration (M = 128 x SM count,
+    three 128-column tiles of N): 4-D plane boxes at N = 384, per-chunk 3-D boxes
+    at N = 380.  Three 128-row tiles are checked."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, K = 128 * sms, 512
+    p = gen.slide_problem(M, K, N, 4, seed=N, dtype=dtype)
+    F = spmm.spmm_build_slide(_on_dev(p["A"], dtype), 4)
+    O = oracle.slide_build(p["A"], 4, dtype)
+    C = spmm.spmm_slide(F, padded_b(p["B"], dtype))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    for r0 in (0, 128 * (sms // 2), M - 128):
+        assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.slide_spmm(O, p["B"], rows=(r0, r0 + 128)),
+                     f"slide {dtype} wide {r0}")
