@@ -757,3 +757,22 @@ void orc_permute_sym(int64_t n, int64_t ld, int dtype, const void *A, const int3
     for (int64_t i = 0; i < n; i++)
         for (int64_t j = 0; j < n; j++) copy_elem(out, i * n + j, A, perm[i] * ld + perm[j], dtype);
 }
+
+/* ================================================================== SDDMM
+ * "Magicube" (abstract: SpMM and SDDMM, the two sparse operations the library
+ * supports).  Reading (the page gives no definition): the sampled dense-dense
+ * product, out[e] = sum_k A[i][k] * Bt[j][k] for every stored entry e = (i, j)
+ * of a CSR pattern, i.e. (A B) at the pattern's positions with B = Bt^T given
+ * as Bt (N x K, row-major; attention's Q K^T has this form).  The pattern's
+ * values are not used.  Products and sums in fp64, ascending k. */
+void orc_sddmm(int64_t M, int64_t K, int dtype, const int32_t *row_ptr, const int32_t *col, const void *A,
+               const void *Bt, double *out) {
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < M; i++)
+        for (int32_t e = row_ptr[i]; e < row_ptr[i + 1]; e++) {
+            int64_t j = col[e];
+            double s = 0.0;
+            for (int64_t k = 0; k < K; k++) s += get_f(A, i * K + k, dtype) * get_f(Bt, j * K + k, dtype);
+            out[e] = s;
+        }
+}

@@ -555,3 +555,32 @@ def test_permute_sym_and_permuted_spmm_equal_the_plain_product():
     F = oracle.bcsr_build(oracle.permute_sym(q["A"], perm, "bf16"), 16, 16, "bf16")
     np.testing.assert_allclose(oracle.bcsr_spmm_permuted(F, perm, q["B"]),
                                bits_to_f64(q["A"], "bf16") @ bits_to_f64(q["B"], "bf16"), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- SDDMM
+def test_sddmm_golden():
+    g = golden("sddmm_int8_3x4.json")
+    out = oracle.sddmm(np.array(g["row_ptr"]), np.array(g["col"]), np.array(g["A"], np.int8),
+                       np.array(g["Bt"], np.int8), "i8")
+    assert out.tolist() == g["out"]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_sddmm_is_the_dense_product_at_the_pattern(dtype):
+    """Every output equals the entry of the dense product A Bt^T (numpy, fp64) at its
+    position (an emptied row included); a full pattern gives the whole product."""
+    q = gen.csr_lognormal_problem(60, 45, 1, seed=4, mean=6.0, sigma=1.0, clip=45, dtype=dtype)
+    rows = np.repeat(np.arange(60), np.diff(q["row_ptr"]))
+    keep = rows != 7                                             # row 7 emptied
+    rp = np.concatenate([[0], np.cumsum(np.bincount(rows[keep], minlength=60))]).astype(np.int32)
+    cl = q["col"][keep].astype(np.int32)
+    rng = np.random.default_rng(1)
+    A = gen.normal_bits(rng, (60, 33), dtype)
+    Bt = gen.normal_bits(rng, (45, 33), dtype)
+    D = bits_to_f64(A, dtype) @ bits_to_f64(Bt, dtype).T
+    out = oracle.sddmm(rp, cl, A, Bt, dtype)
+    np.testing.assert_allclose(out, D[rows[keep], cl], rtol=1e-12, atol=1e-12)
+    assert rp[7] == rp[8]
+    full_rp = (np.arange(61) * 45).astype(np.int32)
+    full_cl = np.tile(np.arange(45), 60).astype(np.int32)
+    np.testing.assert_allclose(oracle.sddmm(full_rp, full_cl, A, Bt, dtype).reshape(60, 45), D, rtol=1e-12, atol=1e-12)
