@@ -9,7 +9,8 @@ TFLOP/s = 2 * nnz * N / time.
 
 The same line carries, per other workload (BCSR LLM-shaped, tile-vector-wise,
 row-window CSR, fp16 2:4, 6:8 through overlapping 2:4 windows, a scrambled band
-multiplied after Reverse Cuthill-McKee, the two pruning builders, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
+multiplied after Reverse Cuthill-McKee, SDDMM on the row-window pattern, the two
+pruning builders, BCSR tiny), its own time, TFLOP/s, GB/s and roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -62,6 +63,7 @@ KERNEL_SOURCES = {
     "sparse_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/spmm24.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "bcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/bcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "wcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
+    "sddmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/sddmm.cu",),
 }
 
 
@@ -393,6 +395,24 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             spmm.spmm_24(F, Bx, Cd, wsp)
+    elif c["kind"] == "sddmm":
+        # sampled dense-dense product on the row-window workload's CSR pattern, A and Bt N(0,1) fp16
+        p = gen.config_problem(name)
+        dt = torch.float16
+        S = spmm.CSR(c["M"], c["K"], int(p["row_ptr"][-1]), dt, to_dev(p["row_ptr"]), to_dev(p["col"]),
+                     to_dev(p["val"], dt))
+        Ax, Btx = to_dev(p["A"], dt), to_dev(p["Bt"], dt)
+        out_d = torch.empty(S.nnz, dtype=torch.float32, device="cuda")
+        build_ms = 0.0
+        nnz = S.nnz
+        K_in = c["inner"]
+        # pattern (row_ptr, col), A and Bt read once, one fp32 per entry written
+        alg = (c["M"] + 1) * 4 + nnz * 4 + c["M"] * K_in * 2 + c["K"] * K_in * 2 + nnz * 4
+        kern, kid = "sddmm_kernel", spmm._lib.KERNEL_SDDMM
+        extra_fields["inner"] = K_in
+
+        def step():
+            spmm.spmm_sddmm(S, Ax, Btx, out_d)
     elif c["kind"] == "rcm":
         # a scrambled band: RCM (host) on its pattern, P A P^T and its BCSR on the device; the step is
         # the permuted product (B gathered, BCSR, C scattered); context: BCSR of the scrambled matrix as is
@@ -526,7 +546,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
     else:
         raise ValueError(name)
     builder = c["kind"] in ("prune24", "prunetvw")
-    flops = 0.0 if builder else 2.0 * nnz * c["N"]
+    flops = 0.0 if builder else 2.0 * nnz * (c["inner"] if c["kind"] == "sddmm" else c["N"])
     spmm.trace_enable(True)
     for _ in range(args.warmup):
         step()
@@ -662,8 +682,8 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "slide68_f16", "bcsr_rcm", "prune24_f16",
-                     "prune_tvw_f16", "bcsr_tiny"):
+        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "slide68_f16", "bcsr_rcm", "sddmm_lognormal",
+                     "prune24_f16", "prune_tvw_f16", "bcsr_tiny"):
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden

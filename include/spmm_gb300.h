@@ -11,7 +11,7 @@
  *         kept column set, 2:4 inside it       Tiled GEMM", abstract)
  * and two routes onto them: (2n-2):2n lifted into overlapping 2:4 windows
  * ("SlideSparse", abstract) and a Reverse Cuthill-McKee permutation before
- * BCSR ("SMaT", abstract).
+ * BCSR ("SMaT", abstract).  SDDMM samples a dense product at a CSR pattern.
  *
  * Conventions shared by every entry point
  *   - All matrix pointers are DEVICE pointers owned by the caller.  The library
@@ -201,6 +201,7 @@ SPMM_API spmm_status spmm_selftest_timeout(uint64_t timeout_ns, spmm_stream_t st
 #define SPMM_KERNEL_WCSR 4    /* row-window SpMM                                   */
 #define SPMM_KERNEL_PRUNE 5   /* dense -> 2:4 magnitude pruning                    */
 #define SPMM_KERNEL_PERMUTE 6 /* row gather / scatter (permuted BCSR product)      */
+#define SPMM_KERNEL_SDDMM 7   /* sampled dense-dense product                       */
 /* Turns tracing on (clearing earlier records) or off. */
 SPMM_API spmm_status spmm_trace_enable(int32_t on);
 /* Synchronises the traced events and reports launches and total milliseconds
@@ -354,6 +355,21 @@ SPMM_API spmm_status spmm_prune_tvw(const void *dense, int64_t M, int64_t K, int
  * SPMM_ERR_FORMAT.  Synchronises `stream`. */
 SPMM_API spmm_status spmm_build_slide(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, int32_t n,
                                       void *vals, uint8_t *meta, spmm_stream_t stream);
+
+/* ---------------------------------------------------------------- SDDMM
+ * The sampled dense-dense product, the second sparse operation of "Magicube"
+ * (abstract: SpMM and SDDMM).  out[e] = sum_k A[i][k] * Bt[j][k] for every
+ * stored entry e = (i, j) of the CSR pattern S, i.e. (A B) at the pattern's
+ * positions with B given transposed as Bt.  S->M rows, S->K columns (= rows of
+ * Bt), S->nnz entries; S->dtype (SPMM_F16 or SPMM_BF16) is the type of A and
+ * Bt; S->val is not read.  A is S->M x K (row pitch lda), Bt is S->K x K (row
+ * pitch ldbt), both device arrays, 16-byte aligned with lda, ldbt and K
+ * multiples of 8 (else SPMM_ERR_SHAPE).  out[S->nnz] is fp32 in pattern order.
+ * Products are summed in fp32.  A column outside [0, S->K) sets
+ * SPMM_DEVERR_INDEX and writes 0; row_ptr is read within [0, S->M].
+ * Asynchronous on `stream`. */
+SPMM_API spmm_status spmm_sddmm(const spmm_csr_t *S, int64_t K, const void *A, int64_t lda, const void *Bt,
+                                int64_t ldbt, float *out, spmm_stream_t stream);
 
 /* ---------------------------------------------------------------- permutation
  * Permuting a square sparse matrix to cut its nonzero blocks before the

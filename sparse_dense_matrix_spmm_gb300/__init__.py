@@ -30,7 +30,7 @@ __all__ = ["BCSR", "Mat24", "Slide", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bc
            "spmm_build_tvw", "spmm_prune_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
            "spmm_build_slide", "spmm_slide", "spmm_slide_workspace_size",
-           "rcm_order", "spmm_permute_sym", "spmm_permute_rows", "spmm_bcsr_permuted", "spmm_bcsr_permuted_workspace_size",
+           "spmm_sddmm", "rcm_order", "spmm_permute_sym", "spmm_permute_rows", "spmm_bcsr_permuted", "spmm_bcsr_permuted_workspace_size",
            "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
 
 _DT = {torch.bfloat16: _lib.SPMM_BF16, torch.float16: _lib.SPMM_F16, torch.int8: _lib.SPMM_I8}
@@ -235,6 +235,19 @@ def spmm_bcsr(A: BCSR, B: torch.Tensor, C_: Optional[torch.Tensor] = None, strea
     out = _out(C_, A.M, N, torch.float32, B.device)
     a = A.c()
     _lib.call("spmm_bcsr", C.byref(a), _ptr(B), B.stride(0), _ptr(out), out.stride(0), N, _stream(stream))
+    return out
+
+
+# ------------------------------------------------------------------ SDDMM
+def spmm_sddmm(S: CSR, A: torch.Tensor, Bt: torch.Tensor, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """out[e] = A[i] . Bt[j] for every stored (i, j) of the CSR pattern S (fp32, pattern order)."""
+    _check_dev(A, Bt, out)
+    K = A.shape[1]
+    if out is None:
+        out = torch.empty(S.nnz, dtype=torch.float32, device=A.device)
+    s = S.c()
+    _lib.call("spmm_sddmm", C.byref(s), K, _ptr(A), A.stride(0), _ptr(Bt), Bt.stride(0), _ptr(out), _stream(stream))
     return out
 
 

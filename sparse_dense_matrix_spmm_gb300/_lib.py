@@ -9,7 +9,7 @@ LIB_PATH = os.path.join(_PKG, "libspmm_gb300.so")
 
 SPMM_BF16, SPMM_F16, SPMM_I8 = 0, 1, 2
 DEVERR_TIMEOUT, DEVERR_INDEX, DEVERR_FORMAT = 1, 2, 4
-KERNEL_BCSR, KERNEL_SPARSE, KERNEL_WIDEN, KERNEL_WCSR, KERNEL_PRUNE, KERNEL_PERMUTE = 1, 2, 3, 4, 5, 6
+KERNEL_BCSR, KERNEL_SPARSE, KERNEL_WIDEN, KERNEL_WCSR, KERNEL_PRUNE, KERNEL_PERMUTE, KERNEL_SDDMM = 1, 2, 3, 4, 5, 6, 7
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_NULL", 2: "SPMM_ERR_SHAPE", 3: "SPMM_ERR_DTYPE", 4: "SPMM_ERR_FORMAT",
           5: "SPMM_ERR_WORKSPACE", 6: "SPMM_ERR_TIMEOUT", 7: "SPMM_ERR_CUDA", 8: "SPMM_ERR_UNSUPPORTED"}
 
@@ -80,6 +80,7 @@ SIGNATURES = {
     "spmm_prune_tvw": (I32, [P, I64, I64, I64, I32, I32, P, P, I64, I64, P, P, P]),
     "spmm_build_slide": (I32, [P, I64, I64, I64, I32, I32, P, P, P]),
     "spmm_rcm_order": (I32, [I64, P, P, P]),
+    "spmm_sddmm": (I32, [C.POINTER(CsrT), I64, P, I64, P, I64, P, P]),
     "spmm_permute_sym": (I32, [P, I64, I64, I32, P, P, I64, P]),
     "spmm_permute_rows": (I32, [P, I64, P, I64, I64, I64, I32, P, I32, P]),
     "spmm_bcsr_permuted_workspace_size": (I32, [C.POINTER(BcsrT), I64, C.POINTER(SZ)]),

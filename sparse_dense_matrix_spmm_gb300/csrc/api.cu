@@ -265,6 +265,22 @@ spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C
     return launch_bcsr(A, B, ldb, C, ldc, N, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---------------------------------------------------------------- SDDMM
+
+spmm_status spmm_sddmm(const spmm_csr_t* S, int64_t K, const void* A, int64_t lda, const void* Bt, int64_t ldbt,
+                       float* out, spmm_stream_t stream) {
+    if (!S) return SPMM_ERR_NULL;
+    if (S->dtype != SPMM_BF16 && S->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
+    if (S->M < 0 || S->K < 0 || S->nnz < 0 || K <= 0 || K % 8 || lda < K || ldbt < K || lda % 8 || ldbt % 8)
+        return SPMM_ERR_SHAPE;
+    if (S->nnz == 0) return SPMM_OK;
+    if (!S->row_ptr || !S->col || !A || !Bt || !out) return SPMM_ERR_NULL;
+    if (S->M == 0 || !aligned16(A) || !aligned16(Bt)) return SPMM_ERR_SHAPE;
+    if (S->M >= (int64_t(1) << 31) || S->K >= (int64_t(1) << 31) || S->nnz >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    return launch_sddmm(S, K, A, lda, Bt, ldbt, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------- permutation
 
 spmm_status spmm_rcm_order(int64_t n, const int32_t* row_ptr, const int32_t* col, int32_t* perm) {

@@ -248,6 +248,9 @@ CONFIGS = {
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
                      dtype=BF16, std=0.02),
     "tvw": dict(kind="tvw", M=4096, K=4096, N=4096, tile_rows=128, keep=2048, seed=5, dtype=F16),
+    # SDDMM on the row-window workload's pattern: A, Bt 65536 x 128 (a sparse attention score)
+    "sddmm_lognormal": dict(kind="sddmm", M=65536, K=65536, N=0, inner=128, seed=3, mean=16.0, sigma=1.5,
+                            clip=4096, dtype=F16),
     # a scrambled band (half-width 48) before and after RCM, 64 x 64 blocks
     "bcsr_rcm": dict(kind="rcm", M=16384, K=16384, N=2048, w=48, bh=64, bw=64, seed=10, dtype=F16),
     # 6:8 on a Qwen2.5-7B-sized FFN projection (18944 x 3584), 8192 tokens
@@ -273,6 +276,14 @@ def config_problem(name: str, **overrides) -> dict:
     if kind == "tvw":
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))
+    if kind == "sddmm":  # the CSR pattern of csr_lognormal_problem, then A (M x inner) and Bt (K x inner)
+        p = csr_lognormal_problem(c["M"], c["K"], 1, c["seed"], c.get("mean", 16.0), c.get("sigma", 1.5),
+                                  c.get("clip", 4096), c.get("dtype", F16))
+        rng = np.random.default_rng(c["seed"] + 1000)
+        p["A"] = normal_bits(rng, (c["M"], c["inner"]), c.get("dtype", F16))
+        p["Bt"] = normal_bits(rng, (c["K"], c["inner"]), c.get("dtype", F16))
+        del p["B"]
+        return p
     if kind == "rcm":
         return banded_scrambled_problem(c["M"], c["w"], c["N"], c["seed"], c.get("dtype", F16))
     if kind == "slide":

@@ -114,3 +114,15 @@ def test_host_rcm_equals_the_oracle():
     L.spmm_rcm_order(300, rp.ctypes.data_as(ctypes.c_void_p), col.ctypes.data_as(ctypes.c_void_p),
                      perm.ctypes.data_as(ctypes.c_void_p))
     assert np.array_equal(perm, oracle.rcm_dense(p["A"]))
+
+
+def test_sddmm_validation():
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    L = _lib.load()
+    S = _lib.CsrT(64, 64, 10, 1, 16, 16, 16)
+    assert L.spmm_sddmm(ctypes.byref(S), 12, 16, 16, 16, 16, 16, None) == 2      # K % 8 != 0
+    assert L.spmm_sddmm(ctypes.byref(S), 16, 16, 8, 16, 16, 16, None) == 2       # lda < K
+    S8 = _lib.CsrT(64, 64, 10, 2, 16, 16, 16)
+    assert L.spmm_sddmm(ctypes.byref(S8), 16, 16, 16, 16, 16, 16, None) == 3     # int8 -> SPMM_ERR_DTYPE
+    E = _lib.CsrT(64, 64, 0, 1, None, None, None)
+    assert L.spmm_sddmm(ctypes.byref(E), 16, None, 16, None, 16, None, None) == 0  # no entries: nothing to do
