@@ -7,8 +7,8 @@
 // Each warp takes a fixed slice of the nonzero array (so one long row does not
 // serialise on one warp), finds the slice's first row by binary search in
 // row_ptr (a dependent chain of about log2(M) loads, so slices are long), and
-// preloads the slice's (row, column) pairs with coalesced loads, handing them
-// to the lane groups by shuffles.  L = min(32, K / 8) lanes form one
+// preloads the slice's (row, column) pairs with coalesced loads into shared
+// memory, where the lane groups read them.  L = min(32, K / 8) lanes form one
 // output's group: each lane loads 8 elements (16 bytes) of A's row and of Bt's
 // row per step, and the group sums by shuffles.  Each lane keeps ILP outputs in
 // flight to hide the latency of the Bt row gathers.
@@ -87,15 +87,18 @@ __global__ void __launch_bounds__(kThreads) sddmm_kernel(const SddmmArgs a) {
         lo = lo + step * k;
         hi = lo + step < hi ? lo + step : hi;
     }
-    // Preload the slice's (row, column) pairs, lane l holding entries e0 + l + 32 t
-    // (coalesced), so the passes below wait on no index load.  Rows: the lanes
+    // Preload the slice's (row, column) pairs into this warp's shared arrays, lane l
+    // writing entries e0 + l + 32 t (coalesced loads), so the passes below wait on
+    // no index load.  Rows: the lanes
     // load the ends of 32 consecutive rows rb .. rb + 31 (one coalesced load); an
     // entry before the last of those ends lies in row rb + (number of ends at or
     // before it), found by a 5-step search over the 32 sorted ends.  Entries past
     // the window retry with the next 32 rows.  Each group of 32 entries starts
     // at the row of its first entry, so one window usually serves it.
     constexpr int64_t kPastEnd = int64_t(1) << 62;  // row ends beyond row M - 1
-    int32_t pr[kRegs], pc[kRegs];
+    __shared__ int32_t s_row[kThreads / 32][kSlice], s_col[kThreads / 32][kSlice];
+    int32_t* pr_s = s_row[threadIdx.x >> 5];
+    int32_t* pc_s = s_col[threadIdx.x >> 5];
     int64_t rb = lo;  // a row at or before the group's first entry
 #pragma unroll
     for (int t = 0; t < kRegs; ++t) {
@@ -114,21 +117,20 @@ __global__ void __launch_bounds__(kThreads) sddmm_kernel(const SddmmArgs a) {
             if (live && row < 0 && e < last) row = w + c;
             if (__all_sync(0xffffffffu, !live || row >= 0) || w + 32 >= a.M) break;
         }
-        pr[t] = row >= 0 ? static_cast<int32_t>(row) : 0;
-        pc[t] = live && row >= 0 ? __ldg(a.col + e) : -1;
+        pr_s[lane + 32 * t] = row >= 0 ? static_cast<int32_t>(row) : 0;
+        pc_s[lane + 32 * t] = live && row >= 0 ? __ldg(a.col + e) : -1;
         // the next group starts at or after this group's last row
         const int64_t last_row = __shfl_sync(0xffffffffu, row, 31);
         rb = last_row >= 0 ? last_row : rb;
     }
     float* __restrict__ out = a.out;
-    // entry p kPer + u G + sub of the slice sits in lane (p kPer + u G) % 32 + sub
-    // (no wrap: the base is a multiple of G), register (p kPer + u G) / 32
+    __syncwarp();  // the slice's pairs are in shared memory for every lane
     auto fetch = [&](int p, int32_t (&jj)[kIlp], int32_t (&ri)[kIlp], bool (&ok)[kIlp]) {
 #pragma unroll
         for (int u = 0; u < kIlp; ++u) {
             const int base = p * kPer + u * G;
-            jj[u] = __shfl_sync(0xffffffffu, pc[base / 32], (base % 32) + sub);
-            ri[u] = __shfl_sync(0xffffffffu, pr[base / 32], (base % 32) + sub);
+            jj[u] = pc_s[base + sub];
+            ri[u] = pr_s[base + sub];
             const bool live = e0 + base + sub < e1;
             ok[u] = live && jj[u] >= 0 && jj[u] < a.N;
             if (live && !ok[u] && sl == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) sddmm_kernel(const SddmmArgs a) {
             if (sl == 0 && e < e1) out[e] = ok[u] ? acc[u] : 0.f;
         }
     };
-#pragma unroll
+#pragma unroll 1
     for (int p = 0; p < kPasses; ++p) {
         int32_t jj[kIlp], ri[kIlp];
         bool ok[kIlp];
