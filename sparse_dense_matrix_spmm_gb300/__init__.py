@@ -13,6 +13,11 @@ Format containers hold device tensors:
   TVW(M, K, tile_rows, dtype, n_tiles, Kp, tile_ptr, cols, vals, meta)
   CSR(M, K, nnz, dtype, row_ptr, col, val)
   WCSR(...)  (see include/spmm_gb300.h for the field meanings)
+
+Beyond C = A B for those formats: spmm_slide ((2n-2):2n as overlapping 2:4
+windows), spmm_bcsr_permuted (BCSR after a Reverse Cuthill-McKee order from
+rcm_order), spmm_sddmm (A B sampled at a CSR pattern) and the pruning
+builders spmm_prune_24 / spmm_prune_tvw.
 """
 from __future__ import annotations
 
