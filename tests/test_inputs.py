@@ -68,3 +68,14 @@ def test_banded_scrambled_problem_is_a_permuted_band():
     band = p["A"][np.ix_(inv, inv)]
     i = np.arange(64)
     assert np.all((band != 0) == (np.abs(i[:, None] - i[None, :]) <= 3))
+
+
+def test_sddmm_config_shares_the_row_window_pattern():
+    """The SDDMM workload samples the row-window workload's CSR pattern (same seed,
+    rows sorted and unique) with dense A and Bt of the stated inner size."""
+    c = dict(gen.CONFIGS["sddmm_lognormal"])
+    q = gen.config_problem("sddmm_lognormal", M=512, K=512, inner=16)
+    w = gen.config_problem("wcsr_lognormal", M=512, K=512, N=1)
+    assert np.array_equal(q["row_ptr"], w["row_ptr"]) and np.array_equal(q["col"], w["col"])
+    assert q["A"].shape == (512, 16) and q["Bt"].shape == (512, 16) and c["inner"] == 128
+    assert "B" not in q
