@@ -27,7 +27,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "spmm_oracle.c")
 _LIB = os.path.join(_HERE, "libspmm_oracle.so")
 
-DTYPES = {"bf16": 0, "f16": 1, "i8": 2}
+DTYPES = {"bf16": 0, "f16": 1, "i8": 2, "e4m3": 3, "e5m2": 4}
+FP8 = ("e4m3", "e5m2")
 ERR_SHAPE, ERR_FORMAT = 2, 4
 
 
@@ -58,6 +59,10 @@ def lib():
         L.orc_decode_bf16.argtypes = [C.c_uint16]
         L.orc_decode_f16.restype = C.c_double
         L.orc_decode_f16.argtypes = [C.c_uint16]
+        L.orc_decode_e4m3.restype = C.c_double
+        L.orc_decode_e4m3.argtypes = [C.c_uint8]
+        L.orc_decode_e5m2.restype = C.c_double
+        L.orc_decode_e5m2.argtypes = [C.c_uint8]
         L.orc_num_threads.restype = I32
         L.orc_bcsr_count.restype = I64
         L.orc_bcsr_count.argtypes = [P, I64, I64, I64, I32, I32, I32, P]
@@ -125,9 +130,10 @@ def num_threads() -> int:
 
 
 def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """Element-wise decode of stored bf16/fp16 bits (or int8) to float64."""
+    """Element-wise decode of stored bf16/fp16/fp8 bits (or int8) to float64."""
     L = lib()
-    f = L.orc_decode_bf16 if dtype == "bf16" else L.orc_decode_f16
+    f = {"bf16": L.orc_decode_bf16, "f16": L.orc_decode_f16, "e4m3": L.orc_decode_e4m3,
+         "e5m2": L.orc_decode_e5m2}.get(dtype)
     if dtype == "i8":
         return bits.astype(np.float64)
     flat = bits.reshape(-1)
@@ -138,7 +144,9 @@ def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def _edt(dtype):
-    return np.int8 if dtype == "i8" else np.uint16
+    if dtype == "i8":
+        return np.int8
+    return np.uint8 if dtype in FP8 else np.uint16
 
 
 # ------------------------------------------------------------------ BCSR
@@ -282,7 +290,7 @@ def densify24(F):
 
 
 def spmm24(F, B, rows=None, cols=None):
-    """int8 -> exact int64; bf16/fp16 -> fp64."""
+    """int8 -> exact int64; bf16/fp16/fp8 -> fp64 (B of the operand's type)."""
     H = _hold(F)
     B = _c(B, _edt(F["dtype"]))
     r0, r1, colarr, ncols = _sel(B.shape[1], rows, cols)

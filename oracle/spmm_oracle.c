@@ -24,8 +24,20 @@
  * definition: no blocking, no fusion, no reordering beyond "ascending k".
  *
  * Element encodings: dtype 0 = bf16 bits (uint16), 1 = fp16 bits (uint16),
- * 2 = int8.  A stored element is "zero" iff it compares equal to 0 in IEEE
- * arithmetic (so -0.0 is zero, NaN is nonzero); for int8 iff it is 0.
+ * 2 = int8, 3 = fp8 E4M3 bits (uint8), 4 = fp8 E5M2 bits (uint8).  A stored
+ * element is "zero" iff it compares equal to 0 in IEEE arithmetic (so -0.0 is
+ * zero, NaN is nonzero); for int8 iff it is 0.
+ *
+ * The 8-bit floating-point types are the ones the pages pair with 2:4 on
+ * recent GPUs ("Spense", abstract on the "sparse FP4 GEMM" search page: 2:4
+ * sparse tensor cores on B200 in FP8; "SlideSparse", same page: FP8 among its
+ * precisions).  The pages do not define the encodings; the reading taken is
+ * the two 8-bit formats of the OCP 8-bit floating-point specification, which
+ * is what the tensor core's e4m3 / e5m2 operand types implement:
+ *   E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent field 0 is
+ *         subnormal (m * 2^-9); S.1111.111 is NaN; no infinities (max 448).
+ *   E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent field 0 is
+ *         subnormal (m * 2^-16); exponent field 31 is infinity (m = 0) or NaN.
  */
 #include <math.h>
 #include <stdint.h>
@@ -35,7 +47,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_I8 = 2 };
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_I8 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
 enum { ORC_OK = 0, ORC_ERR_SHAPE = 2, ORC_ERR_FORMAT = 4 };
 
 /* ------------------------------------------------------------------ values */
@@ -59,11 +71,43 @@ double orc_decode_f16(uint16_t h) {
     return sign ? -v : v;
 }
 
-static int esize(int dtype) { return dtype == ORC_I8 ? 1 : 2; }
+/* OCP E4M3: (-1)^s * 2^(e-7) * (1 + m/8) for e = 1..15 (except e = 15, m = 7:
+ * NaN), (-1)^s * m * 2^-9 for e = 0. */
+double orc_decode_e4m3(uint8_t b) {
+    int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(m + 8), e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* OCP E5M2: (-1)^s * 2^(e-15) * (1 + m/4) for e = 1..30, m * 2^-16 for e = 0,
+ * infinity (m = 0) or NaN for e = 31. */
+double orc_decode_e5m2(uint8_t b) {
+    int sign = b >> 7, e = (b >> 2) & 31, m = b & 3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -16);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 4), e - 17);        /* (1 + m/4) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+static int is_byte_type(int dtype) { return dtype == ORC_I8 || dtype == ORC_E4M3 || dtype == ORC_E5M2; }
+
+static int esize(int dtype) { return is_byte_type(dtype) ? 1 : 2; }
 
 static double get_f(const void *p, int64_t idx, int dtype) {
     if (dtype == ORC_BF16) return orc_decode_bf16(((const uint16_t *)p)[idx]);
     if (dtype == ORC_F16) return orc_decode_f16(((const uint16_t *)p)[idx]);
+    if (dtype == ORC_E4M3) return orc_decode_e4m3(((const uint8_t *)p)[idx]);
+    if (dtype == ORC_E5M2) return orc_decode_e5m2(((const uint8_t *)p)[idx]);
     return (double)((const int8_t *)p)[idx];
 }
 
@@ -71,16 +115,17 @@ static int64_t get_i(const void *p, int64_t idx) { return (int64_t)((const int8_
 
 static int is_zero(const void *p, int64_t idx, int dtype) {
     if (dtype == ORC_I8) return ((const int8_t *)p)[idx] == 0;
+    if (dtype == ORC_E4M3 || dtype == ORC_E5M2) return (((const uint8_t *)p)[idx] & 0x7F) == 0;
     return (((const uint16_t *)p)[idx] & 0x7FFF) == 0;   /* +0.0 or -0.0 */
 }
 
 static void copy_elem(void *dst, int64_t di, const void *src, int64_t si, int dtype) {
-    if (dtype == ORC_I8) ((int8_t *)dst)[di] = ((const int8_t *)src)[si];
+    if (is_byte_type(dtype)) ((uint8_t *)dst)[di] = ((const uint8_t *)src)[si];
     else ((uint16_t *)dst)[di] = ((const uint16_t *)src)[si];
 }
 
 static void zero_elem(void *dst, int64_t di, int dtype) {
-    if (dtype == ORC_I8) ((int8_t *)dst)[di] = 0;
+    if (is_byte_type(dtype)) ((uint8_t *)dst)[di] = 0;
     else ((uint16_t *)dst)[di] = 0;
 }
 
@@ -391,13 +436,14 @@ int orc_compress24(const void *A, int64_t M, int64_t K, int64_t ld, int dtype, v
 }
 
 /* Magnitude of element idx as an unsigned key that orders by |a|: |v| for int8
- * (0..128); for bf16/fp16 the bit pattern without its sign bit, which orders
+ * (0..128); for bf16/fp16/fp8 the bit pattern without its sign bit, which orders
  * finite values and infinities by magnitude and puts NaN above every number. */
 static unsigned mag_key(const void *p, int64_t idx, int dtype) {
     if (dtype == ORC_I8) {
         int v = ((const int8_t *)p)[idx];
         return (unsigned)(v < 0 ? -v : v);
     }
+    if (dtype == ORC_E4M3 || dtype == ORC_E5M2) return ((const uint8_t *)p)[idx] & 0x7Fu;
     return ((const uint16_t *)p)[idx] & 0x7FFFu;
 }
 
@@ -551,7 +597,11 @@ void orc_densify24(int64_t M, int64_t K, int dtype, const void *vals, const uint
         }
 }
 
-/* Float 2:4 SpMM (fp64 accumulate). */
+/* Float 2:4 SpMM (fp64 accumulate): bf16/fp16, and fp8 E4M3/E5M2 with B of
+ * the same type.  For E4M3 the result is exact: every value is a multiple of
+ * 2^-9 below 2^9, so every product is a multiple of 2^-18 below 2^18 and, for
+ * K below 2^17, every partial sum is a multiple of 2^-18 below 2^35, which
+ * fp64 holds exactly. */
 void orc_spmm24_f64(int64_t M, int64_t K, int dtype, const void *vals, const uint8_t *meta,
                     const void *B, int64_t ldb, int64_t r0, int64_t r1, const int64_t *cols,
                     int64_t ncols, double *C) {

@@ -8,7 +8,8 @@ produced here.
 
 Every generator uses numpy's PCG64 (``numpy.random.default_rng(seed)``).
 Floating-point values are drawn in fp32 from N(0, std) and rounded to
-bf16 / fp16 with round-to-nearest-even; both sides read the rounded bits.
+bf16 / fp16 / fp8 (E4M3, E5M2) with round-to-nearest-even; both sides read
+the rounded bits.  The fp8 rounding is torch's fp32 -> float8 conversion.
 
 Workload recipes (sizes follow the five configurations the library is
 measured on):
@@ -31,10 +32,12 @@ from __future__ import annotations
 
 import numpy as np
 
-BF16, F16, I8 = "bf16", "f16", "i8"
+BF16, F16, I8, E4M3, E5M2 = "bf16", "f16", "i8", "e4m3", "e5m2"
+FP8 = (E4M3, E5M2)
 
 __all__ = [
-    "BF16", "F16", "I8", "round_f32_to_bf16_bits", "normal_bits", "mask24_float_problem",
+    "BF16", "F16", "I8", "E4M3", "E5M2", "FP8", "round_f32_to_bf16_bits", "round_f32_to_fp8_bits",
+    "normal_bits", "mask24_float_problem",
     "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem", "slide_problem", "banded_scrambled_problem",
     "CONFIGS", "config_problem",
 ]
@@ -51,8 +54,18 @@ def round_f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return r
 
 
+def round_f32_to_fp8_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """fp32 -> fp8 (E4M3 or E5M2) bit patterns, round-to-nearest-even (torch's
+    conversion; magnitudes beyond the largest finite value are not expected)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    fd = torch.float8_e4m3fn if dtype == E4M3 else torch.float8_e5m2
+    return t.to(fd).view(torch.uint8).numpy().copy()
+
+
 def normal_bits(rng: np.random.Generator, shape, dtype: str, std: float = 1.0) -> np.ndarray:
-    """N(0, std) drawn in fp32, returned as uint16 bit patterns of ``dtype``."""
+    """N(0, std) drawn in fp32, returned as uint16 (bf16/fp16) or uint8 (fp8) bit
+    patterns of ``dtype``."""
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
@@ -60,6 +73,8 @@ def normal_bits(rng: np.random.Generator, shape, dtype: str, std: float = 1.0) -
         return round_f32_to_bf16_bits(x)
     if dtype == F16:
         return x.astype(np.float16).view(np.uint16)
+    if dtype in FP8:
+        return round_f32_to_fp8_bits(x, dtype)
     raise ValueError(dtype)
 
 
@@ -102,9 +117,9 @@ def mask24_problem(M: int, K: int, N: int, seed: int) -> dict:
 
 
 def mask24_float_problem(M: int, K: int, N: int, seed: int, dtype: str = F16) -> dict:
-    """16-bit A keeping 2 of every 4 consecutive K-entries (positions uniform over the
-    6 pairs, values N(0,1); a kept value may round to zero), B (K x N) N(0,1); all as
-    raw bits."""
+    """bf16 / fp16 / fp8 A keeping 2 of every 4 consecutive K-entries (positions uniform
+    over the 6 pairs, values N(0,1); a kept value may round to zero), B (K x N) N(0,1) of
+    the same type; all as raw bits."""
     assert K % 4 == 0
     rng = np.random.default_rng(seed)
     pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)], dtype=np.int64)
@@ -241,6 +256,8 @@ CONFIGS = {
                       dtype=BF16, std=1.0),
     "mask24_int8": dict(kind="24", M=8192, K=8192, N=4096, seed=2),
     "mask24_f16": dict(kind="24f", M=8192, K=8192, N=4096, seed=6, dtype=F16),
+    # fp8 (E4M3) 2:4 at the same shape: A and B N(0,1) rounded to E4M3
+    "mask24_e4m3": dict(kind="24f", M=8192, K=8192, N=4096, seed=11, dtype=E4M3),
     "prune24_f16": dict(kind="prune24", M=8192, K=8192, N=0, seed=7, dtype=F16),
     "prune_tvw_f16": dict(kind="prunetvw", M=4096, K=4096, N=0, tile_rows=128, keep=2048, seed=8, dtype=F16),
     "wcsr_lognormal": dict(kind="wcsr", M=65536, K=65536, N=128, seed=3, mean=16.0,

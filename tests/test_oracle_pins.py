@@ -1,6 +1,8 @@
 """Pins for the CPU oracle: each check ties it to something other than itself.
 
-* fp16 / bf16 decoding: exhaustive over all 65536 bit patterns, against numpy.
+* fp16 / bf16 decoding: exhaustive over all 65536 bit patterns, against numpy;
+  fp8 (E4M3, E5M2) decoding: exhaustive over all 256 patterns, against torch's
+  float8 types, plus the extreme codes of the format definition.
 * hand-worked fixtures under tests/golden/ (each cites the passage it reads).
 * brute-force dense GEMM (numpy) on the densified operand.
 * format round trips, invariants, and reductions to textbook routines
@@ -33,6 +35,29 @@ def test_decode_bf16_exhaustive():
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2"])
+def test_decode_fp8_exhaustive(dtype):
+    torch = pytest.importorskip("torch")
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = oracle.decode(bits, dtype)
+    fd = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+    ref = torch.from_numpy(bits.copy()).view(fd).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_decode_fp8_extreme_codes():
+    # the format definitions' landmarks: largest finite, smallest subnormal, NaN, infinity
+    e4 = oracle.decode(np.array([0x7E, 0x01, 0x08, 0x7F, 0xFF, 0x80, 0x38], np.uint8), "e4m3")
+    assert e4[0] == 448.0 and e4[1] == 2.0 ** -9 and e4[2] == 2.0 ** -6 and e4[6] == 1.0
+    assert np.isnan(e4[3]) and np.isnan(e4[4]) and e4[5] == 0.0 and np.signbit(e4[5])
+    e5 = oracle.decode(np.array([0x7B, 0x01, 0x04, 0x7C, 0xFC, 0x7D, 0x3C], np.uint8), "e5m2")
+    assert e5[0] == 57344.0 and e5[1] == 2.0 ** -16 and e5[2] == 2.0 ** -14 and e5[6] == 1.0
+    assert e5[3] == np.inf and e5[4] == -np.inf and np.isnan(e5[5])
 
 
 def test_bf16_rounding_is_rne():
@@ -189,6 +214,47 @@ def test_24_golden():
     assert oracle.spmm24(F, B).tolist() == g["C"]
 
 
+def test_24_fp8_golden():
+    g = golden("mask24_e4m3_2x8.json")
+    A, B = np.array(g["A"], np.uint8), np.array(g["B"], np.uint8)
+    F = oracle.compress24(A, "e4m3")
+    assert F["vals"].tolist() == g["vals"] and F["meta"].tolist() == g["meta"]
+    assert oracle.spmm24(F, B).tolist() == g["C"]
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2"])
+def test_24_fp8_vs_dense_gemm_and_round_trip(dtype):
+    """E4M3: every product and partial sum is exact in fp64, so the oracle equals a dense
+    numpy GEMM on the densified operand (decoded by torch) bit for bit; E5M2 to 1e-12."""
+    pytest.importorskip("torch")
+    p = gen.mask24_float_problem(40, 256, 24, seed=12, dtype=dtype)
+    F = oracle.compress24(p["A"], dtype)
+    # the round trip holds up to the sign of zero (a value that rounded to -0 is not stored)
+    A0 = np.where((p["A"] & 0x7F) == 0, 0, p["A"]).astype(np.uint8)
+    assert F["vals"].dtype == np.uint8 and np.array_equal(oracle.densify24(F), A0)
+    nib = np.stack([F["meta"] & 15, F["meta"] >> 4], axis=-1).reshape(40, 64)
+    assert np.all((nib & 3) < (nib >> 2))
+    ref = bits_to_f64(p["A"], dtype) @ bits_to_f64(p["B"], dtype)
+    got = oracle.spmm24(F, p["B"])
+    if dtype == "e4m3":
+        assert np.array_equal(got, ref)
+    else:
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # rows and columns selected on the way out are the same numbers
+    sel = oracle.spmm24(F, p["B"], rows=(3, 9), cols=[5, 0, 23])
+    assert np.array_equal(sel, got[3:9][:, [5, 0, 23]])
+
+
+def test_24_fp8_negative_zero_is_zero_and_errors():
+    A = np.zeros((1, 8), np.uint8)
+    A[0, :4] = [0x80, 0x38, 0x80, 0x40]     # -0, 1, -0, 2: two nonzeros, -0 counts as zero
+    F = oracle.compress24(A, "e4m3")
+    assert F["vals"].tolist() == [[0x38, 0x40, 0, 0]] and F["meta"].tolist() == [[0x4D]]
+    A[0, 4:7] = [0x38, 0x7F, 0x01]           # 1, NaN, 2^-9: three nonzeros (NaN is nonzero)
+    with pytest.raises(oracle.OracleError):
+        oracle.compress24(A, "e4m3")
+
+
 def test_24_int8_exact_vs_int64_gemm_and_invariants():
     p = gen.mask24_problem(48, 128, 33, seed=9)
     nz = (p["A"].reshape(48, 32, 4) != 0).sum(axis=2)
@@ -297,7 +363,7 @@ def test_wcsr_windows_with_repeated_columns():
 def _prune_keys(A, dtype):
     if dtype == "i8":
         return np.abs(A.astype(np.int64))
-    return (A.astype(np.int64) & 0x7FFF)
+    return (A.astype(np.int64) & (0x7F if dtype in ("e4m3", "e5m2") else 0x7FFF))
 
 
 def test_prune24_hand_worked_groups():
@@ -313,7 +379,7 @@ def test_prune24_hand_worked_groups():
     assert Fh["meta"].tolist() == [[0x44]]
 
 
-@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16"])
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16", "e4m3"])
 def test_prune24_keeps_the_largest_magnitudes(dtype):
     """Properties any correct magnitude pruning has: exactly two positions per group,
     kept values copied bit for bit, every dropped magnitude at most the smaller kept
@@ -326,7 +392,7 @@ def test_prune24_keeps_the_largest_magnitudes(dtype):
     else:
         A = gen.normal_bits(rng, (M, K), dtype)
         A[rng.random((M, K)) < 0.3] = 0
-        A[rng.random((M, K)) < 0.1] ^= 0x8000                       # sign flips keep magnitudes
+        A[rng.random((M, K)) < 0.1] ^= A.dtype.type(0x80 if A.dtype == np.uint8 else 0x8000)  # sign flips
     F = oracle.prune24(A, dtype)
     D = oracle.densify24(F)
     keys = _prune_keys(A, dtype).reshape(M, K // 4, 4)
@@ -340,7 +406,7 @@ def test_prune24_keeps_the_largest_magnitudes(dtype):
         kept[g, i1[r]] = True
         dense_row = A[r].reshape(K // 4, 4)
         assert np.array_equal(D[r].reshape(K // 4, 4)[kept], dense_row[kept])
-        assert not (D[r].reshape(K // 4, 4)[~kept].astype(np.int64) & (0xFF if dtype == "i8" else 0xFFFF)).any()
+        assert not (D[r].reshape(K // 4, 4)[~kept].astype(np.int64) & (0xFFFF if A.dtype == np.uint16 else 0xFF)).any()
         kr = keys[r]
         kmin = np.minimum(kr[g, i0[r]], kr[g, i1[r]])
         lo_of_min = np.where(kr[g, i0[r]] <= kr[g, i1[r]], np.where(kr[g, i0[r]] == kr[g, i1[r]], i1[r], i0[r]), i1[r])
@@ -353,14 +419,14 @@ def test_prune24_keeps_the_largest_magnitudes(dtype):
         assert np.all(kr[g, i0[r]] + kr[g, i1[r]] == pair_sums.max(axis=1))
 
 
-@pytest.mark.parametrize("dtype", ["i8", "f16"])
+@pytest.mark.parametrize("dtype", ["i8", "f16", "e4m3"])
 def test_prune24_of_a_24_matrix_is_its_compression(dtype):
     """A matrix that already has at most two nonzeros per group loses nothing: pruning
     equals plain 2:4 compression (padding with the lowest zero positions)."""
     if dtype == "i8":
         A = gen.mask24_problem(32, 256, 1, seed=4)["A"]
     else:
-        A = gen.mask24_float_problem(32, 256, 1, seed=4)["A"]
+        A = gen.mask24_float_problem(32, 256, 1, seed=4, dtype=dtype)["A"]
     P, Cq = oracle.prune24(A, dtype), oracle.compress24(A, dtype)
     assert np.array_equal(P["vals"], Cq["vals"]) and np.array_equal(P["meta"], Cq["meta"])
 
