@@ -37,6 +37,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SpMM effective TFLOP/s (2·nnz·N/time) and % of roofline, per sparse format"
 HEADLINE = "mask24_int8"
+EXTRA_WORKLOADS = ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "mask24_e4m3", "slide68_f16", "bcsr_rcm",
+                   "sddmm_lognormal", "prune24_f16", "prune_tvw_f16", "bcsr_tiny")
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -198,9 +200,16 @@ def timed_steps(step, steps, warmup, flush_buf, ws):
     return sum(a.elapsed_time(b) for a, b in evs)
 
 
-def roofline(flops, alg_bytes, t_s, peaks, prefer=None, traffic=None, peak_kind="burst"):
-    """Roofline object for one kernel: bound = the larger of the two time floors."""
+# Dense fp8 tensor rate relative to bf16 (nominal 4.5 vs 2.25 PFLOP/s): no fp8 GEMM
+# is measured on this machine, so the fp8 peak is the measured bf16 figure times this.
+FP8_OVER_BF16 = 2.0
+
+
+def roofline(flops, alg_bytes, t_s, peaks, prefer=None, traffic=None, peak_kind="burst", peak_scale=1.0):
+    """Roofline object for one kernel: bound = the larger of the two time floors.
+    peak_scale multiplies the measured bf16 tensor peak (FP8_OVER_BF16 for fp8)."""
     P = peaks["bf16_tflops"] if peak_kind == "burst" else peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    P = P * peak_scale
     BW = peaks["hbm_gbs"]
     t_tensor = flops / (P * 1e12)
     t_hbm = alg_bytes / (BW * 1e9)
@@ -332,6 +341,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
     g = torch.Generator(device="cuda")
     g.manual_seed(int(c["seed"]))
     extra_fields = {}
+    peak_scale = 1.0
     if c["kind"] == "bcsr":
         p = gen.bcsr_problem(c["M"], c["K"], 8, c["bh"], c["bw"], c["nnzb"], c["seed"], c["dtype"], c["std"])
         dt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float16
@@ -372,15 +382,21 @@ def run_extra(name, args, ws, peaks, flush_buf):
             spmm.spmm_tvw(F, Bx, Cd)
     elif c["kind"] == "24f":
         # the same recipe as the host generator, drawn on the device (the bench checks no values):
-        # per 4-group one of the 6 position pairs, N(0,1) fp16 values; B N(0,1) fp16
+        # per 4-group one of the 6 position pairs, N(0,1) values; B N(0,1); fp16 or fp8 E4M3
         M, K = c["M"], c["K"]
+        fp8 = c.get("dtype") == "e4m3"
+        tdt = torch.float8_e4m3fn if fp8 else torch.float16
         pat = torch.tensor([0b0011, 0b0101, 0b1001, 0b0110, 0b1010, 0b1100], device="cuda")
         sel = pat[torch.randint(0, 6, (M, K // 4), generator=g, device="cuda")]
         bit = torch.arange(4, device="cuda")
         keep = ((sel[:, :, None] >> bit) & 1).bool().reshape(M, K)
-        A = torch.randn((M, K), generator=g, device="cuda").to(torch.float16) * keep
+        A = (torch.randn((M, K), generator=g, device="cuda") * keep).to(tdt)
         del sel, keep
-        Bx = torch.randn((K, c["N"]), generator=g, device="cuda").to(torch.float16)
+        Bx = torch.randn((K, c["N"]), generator=g, device="cuda").to(tdt)
+        if fp8:
+            peak_scale = FP8_OVER_BF16
+            extra_fields["peak_note"] = (f"fp8 peak derived: {FP8_OVER_BF16:g} x the measured bf16 burst "
+                                         "(nominal dense fp8 : bf16 = 4.5 : 2.25 PFLOP/s)")
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         F = spmm.spmm_compress_24(A)
@@ -390,7 +406,8 @@ def run_extra(name, args, ws, peaks, flush_buf):
         Cd = torch.empty((M, c["N"]), dtype=torch.float32, device="cuda")
         wsp = torch.empty(max(1, spmm.spmm_24_workspace_size(F, c["N"])), dtype=torch.uint8, device="cuda")
         nnz = M * K // 2
-        alg = nnz * 2 + M * K // 8 + K * c["N"] * 2 + M * c["N"] * 4
+        es = 1 if fp8 else 2
+        alg = nnz * es + M * K // 8 + K * c["N"] * es + M * c["N"] * 4
         kern, kid = "sparse_spmm_kernel", spmm._lib.KERNEL_SPARSE
 
         def step():
@@ -564,7 +581,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
     # a builder without a traced kernel id (it synchronises inside): time the whole call
     t_kernel = ms / max(n, 1) / 1e3 if kid is not None else total_ms / steps / 1e3
     rl = roofline(flops, alg, t_kernel, peaks, prefer="hbm" if builder else None,
-                  traffic=measured_traffic(kern, name))
+                  traffic=measured_traffic(kern, name), peak_scale=peak_scale)
     rl["kernel"] = kern
     rl["kernel_ms"] = round(t_kernel * 1e3, 4)
     t_step = total_ms / steps / 1e3
@@ -600,6 +617,112 @@ def cpu_baseline(p, target_s=12.0):
             "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of the {p['M']}x{K} int8 2:4 operand times the full {K}x{N} B "
                       f"(int64 accumulation), {dt:.1f} s"}
+
+
+def _time_rows(run, total_rows, step, target_s):
+    """Oracle time on rows [0, r): r grows from `step` until the run takes about
+    target_s seconds (or covers every row); returns (r, seconds)."""
+    r = min(step, total_rows)
+    while True:
+        t0 = time.perf_counter()
+        run(r)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or r >= total_rows:
+            return r, dt
+        grow = target_s / max(dt, 1e-3)
+        r = min(total_rows, max(r + step, int(r * min(grow, 8.0)) // step * step))
+
+
+def cpu_baseline_extra(name, target_s=2.0):
+    """The oracle (as it stands, all host cores) on a bounded row sample of one of the
+    other workloads, in the workload's own unit; the sample is stated."""
+    import oracle
+    import spmm_inputs as gen
+    c = dict(gen.CONFIGS[name])
+    kind = c["kind"]
+    cores = oracle.num_threads()
+    out = {"unit": "TFLOP/s", "cores": cores, "kind": "oracle"}
+    if kind == "bcsr":
+        Ns = min(c["N"], 512)
+        p = gen.bcsr_problem(c["M"], c["K"], Ns, c["bh"], c["bw"], c["nnzb"], c["seed"], c["dtype"], c["std"])
+        F = oracle.bcsr_build(p["A"], c["bh"], c["bw"], c["dtype"])
+        r, dt = _time_rows(lambda r: oracle.bcsr_spmm(F, p["B"], rows=(0, r)), c["M"], c["bh"], target_s)
+        nnz_r = int(F["row_ptr"][r // c["bh"]]) * c["bh"] * c["bw"]
+        flops = 2.0 * nnz_r * Ns
+        sample = f"rows 0..{r - 1} of {c['M']}, {Ns} of {c['N']} columns"
+        if Ns < c["N"]:
+            sample += (f"; extrapolated from the {Ns}-column slice to N = {c['N']} "
+                       "(the oracle's time per column is constant, so the rate stands)")
+    elif kind == "tvw":
+        p = gen.config_problem(name)
+        F = oracle.tvw_build(p["A"], c["tile_rows"], p["tile_ptr"], p["cols"], c["dtype"], Kp=c["keep"])
+        r, dt = _time_rows(lambda r: oracle.tvw_spmm(F, p["B"], rows=(0, r)), c["M"], 8, target_s)
+        flops = 2.0 * r * (c["keep"] // 2) * c["N"]
+        sample = f"rows 0..{r - 1} of {c['M']}, all {c['N']} columns"
+    elif kind == "wcsr":
+        p = gen.config_problem(name)
+        F = oracle.wcsr_build(c["M"], c["K"], p["row_ptr"], p["col"], p["val"], c["dtype"], 16, 32)
+        r, dt = _time_rows(lambda r: oracle.wcsr_spmm(F, p["B"], rows=(0, r)), c["M"], 256, target_s)
+        flops = 2.0 * int(p["row_ptr"][r]) * c["N"]
+        sample = f"rows 0..{r - 1} of {c['M']} (row-window form), all {c['N']} columns"
+    elif kind == "24f":
+        p = gen.config_problem(name)
+        F = oracle.compress24(p["A"], c["dtype"])
+        r, dt = _time_rows(lambda r: oracle.spmm24(F, p["B"], rows=(0, r)), c["M"], 4, target_s)
+        flops = 2.0 * r * (c["K"] // 2) * c["N"]
+        sample = f"rows 0..{r - 1} of {c['M']}, all {c['N']} columns ({c['dtype']}, fp64 sums)"
+    elif kind == "slide":
+        p = gen.config_problem(name)
+        F = oracle.slide_build(p["A"], c["n"], c["dtype"])
+        Kl = oracle.slide_lifted_k(c["K"], c["n"])
+        G = {"M": F["M"], "K": Kl, "dtype": F["dtype"], "vals": F["vals"], "meta": F["meta"]}
+        BL = oracle.slide_lift_b(p["B"], c["K"], c["n"])
+        r, dt = _time_rows(lambda r: oracle.spmm24(G, BL, rows=(0, r)), c["M"], 4, target_s)
+        flops = 2.0 * r * (Kl // 2) * c["N"]
+        sample = f"rows 0..{r - 1} of {c['M']} of the lifted 2:4 operand, all {c['N']} columns"
+    elif kind == "rcm":
+        p = gen.config_problem(name)
+        perm = oracle.rcm_dense(p["A"])
+        F = oracle.bcsr_build(oracle.permute_sym(p["A"], perm, c["dtype"]), c["bh"], c["bw"], c["dtype"])
+        Bp = np.ascontiguousarray(p["B"][perm])
+        r, dt = _time_rows(lambda r: oracle.bcsr_spmm(F, Bp, rows=(0, r)), c["M"], c["bh"], target_s)
+        flops = 2.0 * int(F["row_ptr"][r // c["bh"]]) * c["bh"] * c["bw"] * c["N"]
+        sample = (f"rows 0..{r - 1} of {c['M']} of the BCSR of P A P^T (RCM order) times P B, all {c['N']} "
+                  "columns (the permutations themselves untimed)")
+    elif kind == "sddmm":
+        p = gen.config_problem(name)
+        rp, col = p["row_ptr"], p["col"]
+
+        def run(r):
+            oracle.sddmm(rp[:r + 1], col[:int(rp[r])], p["A"][:r], p["Bt"], c["dtype"])
+        r, dt = _time_rows(run, c["M"], 256, target_s)
+        flops = 2.0 * int(rp[r]) * c["inner"]
+        sample = f"pattern rows 0..{r - 1} of {c['M']}, inner dimension {c['inner']}"
+    elif kind in ("prune24", "prunetvw"):
+        rng = np.random.default_rng(c["seed"])
+        A = gen.normal_bits(rng, (c["M"], c["K"]), c["dtype"])
+        out["unit"] = "GB/s"
+        if kind == "prune24":
+            r, dt = _time_rows(lambda r: oracle.prune24(A[:r], c["dtype"]), c["M"], 8, target_s)
+            by = r * c["K"] * 2 + r * c["K"] // 2 * 2 + r * c["K"] // 8
+        else:
+            tr, keep = c["tile_rows"], c["keep"]
+            n_t = -(-c["M"] // tr)
+            cl = np.concatenate([np.sort(rng.choice(c["K"], keep, replace=False)) for _ in range(n_t)]).astype(np.int32)
+            tp = np.arange(0, n_t * keep + 1, keep, dtype=np.int32)
+
+            def run(r):
+                t = r // tr
+                oracle.prune_tvw(A[:r], tr, tp[:t + 1], cl[:t * keep], c["dtype"], Kp=keep)
+            r, dt = _time_rows(run, c["M"], tr, target_s)
+            by = r * keep * 2 + (r // tr) * keep * 4 + r * keep // 2 * 2 + r * keep // 8
+        out.update({"value": round(by / dt / 1e9, 4),
+                    "sample": f"rows 0..{r - 1} of the {c['M']}x{c['K']} dense matrix, {dt:.1f} s"})
+        return out
+    else:
+        return None
+    out.update({"value": round(flops / dt / 1e12, 6), "sample": f"{sample}, {dt:.1f} s"})
+    return out
 
 
 def run_reference(args, ws, rank):
@@ -649,7 +772,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other formats")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="run one workload (bcsr_llm, tvw, wcsr_lognormal, mask24_f16, prune24_f16, prune_tvw_f16, bcsr_tiny) "
+                    help="run one workload (" + ", ".join(EXTRA_WORKLOADS) + ") "
                          "and print its result; "
                          "for profiling runs, not the benchmark line")
     ap.add_argument("--n", type=int, default=0, help="with --only: override the workload's N")
@@ -682,8 +805,7 @@ def main():
     h = run_headline(args, ws, rank, local, peaks, flush_buf)
     extra = []
     if not args.no_extra:
-        for name in ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "slide68_f16", "bcsr_rcm", "sddmm_lognormal",
-                     "prune24_f16", "prune_tvw_f16", "bcsr_tiny"):
+        for name in EXTRA_WORKLOADS:
             try:
                 extra.append(run_extra(name, args, ws, peaks, flush_buf))
             except Exception as e:  # a format whose kernel is missing is reported, not hidden
@@ -694,6 +816,15 @@ def main():
     if rank != 0:
         return 0
     cpu = None if args.no_cpu_baseline else cpu_baseline(h["problem"])
+    if not args.no_cpu_baseline:
+        # every other workload's oracle baseline, after all GPU timing (host work only)
+        for e in extra:
+            if "error" in e:
+                continue
+            try:
+                e["cpu_baseline"] = cpu_baseline_extra(e["workload"])
+            except Exception as ex:  # reported, not hidden
+                e["cpu_baseline"] = {"error": f"{type(ex).__name__}: {ex}"}
     rl = h["roofline"]
     rl["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json bf16 burst; fp16 tensor rate = bf16 rate)" \
         if rl["bound"] == "tensor" else peak_src

@@ -23,8 +23,8 @@
  *     written (rows without stored entries get 0).  When M or N is 0 there is
  *     nothing to write: B and C may then be null and the call returns SPMM_OK
  *     without launching.
- *   - Floating-point inputs are bf16 or fp16 with fp32 accumulation and fp32 C;
- *     int8 2:4 accumulates exactly and writes int32 C.
+ *   - Floating-point inputs are bf16 or fp16 (2:4 also fp8) with fp32
+ *     accumulation and fp32 C; int8 2:4 accumulates exactly and writes int32 C.
  *   - Every call validates its scalar arguments on the host first and returns a
  *     status without launching anything when they are invalid.  SpMM calls are
  *     asynchronous on `stream`; builders that must report sizes or
@@ -67,7 +67,12 @@ typedef enum {
     SPMM_ERR_UNSUPPORTED = 8  /* valid request outside what the kernels implement    */
 } spmm_status;
 
-typedef enum { SPMM_BF16 = 0, SPMM_F16 = 1, SPMM_I8 = 2 } spmm_dtype;
+/* SPMM_E4M3 / SPMM_E5M2: 8-bit floats in the two encodings of the OCP 8-bit
+ * floating-point specification (E4M3: exponent bias 7, no infinities, max 448;
+ * E5M2: exponent bias 15, IEEE-style infinities and NaN), the FP8 that the
+ * pages pair with 2:4 sparse tensor cores ("Spense", abstract, on the "sparse
+ * FP4 GEMM" search page: B200 with FP8 precision). */
+typedef enum { SPMM_BF16 = 0, SPMM_F16 = 1, SPMM_I8 = 2, SPMM_E4M3 = 3, SPMM_E5M2 = 4 } spmm_dtype;
 
 /* Bits of the sticky device error word. */
 #define SPMM_DEVERR_TIMEOUT 1 /* a bounded pipeline wait gave up                        */
@@ -138,7 +143,7 @@ typedef struct {
  * plus the lowest-index zero positions. */
 typedef struct {
     int64_t M, K;
-    int32_t dtype; /* SPMM_I8 (-> int32 C), SPMM_F16 or SPMM_BF16 (-> fp32 C) */
+    int32_t dtype; /* SPMM_I8 (-> int32 C); SPMM_F16, SPMM_BF16, SPMM_E4M3 or SPMM_E5M2 (-> fp32 C) */
     void *vals;
     uint8_t *meta;
 } spmm_24_t;
@@ -233,7 +238,10 @@ SPMM_API spmm_status spmm_24_workspace_size(const spmm_24_t *A, int64_t N, size_
  * executed inside the sparse tensor core).  int8: C is int32 and exact (the
  * kernel accumulates 2048-wide K chunks in fp32, every partial an integer of
  * magnitude below 2^24, and sums the chunks in int32).  fp16/bf16: C is fp32.
- * Needs K % 128 == 0. */
+ * fp8 (E4M3 / E5M2, "Spense", abstract: 2:4 sparse tensor cores in FP8): B is
+ * K x N of the same 8-bit type (row pitch ldb bytes, a multiple of 16), C is
+ * fp32; products are exact and summed in fp32 by the tensor core.  Needs
+ * K % 128 == 0 (K % 256 == 0 for fp8), else SPMM_ERR_SHAPE. */
 SPMM_API spmm_status spmm_24(const spmm_24_t *A, const void *B, int64_t ldb, void *C, int64_t ldc, int64_t N,
                              void *workspace, size_t workspace_bytes, spmm_stream_t stream);
 
@@ -249,8 +257,10 @@ SPMM_API spmm_status spmm_24(const spmm_24_t *A, const void *B, int64_t ldb, voi
  * the process exits.  A call whose scratch would exceed 32 MiB returns
  * SPMM_ERR_WORKSPACE without launching; fp16/bf16 operands need no scratch.
  * The call allocates nothing.  Its first call on a device looks up the array's
- * device address for that device; make that first call before any stream
- * capture.  All calls share the one array, and each call rewrites every byte
+ * device address for that device and keeps it for the life of the process;
+ * make that first call before any stream capture, and do not keep using the
+ * library on a device after cudaDeviceReset (the kept address then belongs to
+ * the old context).  fp8 and 16-bit operands use no scratch at all.  All calls share the one array, and each call rewrites every byte
  * it later reads, so nothing has to be cleared between calls; calls that can
  * overlap on the GPU (different streams, or different host threads) race on
  * the array and must be serialised by the caller. */
@@ -304,7 +314,9 @@ SPMM_API spmm_status spmm_build_wcsr_fill(const spmm_csr_t *A, int32_t h, int32_
                                           size_t workspace_bytes, spmm_wcsr_t *out, spmm_stream_t stream);
 
 /* dense (M x K) -> 2:4 vals[M][K/2] + meta[M][K/8].  K % 8 == 0.  More than
- * two nonzeros in a group -> SPMM_ERR_FORMAT.  Synchronises `stream`. */
+ * two nonzeros in a group -> SPMM_ERR_FORMAT.  Any 2:4 dtype (fp8: an entry is
+ * zero iff its bits without the sign are 0; values copied bit for bit).
+ * Synchronises `stream`. */
 SPMM_API spmm_status spmm_compress_24(const void *dense, int64_t M, int64_t K, int64_t ld, int32_t dtype,
                                       void *vals, uint8_t *meta, spmm_stream_t stream);
 
@@ -314,7 +326,7 @@ SPMM_API spmm_status spmm_compress_24(const void *dense, int64_t M, int64_t K, i
  * in the layout of spmm_compress_24 (caller-allocated device arrays).  In every
  * group of 4 consecutive K entries the two of largest magnitude are kept, ties
  * going to the lower index; magnitude is |v| for int8 and the bit pattern
- * without its sign for bf16/fp16 (so NaN ranks above every number).  The result
+ * without its sign for bf16/fp16/fp8 (so NaN ranks above every number).  The result
  * equals spmm_compress_24 of the matrix with the other two entries zeroed.
  * K % 8 == 0 (else SPMM_ERR_SHAPE); never fails on data.  Asynchronous on
  * `stream`. */

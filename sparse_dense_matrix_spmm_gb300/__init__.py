@@ -38,7 +38,8 @@ __all__ = ["BCSR", "Mat24", "Slide", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bc
            "spmm_sddmm", "rcm_order", "spmm_permute_sym", "spmm_permute_rows", "spmm_bcsr_permuted", "spmm_bcsr_permuted_workspace_size",
            "last_device_error", "selftest_timeout", "library_path", "trace_enable", "trace_read"]
 
-_DT = {torch.bfloat16: _lib.SPMM_BF16, torch.float16: _lib.SPMM_F16, torch.int8: _lib.SPMM_I8}
+_DT = {torch.bfloat16: _lib.SPMM_BF16, torch.float16: _lib.SPMM_F16, torch.int8: _lib.SPMM_I8,
+       torch.float8_e4m3fn: _lib.SPMM_E4M3, torch.float8_e5m2: _lib.SPMM_E5M2}
 
 
 def library_path() -> str:

@@ -7,7 +7,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspmm_gb300.so")
 
-SPMM_BF16, SPMM_F16, SPMM_I8 = 0, 1, 2
+SPMM_BF16, SPMM_F16, SPMM_I8, SPMM_E4M3, SPMM_E5M2 = 0, 1, 2, 3, 4
 DEVERR_TIMEOUT, DEVERR_INDEX, DEVERR_FORMAT = 1, 2, 4
 KERNEL_BCSR, KERNEL_SPARSE, KERNEL_WIDEN, KERNEL_WCSR, KERNEL_PRUNE, KERNEL_PERMUTE, KERNEL_SDDMM = 1, 2, 3, 4, 5, 6, 7
 STATUS = {0: "SPMM_OK", 1: "SPMM_ERR_NULL", 2: "SPMM_ERR_SHAPE", 3: "SPMM_ERR_DTYPE", 4: "SPMM_ERR_FORMAT",

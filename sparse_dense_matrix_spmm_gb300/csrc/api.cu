@@ -15,7 +15,7 @@ __device__ int g_device_error;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxKernelSlots = 16;
+constexpr int kMaxKernelSlots = 32;
 DeviceInfo g_info[kMaxDevices];
 bool g_info_ok[kMaxDevices];
 bool g_attr_done[kMaxDevices][kMaxKernelSlots];
@@ -167,6 +167,31 @@ bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType type, const void* base
     std::memset(map, 0, sizeof(*map));
     return f(map, type, 4, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+spmm_status check_24(const spmm_24_t* A, int64_t N) {
+    if (!A) return SPMM_ERR_NULL;
+    if (!dtype_24(A->dtype)) return SPMM_ERR_DTYPE;
+    if (A->M < 0 || A->K <= 0 || N < 0) return SPMM_ERR_SHAPE;
+    if (A->K % (is_fp8(A->dtype) ? 256 : 128)) return SPMM_ERR_SHAPE;  // whole K steps of the kernel
+    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+        return SPMM_ERR_UNSUPPORTED;
+    return SPMM_OK;
+}
+
+}  // namespace
+
+// Every check spmm_24 makes before it launches, except the workspace's.
+spmm_status check_24_call(const spmm_24_t* A, const void* B, int64_t ldb, const void* C, int64_t ldc, int64_t N) {
+    spmm_status st = check_24(A, N);
+    if (st != SPMM_OK) return st;
+    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
+    if (A->M > 0 && (!A->vals || !A->meta)) return SPMM_ERR_NULL;
+    if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
+    // B is read by TMA (not for int8, which is widened first): 16-byte aligned rows
+    if (A->dtype != SPMM_I8 && ((ldb * dtype_bytes(A->dtype)) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
+    return SPMM_OK;
 }
 
 }  // namespace spmm
@@ -360,7 +385,7 @@ spmm_status spmm_build_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_
 spmm_status spmm_compress_24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
                              uint8_t* meta, spmm_stream_t stream) {
     if (M > 0 && K > 0 && (!dense || !vals || !meta)) return SPMM_ERR_NULL;
-    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (!dtype_24(dtype)) return SPMM_ERR_DTYPE;
     if (M < 0 || K < 0 || K % 8 || ld < K) return SPMM_ERR_SHAPE;
     return run_compress24(dense, M, K, ld, dtype, vals, meta, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -368,7 +393,7 @@ spmm_status spmm_compress_24(const void* dense, int64_t M, int64_t K, int64_t ld
 spmm_status spmm_prune_24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
                           uint8_t* meta, spmm_stream_t stream) {
     if (M > 0 && K > 0 && (!dense || !vals || !meta)) return SPMM_ERR_NULL;
-    if (dtype != SPMM_BF16 && dtype != SPMM_F16 && dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (!dtype_24(dtype)) return SPMM_ERR_DTYPE;
     if (M < 0 || K < 0 || K % 8 || ld < K) return SPMM_ERR_SHAPE;
     return run_prune24(dense, M, K, ld, dtype, vals, meta, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -499,16 +524,6 @@ spmm_status spmm_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C
     return launch_wcsr(A, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
-static spmm_status check_24(const spmm_24_t* A, int64_t N) {
-    if (!A) return SPMM_ERR_NULL;
-    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
-    if (A->M < 0 || A->K <= 0 || N < 0) return SPMM_ERR_SHAPE;
-    if (A->K % 128) return SPMM_ERR_SHAPE;
-    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
-        return SPMM_ERR_UNSUPPORTED;
-    return SPMM_OK;
-}
-
 spmm_status spmm_24_workspace_size(const spmm_24_t* A, int64_t N, size_t* bytes) {
     if (!bytes) return SPMM_ERR_NULL;
     spmm_status st = check_24(A, N);
@@ -519,12 +534,8 @@ spmm_status spmm_24_workspace_size(const spmm_24_t* A, int64_t N, size_t* bytes)
 
 spmm_status spmm_24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
                     void* workspace, size_t workspace_bytes, spmm_stream_t stream) {
-    spmm_status st = check_24(A, N);
+    spmm_status st = check_24_call(A, B, ldb, C, ldc, N);
     if (st != SPMM_OK) return st;
-    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
-    if (A->M > 0 && (!A->vals || !A->meta)) return SPMM_ERR_NULL;
-    if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
-    if (A->dtype != SPMM_I8 && ((ldb * 2) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
     const size_t need = spmm24_workspace_bytes(A, N);
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SPMM_ERR_WORKSPACE;
     return launch_spmm24(A, B, ldb, C, ldc, N, workspace, reinterpret_cast<cudaStream_t>(stream));

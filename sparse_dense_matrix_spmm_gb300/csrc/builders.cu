@@ -24,6 +24,9 @@ template <>
 __device__ __forceinline__ bool nz<uint16_t>(uint16_t v) { return (v & 0x7FFFu) != 0; }
 template <>
 __device__ __forceinline__ bool nz<int8_t>(int8_t v) { return v != 0; }
+// fp8 (E4M3 / E5M2) bit patterns: zero iff every bit but the sign is 0
+template <>
+__device__ __forceinline__ bool nz<uint8_t>(uint8_t v) { return (v & 0x7Fu) != 0; }
 
 // ---------------------------------------------------------------- scan
 // In-place exclusive prefix sum of a[0..n) with one CTA of 1024 threads.
@@ -255,6 +258,10 @@ __device__ __forceinline__ unsigned mag_key<int8_t>(int8_t v) {
 template <>
 __device__ __forceinline__ unsigned mag_key<uint16_t>(uint16_t v) {
     return v & 0x7FFFu;
+}
+template <>
+__device__ __forceinline__ unsigned mag_key<uint8_t>(uint8_t v) {  // fp8: bits without the sign
+    return v & 0x7Fu;
 }
 
 // The two positions of largest key (lowest index among equals), ascending.
@@ -537,7 +544,7 @@ spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, 
     spmm_status st = build_begin(e, s);
     if (st != SPMM_OK) return st;
     const int64_t n = M * (K / 8);
-    const int64_t es = dtype == SPMM_I8 ? 1 : 2;  // 8 elements: 16 (or 8) bytes per access
+    const int64_t es = dtype_bytes(dtype);  // 8 elements: 16 (or 8) bytes per access
     const int vec = (reinterpret_cast<uintptr_t>(dense) % (8 * es) == 0) && ((ld * es) % (8 * es) == 0) &&
                     (reinterpret_cast<uintptr_t>(vals) % (4 * es) == 0);
     const dim3 grid(static_cast<unsigned>((K / 8 + 255) / 256), static_cast<unsigned>(M < 65535 ? (M > 0 ? M : 1) : 65535));
@@ -545,6 +552,9 @@ spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, 
         if (dtype == SPMM_I8)
             compress24_kernel<int8_t><<<grid, 256, 0, s>>>(
                 static_cast<const int8_t*>(dense), M, K, ld, static_cast<int8_t*>(vals), meta, vec, e);
+        else if (is_fp8(dtype))
+            compress24_kernel<uint8_t><<<grid, 256, 0, s>>>(
+                static_cast<const uint8_t*>(dense), M, K, ld, static_cast<uint8_t*>(vals), meta, vec, e);
         else
             compress24_kernel<uint16_t><<<grid, 256, 0, s>>>(
                 static_cast<const uint16_t*>(dense), M, K, ld, static_cast<uint16_t*>(vals), meta, vec, e);
@@ -555,7 +565,7 @@ spmm_status run_compress24(const void* dense, int64_t M, int64_t K, int64_t ld, 
 spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int32_t dtype, void* vals,
                         uint8_t* meta, cudaStream_t s) {
     const int64_t n = M * (K / 8);
-    const int64_t es = dtype == SPMM_I8 ? 1 : 2;  // 8 elements: 16 (or 8) bytes per access
+    const int64_t es = dtype_bytes(dtype);  // 8 elements: 16 (or 8) bytes per access
     const int vec = (reinterpret_cast<uintptr_t>(dense) % (8 * es) == 0) && ((ld * es) % (8 * es) == 0) &&
                     (reinterpret_cast<uintptr_t>(vals) % (4 * es) == 0);
     const dim3 grid(static_cast<unsigned>((K / 8 + 255) / 256), static_cast<unsigned>(M < 65535 ? (M > 0 ? M : 1) : 65535));
@@ -564,6 +574,9 @@ spmm_status run_prune24(const void* dense, int64_t M, int64_t K, int64_t ld, int
         if (dtype == SPMM_I8)
             prune24_kernel<int8_t><<<grid, 256, 0, s>>>(
                 static_cast<const int8_t*>(dense), M, K, ld, static_cast<int8_t*>(vals), meta, vec);
+        else if (is_fp8(dtype))
+            prune24_kernel<uint8_t><<<grid, 256, 0, s>>>(
+                static_cast<const uint8_t*>(dense), M, K, ld, static_cast<uint8_t*>(vals), meta, vec);
         else
             prune24_kernel<uint16_t><<<grid, 256, 0, s>>>(
                 static_cast<const uint16_t*>(dense), M, K, ld, static_cast<uint16_t*>(vals), meta, vec);

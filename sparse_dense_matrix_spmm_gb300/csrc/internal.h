@@ -45,6 +45,17 @@ inline CUtensorMapDataType half_type(int32_t dtype) {
     return dtype == SPMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
+// Element types of the 2:4 operand: bf16, fp16, int8, fp8 E4M3 / E5M2.
+inline bool dtype_24(int32_t dtype) {
+    return dtype == SPMM_BF16 || dtype == SPMM_F16 || dtype == SPMM_I8 || dtype == SPMM_E4M3 || dtype == SPMM_E5M2;
+}
+inline int dtype_bytes(int32_t dtype) { return (dtype == SPMM_BF16 || dtype == SPMM_F16) ? 2 : 1; }
+inline bool is_fp8(int32_t dtype) { return dtype == SPMM_E4M3 || dtype == SPMM_E5M2; }
+
+// Argument checks shared by spmm_24 and spmm_24_noalloc (everything except the
+// workspace): status of the first failing check, SPMM_OK otherwise.
+spmm_status check_24_call(const spmm_24_t* A, const void* B, int64_t ldb, const void* C, int64_t ldc, int64_t N);
+
 // Tracing hooks: no-ops unless spmm_trace_enable(1) is in effect.
 void trace_begin(int kernel, cudaStream_t s);
 void trace_end(int kernel, cudaStream_t s);

@@ -28,7 +28,9 @@ void* g_addr[kMaxDevices];
 bool g_ready[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up once per
-// device with that device current.
+// device with that device current and kept for the process's lifetime (a
+// cudaDeviceReset would leave the kept address pointing into the old context;
+// the library is not meant to be used across one).
 spmm_status scratch_address(void** out) {
     int d = 0;
     if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return SPMM_ERR_CUDA;
@@ -50,15 +52,9 @@ using namespace spmm;
 
 extern "C" spmm_status spmm_24_noalloc(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc,
                                        int64_t N, spmm_stream_t stream) {
-    if (!A) return SPMM_ERR_NULL;
-    if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
-    if (A->dtype != SPMM_BF16 && A->dtype != SPMM_F16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
-    if (A->M < 0 || A->K <= 0 || N < 0 || A->K % 128) return SPMM_ERR_SHAPE;
-    if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
-        return SPMM_ERR_UNSUPPORTED;
-    if (A->M > 0 && (!A->vals || !A->meta)) return SPMM_ERR_NULL;
-    if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
-    if (A->dtype != SPMM_I8 && ((ldb * 2) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
+    // the same checks spmm_24 makes, from the one shared function
+    const spmm_status chk = check_24_call(A, B, ldb, C, ldc, N);
+    if (chk != SPMM_OK) return chk;
     // Same scratch as spmm_24 would ask for; refuse anything larger than the array.
     const size_t need = spmm24_workspace_bytes(A, N);
     if (need > kNoAllocScratchBytes) return SPMM_ERR_WORKSPACE;

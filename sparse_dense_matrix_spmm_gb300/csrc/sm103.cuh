@@ -239,6 +239,18 @@ __device__ __forceinline__ void mma_sp_f16(uint32_t d, uint64_t adesc, uint64_t 
         : "memory");
 }
 
+// Sparse MMA on 8-bit floating-point operands (kind::f8f6f4, E4M3 / E5M2):
+// K = 64 dense per instruction; the metadata of one MMA is two TMEM columns.
+__device__ __forceinline__ void mma_sp_f8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t meta,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.sp.cta_group::1.kind::f8f6f4 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(meta), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -264,6 +276,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
+// Two consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t v0, uint32_t v1) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v0), "r"(v1) : "memory");
+}
 
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
@@ -286,6 +302,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
     return (sel & 3u) | (sparse ? (1u << 2) : 0u) | (1u << 4) | ((bf16 ? 1u : 0u) << 7) |
            ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with fp32 accumulation: the same
+// fields as kind::f16, with A/B formats 0 = E4M3, 1 = E5M2.
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N, bool e5m2, bool a_mn_major, bool b_mn_major,
+                                                bool sparse) {
+    return (sparse ? (1u << 2) : 0u) | (1u << 4) | ((e5m2 ? 1u : 0u) << 7) | ((e5m2 ? 1u : 0u) << 10) |
+           ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 }  // namespace ptx

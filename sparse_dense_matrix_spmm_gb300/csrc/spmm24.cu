@@ -81,19 +81,27 @@ constexpr int META_RING = 8, META_AHEAD = 6;
 // of tile waves favours it (wide_tile).  Producer p fills
 // the steps at positions t with t % PRODUCERS == p into slot t % STAGES, so each
 // slot has one producer.
-template <int BN_>
+//
+// F8: fp8 (E4M3 / E5M2) operands on kind::f8f6f4.  A stage then holds 256 dense
+// K: the compressed A tile is still 128 rows x 128 bytes, the B tile one
+// 128-byte-wide chunk of 256 K rows (32 KB), and each of the four K = 64 sparse
+// MMAs reads 8 stored metadata bytes per row.  (No TVW gathers or lifted planes.)
+template <int BN_, bool F8_ = false>
 struct Tile {
     static constexpr int BN = BN_;
-    static constexpr int CHUNKS = BN_ / 64;  // 64-column B chunks (128-byte swizzle rows)
-    static constexpr uint32_t B_BYTES = KS * BN_ * 2;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + M_BYTES;  // 1024-aligned
+    static constexpr int KSD = F8_ ? 2 * KS : KS;          // dense K per stage
+    static constexpr int CHUNKS = F8_ ? 1 : BN_ / 64;       // 128-byte-wide B chunks (128-byte swizzle rows)
+    static constexpr uint32_t B_BYTES = KSD * BN_ * (F8_ ? 1 : 2);
+    static constexpr uint32_t MB = BM * (KSD / 8);          // stored metadata bytes per step
+    // 1024-aligned; the per-stage metadata copy is used by TVW only
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + (F8_ ? 0 : M_BYTES);
     static constexpr int STAGES = BN_ == 128 ? 4 : 3;
     static constexpr int PRODUCERS = BN_ == 128 ? 2 : 3;
     static constexpr int MMA_WARP = PRODUCERS;
     static constexpr int META_WARP0 = PRODUCERS + 1;
     static constexpr uint32_t META_COL = NACC * BN_;  // metadata columns after the accumulators
     static constexpr uint32_t RING_OFF = STAGES * STAGE_BYTES;
-    static constexpr int SMEM = 1024 + RING_OFF + META_RING * M_BYTES + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+    static constexpr int SMEM = 1024 + RING_OFF + META_RING * MB + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
     __host__ __device__ static constexpr int epi_warp0(bool gather) {
         return META_WARP0 + kMetaWarps + gather_warps(gather);
     }
@@ -104,7 +112,9 @@ static_assert(Tile<128>::STAGES % Tile<128>::PRODUCERS == 0 && Tile<192>::STAGES
 static_assert(Tile<192>::META_COL + META_STRIDE * 4 * Tile<192>::STAGES <= TMEM_COLS &&
                   Tile<128>::META_COL + META_STRIDE * 4 * Tile<128>::STAGES <= TMEM_COLS,
               "accumulators and metadata fit in TMEM");
-static_assert(Tile<192>::SMEM <= 232448 && Tile<128>::SMEM <= 232448, "shared memory per block");
+static_assert(Tile<192>::SMEM <= 232448 && Tile<128>::SMEM <= 232448 && Tile<128, true>::SMEM <= 232448,
+              "shared memory per block");
+static_assert(Tile<128, true>::STAGE_BYTES % 1024 == 0, "swizzle alignment");
 static_assert(Tile<192>::STAGE_BYTES % 1024 == 0 && Tile<128>::STAGE_BYTES % 1024 == 0, "swizzle alignment");
 
 using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
@@ -159,7 +169,8 @@ __device__ __forceinline__ void tile_of(const SpArgs& a, int u, int& mt, int& nt
     nt = g * kGroupN + (r - (r / gw) * gw);
 }
 
-__device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int& kt, bool gather) {
+// K steps of row tile mt (ksd dense K per step).
+__device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int& kt, bool gather, int ksd = KS) {
     if (gather) {
         kb = __ldg(a.tile_ptr + mt);
         kt = __ldg(a.tile_ptr + mt + 1) - kb;
@@ -167,23 +178,26 @@ __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int&
     }
     kb = 0;
     kt = static_cast<int>(a.K);
-    return static_cast<int>(a.K / KS);
+    return static_cast<int>(a.K / ksd);
 }
 
-template <bool GATHER, bool INT_EXACT, int PLANES, int BNT>
-__global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
+template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false>
+__global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
     sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
                        const __grid_constant__ BMaps<PLANES> tmB, const SpArgs a) {
-    using Cfg = Tile<BNT>;
+    using Cfg = Tile<BNT, F8>;
     static_assert(!INT_EXACT || BNT == 128, "the int8 epilogue keeps 128 sums per thread");
     static_assert(!GATHER || BNT == 128, "TVW gathers two 64-column chunks");
+    static_assert(!F8 || (BNT == 128 && !GATHER && !INT_EXACT && PLANES == 1), "fp8: plain 2:4, 128-column tiles");
     constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, kProducers = Cfg::PRODUCERS;
     constexpr int kMmaWarp = Cfg::MMA_WARP, kMetaWarp0 = Cfg::META_WARP0;
     constexpr uint32_t B_BYTES = Cfg::B_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES, RING_OFF = Cfg::RING_OFF;
     constexpr uint32_t META_COL = Cfg::META_COL;
+    constexpr int KSD = Cfg::KSD;
+    constexpr uint32_t MB = Cfg::MB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + META_RING * M_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + META_RING * MB);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int kGatherWarps = gather_warps(GATHER);
@@ -247,7 +261,7 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
             tile_of(a, u, mt, nt);
             const int m0 = mt * BM, n0 = nt * BN;
             int kb, kt;
-            const int nk = tile_steps(a, mt, kb, kt, GATHER);
+            const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
             // this producer's steps of the tile: t + ks = p (mod kProducers)
             for (int ks = (p - t % kProducers + kProducers) % kProducers; ks < nk; ks += kProducers) {
                 const int tt = t + ks;
@@ -259,7 +273,8 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : A_BYTES + B_BYTES);
-                    tma_load_2d_hint(a_s(s), &tmA, full_bar(s), ks * (KS / 2), m0, pol_stream);
+                    // compressed A: 128 stored bytes per row and step for fp8, 64 elements for 16-bit
+                    tma_load_2d_hint(a_s(s), &tmA, full_bar(s), ks * (F8 ? KSD / 2 : KS / 2), m0, pol_stream);
                     if (GATHER) tma_load_2d_hint(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0, pol_stream);
                     if constexpr (!GATHER && PLANES > 1) {
                         // lifted rows ks KS .. ks KS + 127: windows w0 .. w0 + 31 of plane j
@@ -275,6 +290,9 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
                             for (int h = 0; h < Cfg::CHUNKS; ++h)
                                 tma_load_3d(b_s(s) + h * B_CHUNK, bm, full_bar(s), n0 + 64 * h, 0, g0);
                         }
+                    } else if constexpr (F8) {
+                        // one 128-byte-wide chunk of KSD rows (columns n0 .. n0 + 127)
+                        tma_load_2d(b_s(s), &tmB.m[0], full_bar(s), n0, ks * KSD);
                     } else if constexpr (!GATHER) {
                         if (a.b3d) {
                             tma_load_3d(b_s(s), &tmB.m[0], full_bar(s), 0, ks * KS, n0 / 64);
@@ -303,7 +321,7 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
             // stage 0 descriptors; stage s adds s * STAGE_BYTES, MMA i adds 32 B
             // (A: 16 stored K elements) or 4 KB (B: 32 K rows), in 16-byte units
             const uint64_t adesc0 = smem_desc(a_s(0), 16u, 1024u, SWZ_128B);
-            const uint64_t bdesc0 = smem_desc(b_s(0), B_CHUNK, 1024u, SWZ_128B);
+            const uint64_t bdesc0 = smem_desc(b_s(0), F8 ? B_BYTES : B_CHUNK, 1024u, SWZ_128B);
             int s = 0, acc_i = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -311,7 +329,7 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
                 int mt, nt;
                 tile_of(a, u, mt, nt);  // the MMA issuer needs only the row tile
                 int kb, kt;
-                const int nk = tile_steps(a, mt, kb, kt, GATHER);
+                const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
                 const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
                 for (int c = 0; c < nch && ok; ++c, ++acc_i) {
                     const int b = acc_i & 1;
@@ -334,9 +352,15 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
                         const uint32_t mcol = tmem + META_COL + META_STRIDE * 4u * s;
                         const uint64_t so = static_cast<uint64_t>(static_cast<uint32_t>(s) * (STAGE_BYTES >> 4));
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            mma_sp_f16(d, adesc0 + so + 2u * i, bdesc0 + so + 256u * i, mcol + META_STRIDE * i, a.idesc,
-                                       (ks > k_lo || i > 0) ? 1u : 0u);
+                        for (int i = 0; i < 4; ++i) {
+                            // MMA i: A +32 stored bytes; B +32 K rows (16-bit) or +64 K rows (fp8) of 128 B
+                            if constexpr (F8)
+                                mma_sp_f8(d, adesc0 + so + 2u * i, bdesc0 + so + 512u * i, mcol + META_STRIDE * i,
+                                          a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
+                            else
+                                mma_sp_f16(d, adesc0 + so + 2u * i, bdesc0 + so + 256u * i, mcol + META_STRIDE * i,
+                                           a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
+                        }
                         mma_commit(empty_bar(s));
                         if (++s == STAGES) {
                             s = 0;
@@ -366,7 +390,7 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
             w.ks = 0;
             while (w.u < total) {
                 tile_of(a, w.u, w.mt, w.nt);
-                w.nk = tile_steps(a, w.mt, w.kb, w.kt, GATHER);
+                w.nk = tile_steps(a, w.mt, w.kb, w.kt, GATHER, KSD);
                 if (w.nk > 0) break;
                 w.u += gridDim.x;
             }
@@ -388,9 +412,10 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
         auto meta_copy = [&]() {
             const int64_t grow = static_cast<int64_t>(f.mt) * BM + row;
             const bool live = f.u < total && grow < a.M;
-            const uint8_t* src = live ? a.meta + grow * a.ldm + static_cast<int64_t>(f.ks) * (KS / 8) : a.meta;
-            cp_async16(s0 + RING_OFF + static_cast<uint32_t>(f_step % META_RING) * M_BYTES + 16u * row, src,
-                       live ? 16u : 0u);
+            const uint8_t* src = live ? a.meta + grow * a.ldm + static_cast<int64_t>(f.ks) * (KSD / 8) : a.meta;
+            const uint32_t dst = s0 + RING_OFF + static_cast<uint32_t>(f_step % META_RING) * MB + (MB / BM) * row;
+            cp_async16(dst, src, live ? 16u : 0u);
+            if constexpr (F8) cp_async16(dst + 16u, live ? src + 16 : src, live ? 16u : 0u);
             cp_async_commit();
             ++f_step;
             if (f.u < total) advance(f);
@@ -415,7 +440,30 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
                 w = *reinterpret_cast<const uint4*>(mc + 16 * row);
             } else {
                 cp_async_wait<META_AHEAD - 1>();  // this thread's copy for this step has landed
-                w = *reinterpret_cast<const uint4*>(smem + RING_OFF + (m_step % META_RING) * M_BYTES + 16 * row);
+                const uint8_t* mine = smem + RING_OFF + (m_step % META_RING) * MB + (MB / BM) * row;
+                w = *reinterpret_cast<const uint4*>(mine);
+                if constexpr (F8) {
+                    // kind::f8f6f4 reads row r's 64 bits of one MMA from TMEM lane r, two
+                    // consecutive columns, in stored order (measured): copy them as they are
+                    uint4 w2 = *reinterpret_cast<const uint4*>(mine + 16);
+                    ++m_step;
+                    meta_copy();
+                    if (!mbar_wait(empty_bar(slot), par ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
+                    if (!row_live) {
+                        w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+                        w2 = w;
+                    }
+                    const uint32_t tb = tl + META_STRIDE * 4u * slot;
+                    tmem_st2(tb, w.x, w.y);
+                    tmem_st2(tb + META_STRIDE, w.z, w.w);
+                    tmem_st2(tb + 2 * META_STRIDE, w2.x, w2.y);
+                    tmem_st2(tb + 3 * META_STRIDE, w2.z, w2.w);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(mready_bar(slot));
+                    return true;
+                }
                 ++m_step;
                 meta_copy();
                 // the MMAs that read this slot's metadata columns last time are done
@@ -502,7 +550,7 @@ __global__ void __launch_bounds__(Tile<BNT>::threads(GATHER), 1)
             int mt, nt;
             tile_of(a, u, mt, nt);
             int kb, kt;
-            const int nk = tile_steps(a, mt, kb, kt, GATHER);
+            const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
             const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
             const int64_t row = static_cast<int64_t>(mt) * BM + q * 32 + lane;
             const int64_t n0 = static_cast<int64_t>(nt) * BN;
@@ -631,20 +679,20 @@ __global__ void widen_i8_kernel(const WidenJob j0, const WidenJob j1) {
     }
 }
 
-template <bool GATHER, bool INT_EXACT, int PLANES, int BNT>
+template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false>
 spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const BMaps<PLANES>& tmB, const SpArgs& a,
                           cudaStream_t stream, int slot) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
-    constexpr int kSmem = Tile<BNT>::SMEM;
+    constexpr int kSmem = Tile<BNT, F8>::SMEM;
     if (dev->max_smem_optin < kSmem) return SPMM_ERR_UNSUPPORTED;
-    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES, BNT>;
+    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES, BNT, F8>;
     if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem, slot)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
     if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_SPARSE, stream);
-    kern<<<grid, Tile<BNT>::threads(GATHER), kSmem, stream>>>(tmA, tmM, tmB, a);
+    kern<<<grid, Tile<BNT, F8>::threads(GATHER), kSmem, stream>>>(tmA, tmM, tmB, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_SPARSE, stream);
     return cuda_status(e);
@@ -734,11 +782,31 @@ size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N) {
     return A->dtype == SPMM_I8 ? widen_bytes(A->M, A->K / 2, A->K, N) : 0;
 }
 
+// fp8 operands (kind::f8f6f4): A's stored bytes in 128 x 128-byte boxes, B in
+// 256-row x 128-byte boxes (128 columns), both 128-byte swizzled.
+spmm_status launch_spmm24_f8(const DeviceInfo* dev, const spmm_24_t* A, const void* B, int64_t ldb, void* C,
+                             int64_t ldc, int64_t N, cudaStream_t stream) {
+    CUtensorMap tmA, tmM;
+    BMaps<1> tmB;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!encode_tmap_2d(&tmA, u8, A->vals, static_cast<uint64_t>(A->K / 2), static_cast<uint64_t>(A->M),
+                        static_cast<uint64_t>(A->K / 2), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tmM, u8, A->meta, static_cast<uint64_t>(A->K / 8), static_cast<uint64_t>(A->M),
+                        static_cast<uint64_t>(A->K / 8), 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_2d(&tmB.m[0], u8, B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
+                        static_cast<uint64_t>(ldb), 128, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPMM_ERR_CUDA;
+    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, 128);
+    a.idesc = idesc_f8(128, 128, A->dtype == SPMM_E5M2, false, true, true);
+    return launch_sparse<false, false, 1, 128, true>(tmA, tmM, tmB, a, stream, 15);
+}
+
 spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
                           void* ws, cudaStream_t stream) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
     if (A->M == 0 || N == 0) return SPMM_OK;
+    if (A->dtype == SPMM_E4M3 || A->dtype == SPMM_E5M2) return launch_spmm24_f8(dev, A, B, ldb, C, ldc, N, stream);
     const bool i8 = A->dtype == SPMM_I8;
     const void* vals = A->vals;
     const void* bsrc = B;

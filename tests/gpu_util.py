@@ -27,12 +27,32 @@ def dev_half(bits, dtype):
     return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16)
 
 
+def dev_fp8(bits, dtype):
+    """uint8 fp8 bit patterns -> a device tensor of torch's float8 type."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).cuda()
+    return t.view(torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2)
+
+
 def host_bits(t):
-    """Device tensor -> numpy raw bits (uint16 for 16-bit types)."""
+    """Device tensor -> numpy raw bits (uint16 for 16-bit types, uint8 for fp8)."""
     import torch
     if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.view(torch.uint8).cpu().numpy()
     return t.cpu().numpy()
+
+
+def padded_b8(bits, dtype):
+    """fp8 B on the device with its row pitch rounded up to 16 bytes, as a K x N view."""
+    import torch
+    K, N = bits.shape
+    ld = -(-N // 16) * 16
+    full = torch.zeros((K, ld), dtype=torch.uint8, device="cuda")
+    full[:, :N] = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).cuda()
+    full = full.view(torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2)
+    return full[:, :N]
 
 
 def assert_close(got, ref, what=""):

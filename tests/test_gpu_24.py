@@ -34,8 +34,10 @@ def test_24_int8_exact(M, K, N):
 
 
 def test_24_int8_extreme_values_stay_exact():
-    """Every product 127*127 with equal signs: each 512-wide chunk reaches its
-    largest partial sum (256 * 16129), so any lost bit would show."""
+    """Every product 127*127 with equal signs: the kernel drains its fp32
+    accumulator every 2048 dense K, so each chunk of 1024 products reaches the
+    largest partial sum it can hold exactly (1024 * 16129 < 2^24), and any lost
+    bit would show."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     M, K, N = 128, 4096, 128
