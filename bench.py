@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SpMM effective TFLOP/s (2·nnz·N/time) and % of roofline, per sparse format"
 HEADLINE = "mask24_int8"
-EXTRA_WORKLOADS = ("bcsr_llm", "tvw", "wcsr_lognormal", "mask24_f16", "mask24_e4m3", "slide68_f16", "bcsr_rcm",
+EXTRA_WORKLOADS = ("bcsr_llm", "tvw", "wcsr_lognormal", "wcsr_clustered", "mask24_f16", "mask24_e4m3", "slide68_f16", "bcsr_rcm",
                    "sddmm_lognormal", "prune24_f16", "prune_tvw_f16", "bcsr_tiny")
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -540,7 +540,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
 
         def step():
             out["F"] = spmm.spmm_prune_tvw(A, tr, tp, cl, Kp=keep)
-    elif c["kind"] == "wcsr":
+    elif c["kind"] in ("wcsr", "wcsrc"):
         p = gen.config_problem(name, **({"N": args.n} if args.n else {}))
         dt = torch.float16
         csr = spmm.CSR(c["M"], c["K"], int(p["row_ptr"][-1]), dt, to_dev(p["row_ptr"]), to_dev(p["col"]),
@@ -551,6 +551,10 @@ def run_extra(name, args, ws, peaks, flush_buf):
         F = spmm.build_wcsr(csr, 16, 32)
         torch.cuda.synchronize()
         build_ms = (time.perf_counter() - t0) * 1e3
+        extra_fields["nonzeros_per_window_column"] = round(F.nnz / max(F.n_wcols, 1), 3)
+        # the library's rule: tensor core when >= 4 nonzeros per window column and >= 384 per work unit
+        tcore = F.nnz >= 4 * F.n_wcols and F.nnz >= 384 * F.n_units
+        extra_fields["window_products"] = "tensor core" if tcore else "CUDA cores"
         Cd = torch.empty((c["M"], c["N"]), dtype=torch.float32, device="cuda")
         wsp = torch.zeros(max(1, spmm.spmm_wcsr_workspace_size(F, c["N"])), dtype=torch.uint8, device="cuda")
         nnz = csr.nnz
@@ -659,7 +663,7 @@ def cpu_baseline_extra(name, target_s=2.0):
         r, dt = _time_rows(lambda r: oracle.tvw_spmm(F, p["B"], rows=(0, r)), c["M"], 8, target_s)
         flops = 2.0 * r * (c["keep"] // 2) * c["N"]
         sample = f"rows 0..{r - 1} of {c['M']}, all {c['N']} columns"
-    elif kind == "wcsr":
+    elif kind in ("wcsr", "wcsrc"):
         p = gen.config_problem(name)
         F = oracle.wcsr_build(c["M"], c["K"], p["row_ptr"], p["col"], p["val"], c["dtype"], 16, 32)
         r, dt = _time_rows(lambda r: oracle.wcsr_spmm(F, p["B"], rows=(0, r)), c["M"], 256, target_s)

@@ -220,14 +220,20 @@ SPMM_API spmm_status spmm_trace_read(int32_t kernel, int64_t *launches, double *
 SPMM_API spmm_status spmm_bcsr(const spmm_bcsr_t *A, const void *B, int64_t ldb, float *C, int64_t ldc, int64_t N,
                                spmm_stream_t stream);
 
-/* Workspace bytes spmm_wcsr needs for this operand and N (partials of split
- * windows plus one arrival counter per split window). */
+/* Workspace bytes spmm_wcsr needs for this operand and N: a work counter, one
+ * arrival counter per (window, 128-column slab), and the partial tiles of
+ * split windows (n_units x h x N fp32). */
 SPMM_API spmm_status spmm_wcsr_workspace_size(const spmm_wcsr_t *A, int64_t N, size_t *bytes);
-/* C = A * B with A in row-window CSR ("AsyncSparse": per-window loads, long
- * windows split across CTAs).  Split windows are summed in split order by the
- * last CTA to finish, so results are run-to-run identical.  The workspace must
- * be zero-filled before its first use; a successful call leaves its counters
- * at zero again.  fp16/bf16 in, fp32 C. */
+/* C = A * B with A in row-window CSR ("AsyncSparse", abstract and Fig. 2:
+ * the sparse operand loaded per row window, long windows split across thread
+ * blocks).  Each window's product runs on the tensor core: for every 16 of its
+ * column slots, D (128 output columns x h rows) += (the 16 gathered B rows)^T
+ * x (the window's h x 16 value tile)^T with fp32 accumulation in TMEM.  Split
+ * windows are summed in split order by the last unit to finish, so results are
+ * run-to-run identical.  The workspace needs no clearing: its counters carry
+ * a per-call tag, so a call that stopped early (a timed-out wait) does not
+ * affect later ones; calls sharing one workspace must not overlap on the GPU.
+ * h <= 64.  fp16/bf16 in, fp32 C. */
 SPMM_API spmm_status spmm_wcsr(const spmm_wcsr_t *A, const void *B, int64_t ldb, float *C, int64_t ldc, int64_t N,
                                void *workspace, size_t workspace_bytes, spmm_stream_t stream);
 

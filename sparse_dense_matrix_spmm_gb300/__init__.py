@@ -487,7 +487,8 @@ def spmm_wcsr_workspace_size(A: WCSR, N: int) -> int:
 
 def spmm_wcsr(A: WCSR, B: torch.Tensor, C_: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """The workspace must start zero-filled; a successful call leaves it reusable."""
+    """C = A B for a row-window operand (tensor-core window products).  The
+    workspace (kept on A when not given) needs no clearing between calls."""
     _check_dev(B, C_, workspace)
     N = B.shape[1]
     out = _out(C_, A.M, N, torch.float32, B.device)

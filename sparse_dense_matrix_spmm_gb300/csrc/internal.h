@@ -87,6 +87,9 @@ size_t wcsr_spmm_ws_bytes(const spmm_wcsr_t* A, int64_t N);
 spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
                         void* ws, cudaStream_t s);
 int wcsr_max_h();
+// Whether spmm_wcsr runs this operand's window products on the tensor core
+// (enough nonzeros per distinct window column) or on CUDA cores.
+bool wcsr_uses_tensor_core(const spmm_wcsr_t* A);
 
 spmm_status run_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, int bh, int bw, int32_t dtype,
                            int32_t* row_ptr, int64_t* nnzb, cudaStream_t s);

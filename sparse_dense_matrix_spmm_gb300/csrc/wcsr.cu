@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -51,12 +52,7 @@ __device__ int g_wcsr_build_error;  // data-dependent builder errors (SPMM_DEVER
 
 namespace {
 
-constexpr int kWarps = 4;     // several CTAs per SM: one CTA's staging overlaps the others' gathers
-constexpr int kMinBlocks = 8; // resident CTAs per SM the register budget is sized for (64 registers)
-constexpr int kThreads = kWarps * 32;
-constexpr int kSlab = 128;    // output columns per pass (8 per lane of a half-warp)
-static_assert(kThreads >= kSlab, "the boundary fix-up gives one thread to each slab column");
-constexpr int kMaxH = 64;   // largest window height the SpMM kernel accepts
+constexpr int kMaxH = 64;   // largest window height the SpMM kernel accepts (MMA N <= 64)
 
 std::mutex g_mu;
 
@@ -248,7 +244,39 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* a, int64_t n) {
     }
 }
 
-// ---------------------------------------------------------------- SpMM
+// Open this call's generation on a tagged counter (gen << 32 | count): the first
+// caller that sees an older tag resets the count to 0; everyone returns once
+// the word carries this call's tag.  Exactly one reset happens per call, and it
+// happens before any increment of that call, because increments come only
+// from threads that saw the new tag.
+__device__ __forceinline__ bool open_tag(unsigned long long* w, uint32_t gen, int* err) {
+    unsigned long long cur = atomicAdd(w, 0ull);
+#pragma unroll 1
+    for (int it = 0; it < (1 << 20); ++it) {
+        if (static_cast<uint32_t>(cur >> 32) == gen) return true;
+        const unsigned long long prev = atomicCAS(w, cur, static_cast<unsigned long long>(gen) << 32);
+        if (prev == cur) return true;
+        cur = prev;
+    }
+    atomicOr(err, SPMM_DEVERR_TIMEOUT);
+    return false;
+}
+
+// ---------------------------------------------------------------- SpMM on CUDA cores
+// For windows whose column slots hold about one nonzero each (no column reuse
+// inside the window), a dense tile per window is ~6% full and the tensor
+// core gathers as many B rows as the plain product does; this kernel keeps
+// the gathers and does the multiply-adds on CUDA cores.  One CTA per work
+// unit, 8 CTAs of 4 warps per SM, so many units' chains of dependent loads
+// (unit header -> window header and nonzeros -> column list -> B rows) are in
+// flight at once.
+namespace cc {
+
+constexpr int kWarps = 4;     // several CTAs per SM: one CTA's staging overlaps the others' gathers
+constexpr int kMinBlocks = 8; // resident CTAs per SM the register budget is sized for (64 registers)
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlab = 128;    // output columns per pass (8 per lane of a half-warp)
+static_assert(kThreads >= kSlab, "the boundary fix-up gives one thread to each slab column");
 constexpr int kPfArrays = 10;
 
 struct WcsrArgs {
@@ -269,7 +297,9 @@ struct WcsrArgs {
     int32_t b_vec;    // B rows can be read as 16-byte pieces (16-byte aligned base, ldb % 8 == 0, K * ldb < 2^31)
     int32_t c_vec;    // C and the partials can be written as float4 (aligned base, ldc % 4 == 0, N % 4 == 0)
     float* partial;   // [n_units][h][N]
-    int32_t* ticket;  // [n_windows]
+    unsigned long long* ticket;  // [n_windows * nslabs] arrival counters (generation-tagged; slab 0's word)
+    int32_t nslabs;
+    uint32_t gen;     // this call's generation tag (never 0)
     int* err;
     // L2 warm-up: the first pf_ctas CTAs each prefetch their share of these
     // arrays (format arrays and B), so later index and B-row loads hit L2
@@ -560,8 +590,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) wcsr_spmm_kernel(const W
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const int t = atomicAdd(a.ticket + w, 1);
-        s_last = (t == units_in_window - 1);
+        unsigned long long* t = a.ticket + static_cast<int64_t>(w) * a.nslabs;
+        int last = 0;
+        if (open_tag(t, a.gen, a.err)) {
+            const unsigned long long old = atomicAdd(t, 1ull);
+            last = static_cast<int>(old & 0xffffffffull) == units_in_window - 1;
+        }
+        s_last = last;
     }
     __syncthreads();
     if (!s_last) return;
@@ -616,8 +651,418 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) wcsr_spmm_kernel(const W
             a.C[(r0 + r) * a.ldc + c] = s;
         }
     }
-    if (tid == 0) a.ticket[w] = 0;  // ready for the next call
 }
+
+}  // namespace cc
+
+
+// ---------------------------------------------------------------- SpMM on the tensor core
+// Tensor-core row-window product.  For one work item (a unit, i.e. a window or
+// one split of it, and one 128-column slab of B) the unit's column slots are
+// taken 16 at a time (a "K step"):
+//     D (128 x h) += G^T (128 x 16) * W^T (16 x h)
+// where G holds the 16 gathered B rows of the step's slots (the slab's 128
+// columns are the MMA's M dimension) and W is the dense h x 16 tile of the
+// window's values at those slots (zero where a row has no nonzero).  D lives in
+// TMEM as 128 lanes (output columns) x h columns (window rows), so each lane
+// of the epilogue holds one output column of all h rows and stores it
+// coalesced.
+//
+// One CTA per SM, four warpgroups, each working through its own items:
+//   - the warpgroup's 128 threads copy the unit's column list and place its
+//     nonzeros into the W tiles of up to 32 K steps (a "chunk") in shared memory;
+//   - per stage of four K steps, warp q of the warpgroup gathers step q's 16 B
+//     rows (16-byte loads) into a 128-byte-swizzled stage buffer (two buffers);
+//   - after a named barrier, one thread issues the stage's MMAs and commits them
+//     to the buffer's mbarrier;
+//   - at the end of the item the four warps read their TMEM lane quarter and
+//     write C (or, for a split window, a partial tile; the last unit of the
+//     window sums the partials in unit order).
+// All synchronisation inside a warpgroup is a named barrier or an mbarrier the
+// MMAs arrive on; warpgroups share nothing but the TMEM allocation.
+namespace tc {
+
+constexpr int kWG = 4;                   // warpgroups per CTA
+constexpr int kThreads = 128 * kWG;
+constexpr int kSteps = 4;                // K steps per stage, one per warp of the warpgroup
+constexpr int kSlab = 128;               // output columns per item (the MMA's M)
+constexpr uint32_t kStepBytes = 16 * kSlab * 2;        // 16 gathered rows of 256 bytes
+constexpr uint32_t kStageBytes = kSteps * kStepBytes;  // 16 KB
+constexpr uint32_t kWBytes = 16384;      // W tiles of one chunk
+constexpr int kMaxNp = 64;               // window rows rounded up to 16 (MMA N), at most 64
+constexpr int kChunkSlots = 512;         // column slots of one chunk, at most (Np = 16: 32 steps)
+constexpr uint32_t kColBytes = kChunkSlots * 4;
+constexpr uint32_t kWGBytes = 2 * kStageBytes + kWBytes + kColBytes;  // 50 KB, 1024-aligned
+static_assert(kWGBytes % 1024 == 0, "swizzle alignment of every warpgroup's stage buffers");
+
+struct Args {
+    const int32_t* wcol_ptr;
+    const int32_t* wcols;
+    const int32_t* unit_ptr;
+    const int32_t* unit_win;
+    const int32_t* unit_nz_ptr;
+    const uint8_t* lrow;
+    const int32_t* slot;
+    const uint16_t* val;
+    const uint16_t* B;
+    int64_t ldb;
+    float* C;
+    int64_t ldc;
+    int64_t M, K, N;
+    int32_t h, S, Np, nslabs;
+    int64_t n_windows, n_units, n_items;
+    int32_t b_vec;                  // B rows readable as 16-byte pieces
+    uint32_t idesc;
+    uint32_t gen;                   // this call's generation tag (never 0)
+    unsigned long long* ticket;     // [n_windows * nslabs] arrival counters of split windows
+    float* partial;                 // [n_units][h][N]
+    int* err;
+    uint64_t timeout_ns;
+    // L2 warm-up: every CTA prefetches its share of these arrays at the start
+    const void* pf_ptr[10];
+    int64_t pf_bytes[10];
+    int32_t pf_n;
+};
+
+__host__ __device__ constexpr int smem_bytes() { return 1024 + kWG * static_cast<int>(kWGBytes) + 8 * 3 * kWG + 16 + 16 * kWG; }
+
+// Named barrier over `count` threads that also ANDs a per-thread flag: every
+// thread gets the same answer, so a warpgroup leaves its loop together when
+// any of its bounded waits gave up.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Columns n .. n+7 of B row `row` (this lane's 16-byte piece of the slab), zero
+// past N or for row < 0; one vector load when the piece is whole and aligned.
+__device__ __forceinline__ uint4 load_piece(const Args& a, int row, int64_t n) {
+    if (row < 0) return make_uint4(0u, 0u, 0u, 0u);
+    const uint16_t* p = a.B + static_cast<int64_t>(row) * a.ldb + n;
+    if (a.b_vec && n + 8 <= a.N) return __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t e[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) e[t] = (n + t < a.N) ? static_cast<uint32_t>(__ldg(p + t)) : 0u;
+    return make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+}
+
+// One item's header.
+struct Item {
+    int32_t u, w, n0, r0, nrows, wbase, slot0, Tu, nk, nz0, nz1, U, u0;
+    bool ok;
+};
+
+__device__ __forceinline__ Item load_item(const Args& a, int64_t id) {
+    Item it{};
+    const int64_t u = id / a.nslabs;
+    it.u = static_cast<int32_t>(u);
+    it.n0 = static_cast<int32_t>((id - u * a.nslabs) * kSlab);
+    const int w = __ldg(a.unit_win + u);
+    it.ok = w >= 0 && w < a.n_windows;
+    if (!it.ok) return it;
+    const int32_t up0 = __ldg(a.unit_ptr + w), up1 = __ldg(a.unit_ptr + w + 1);
+    const int32_t wb = __ldg(a.wcol_ptr + w), we = __ldg(a.wcol_ptr + w + 1);
+    const int32_t z0 = __ldg(a.unit_nz_ptr + u), z1 = __ldg(a.unit_nz_ptr + u + 1);
+    const int64_t span = 16 * static_cast<int64_t>(a.S);
+    const int64_t sl0 = span * (u - up0);
+    int64_t tu = static_cast<int64_t>(we - wb) - sl0;
+    tu = tu < 0 ? 0 : (tu > span ? span : tu);
+    const int64_t r0 = static_cast<int64_t>(w) * a.h;
+    it.w = w;
+    it.r0 = static_cast<int32_t>(r0);
+    it.nrows = static_cast<int32_t>(a.M - r0 < a.h ? a.M - r0 : a.h);
+    it.wbase = wb;
+    it.slot0 = static_cast<int32_t>(sl0);
+    it.Tu = static_cast<int32_t>(tu);
+    it.nk = static_cast<int32_t>((tu + 15) / 16);
+    it.nz0 = z0;
+    it.nz1 = z1 < z0 ? z0 : z1;
+    it.U = up1 - up0;
+    it.u0 = up0;
+    return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) wcsr_tc_kernel(const Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int wg = warp / 4, q = warp % 4;  // q: the warp's TMEM lane quarter and its step in every stage
+    const int tw = threadIdx.x % 128;       // thread within the warpgroup
+    uint8_t* wgs = smem + wg * kWGBytes;    // [stage 0 | stage 1 | W tiles | column list]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWG * kWGBytes);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * kWG);
+    int* s_last = reinterpret_cast<int*>(tslot + 4) + wg;
+    const uint32_t sw = ptx::smem_u32(wgs);
+    const uint32_t w_tiles = sw + 2 * kStageBytes;
+    int32_t* collist = reinterpret_cast<int32_t*>(wgs + 2 * kStageBytes + kWBytes);
+    const uint32_t sdone0 = ptx::smem_u32(bars + 3 * wg), sdone1 = sdone0 + 8, adone = sdone0 + 16;
+    const uint32_t bar_id = 1 + wg;
+    const uint32_t tstep = static_cast<uint32_t>(a.Np) * 32u;  // one K step's W tile
+    const int chunk_steps = static_cast<int>(kWBytes / tstep) < kChunkSlots / 16 ? static_cast<int>(kWBytes / tstep)
+                                                                                  : kChunkSlots / 16;
+    const uint32_t tmem_cols = kWG * a.Np <= 64 ? 64u : (kWG * a.Np <= 128 ? 128u : 256u);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3 * kWG; ++i) ptx::mbar_init(ptx::smem_u32(bars + i), 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(tslot), tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    if (threadIdx.x < a.pf_n) {
+        // L2 warm-up: this CTA's share of one of the format arrays or B
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.pf_ptr[threadIdx.x]);
+        const int64_t n = a.pf_bytes[threadIdx.x];
+        const uintptr_t lo = (b0 + n * blockIdx.x / gridDim.x + 15) & ~uintptr_t(15);
+        uintptr_t hi = (b0 + n * (blockIdx.x + 1) / gridDim.x) & ~uintptr_t(15);
+        const uintptr_t end = (b0 + n) & ~uintptr_t(15);
+        if (hi > end) hi = end;
+        for (uintptr_t x = lo; x < hi; x += 65536u)
+            ptx::bulk_prefetch_l2(reinterpret_cast<const void*>(x), static_cast<uint32_t>(hi - x < 65536u ? hi - x : 65536u));
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t dacc = tmem + static_cast<uint32_t>(wg * a.Np);
+
+    // A operand: the gathered rows, M = 128 columns x K = 16 slots, MN-major,
+    // 128-byte swizzle, two 64-column chunks 2 KB apart.  B operand: the W tile,
+    // N = Np rows x K = 16 slots, K-major without swizzle: (row, slot) at
+    // (row / 8) 256 + (slot / 8) 128 + (row % 8) 16 + (slot % 8) 2.
+    const uint64_t adesc0 = ptx::smem_desc(sw, 2048u, 1024u, ptx::SWZ_128B);
+    const uint64_t bdesc0 = ptx::smem_desc(w_tiles, 128u, 256u, ptx::SWZ_NONE);
+    const int hl = lane & 15, hi = lane >> 4;
+    const uint32_t piece_off = static_cast<uint32_t>(hl / 8) * 2048u;
+    const int gq = hl % 8;
+    const int64_t nwg = static_cast<int64_t>(gridDim.x) * kWG;
+    int sc = 0, ic = 0;  // stages and items of this warpgroup so far
+    bool ok = true;
+    Item nxt = load_item(a, static_cast<int64_t>(blockIdx.x) * kWG + wg < a.n_items
+                                ? static_cast<int64_t>(blockIdx.x) * kWG + wg : 0);
+    for (int64_t id = static_cast<int64_t>(blockIdx.x) * kWG + wg; id < a.n_items && ok; id += nwg) {
+        const Item it = nxt;
+        if (id + nwg < a.n_items) nxt = load_item(a, id + nwg);  // next item's header, in flight meanwhile
+        if (!it.ok) {
+            if (tw == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);  // malformed unit list: skip the unit
+            continue;
+        }
+        const int64_t n = static_cast<int64_t>(it.n0) + 8 * hl;
+        for (int c0 = 0; c0 < it.nk && ok; c0 += chunk_steps) {
+            const int cs = it.nk - c0 < chunk_steps ? it.nk - c0 : chunk_steps;
+            // the W tiles and column list are rewritten: the last stage's MMAs must be done
+            const bool free_ok = sc == 0 || ptx::mbar_wait((sc - 1) % 2 ? sdone1 : sdone0,
+                                                           static_cast<uint32_t>((sc - 1) / 2) & 1u, a.timeout_ns,
+                                                           a.err, SPMM_DEVERR_TIMEOUT);
+            if (!bar_and(bar_id, 128, free_ok)) {
+                ok = false;
+                break;
+            }
+            for (uint32_t o = 16u * tw; o < static_cast<uint32_t>(cs) * tstep; o += 16u * 128u)
+                st_shared_v4(w_tiles + o, make_uint4(0u, 0u, 0u, 0u));
+            {
+                // at most 4 slots per thread (a chunk has at most 512): all loads in flight together
+                int cv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tw + 128 * k, sl = 16 * c0 + e;
+                    cv[k] = (e < 16 * cs && sl < it.Tu) ? __ldg(a.wcols + it.wbase + it.slot0 + sl) : -1;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = tw + 128 * k, sl = 16 * c0 + e;
+                    if (e < 16 * cs) {
+                        const bool good = cv[k] >= 0 && cv[k] < a.K;
+                        if (sl < it.Tu && !good) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                        collist[e] = good ? cv[k] : -1;
+                    }
+                }
+            }
+            ptx::named_barrier(bar_id, 128);
+            // the chunk's nonzeros into their W tiles, eight per thread loaded together
+            const int lo = 16 * c0, hiw = 16 * (c0 + cs);
+            for (int e0 = it.nz0 + tw; e0 < it.nz1; e0 += 128 * 8) {
+                int lr[8], sl[8];
+                uint16_t v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int e = e0 + 128 * k;
+                    lr[k] = 255;
+                    sl[k] = -1;
+                    v[k] = 0;
+                    if (e < it.nz1) {
+                        lr[k] = a.lrow[e];
+                        sl[k] = __ldg(a.slot + e) - it.slot0;
+                        v[k] = __ldg(a.val + e);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (e0 + 128 * k >= it.nz1) continue;
+                    if (sl[k] < 0 || sl[k] >= it.Tu || lr[k] >= it.nrows) {
+                        if (c0 == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);  // skipped, reported once
+                        continue;
+                    }
+                    if (sl[k] < lo || sl[k] >= hiw) continue;
+                    const int kk = sl[k] - lo, kx = kk & 15;
+                    st_shared_u16(w_tiles + (kk >> 4) * tstep + (lr[k] >> 3) * 256u + (kx >> 3) * 128u +
+                                      (lr[k] & 7) * 16u + (kx & 7) * 2u,
+                                  v[k]);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_barrier(bar_id, 128);
+            // stages of the chunk: warp q gathers step 4 j + q (its 16 rows are
+            // loaded while the buffer's previous MMAs are waited for)
+            const int nst = (cs + kSteps - 1) / kSteps;
+            for (int j = 0; j < nst; ++j) {
+                const int b = sc % 2;
+                const uint32_t sdone = b ? sdone1 : sdone0;
+                uint4 r[8];
+                {
+                    const int ks = kSteps * j + q;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int col = ks < cs ? collist[16 * ks + 2 * t + hi] : -1;
+                        r[t] = load_piece(a, col, n);
+                    }
+                }
+                // buffer b was last read by the MMAs of stage sc - 2
+                const bool buf_ok = sc < 2 || ptx::mbar_wait(sdone, static_cast<uint32_t>((sc - 2) / 2) & 1u,
+                                                             a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+                if (buf_ok && kSteps * j + q < cs) {
+                    const uint32_t dst = sw + b * kStageBytes + q * kStepBytes + piece_off;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int s = 2 * t + hi;  // slot within the step
+                        st_shared_v4(dst + s * 128u + (static_cast<uint32_t>(gq ^ (s & 7)) << 4), r[t]);
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                ptx::tc_fence_before();
+                if (!bar_and(bar_id, 128, buf_ok)) {
+                    ok = false;
+                    break;
+                }
+                if (tw == 0) {
+                    ptx::tc_fence_after();
+                    const uint64_t so = static_cast<uint64_t>((b * kStageBytes) >> 4);
+                    const int nq = cs - kSteps * j < kSteps ? cs - kSteps * j : kSteps;
+                    for (int qq = 0; qq < nq; ++qq)
+                        ptx::mma_f16(dacc, adesc0 + so + static_cast<uint64_t>(qq) * (kStepBytes >> 4),
+                                     bdesc0 + static_cast<uint64_t>(kSteps * j + qq) * (tstep >> 4), a.idesc,
+                                     (c0 + kSteps * j + qq > 0) ? 1u : 0u);
+                    ptx::mma_commit(sdone);
+                }
+                ++sc;
+            }
+        }
+        if (!ok) break;
+        // ---- epilogue: this warp's lane quarter = output columns 32 q .. 32 q + 31 of the slab
+        if (tw == 0) ptx::mma_commit(adone);  // arrives once every MMA issued so far is done
+        const bool acc_ok = ptx::mbar_wait(adone, static_cast<uint32_t>(ic) & 1u, a.timeout_ns, a.err,
+                                           SPMM_DEVERR_TIMEOUT);
+        if (!bar_and(bar_id, 128, acc_ok)) {
+            ok = false;
+            break;
+        }
+        ++ic;
+        ptx::tc_fence_after();
+        const int64_t ncol = static_cast<int64_t>(it.n0) + 32 * q + lane;
+        const bool split = it.U > 1;
+        float* base = split ? a.partial + static_cast<int64_t>(it.u) * a.h * a.N
+                            : a.C + static_cast<int64_t>(it.r0) * a.ldc;
+        const int64_t ld = split ? a.N : a.ldc;
+        const uint32_t tl = dacc + (static_cast<uint32_t>(32 * q) << 16);
+        for (int c = 0; c < a.Np / 16; ++c) {
+            uint32_t v[16];
+            if (it.nk > 0) {
+                ptx::tmem_ld16(tl + 16 * c, v);
+                ptx::tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] = 0u;  // a window without nonzeros
+            }
+            if (ncol < a.N) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int rr = 16 * c + t;
+                    if (rr < it.nrows) {
+                        float* p = base + rr * ld + ncol;
+                        if (split) __stcg(p, __uint_as_float(v[t]));
+                        else __stcs(p, __uint_as_float(v[t]));
+                    }
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        if (!split) continue;
+        // Split window: the last of its units (arrival counter) sums the partials
+        // of all units in unit order, so the result does not depend on timing.
+        __threadfence();
+        ptx::named_barrier(bar_id, 128);
+        if (tw == 0) {
+            unsigned long long* t = a.ticket + static_cast<int64_t>(it.w) * a.nslabs + it.n0 / kSlab;
+            int last = 0;
+            if (open_tag(t, a.gen, a.err)) {
+                const unsigned long long old = atomicAdd(t, 1ull);
+                last = static_cast<int>(old & 0xffffffffull) == it.U - 1;
+            }
+            *s_last = last;
+        }
+        ptx::named_barrier(bar_id, 128);
+        if (!*s_last) continue;
+        __threadfence();
+        if (ncol < a.N) {
+            // 8 rows at a time: those rows of one unit are loaded together, the
+            // units are added in unit order
+            for (int rb = 0; rb < it.nrows; rb += 8) {
+                float acc[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+                for (int k = 0; k < it.U; ++k) {
+                    const float* pp = a.partial + (static_cast<int64_t>(it.u0 + k) * a.h + rb) * a.N + ncol;
+                    float x[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) x[t] = rb + t < it.nrows ? __ldcg(pp + t * a.N) : 0.f;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) acc[t] += x[t];
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    if (rb + t < it.nrows) a.C[(static_cast<int64_t>(it.r0) + rb + t) * a.ldc + ncol] = acc[t];
+            }
+        }
+    }
+    // leave no MMA in flight (after a timeout too): wait, bounded, for the last commit
+    if (sc > 0 && tw == 0) {
+        ptx::mma_commit(adone);
+        ptx::mbar_wait(adone, static_cast<uint32_t>(ic) & 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+}  // namespace tc
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -704,17 +1149,124 @@ spmm_status run_wcsr_fill(const spmm_csr_t* A, int32_t h, int32_t S, void* ws, s
     return cuda_status(cudaGetLastError());
 }
 
-size_t wcsr_spmm_ws_bytes(const spmm_wcsr_t* A, int64_t N) {
-    return align256(sizeof(int32_t) * static_cast<size_t>(A->n_windows)) +
-           align256(sizeof(float) * static_cast<size_t>(A->n_units) * A->h * N);
+namespace {
+
+// Workspace of the SpMM: one arrival counter per (window, 128-column slab)
+// and the partial tiles of split windows.  The counters carry the generation
+// tag of the call that last used them, so the workspace needs no clearing
+// between calls, and a call that stopped early (a timed-out wait) leaves
+// nothing that a later call would misread.
+struct SpmmWs {
+    unsigned long long* ticket;
+    float* partial;
+};
+
+size_t wcsr_nslabs(int64_t N) { return static_cast<size_t>((N + tc::kSlab - 1) / tc::kSlab); }
+
+size_t wcsr_ticket_bytes(const spmm_wcsr_t* A, int64_t N) {
+    return align256(sizeof(unsigned long long) * static_cast<size_t>(A->n_windows) * wcsr_nslabs(N));
 }
 
-spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
-                        void* ws, cudaStream_t s) {
-    const DeviceInfo* dev = device_info();
-    if (!dev) return SPMM_ERR_CUDA;
-    if (A->M == 0 || N == 0) return SPMM_OK;
-    WcsrArgs a{};
+SpmmWs carve_spmm(void* ws, const spmm_wcsr_t* A, int64_t N) {
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    SpmmWs w;
+    p += 256;
+    w.ticket = reinterpret_cast<unsigned long long*>(p);
+    p += wcsr_ticket_bytes(A, N);
+    w.partial = reinterpret_cast<float*>(p);
+    return w;
+}
+
+std::atomic<uint32_t> g_call_gen{0};
+
+}  // namespace
+
+size_t wcsr_spmm_ws_bytes(const spmm_wcsr_t* A, int64_t N) {
+    return 256 + wcsr_ticket_bytes(A, N) + align256(sizeof(float) * static_cast<size_t>(A->n_units) * A->h * N);
+}
+
+namespace {
+
+// L2 warm-up set shared by both kernels: the format arrays, and B when its rows
+// are not much wider than N.
+template <typename Args>
+void warmup_set(Args& a, const spmm_wcsr_t* A, const void* B, int64_t ldb, int64_t N) {
+    int n = 0;
+    auto add = [&](const void* p, int64_t bytes) {
+        if (p && bytes >= 16 && n < 10) {
+            a.pf_ptr[n] = p;
+            a.pf_bytes[n] = bytes;
+            ++n;
+        }
+    };
+    add(A->unit_win, 4 * A->n_units);
+    add(A->unit_nz_ptr, 4 * (A->n_units + 1));
+    add(A->unit_ptr, 4 * (A->n_windows + 1));
+    add(A->wcol_ptr, 4 * (A->n_windows + 1));
+    add(A->lrow, A->nnz);
+    add(A->slot, 4 * A->nnz);
+    add(A->val, 2 * A->nnz);
+    add(A->wcols, 4 * A->n_wcols);
+    if (ldb <= 2 * N && A->K * ldb * 2 <= (int64_t(64) << 20)) add(B, A->K * ldb * 2);
+    a.pf_n = n;
+}
+
+uint32_t next_gen() {
+    uint32_t gen = ++g_call_gen;
+    if (gen == 0) gen = ++g_call_gen;
+    return gen;
+}
+
+spmm_status launch_wcsr_tc(const DeviceInfo* dev, const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C,
+                           int64_t ldc, int64_t N, void* ws, cudaStream_t s) {
+    tc::Args a{};
+    a.wcol_ptr = A->wcol_ptr;
+    a.wcols = A->wcols;
+    a.unit_ptr = A->unit_ptr;
+    a.unit_win = A->unit_win;
+    a.unit_nz_ptr = A->unit_nz_ptr;
+    a.lrow = A->lrow;
+    a.slot = A->slot;
+    a.val = static_cast<const uint16_t*>(A->val);
+    a.B = static_cast<const uint16_t*>(B);
+    a.ldb = ldb;
+    a.C = C;
+    a.ldc = ldc;
+    a.M = A->M;
+    a.K = A->K;
+    a.N = N;
+    a.h = A->h;
+    a.S = A->S;
+    a.Np = (A->h + 15) / 16 * 16;
+    a.nslabs = static_cast<int32_t>(wcsr_nslabs(N));
+    a.n_windows = A->n_windows;
+    a.n_units = A->n_units;
+    a.n_items = A->n_units * a.nslabs;
+    a.b_vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 8 == 0);
+    a.idesc = ptx::idesc_f16(128, a.Np, A->dtype == SPMM_BF16, true, false, false);
+    a.gen = next_gen();
+    const SpmmWs w = carve_spmm(ws, A, N);
+    a.ticket = w.ticket;
+    a.partial = w.partial;
+    a.err = dev->err;
+    a.timeout_ns = kWaitTimeoutNs;
+    warmup_set(a, A, B, ldb, N);
+    // one CTA (four warpgroups) per SM, no more than there are items for
+    const int64_t need = (a.n_items + tc::kWG - 1) / tc::kWG;
+    const unsigned grid = static_cast<unsigned>(need < dev->sms ? need : dev->sms);
+    const int smem = tc::smem_bytes();
+    if (dev->max_smem_optin < smem) return SPMM_ERR_UNSUPPORTED;
+    if (!set_smem_attr_once(reinterpret_cast<const void*>(tc::wcsr_tc_kernel), smem, 16)) return SPMM_ERR_CUDA;
+    trace_begin(SPMM_KERNEL_WCSR, s);
+    tc::wcsr_tc_kernel<<<grid, tc::kThreads, smem, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_WCSR, s);
+    return cuda_status(e);
+}
+
+spmm_status launch_wcsr_cc(const DeviceInfo* dev, const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C,
+                           int64_t ldc, int64_t N, void* ws, cudaStream_t s) {
+    cc::WcsrArgs a{};
     a.wcol_ptr = A->wcol_ptr;
     a.wcols = A->wcols;
     a.unit_ptr = A->unit_ptr;
@@ -731,51 +1283,62 @@ spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float*
     a.K = A->K;
     a.N = N;
     a.h = A->h;
-    a.ticket = static_cast<int32_t*>(ws);
-    a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                         align256(sizeof(int32_t) * static_cast<size_t>(A->n_windows)));
+    const SpmmWs w = carve_spmm(ws, A, N);
+    a.ticket = w.ticket;
+    a.partial = w.partial;
+    a.nslabs = static_cast<int32_t>(wcsr_nslabs(N));
+    a.gen = next_gen();
     a.err = dev->err;
-    {
-        // L2 warm-up set: the format arrays, and B when its rows are not much wider than N
-        int n = 0;
-        auto add = [&](const void* p, int64_t bytes) {
-            if (p && bytes >= 16 && n < kPfArrays) {
-                a.pf_ptr[n] = p;
-                a.pf_bytes[n] = bytes;
-                ++n;
-            }
-        };
-        add(A->unit_win, 4 * A->n_units);
-        add(A->unit_nz_ptr, 4 * (A->n_units + 1));
-        add(A->unit_ptr, 4 * (A->n_windows + 1));
-        add(A->wcol_ptr, 4 * (A->n_windows + 1));
-        add(A->lrow, A->nnz);
-        add(A->slot, 4 * A->nnz);
-        add(A->val, 2 * A->nnz);
-        add(A->wcols, 4 * A->n_wcols);
-        if (ldb <= 2 * N && A->K * ldb * 2 <= (int64_t(64) << 20)) add(B, A->K * ldb * 2);
-        a.pf_n = n;
-        const int64_t wave = static_cast<int64_t>(dev->sms) * kMinBlocks;
-        a.pf_ctas = static_cast<int32_t>(A->n_units < wave ? A->n_units : wave);
-    }
+    warmup_set(a, A, B, ldb, N);
+    const int64_t wave = static_cast<int64_t>(dev->sms) * cc::kMinBlocks;
+    a.pf_ctas = static_cast<int32_t>(A->n_units < wave ? A->n_units : wave);
     a.b_vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 8 == 0) && (A->K * ldb < (int64_t(1) << 31));
     a.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (ldc % 4 == 0) && (N % 4 == 0);
     auto smem_for = [](int h) {
-        return static_cast<int>(sizeof(float) * (h * kSlab + kBnd * kSlab) + sizeof(int2) * kStage +
-                                sizeof(int) * kBnd);
+        return static_cast<int>(sizeof(float) * (h * cc::kSlab + cc::kBnd * cc::kSlab) + sizeof(int2) * cc::kStage +
+                                sizeof(int) * cc::kBnd);
     };
     const int smem = smem_for(A->h), smem_max = smem_for(kMaxH);
-    const void* kern = A->dtype == SPMM_BF16 ? reinterpret_cast<const void*>(wcsr_spmm_kernel<__nv_bfloat16>)
-                                             : reinterpret_cast<const void*>(wcsr_spmm_kernel<__half>);
+    const void* kern = A->dtype == SPMM_BF16 ? reinterpret_cast<const void*>(cc::wcsr_spmm_kernel<__nv_bfloat16>)
+                                             : reinterpret_cast<const void*>(cc::wcsr_spmm_kernel<__half>);
     if (!set_smem_attr_once(kern, smem_max, A->dtype == SPMM_BF16 ? 4 : 5)) return SPMM_ERR_CUDA;
     trace_begin(SPMM_KERNEL_WCSR, s);
     if (A->dtype == SPMM_BF16)
-        wcsr_spmm_kernel<__nv_bfloat16><<<static_cast<unsigned>(A->n_units), kThreads, smem, s>>>(a);
+        cc::wcsr_spmm_kernel<__nv_bfloat16><<<static_cast<unsigned>(A->n_units), cc::kThreads, smem, s>>>(a);
     else
-        wcsr_spmm_kernel<__half><<<static_cast<unsigned>(A->n_units), kThreads, smem, s>>>(a);
+        cc::wcsr_spmm_kernel<__half><<<static_cast<unsigned>(A->n_units), cc::kThreads, smem, s>>>(a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_WCSR, s);
     return cuda_status(e);
+}
+
+}  // namespace
+
+// When the window products run on the tensor core.  That kernel gathers each
+// B row once per window column, so it needs column reuse (several nonzeros per
+// distinct window column) to gather fewer rows than the CUDA-core kernel, which
+// gathers one per nonzero; and its time per work unit is dominated by a fixed
+// chain of dependent loads, so units must carry enough nonzeros to amortise
+// it.  Measured on GB300 (65536 x 65536, 128 columns of B): with 4 to 16
+// nonzeros per window column but 256 per unit the CUDA-core kernel is 5-13%
+// faster; with 8 to 16 per column and 512 to 1024 per unit the tensor core is
+// 1.26-1.66x faster; with ~1 per column it is 2.4x slower.
+constexpr double kTensorCoreReuse = 4.0;      // nonzeros per distinct window column
+constexpr double kTensorCoreUnitNnz = 384.0;  // nonzeros per work unit
+
+spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C, int64_t ldc, int64_t N,
+                        void* ws, cudaStream_t s) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return SPMM_ERR_CUDA;
+    if (A->M == 0 || N == 0) return SPMM_OK;
+    if (wcsr_uses_tensor_core(A)) return launch_wcsr_tc(dev, A, B, ldb, C, ldc, N, ws, s);
+    return launch_wcsr_cc(dev, A, B, ldb, C, ldc, N, ws, s);
+}
+
+bool wcsr_uses_tensor_core(const spmm_wcsr_t* A) {
+    const double nnz = static_cast<double>(A->nnz);
+    return A->n_wcols > 0 && A->n_units > 0 && nnz >= kTensorCoreReuse * static_cast<double>(A->n_wcols) &&
+           nnz >= kTensorCoreUnitNnz * static_cast<double>(A->n_units);
 }
 
 int wcsr_max_h() { return kMaxH; }

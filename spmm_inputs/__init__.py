@@ -23,6 +23,10 @@ measured on):
 * ``csr_lognormal_problem`` irregular CSR A: row lengths
   clip(round(LogNormal(ln(mean) - sigma^2/2, sigma)), 1, clip), columns
   uniform without duplicates per row (ascending), values N(0, 1); B N(0, 1).
+* ``csr_window_clustered_problem`` CSR A with column reuse inside row windows:
+  every window of h consecutive rows draws ``pool`` distinct columns uniform
+  on [0, K) and each of its rows takes ``per_row`` of them (ascending), values
+  N(0, 1); B N(0, 1).
 * ``tvw_problem``    tile-vector-wise A: per tile of ``tile_rows`` rows a
   uniform random kept subset of K columns (ascending), then inside every
   group of 4 consecutive kept columns exactly 2 positions per row hold
@@ -37,7 +41,7 @@ FP8 = (E4M3, E5M2)
 
 __all__ = [
     "BF16", "F16", "I8", "E4M3", "E5M2", "FP8", "round_f32_to_bf16_bits", "round_f32_to_fp8_bits",
-    "normal_bits", "mask24_float_problem",
+    "normal_bits", "mask24_float_problem", "csr_window_clustered_problem",
     "bcsr_problem", "mask24_problem", "csr_lognormal_problem", "tvw_problem", "slide_problem", "banded_scrambled_problem",
     "CONFIGS", "config_problem",
 ]
@@ -219,6 +223,30 @@ def csr_lognormal_problem(M: int, K: int, N: int, seed: int, mean: float = 16.0,
             "B": B, "M": M, "K": K, "N": N, "dtype": dtype}
 
 
+def csr_window_clustered_problem(M: int, K: int, N: int, seed: int, h: int = 16, pool: int = 64,
+                                 per_row: int = 16, dtype: str = F16) -> dict:
+    """CSR A whose rows, h at a time, share a column pool: each window of h
+    consecutive rows has ``pool`` distinct columns drawn uniformly from [0, K), and
+    each row takes ``per_row`` distinct columns of its window's pool (ascending);
+    values N(0,1), B (K x N) N(0,1).  A window's distinct columns then hold about
+    h * per_row / pool nonzeros each (the column reuse of matrices with locality,
+    such as meshes or graphs after a bandwidth-reducing reordering)."""
+    assert per_row <= pool <= K
+    rng = np.random.default_rng(seed)
+    nw = (M + h - 1) // h
+    cols = np.empty((M, per_row), dtype=np.int64)
+    for w in range(nw):
+        r0, r1 = w * h, min(M, (w + 1) * h)
+        pw = rng.choice(K, size=pool, replace=False)
+        pick = np.argsort(rng.random((r1 - r0, pool)), axis=1)[:, :per_row]
+        cols[r0:r1] = np.sort(pw[pick], axis=1)
+    row_ptr = np.arange(0, M * per_row + 1, per_row, dtype=np.int64)
+    val = normal_bits(rng, (M * per_row,), dtype)
+    B = normal_bits(rng, (K, N), dtype)
+    return {"row_ptr": row_ptr.astype(np.int32), "col": cols.reshape(-1).astype(np.int32), "val": val,
+            "B": B, "M": M, "K": K, "N": N, "dtype": dtype}
+
+
 def tvw_problem(M: int, K: int, N: int, tile_rows: int, keep, seed: int,
                 dtype: str = F16) -> dict:
     """Dense A (bits) in tile-vector-wise form plus the per-tile kept columns.
@@ -262,6 +290,8 @@ CONFIGS = {
     "prune_tvw_f16": dict(kind="prunetvw", M=4096, K=4096, N=0, tile_rows=128, keep=2048, seed=8, dtype=F16),
     "wcsr_lognormal": dict(kind="wcsr", M=65536, K=65536, N=128, seed=3, mean=16.0,
                            sigma=1.5, clip=4096, dtype=F16),
+    # row windows with column reuse: every 16-row window's rows take 64 of a shared pool of 128 columns
+    "wcsr_clustered": dict(kind="wcsrc", M=65536, K=65536, N=128, seed=12, h=16, pool=128, per_row=64, dtype=F16),
     "bcsr_llm": dict(kind="bcsr", M=18944, K=3584, N=65536, bh=64, bw=64, nnzb=1658, seed=4,
                      dtype=BF16, std=0.02),
     "tvw": dict(kind="tvw", M=4096, K=4096, N=4096, tile_rows=128, keep=2048, seed=5, dtype=F16),
@@ -290,6 +320,9 @@ def config_problem(name: str, **overrides) -> dict:
     if kind == "wcsr":
         return csr_lognormal_problem(c["M"], c["K"], c["N"], c["seed"], c.get("mean", 16.0),
                                      c.get("sigma", 1.5), c.get("clip", 4096), c.get("dtype", F16))
+    if kind == "wcsrc":
+        return csr_window_clustered_problem(c["M"], c["K"], c["N"], c["seed"], c.get("h", 16), c.get("pool", 64),
+                                            c.get("per_row", 16), c.get("dtype", F16))
     if kind == "tvw":
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))

@@ -82,20 +82,147 @@ def test_wcsr_builder_rejects_unsorted_columns():
     assert e.value.name == "SPMM_ERR_FORMAT"
 
 
-def test_wcsr_full_size_sampled_rows():
+def test_wcsr_full_size_every_row():
     """A 65536 x 65536 with log-normal rows (mean 16, sigma 1.5, clipped to 4096),
-    B 65536 x 128: builder bit-exact in full, SpMM checked on 4 seeded windows
-    of rows plus the longest row."""
+    B 65536 x 128: builder bit-exact in full, and every one of the 65536 x 128
+    outputs of the SpMM (all work units, split windows and the longest row
+    included) within tolerance of the oracle; a second call is bitwise equal."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     p = gen.config_problem("wcsr_lognormal")
     W, O = _build(p, 16, 32)
-    C = spmm.spmm_wcsr(W, dev_half(p["B"], "f16"))
+    B = dev_half(p["B"], "f16")
+    C = spmm.spmm_wcsr(W, B)
+    C2 = spmm.spmm_wcsr(W, B)
     torch.cuda.synchronize()
     assert spmm.last_device_error() == 0
-    longest = int(np.argmax(np.diff(p["row_ptr"])))
-    rng = np.random.default_rng(31)
-    starts = sorted(set([int(w) * 16 for w in rng.choice(p["M"] // 16, 4, replace=False)] + [longest // 16 * 16]))
-    for r0 in starts:
-        got = C[r0:r0 + 16].cpu().numpy()
-        assert_close(got, oracle.wcsr_spmm(O, p["B"], rows=(r0, r0 + 16)), f"wcsr rows {r0}..")
+    assert torch.equal(C, C2)
+    assert int(np.max(np.diff(O["unit_ptr"]))) > 1          # the workload has split windows
+    assert_close(C.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), "wcsr full size")
+
+
+def test_wcsr_workspace_needs_no_clearing():
+    """The workspace's counters carry a per-call tag: a workspace full of arbitrary
+    bytes (as a call that stopped early could leave it) gives the same, correct
+    result, twice in a row."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.csr_lognormal_problem(400, 4000, 136, seed=17, mean=12.0, sigma=2.0, clip=2048)
+    W, O = _build(p, 16, 1)                                  # S = 1: most windows split
+    B = padded_b(p["B"], "f16")
+    need = spmm.spmm_wcsr_workspace_size(W, 136)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    ws = torch.randint(0, 256, (need,), generator=g, dtype=torch.uint8, device="cuda")
+    C1 = spmm.spmm_wcsr(W, B, workspace=ws)
+    ws[:4096] = torch.randint(0, 256, (4096,), generator=g, dtype=torch.uint8, device="cuda")
+    C2 = spmm.spmm_wcsr(W, B, workspace=ws)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert torch.equal(C1, C2)
+    assert_close(C1.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), "wcsr arbitrary workspace")
+
+
+@pytest.mark.parametrize("h", [8, 40, 64])
+def test_wcsr_window_heights(h):
+    """Window heights that are not a multiple of 16 (the MMA's N is h rounded up to
+    16) and the largest supported one, with ragged N and split windows."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.csr_lognormal_problem(333, 6000, 72, seed=h, mean=10.0, sigma=1.8, clip=3000)
+    W, O = _build(p, h, 2)
+    C = spmm.spmm_wcsr(W, padded_b(p["B"], "f16"))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert_close(C.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), f"wcsr h={h}")
+
+
+def test_wcsr_bf16():
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.csr_lognormal_problem(520, 9000, 128, seed=9, mean=14.0, sigma=1.5, clip=4000, dtype="bf16")
+    W, O = _build(p, 16, 4)
+    C = spmm.spmm_wcsr(W, padded_b(p["B"], "bf16"))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert_close(C.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), "wcsr bf16")
+
+
+# ---------------------------------------------------------------- tensor-core window products
+# Operands whose windows reuse columns (at least 4 nonzeros per distinct window
+# column) and whose work units carry at least 384 nonzeros on average run their
+# window products on the tensor core.
+
+def _tensor_core_path(W):
+    return W.nnz >= 4 * W.n_wcols and W.nnz >= 384 * W.n_units
+
+@pytest.mark.parametrize("M,K,N,h,S,pool,per_row", [
+    (512, 4000, 128, 16, 32, 64, 32),      # whole windows, one slab
+    (333, 5000, 72, 16, 2, 64, 56),        # ragged last window, ragged N, S = 2: every window split in two
+    (500, 9000, 200, 32, 4, 96, 32),       # taller windows, two slabs (128 + 72 columns), splits
+    (260, 3000, 136, 8, 4, 64, 56),        # h = 8 (MMA N rounded up to 16)
+    (200, 2500, 64, 48, 32, 200, 20),      # h = 48: several chunks of W tiles per unit
+])
+def test_wcsr_tensor_core_parity(M, K, N, h, S, pool, per_row):
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.csr_window_clustered_problem(M, K, N, seed=M + h, h=h, pool=pool, per_row=per_row)
+    W, O = _build(p, h, S)
+    assert _tensor_core_path(W)
+    B = padded_b(p["B"], "f16")
+    C1 = spmm.spmm_wcsr(W, B)
+    C2 = spmm.spmm_wcsr(W, B)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert torch.equal(C1, C2)
+    assert_close(C1.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), "wcsr tensor core")
+
+
+def test_wcsr_tensor_core_bf16_and_arbitrary_workspace():
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.csr_window_clustered_problem(640, 7000, 128, seed=3, h=16, pool=64, per_row=56, dtype="bf16")
+    W, O = _build(p, 16, 2)
+    assert _tensor_core_path(W)
+    need = spmm.spmm_wcsr_workspace_size(W, 128)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    ws = torch.randint(0, 256, (need,), generator=g, dtype=torch.uint8, device="cuda")
+    C = spmm.spmm_wcsr(W, padded_b(p["B"], "bf16"), workspace=ws)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert_close(C.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), "wcsr tensor core bf16")
+
+
+def test_wcsr_tensor_core_bad_slot_is_skipped_and_reported():
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.csr_window_clustered_problem(256, 3000, 128, seed=5, h=16, pool=64, per_row=32)
+    W, O = _build(p, 16, 32)
+    assert _tensor_core_path(W)
+    spmm.last_device_error()
+    W.slot[0] = 1 << 30                    # first entry of window 0 points past its column list
+    C = spmm.spmm_wcsr(W, padded_b(p["B"], "f16"))
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() & 2
+    got = C.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert_close(got[16:], oracle.wcsr_spmm(O, p["B"])[16:], "wcsr tensor core other windows")
+
+
+def test_wcsr_clustered_full_size_every_row():
+    """The clustered workload at its benchmarked size (65536 x 65536, 16-row windows
+    whose rows take 64 of 128 shared columns, B 65536 x 128): every output within
+    tolerance, bitwise equal across two calls."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.config_problem("wcsr_clustered")
+    W, O = _build(p, 16, 32)
+    assert _tensor_core_path(W)
+    B = dev_half(p["B"], "f16")
+    C = spmm.spmm_wcsr(W, B)
+    C2 = spmm.spmm_wcsr(W, B)
+    torch.cuda.synchronize()
+    assert spmm.last_device_error() == 0
+    assert torch.equal(C, C2)
+    assert_close(C.cpu().numpy(), oracle.wcsr_spmm(O, p["B"]), "wcsr clustered full size")
