@@ -765,11 +765,18 @@ int orc_rcm(int64_t n, const int32_t *row_ptr, const int32_t *col, int32_t *perm
     int32_t *order = malloc(sizeof(int32_t) * (size_t)n);
     int32_t *nb = malloc(sizeof(int32_t) * (size_t)n);
     uint8_t *seen = calloc((size_t)n, 1);
-    if (!adj || !deg || !order || !nb || !seen) return ORC_ERR_SHAPE;
+    int rc = ORC_OK;
+    if (!adj || !deg || !order || !nb || !seen) {
+        rc = ORC_ERR_SHAPE;
+        goto done;
+    }
     for (int64_t i = 0; i < n; i++)
         for (int32_t e = row_ptr[i]; e < row_ptr[i + 1]; e++) {
             int64_t j = col[e];
-            if (j < 0 || j >= n) return ORC_ERR_FORMAT;
+            if (j < 0 || j >= n) {
+                rc = ORC_ERR_FORMAT;
+                goto done;
+            }
             if (j != i) adj[i * n + j] = adj[j * n + i] = 1;
         }
     for (int64_t i = 0; i < n; i++)
@@ -794,12 +801,13 @@ int orc_rcm(int64_t n, const int32_t *row_ptr, const int32_t *col, int32_t *perm
         }
     }
     for (int64_t i = 0; i < n; i++) perm[i] = order[n - 1 - i];
+done:
     free(adj);
     free(deg);
     free(order);
     free(nb);
     free(seen);
-    return ORC_OK;
+    return rc;
 }
 
 /* A'[i][j] = A[perm[i]][perm[j]] (n x n, leading dims ld / n). */
