@@ -65,6 +65,7 @@ KERNEL_SOURCES = {
     "sparse_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/spmm24.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "bcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/bcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "wcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
+    "wcsr_tc_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "sddmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/sddmm.cu",),
 }
 
@@ -555,12 +556,13 @@ def run_extra(name, args, ws, peaks, flush_buf):
         # the library's rule: tensor core when >= 4 nonzeros per window column and >= 384 per work unit
         tcore = F.nnz >= 4 * F.n_wcols and F.nnz >= 384 * F.n_units
         extra_fields["window_products"] = "tensor core" if tcore else "CUDA cores"
+        wkern = "wcsr_tc_kernel" if tcore else "wcsr_spmm_kernel"
         Cd = torch.empty((c["M"], c["N"]), dtype=torch.float32, device="cuda")
         wsp = torch.zeros(max(1, spmm.spmm_wcsr_workspace_size(F, c["N"])), dtype=torch.uint8, device="cuda")
         nnz = csr.nnz
         # CSR-equivalent stored A (row_ptr, col, val) + B read once + C written once
         alg = (c["M"] + 1) * 4 + nnz * 4 + nnz * 2 + c["K"] * c["N"] * 2 + c["M"] * c["N"] * 4
-        kern, kid = "wcsr_spmm_kernel", spmm._lib.KERNEL_WCSR
+        kern, kid = wkern, spmm._lib.KERNEL_WCSR
 
         def step():
             spmm.spmm_wcsr(F, Bx, Cd, wsp)
