@@ -94,6 +94,7 @@ def lib():
         L.orc_rcm.argtypes = [I64, P, P, P]
         L.orc_permute_sym.argtypes = [I64, I64, I32, P, P, P]
         L.orc_sddmm.argtypes = [I64, I64, I32, P, P, P, P, P]
+        L.orc_sddmm_i64.argtypes = [I64, I64, P, P, P, P, P]
         L.orc_spmm24_f64.argtypes = [I64, I64, I32, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_spmm24_i64.argtypes = [I64, I64, P, P, P, I64, I64, I64, P, I64, P]
         L.orc_tvw_build.restype = I32
@@ -464,4 +465,18 @@ def sddmm(row_ptr, col, A, Bt, dtype):
         raise OracleError("sddmm shape error")
     out = np.zeros(int(row_ptr[-1]), dtype=np.float64)
     lib().orc_sddmm(M, K, DTYPES[dtype], _p(row_ptr), _p(col), _p(A), _p(Bt), _p(out))
+    return out
+
+
+def sddmm_i64(row_ptr, col, A, Bt):
+    """int8 A, Bt: out[e] = sum_k A[i][k] Bt[j][k] for every stored (i, j), exact (int64)."""
+    row_ptr = _c(row_ptr, np.int32)
+    col = _c(col, np.int32)
+    A = _c(A, np.int8)
+    Bt = _c(Bt, np.int8)
+    M, K = A.shape
+    if Bt.shape[1] != K or row_ptr.shape[0] != M + 1:
+        raise OracleError("sddmm shape error")
+    out = np.zeros(int(row_ptr[-1]), dtype=np.int64)
+    lib().orc_sddmm_i64(M, K, _p(row_ptr), _p(col), _p(A), _p(Bt), _p(out))
     return out

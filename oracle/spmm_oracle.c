@@ -834,3 +834,18 @@ void orc_sddmm(int64_t M, int64_t K, int dtype, const int32_t *row_ptr, const in
             out[e] = s;
         }
 }
+
+/* The quantized SDDMM ("Magicube", abstract: SpMM and SDDMM on low-precision
+ * integers): int8 A and Bt, every product and sum in int64, so out[e] is the
+ * exact integer sum_k A[i][k] * Bt[j][k] at every stored (i, j). */
+void orc_sddmm_i64(int64_t M, int64_t K, const int32_t *row_ptr, const int32_t *col, const int8_t *A,
+                   const int8_t *Bt, int64_t *out) {
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < M; i++)
+        for (int32_t e = row_ptr[i]; e < row_ptr[i + 1]; e++) {
+            int64_t j = col[e];
+            int64_t s = 0;
+            for (int64_t k = 0; k < K; k++) s += (int64_t)A[i * K + k] * (int64_t)Bt[j * K + k];
+            out[e] = s;
+        }
+}

@@ -631,6 +631,44 @@ def test_sddmm_golden():
     assert out.tolist() == g["out"]
 
 
+def test_sddmm_i64_golden():
+    """The exact int8 SDDMM on the hand-worked fixture (its operands are int8)."""
+    g = golden("sddmm_int8_3x4.json")
+    out = oracle.sddmm_i64(np.array(g["row_ptr"]), np.array(g["col"]), np.array(g["A"], np.int8),
+                           np.array(g["Bt"], np.int8))
+    assert out.dtype == np.int64 and out.tolist() == g["out"]
+
+
+def test_sddmm_i64_is_the_integer_product_at_the_pattern():
+    """Full-range int8 operands: every output equals the entry of the int64 product
+    A Bt^T (numpy) at its position; an emptied row and a non-square pattern
+    (M != N) catch a dropped row offset or a transposed operand."""
+    q = gen.csr_lognormal_problem(70, 41, 1, seed=9, mean=6.0, sigma=1.0, clip=41, dtype="f16")
+    rows = np.repeat(np.arange(70), np.diff(q["row_ptr"]))
+    keep = rows != 11
+    rp = np.concatenate([[0], np.cumsum(np.bincount(rows[keep], minlength=70))]).astype(np.int32)
+    cl = q["col"][keep].astype(np.int32)
+    rng = np.random.default_rng(2)
+    A = rng.integers(-128, 128, size=(70, 48), dtype=np.int8)
+    Bt = rng.integers(-128, 128, size=(41, 48), dtype=np.int8)
+    D = A.astype(np.int64) @ Bt.astype(np.int64).T
+    out = oracle.sddmm_i64(rp, cl, A, Bt)
+    assert np.array_equal(out, D[rows[keep], cl])
+    assert rp[11] == rp[12]
+
+
+@pytest.mark.parametrize("a,b", [(-128, -128), (-128, 127), (127, 127)])
+def test_sddmm_i64_extreme_values(a, b):
+    """Constant operands give the closed form K * a * b at every entry (K = 4096:
+    |sum| up to 2^26, well inside int64 and still exact in int32)."""
+    K = 4096
+    rp = np.array([0, 3, 3, 5], np.int32)
+    cl = np.array([0, 2, 4, 1, 3], np.int32)
+    A = np.full((3, K), a, np.int8)
+    Bt = np.full((5, K), b, np.int8)
+    assert oracle.sddmm_i64(rp, cl, A, Bt).tolist() == [K * a * b] * 5
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_sddmm_is_the_dense_product_at_the_pattern(dtype):
     """Every output equals the entry of the dense product A Bt^T (numpy, fp64) at its
