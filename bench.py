@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 METRIC = "SpMM effective TFLOP/s (2·nnz·N/time) and % of roofline, per sparse format"
 HEADLINE = "mask24_int8"
 EXTRA_WORKLOADS = ("bcsr_llm", "tvw", "wcsr_lognormal", "wcsr_clustered", "mask24_f16", "mask24_e4m3", "slide68_f16", "bcsr_rcm",
-                   "sddmm_lognormal", "prune24_f16", "prune_tvw_f16", "bcsr_tiny")
+                   "sddmm_lognormal", "sddmm_lognormal_i8", "prune24_f16", "prune_tvw_f16", "bcsr_tiny")
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -414,18 +414,22 @@ def run_extra(name, args, ws, peaks, flush_buf):
         def step():
             spmm.spmm_24(F, Bx, Cd, wsp)
     elif c["kind"] == "sddmm":
-        # sampled dense-dense product on the row-window workload's CSR pattern, A and Bt N(0,1) fp16
+        # sampled dense-dense product on the row-window workload's CSR pattern: A and Bt N(0,1) fp16
+        # (fp32 out), or uniform int8 (exact int32 out)
         p = gen.config_problem(name)
-        dt = torch.float16
-        S = spmm.CSR(c["M"], c["K"], int(p["row_ptr"][-1]), dt, to_dev(p["row_ptr"]), to_dev(p["col"]),
-                     to_dev(p["val"], dt))
-        Ax, Btx = to_dev(p["A"], dt), to_dev(p["Bt"], dt)
-        out_d = torch.empty(S.nnz, dtype=torch.float32, device="cuda")
+        i8 = c["dtype"] == "i8"
+        dt = torch.int8 if i8 else torch.float16
+        val = torch.zeros(int(p["row_ptr"][-1]), dtype=torch.int8, device="cuda") if i8 else to_dev(p["val"], dt)
+        S = spmm.CSR(c["M"], c["K"], int(p["row_ptr"][-1]), dt, to_dev(p["row_ptr"]), to_dev(p["col"]), val)
+        Ax, Btx = (torch.from_numpy(p["A"]).cuda(), torch.from_numpy(p["Bt"]).cuda()) if i8 else \
+            (to_dev(p["A"], dt), to_dev(p["Bt"], dt))
+        out_d = torch.empty(S.nnz, dtype=torch.int32 if i8 else torch.float32, device="cuda")
         build_ms = 0.0
         nnz = S.nnz
         K_in = c["inner"]
-        # pattern (row_ptr, col), A and Bt read once, one fp32 per entry written
-        alg = (c["M"] + 1) * 4 + nnz * 4 + c["M"] * K_in * 2 + c["K"] * K_in * 2 + nnz * 4
+        es = 1 if i8 else 2
+        # pattern (row_ptr, col), A and Bt read once, one fp32 / int32 per entry written
+        alg = (c["M"] + 1) * 4 + nnz * 4 + c["M"] * K_in * es + c["K"] * K_in * es + nnz * 4
         kern, kid = "sddmm_kernel", spmm._lib.KERNEL_SDDMM
         extra_fields["inner"] = K_in
 
@@ -700,7 +704,10 @@ def cpu_baseline_extra(name, target_s=2.0):
         rp, col = p["row_ptr"], p["col"]
 
         def run(r):
-            oracle.sddmm(rp[:r + 1], col[:int(rp[r])], p["A"][:r], p["Bt"], c["dtype"])
+            if c["dtype"] == "i8":
+                oracle.sddmm_i64(rp[:r + 1], col[:int(rp[r])], p["A"][:r], p["Bt"])
+            else:
+                oracle.sddmm(rp[:r + 1], col[:int(rp[r])], p["A"][:r], p["Bt"], c["dtype"])
         r, dt = _time_rows(run, c["M"], 256, target_s)
         flops = 2.0 * int(rp[r]) * c["inner"]
         sample = f"pattern rows 0..{r - 1} of {c['M']}, inner dimension {c['inner']}"

@@ -103,7 +103,7 @@ typedef struct {
  * strictly ascending inside a row, val[nnz]. */
 typedef struct {
     int64_t M, K, nnz;
-    int32_t dtype; /* SPMM_F16 or SPMM_BF16 */
+    int32_t dtype; /* SPMM_F16 or SPMM_BF16; SPMM_I8 as the pattern of an int8 spmm_sddmm */
     int32_t *row_ptr;
     int32_t *col;
     void *val;
@@ -376,18 +376,23 @@ SPMM_API spmm_status spmm_build_slide(const void *dense, int64_t M, int64_t K, i
 
 /* ---------------------------------------------------------------- SDDMM
  * The sampled dense-dense product, the second sparse operation of "Magicube"
- * (abstract: SpMM and SDDMM).  out[e] = sum_k A[i][k] * Bt[j][k] for every
- * stored entry e = (i, j) of the CSR pattern S, i.e. (A B) at the pattern's
- * positions with B given transposed as Bt.  S->M rows, S->K columns (= rows of
- * Bt), S->nnz entries; S->dtype (SPMM_F16 or SPMM_BF16) is the type of A and
- * Bt; S->val is not read.  A is S->M x K (row pitch lda), Bt is S->K x K (row
- * pitch ldbt), both device arrays, 16-byte aligned with lda, ldbt and K
- * multiples of 8 (else SPMM_ERR_SHAPE).  out[S->nnz] is fp32 in pattern order.
- * Products are summed in fp32.  A column outside [0, S->K) sets
+ * (abstract: SpMM and SDDMM on low-precision, quantized integers).  out[e] =
+ * sum_k A[i][k] * Bt[j][k] for every stored entry e = (i, j) of the CSR
+ * pattern S, i.e. (A B) at the pattern's positions with B given transposed as
+ * Bt.  S->M rows, S->K columns (= rows of Bt), S->nnz entries; S->val is not
+ * read.  S->dtype is the type of A and Bt:
+ *   SPMM_F16 / SPMM_BF16: out is fp32, products summed in fp32; K, lda and
+ *     ldbt multiples of 8;
+ *   SPMM_I8: out is int32 and exact (products of signed bytes summed in int32;
+ *     K * 16384 < 2^31, so no sum can overflow); K, lda and ldbt multiples of 16.
+ * A is S->M x K (row pitch lda elements), Bt is S->K x K (row pitch ldbt), both
+ * device arrays, 16-byte aligned; out[S->nnz] in pattern order, device memory,
+ * owned by the caller.  A bad shape, pitch or alignment -> SPMM_ERR_SHAPE, any
+ * other dtype -> SPMM_ERR_DTYPE.  A column outside [0, S->K) sets
  * SPMM_DEVERR_INDEX and writes 0; row_ptr is read within [0, S->M].
  * Asynchronous on `stream`. */
 SPMM_API spmm_status spmm_sddmm(const spmm_csr_t *S, int64_t K, const void *A, int64_t lda, const void *Bt,
-                                int64_t ldbt, float *out, spmm_stream_t stream);
+                                int64_t ldbt, void *out, spmm_stream_t stream);
 
 /* ---------------------------------------------------------------- permutation
  * Permuting a square sparse matrix to cut its nonzero blocks before the

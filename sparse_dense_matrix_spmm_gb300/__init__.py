@@ -247,11 +247,13 @@ def spmm_bcsr(A: BCSR, B: torch.Tensor, C_: Optional[torch.Tensor] = None, strea
 # ------------------------------------------------------------------ SDDMM
 def spmm_sddmm(S: CSR, A: torch.Tensor, Bt: torch.Tensor, out: Optional[torch.Tensor] = None,
                stream=None) -> torch.Tensor:
-    """out[e] = A[i] . Bt[j] for every stored (i, j) of the CSR pattern S (fp32, pattern order)."""
+    """out[e] = A[i] . Bt[j] for every stored (i, j) of the CSR pattern S, in pattern
+    order: fp32 for fp16/bf16 operands, exact int32 for int8 (S.dtype torch.int8)."""
     _check_dev(A, Bt, out)
     K = A.shape[1]
     if out is None:
-        out = torch.empty(S.nnz, dtype=torch.float32, device=A.device)
+        odt = torch.int32 if S.dtype == torch.int8 else torch.float32
+        out = torch.empty(S.nnz, dtype=odt, device=A.device)
     s = S.c()
     _lib.call("spmm_sddmm", C.byref(s), K, _ptr(A), A.stride(0), _ptr(Bt), Bt.stride(0), _ptr(out), _stream(stream))
     return out

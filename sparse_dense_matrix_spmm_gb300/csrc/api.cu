@@ -293,11 +293,15 @@ spmm_status spmm_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float* C
 // ---------------------------------------------------------------- SDDMM
 
 spmm_status spmm_sddmm(const spmm_csr_t* S, int64_t K, const void* A, int64_t lda, const void* Bt, int64_t ldbt,
-                       float* out, spmm_stream_t stream) {
+                       void* out, spmm_stream_t stream) {
     if (!S) return SPMM_ERR_NULL;
-    if (S->dtype != SPMM_BF16 && S->dtype != SPMM_F16) return SPMM_ERR_DTYPE;
-    if (S->M < 0 || S->K < 0 || S->nnz < 0 || K <= 0 || K % 8 || lda < K || ldbt < K || lda % 8 || ldbt % 8)
+    if (S->dtype != SPMM_BF16 && S->dtype != SPMM_F16 && S->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    // one 16-byte load covers 8 16-bit or 16 int8 elements
+    const int64_t e = S->dtype == SPMM_I8 ? 16 : 8;
+    if (S->M < 0 || S->K < 0 || S->nnz < 0 || K <= 0 || K % e || lda < K || ldbt < K || lda % e || ldbt % e)
         return SPMM_ERR_SHAPE;
+    // int8: every sum is exact in int32 while K * 128 * 128 < 2^31
+    if (S->dtype == SPMM_I8 && K * 16384 >= (int64_t(1) << 31)) return SPMM_ERR_SHAPE;
     if (S->nnz == 0) return SPMM_OK;
     if (!S->row_ptr || !S->col || !A || !Bt || !out) return SPMM_ERR_NULL;
     if (S->M == 0 || !aligned16(A) || !aligned16(Bt)) return SPMM_ERR_SHAPE;

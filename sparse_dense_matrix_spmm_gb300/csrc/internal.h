@@ -106,7 +106,7 @@ spmm_status run_build_slide(const void* dense, int64_t M, int64_t K, int64_t ld,
                             void* vals, uint8_t* meta, cudaStream_t s);
 
 spmm_status launch_sddmm(const spmm_csr_t* S, int64_t K, const void* A, int64_t lda, const void* Bt, int64_t ldbt,
-                         float* out, cudaStream_t s);
+                         void* out, cudaStream_t s);
 spmm_status rcm_order_host(int64_t n, const int32_t* row_ptr, const int32_t* col, int32_t* perm);
 spmm_status run_permute_rows(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t rows, int64_t cols,
                              int32_t elem_bytes, const int32_t* perm, bool scatter, int* err, cudaStream_t s);

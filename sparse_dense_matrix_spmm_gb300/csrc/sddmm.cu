@@ -1,6 +1,8 @@
 // sddmm.cu -- sampled dense-dense product, the second sparse operation of
-// "Magicube" (abstract: SpMM and SDDMM): out[e] = sum_k A[i][k] * Bt[j][k] for
-// every stored entry e = (i, j) of a CSR pattern, fp16/bf16 in, fp32 out.
+// "Magicube" (abstract: SpMM and SDDMM on low-precision integers): out[e] =
+// sum_k A[i][k] * Bt[j][k] for every stored entry e = (i, j) of a CSR pattern;
+// fp16/bf16 in with fp32 out, or int8 in with exact int32 out (four-way byte
+// dot products, dp4a, summed in int32).
 //
 // A dot product of two contiguous K-vectors per output: HBM- and
 // gather-bound work for CUDA cores, not a contraction for the tensor core.
@@ -8,9 +10,10 @@
 // serialise on one warp), finds the slice's first row by binary search in
 // row_ptr (a dependent chain of about log2(M) loads, so slices are long), and
 // preloads the slice's (row, column) pairs with coalesced loads into shared
-// memory, where the lane groups read them.  L = min(32, K / 8) lanes form one
-// output's group: each lane loads 8 elements (16 bytes) of A's row and of Bt's
-// row per step, and the group sums by shuffles.  Each lane keeps ILP outputs in
+// memory, where the lane groups read them.  L = min(32, K / E) lanes form one
+// output's group: each lane loads E elements (16 bytes: E = 8 for 16-bit
+// types, 16 for int8) of A's row and of Bt's row per step, and the group sums
+// by shuffles.  Each lane keeps ILP outputs in
 // flight to hide the latency of the Bt row gathers.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,20 +55,47 @@ __device__ __forceinline__ float dot8<__nv_bfloat16>(uint4 a, uint4 b) {
     return s;
 }
 
+// int8: sixteen signed byte products per 16-byte pair, four per dp4a, summed
+// in int32 (exact: |sum| <= K * 16384 < 2^31, checked on the host).
+__device__ __forceinline__ int dot16_i8(uint4 a, uint4 b) {
+    int s = 0;
+    s = __dp4a(static_cast<int>(a.x), static_cast<int>(b.x), s);
+    s = __dp4a(static_cast<int>(a.y), static_cast<int>(b.y), s);
+    s = __dp4a(static_cast<int>(a.z), static_cast<int>(b.z), s);
+    s = __dp4a(static_cast<int>(a.w), static_cast<int>(b.w), s);
+    return s;
+}
+
+// Per element type: elements per 16-byte load, accumulator / output type.
+template <typename T>
+struct Sd {
+    static constexpr int E = 8;
+    using Acc = float;
+    __device__ static Acc dot(uint4 a, uint4 b) { return dot8<T>(a, b); }
+};
+template <>
+struct Sd<int8_t> {
+    static constexpr int E = 16;
+    using Acc = int;
+    __device__ static Acc dot(uint4 a, uint4 b) { return dot16_i8(a, b); }
+};
+
 struct SddmmArgs {
     const int32_t* row_ptr;
     const int32_t* col;
     int64_t M, N, K, nnz;
-    const uint16_t* A;
+    const uint8_t* A;   // element pitch lda, elements of the kernel's type
     int64_t lda;
-    const uint16_t* Bt;
+    const uint8_t* Bt;
     int64_t ldb;
-    float* out;
+    void* out;          // fp32, or int32 for int8
     int* err;
 };
 
 template <typename T, int L>
 __global__ void __launch_bounds__(kThreads) sddmm_kernel(const SddmmArgs a) {
+    using Acc = typename Sd<T>::Acc;
+    constexpr int E = Sd<T>::E;
     constexpr int G = 32 / L;                   // outputs per warp per pass
     constexpr int kPer = G * kIlp;              // entries per pass
     constexpr int kSlice = kPer * kPasses;      // entries per warp
@@ -123,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) sddmm_kernel(const SddmmArgs a) {
         const int64_t last_row = __shfl_sync(0xffffffffu, row, 31);
         rb = last_row >= 0 ? last_row : rb;
     }
-    float* __restrict__ out = a.out;
+    Acc* __restrict__ out = static_cast<Acc*>(a.out);
     __syncwarp();  // the slice's pairs are in shared memory for every lane
     auto fetch = [&](int p, int32_t (&jj)[kIlp], int32_t (&ri)[kIlp], bool (&ok)[kIlp]) {
 #pragma unroll
@@ -136,36 +166,36 @@ __global__ void __launch_bounds__(kThreads) sddmm_kernel(const SddmmArgs a) {
             if (live && !ok[u] && sl == 0) atomicOr(a.err, SPMM_DEVERR_INDEX);
         }
     };
-    auto finish = [&](int p, float (&acc)[kIlp], const bool (&ok)[kIlp]) {
+    auto finish = [&](int p, Acc (&acc)[kIlp], const bool (&ok)[kIlp]) {
 #pragma unroll
         for (int u = 0; u < kIlp; ++u) {
 #pragma unroll
             for (int o = L / 2; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
             const int64_t e = e0 + p * kPer + u * G + sub;
-            if (sl == 0 && e < e1) out[e] = ok[u] ? acc[u] : 0.f;
+            if (sl == 0 && e < e1) out[e] = ok[u] ? acc[u] : Acc(0);
         }
     };
 #pragma unroll 1
     for (int p = 0; p < kPasses; ++p) {
         int32_t jj[kIlp], ri[kIlp];
         bool ok[kIlp];
-        float acc[kIlp];
+        Acc acc[kIlp];
         fetch(p, jj, ri, ok);
 #pragma unroll
-        for (int u = 0; u < kIlp; ++u) acc[u] = 0.f;
-        for (int64_t k0 = 0; k0 < a.K; k0 += 8 * L) {
-            const int64_t k = k0 + 8 * sl;
+        for (int u = 0; u < kIlp; ++u) acc[u] = Acc(0);
+        for (int64_t k0 = 0; k0 < a.K; k0 += E * L) {
+            const int64_t k = k0 + E * sl;
             if (k >= a.K) continue;
             uint4 x[kIlp], y[kIlp];
 #pragma unroll
             for (int u = 0; u < kIlp; ++u)
                 if (ok[u]) {
-                    x[u] = __ldg(reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(ri[u]) * a.lda + k));
-                    y[u] = __ldg(reinterpret_cast<const uint4*>(a.Bt + static_cast<int64_t>(jj[u]) * a.ldb + k));
+                    x[u] = __ldg(reinterpret_cast<const uint4*>(a.A + (static_cast<int64_t>(ri[u]) * a.lda + k) * sizeof(T)));
+                    y[u] = __ldg(reinterpret_cast<const uint4*>(a.Bt + (static_cast<int64_t>(jj[u]) * a.ldb + k) * sizeof(T)));
                 }
 #pragma unroll
             for (int u = 0; u < kIlp; ++u)
-                if (ok[u]) acc[u] += dot8<T>(x[u], y[u]);
+                if (ok[u]) acc[u] += Sd<T>::dot(x[u], y[u]);
         }
         finish(p, acc, ok);
     }
@@ -181,7 +211,7 @@ void launch_lanes(const SddmmArgs& a, int lanes, unsigned grid, cudaStream_t s) 
 }  // namespace
 
 spmm_status launch_sddmm(const spmm_csr_t* S, int64_t K, const void* A, int64_t lda, const void* Bt, int64_t ldbt,
-                         float* out, cudaStream_t s) {
+                         void* out, cudaStream_t s) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
     if (S->nnz == 0) return SPMM_OK;
@@ -192,20 +222,23 @@ spmm_status launch_sddmm(const spmm_csr_t* S, int64_t K, const void* A, int64_t 
     a.N = S->K;
     a.K = K;
     a.nnz = S->nnz;
-    a.A = static_cast<const uint16_t*>(A);
+    a.A = static_cast<const uint8_t*>(A);
     a.lda = lda;
-    a.Bt = static_cast<const uint16_t*>(Bt);
+    a.Bt = static_cast<const uint8_t*>(Bt);
     a.ldb = ldbt;
     a.out = out;
     a.err = dev->err;
-    // lanes per output: one 16-byte load each covers 8 elements of K
-    const int lanes = K >= 256 ? 32 : (K >= 128 ? 16 : 8);
+    // lanes per output: one 16-byte load each covers E elements of K
+    const int E = S->dtype == SPMM_I8 ? 16 : 8;
+    const int lanes = K >= 32 * E ? 32 : (K >= 16 * E ? 16 : 8);
     const int64_t slice = static_cast<int64_t>(32 / lanes) * kIlp * kPasses;
     const int64_t warps = (S->nnz + slice - 1) / slice;
     const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks >= (int64_t(1) << 31)) return SPMM_ERR_UNSUPPORTED;
     trace_begin(SPMM_KERNEL_SDDMM, s);
-    if (S->dtype == SPMM_BF16)
+    if (S->dtype == SPMM_I8)
+        launch_lanes<int8_t>(a, lanes, static_cast<unsigned>(blocks), s);
+    else if (S->dtype == SPMM_BF16)
         launch_lanes<__nv_bfloat16>(a, lanes, static_cast<unsigned>(blocks), s);
     else
         launch_lanes<__half>(a, lanes, static_cast<unsigned>(blocks), s);

@@ -298,6 +298,9 @@ CONFIGS = {
     # SDDMM on the row-window workload's pattern: A, Bt 65536 x 128 (a sparse attention score)
     "sddmm_lognormal": dict(kind="sddmm", M=65536, K=65536, N=0, inner=128, seed=3, mean=16.0, sigma=1.5,
                             clip=4096, dtype=F16),
+    # the same pattern with quantized operands: A, Bt 65536 x 128 int8, uniform over [-128, 127]
+    "sddmm_lognormal_i8": dict(kind="sddmm", M=65536, K=65536, N=0, inner=128, seed=3, mean=16.0, sigma=1.5,
+                               clip=4096, dtype=I8),
     # a scrambled band (half-width 48) before and after RCM, 64 x 64 blocks
     "bcsr_rcm": dict(kind="rcm", M=16384, K=16384, N=2048, w=48, bh=64, bw=64, seed=10, dtype=F16),
     # 6:8 on a Qwen2.5-7B-sized FFN projection (18944 x 3584), 8192 tokens
@@ -327,11 +330,18 @@ def config_problem(name: str, **overrides) -> dict:
         return tvw_problem(c["M"], c["K"], c["N"], c["tile_rows"], c["keep"], c["seed"],
                            c.get("dtype", F16))
     if kind == "sddmm":  # the CSR pattern of csr_lognormal_problem, then A (M x inner) and Bt (K x inner)
+        dt = c.get("dtype", F16)
+        # int8 operands share the fp16 workload's pattern (same seed, same draws)
         p = csr_lognormal_problem(c["M"], c["K"], 1, c["seed"], c.get("mean", 16.0), c.get("sigma", 1.5),
-                                  c.get("clip", 4096), c.get("dtype", F16))
+                                  c.get("clip", 4096), F16 if dt == I8 else dt)
         rng = np.random.default_rng(c["seed"] + 1000)
-        p["A"] = normal_bits(rng, (c["M"], c["inner"]), c.get("dtype", F16))
-        p["Bt"] = normal_bits(rng, (c["K"], c["inner"]), c.get("dtype", F16))
+        if dt == I8:
+            p["A"] = rng.integers(-128, 128, size=(c["M"], c["inner"]), dtype=np.int8)
+            p["Bt"] = rng.integers(-128, 128, size=(c["K"], c["inner"]), dtype=np.int8)
+            p["dtype"] = I8
+        else:
+            p["A"] = normal_bits(rng, (c["M"], c["inner"]), dt)
+            p["Bt"] = normal_bits(rng, (c["K"], c["inner"]), dt)
         del p["B"]
         return p
     if kind == "rcm":

@@ -122,7 +122,11 @@ def test_sddmm_validation():
     S = _lib.CsrT(64, 64, 10, 1, 16, 16, 16)
     assert L.spmm_sddmm(ctypes.byref(S), 12, 16, 16, 16, 16, 16, None) == 2      # K % 8 != 0
     assert L.spmm_sddmm(ctypes.byref(S), 16, 16, 8, 16, 16, 16, None) == 2       # lda < K
-    S8 = _lib.CsrT(64, 64, 10, 2, 16, 16, 16)
-    assert L.spmm_sddmm(ctypes.byref(S8), 16, 16, 16, 16, 16, 16, None) == 3     # int8 -> SPMM_ERR_DTYPE
+    S8 = _lib.CsrT(64, 64, 10, 2, 16, 16, 16)                                    # int8: 16-element steps
+    assert L.spmm_sddmm(ctypes.byref(S8), 8, 16, 8, 16, 8, 16, None) == 2        # K % 16 != 0
+    assert L.spmm_sddmm(ctypes.byref(S8), 32, 16, 40, 16, 32, 16, None) == 2     # lda % 16 != 0
+    assert L.spmm_sddmm(ctypes.byref(S8), 131072, 16, 131072, 16, 131072, 16, None) == 2  # K * 16384 >= 2^31
+    SF = _lib.CsrT(64, 64, 10, 3, 16, 16, 16)
+    assert L.spmm_sddmm(ctypes.byref(SF), 16, 16, 16, 16, 16, 16, None) == 3     # fp8 -> SPMM_ERR_DTYPE
     E = _lib.CsrT(64, 64, 0, 1, None, None, None)
     assert L.spmm_sddmm(ctypes.byref(E), 16, None, 16, None, 16, None, None) == 0  # no entries: nothing to do

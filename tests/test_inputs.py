@@ -79,3 +79,13 @@ def test_sddmm_config_shares_the_row_window_pattern():
     assert np.array_equal(q["row_ptr"], w["row_ptr"]) and np.array_equal(q["col"], w["col"])
     assert q["A"].shape == (512, 16) and q["Bt"].shape == (512, 16) and c["inner"] == 128
     assert "B" not in q
+
+
+def test_sddmm_i8_config_shares_the_pattern_with_full_range_int8():
+    """The quantized SDDMM workload has the fp16 workload's pattern and int8
+    operands covering the whole range [-128, 127]."""
+    q = gen.config_problem("sddmm_lognormal_i8", M=512, K=512, inner=64)
+    f = gen.config_problem("sddmm_lognormal", M=512, K=512, inner=64)
+    assert np.array_equal(q["row_ptr"], f["row_ptr"]) and np.array_equal(q["col"], f["col"])
+    assert q["A"].dtype == np.int8 and q["Bt"].dtype == np.int8 and q["dtype"] == "i8"
+    assert q["A"].min() == -128 and q["A"].max() == 127
