@@ -40,6 +40,13 @@ HEADLINE = "mask24_int8"
 EXTRA_WORKLOADS = ("bcsr_llm", "tvw", "wcsr_lognormal", "wcsr_clustered", "mask24_f16", "mask24_e4m3", "slide68_f16", "bcsr_rcm",
                    "sddmm_lognormal", "sddmm_lognormal_i8", "prune24_f16", "prune_tvw_f16", "bcsr_tiny")
 FLUSH_BYTES = 256 << 20
+# L2 -> SM gather ceiling (GB/s): 256-byte rows read at random row indices from a
+# 24 MB L2-resident buffer, half-warp per row, 64 warps per SM, four rows in
+# flight per half-warp; measured on this machine's GB300 (21.0 TB/s; streaming
+# 16-byte loads over the same buffer reached 15.5 TB/s).  The gathering kernels
+# (TVW's kept B rows, row-window and SDDMM rows) are reported against it beside
+# their HBM / tensor roofline.
+L2_GATHER_GBS = 21000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -342,6 +349,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
     g = torch.Generator(device="cuda")
     g.manual_seed(int(c["seed"]))
     extra_fields = {}
+    gathered = 0  # bytes a launch gathers from L2 row by row (reported against L2_GATHER_GBS)
     peak_scale = 1.0
     if c["kind"] == "bcsr":
         p = gen.bcsr_problem(c["M"], c["K"], 8, c["bh"], c["bw"], c["nnzb"], c["seed"], c["dtype"], c["std"])
@@ -378,6 +386,8 @@ def run_extra(name, args, ws, peaks, flush_buf):
         alg = nnz * 2 + c["M"] * c["keep"] // 8 + int(p["cols"].size) * 4 + c["K"] * c["N"] * 2 + \
             c["M"] * c["N"] * 4
         kern, kid = "sparse_spmm_kernel", spmm._lib.KERNEL_SPARSE
+        # every (row tile, 128-column tile) gathers its tile's kept B rows: kept x N x 2 bytes per row tile
+        gathered = int(np.diff(p["tile_ptr"]).sum()) * c["N"] * 2
 
         def step():
             spmm.spmm_tvw(F, Bx, Cd)
@@ -432,6 +442,7 @@ def run_extra(name, args, ws, peaks, flush_buf):
         alg = (c["M"] + 1) * 4 + nnz * 4 + c["M"] * K_in * es + c["K"] * K_in * es + nnz * 4
         kern, kid = "sddmm_kernel", spmm._lib.KERNEL_SDDMM
         extra_fields["inner"] = K_in
+        gathered = nnz * K_in * es  # one Bt row per entry
 
         def step():
             spmm.spmm_sddmm(S, Ax, Btx, out_d)
@@ -567,6 +578,8 @@ def run_extra(name, args, ws, peaks, flush_buf):
         # CSR-equivalent stored A (row_ptr, col, val) + B read once + C written once
         alg = (c["M"] + 1) * 4 + nnz * 4 + nnz * 2 + c["K"] * c["N"] * 2 + c["M"] * c["N"] * 4
         kern, kid = wkern, spmm._lib.KERNEL_WCSR
+        # one B row per nonzero on CUDA cores, one per distinct window column on the tensor core
+        gathered = (F.n_wcols if tcore else nnz) * c["N"] * 2
 
         def step():
             spmm.spmm_wcsr(F, Bx, Cd, wsp)
@@ -594,6 +607,10 @@ def run_extra(name, args, ws, peaks, flush_buf):
                   traffic=measured_traffic(kern, name), peak_scale=peak_scale)
     rl["kernel"] = kern
     rl["kernel_ms"] = round(t_kernel * 1e3, 4)
+    if gathered:
+        ach = gathered / t_kernel / 1e9
+        extra_fields["l2_gather"] = {"bytes_per_launch": int(gathered), "achieved_gbs": round(ach, 1),
+                                     "ceiling_gbs": L2_GATHER_GBS, "frac": round(ach / L2_GATHER_GBS, 4)}
     t_step = total_ms / steps / 1e3
     return {"workload": name, "ms_per_step": round(t_step * 1e3, 4),
             "tflops": round(ws * flops / t_step / 1e12, 3), "gbs": round(alg / t_step / 1e9, 1),

@@ -743,10 +743,7 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool v) {
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
+using ptx::st_shared_v4;
 
 // Columns n .. n+7 of B row `row` (this lane's 16-byte piece of the slab), zero
 // past N or for row < 0; one vector load when the piece is whole and aligned.

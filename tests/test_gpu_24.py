@@ -85,7 +85,8 @@ def test_24_compress_rejects_three_nonzeros():
 
 def test_24_int8_full_size_sampled_rows():
     """A 8192 x 8192 int8 (2:4), B 8192 x 4096 int8: the oracle recomputes 96
-    seeded rows exactly (all 4096 columns)."""
+    seeded rows and eight whole 128-row tiles (1024 rows) exactly, all 4096
+    columns."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     p = gen.config_problem("mask24_int8")
@@ -97,11 +98,19 @@ def test_24_int8_full_size_sampled_rows():
     got = C[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.int64)
     ref = np.concatenate([oracle.spmm24(O, p["B"], rows=(int(r), int(r) + 1)) for r in rows])
     assert np.array_equal(got, ref)
+    # eight whole 128-row tiles (1024 rows: the first, the last and six seeded ones)
+    rng = np.random.default_rng(22)
+    tiles = sorted(set([0, p["M"] // 128 - 1] + [int(t) for t in rng.choice(np.arange(1, p["M"] // 128 - 1), 6, replace=False)]))
+    assert len(tiles) == 8
+    for t in tiles:
+        r0 = 128 * t
+        assert np.array_equal(C[r0:r0 + 128].cpu().numpy().astype(np.int64), oracle.spmm24(O, p["B"], rows=(r0, r0 + 128)))
 
 
 def test_24_f16_full_size_sampled_rows():
-    """A 8192 x 8192 fp16 2:4 (N(0,1) values), B 8192 x 4096 fp16, C fp32: three
-    seeded 128-row tiles (one of them the last) against the oracle."""
+    """A 8192 x 8192 fp16 2:4 (N(0,1) values), B 8192 x 4096 fp16, C fp32: eight
+    128-row tiles (1024 rows: the first, the last and six seeded ones) against
+    the oracle."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     p = gen.config_problem("mask24_f16")
@@ -110,7 +119,9 @@ def test_24_f16_full_size_sampled_rows():
     torch.cuda.synchronize()
     assert spmm.last_device_error() == 0
     rng = np.random.default_rng(61)
-    for r0 in sorted(set([int(t) * 128 for t in rng.choice(p["M"] // 128 - 1, 2, replace=False)] + [p["M"] - 128])):
+    tiles = sorted(set([0, p["M"] // 128 - 1] + [int(t) for t in rng.choice(np.arange(1, p["M"] // 128 - 1), 6, replace=False)]))
+    assert len(tiles) == 8
+    for r0 in [128 * t for t in tiles]:
         assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.spmm24(O, p["B"], rows=(r0, r0 + 128)), f"2:4 f16 rows {r0}..")
 
 

@@ -52,7 +52,8 @@ def test_tvw_builder_rejects_nonzero_outside_kept():
 
 def test_tvw_full_size_sampled_rows():
     """A 4096 x 4096 (32 tiles of 128 rows, 2048 kept columns each, 2:4 inside),
-    B 4096 x 4096: the oracle recomputes 2 seeded rows of every tile."""
+    B 4096 x 4096: the oracle recomputes 2 seeded rows of every tile and eight
+    whole tiles (1024 rows)."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     p = gen.config_problem("tvw")
@@ -65,6 +66,12 @@ def test_tvw_full_size_sampled_rows():
     got = C[torch.from_numpy(rows).cuda()].cpu().numpy()
     ref = np.concatenate([oracle.tvw_spmm(O, p["B"], rows=(int(r), int(r) + 1)) for r in rows])
     assert_close(got, ref, "tvw full-size rows")
+    # eight whole tiles (1024 rows: the first, the last and six seeded ones)
+    tiles = sorted(set([0, 31] + [int(t) for t in rng.choice(np.arange(1, 31), 6, replace=False)]))
+    assert len(tiles) == 8
+    for t in tiles:
+        r0 = 128 * t
+        assert_close(C[r0:r0 + 128].cpu().numpy(), oracle.tvw_spmm(O, p["B"], rows=(r0, r0 + 128)), f"tvw tile {t}")
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
