@@ -5,16 +5,18 @@ output buffers, a service that reserves all device memory up front, a latency-
 critical path that cannot absorb cudaMalloc's synchronisation).  For them the
 library keeps the int8 widening scratch in a fixed 32 MiB device array.  These
 tests call the entry point through the C ABI and compare it with spmm_24, the
-entry point that takes a caller-provided workspace, on two calls in a row.
-The file is named so that pytest collects it last.
+entry point that takes a caller-provided workspace, on two calls in a row, and
+with the CPU oracle (bit-exact for int8, within tolerance for bf16, whose calls
+need no scratch).  The file is named so that pytest collects it last.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import spmm_inputs as gen
-from tests.gpu_util import dev, need_gpu
+from tests.gpu_util import assert_close, dev, dev_half, need_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -57,3 +59,39 @@ def test_noalloc_rejects_scratch_beyond_32_mib():
     assert spmm.spmm_24_workspace_size(F, N) > 32 << 20
     assert _call_noalloc(F, B, C, N) == 5                # SPMM_ERR_WORKSPACE, nothing launched
     assert _lib.STATUS[5] == "SPMM_ERR_WORKSPACE"
+
+
+def test_noalloc_ragged_n_after_a_larger_call_matches_oracle():
+    """A ragged N (130: the widened B's padding columns live in the shared array)
+    right after a larger call (N = 384) that left other data there: both results
+    equal the oracle's int64 sums."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    M, K = 256, 1024
+    for N, seed in ((384, 3), (130, 4)):
+        p = gen.mask24_problem(M, K, N, seed=seed)
+        F = spmm.spmm_compress_24(dev(p["A"]))
+        C = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
+        assert _call_noalloc(F, dev(p["B"]), C, N) == 0
+        torch.cuda.synchronize()
+        O = oracle.compress24(p["A"], "i8")
+        assert np.array_equal(C.cpu().numpy().astype(np.int64), oracle.spmm24(O, p["B"]))
+    assert spmm.last_device_error() == 0
+
+
+def test_noalloc_bf16_needs_no_scratch():
+    """bf16 operands go to the kernel as they are (no scratch pointer): the result
+    equals spmm_24's and the oracle's within tolerance."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    M, K, N = 384, 1024, 200
+    p = gen.mask24_float_problem(M, K, N, seed=12, dtype="bf16")
+    F = spmm.spmm_compress_24(dev_half(p["A"], "bf16"))
+    B = dev_half(p["B"], "bf16")
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    assert _call_noalloc(F, B, C, N) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(C, spmm.spmm_24(F, B))
+    O = oracle.compress24(p["A"], "bf16")
+    assert_close(C.cpu().numpy(), oracle.spmm24(O, p["B"]), "noalloc bf16")
+    assert spmm.last_device_error() == 0
