@@ -140,7 +140,9 @@ typedef struct {
  * stored: vals[M][K/2] (group g's entries at 2g, 2g+1), meta[M][K/8] with
  * group g's nibble idx0 | idx1 << 2 (idx0 < idx1) in byte g/2, low nibble for
  * even g.  A group with fewer than two nonzeros stores its nonzero positions
- * plus the lowest-index zero positions. */
+ * plus the lowest-index zero positions.  The SpMM hands meta to the tensor
+ * core as stored: every nibble must have idx0 < idx1, as every builder here
+ * writes; other nibbles lie outside the format. */
 typedef struct {
     int64_t M, K;
     int32_t dtype; /* SPMM_I8 (-> int32 C); SPMM_F16, SPMM_BF16, SPMM_E4M3 or SPMM_E5M2 (-> fp32 C) */
