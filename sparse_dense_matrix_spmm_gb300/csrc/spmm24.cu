@@ -86,22 +86,33 @@ constexpr int META_RING = 8, META_AHEAD = 6;
 // K: the compressed A tile is still 128 rows x 128 bytes, the B tile one
 // 128-byte-wide chunk of 256 K rows (32 KB), and each of the four K = 64 sparse
 // MMAs reads 8 stored metadata bytes per row.  (No TVW gathers or lifted planes.)
-template <int BN_, bool F8_ = false>
+//
+// MT = 2: two 128-row tiles share each B stage (a 256 x 128 output tile per
+// CTA).  Per 128-deep step the CTA moves 2 x 16 KB of A and 32 KB of B for 8
+// MMAs instead of 16 + 32 KB for 4, so L2 -> SM bytes per MAC drop by a third
+// and each of the three 64 KB stages buffers twice the MMA work.  TMEM then
+// holds one accumulator per row tile (2 x 128 columns; the MMAs of the next
+// tile wait for the epilogue to read the last one out) and 2 x 4 metadata
+// columns per stage.  Plain 2:4 with fp16/bf16/fp8 operands.
+template <int BN_, bool F8_ = false, int MT_ = 1>
 struct Tile {
     static constexpr int BN = BN_;
     static constexpr int KSD = F8_ ? 2 * KS : KS;          // dense K per stage
     static constexpr int CHUNKS = F8_ ? 1 : BN_ / 64;       // 128-byte-wide B chunks (128-byte swizzle rows)
     static constexpr uint32_t B_BYTES = KSD * BN_ * (F8_ ? 1 : 2);
-    static constexpr uint32_t MB = BM * (KSD / 8);          // stored metadata bytes per step
+    static constexpr uint32_t MB = BM * (KSD / 8);          // stored metadata bytes per row tile and step
     // 1024-aligned; the per-stage metadata copy is used by TVW only
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + (F8_ ? 0 : M_BYTES);
-    static constexpr int STAGES = BN_ == 128 ? 4 : 3;
-    static constexpr int PRODUCERS = BN_ == 128 ? 2 : 3;
+    static constexpr uint32_t STAGE_BYTES = MT_ * A_BYTES + B_BYTES + ((F8_ || MT_ > 1) ? 0 : M_BYTES);
+    static constexpr int STAGES = MT_ > 1 ? 3 : (BN_ == 128 ? 4 : 3);
+    static constexpr int PRODUCERS = MT_ > 1 ? 3 : (BN_ == 128 ? 2 : 3);
+    static constexpr int NACC_T = MT_ > 1 ? 1 : NACC;       // accumulator buffers per row tile
+    static constexpr int MRING = (MT_ > 1 && F8_) ? 4 : META_RING;    // metadata ring steps
+    static constexpr int MAHEAD = (MT_ > 1 && F8_) ? 3 : META_AHEAD;  // metadata copies ahead of use
     static constexpr int MMA_WARP = PRODUCERS;
     static constexpr int META_WARP0 = PRODUCERS + 1;
-    static constexpr uint32_t META_COL = NACC * BN_;  // metadata columns after the accumulators
+    static constexpr uint32_t META_COL = NACC_T * MT_ * BN_;  // metadata columns after the accumulators
     static constexpr uint32_t RING_OFF = STAGES * STAGE_BYTES;
-    static constexpr int SMEM = 1024 + RING_OFF + META_RING * MB + 8 * (3 * STAGES + 2 * NACC + 1) + 16;
+    static constexpr int SMEM = 1024 + RING_OFF + MRING * MT_ * MB + 8 * (3 * STAGES + 2 * NACC_T + 1) + 16;
     __host__ __device__ static constexpr int epi_warp0(bool gather) {
         return META_WARP0 + kMetaWarps + gather_warps(gather);
     }
@@ -115,6 +126,11 @@ static_assert(Tile<192>::META_COL + META_STRIDE * 4 * Tile<192>::STAGES <= TMEM_
 static_assert(Tile<192>::SMEM <= 232448 && Tile<128>::SMEM <= 232448 && Tile<128, true>::SMEM <= 232448,
               "shared memory per block");
 static_assert(Tile<128, true>::STAGE_BYTES % 1024 == 0, "swizzle alignment");
+static_assert(Tile<128, false, 2>::STAGES % Tile<128, false, 2>::PRODUCERS == 0 &&
+                  Tile<128, false, 2>::META_COL + META_STRIDE * 4 * 2 * Tile<128, false, 2>::STAGES <= TMEM_COLS &&
+                  Tile<128, false, 2>::SMEM <= 232448 && Tile<128, true, 2>::SMEM <= 232448 &&
+                  Tile<128, false, 2>::STAGE_BYTES % 1024 == 0 && Tile<128, true, 2>::STAGE_BYTES % 1024 == 0,
+              "two row tiles per CTA: slots, TMEM, shared memory, swizzle alignment");
 static_assert(Tile<192>::STAGE_BYTES % 1024 == 0 && Tile<128>::STAGE_BYTES % 1024 == 0, "swizzle alignment");
 
 using T16 = uint16_t;  // B elements are moved as raw 16-bit patterns
@@ -181,11 +197,13 @@ __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int&
     return static_cast<int>(a.K / ksd);
 }
 
-template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false>
-__global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
+template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false, int MT = 1>
+__global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
     sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
                        const __grid_constant__ BMaps<PLANES> tmB, const SpArgs a) {
-    using Cfg = Tile<BNT, F8>;
+    using Cfg = Tile<BNT, F8, MT>;
+    static_assert(MT == 1 || (!GATHER && !INT_EXACT && BNT == 128),
+                  "two row tiles per CTA: 2:4 and lifted operands, 128-column tiles, no int8 epilogue");
     static_assert(!INT_EXACT || BNT == 128, "the int8 epilogue keeps 128 sums per thread");
     static_assert(!GATHER || BNT == 128, "TVW gathers two 64-column chunks");
     static_assert(!F8 || (BNT == 128 && !GATHER && !INT_EXACT && PLANES == 1), "fp8: plain 2:4, 128-column tiles");
@@ -195,25 +213,27 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
     constexpr uint32_t META_COL = Cfg::META_COL;
     constexpr int KSD = Cfg::KSD;
     constexpr uint32_t MB = Cfg::MB;
+    constexpr int NAC = Cfg::NACC_T, MRING = Cfg::MRING, MAHEAD = Cfg::MAHEAD;
+    constexpr int BMG = BM * MT;  // rows of A per output tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + META_RING * MB);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NACC + 1);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_OFF + MRING * MT * MB);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * NAC + 1);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int kGatherWarps = gather_warps(GATHER);
     constexpr int kEpiWarp0 = Cfg::epi_warp0(GATHER);
     constexpr int kRowsPerWarp = KS / (GATHER ? kGatherWarps : 1);  // TVW: kept rows each gathering warp copies per step
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
-    // stage s: [A | B chunks 0 .. BN/64 - 1 | stored metadata]
+    // stage s: [A of row tile 0 .. MT - 1 | B chunks 0 .. BN/64 - 1 | stored metadata (TVW)]
     auto a_s = [&](int s) { return s0 + s * STAGE_BYTES; };
-    auto b_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES; };
-    auto mc_s = [&](int s) { return s0 + s * STAGE_BYTES + A_BYTES + B_BYTES; };
+    auto b_s = [&](int s) { return s0 + s * STAGE_BYTES + MT * A_BYTES; };
+    auto mc_s = [&](int s) { return s0 + s * STAGE_BYTES + MT * A_BYTES + B_BYTES; };
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto mready_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + NACC + b); };
-    const uint32_t done_bar = bar0 + 8u * (3 * STAGES + 2 * NACC);
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + NAC + b); };
+    const uint32_t done_bar = bar0 + 8u * (3 * STAGES + 2 * NAC);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
             mbar_init(mready_bar(s), 4);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < NACC; ++b) {
+        for (int b = 0; b < NAC; ++b) {
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 4);
         }
@@ -259,7 +279,7 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
         for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
             int mt, nt;
             tile_of(a, u, mt, nt);
-            const int m0 = mt * BM, n0 = nt * BN;
+            const int m0 = mt * BMG, n0 = nt * BN;
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
             // this producer's steps of the tile: t + ks = p (mod kProducers)
@@ -272,9 +292,13 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : A_BYTES + B_BYTES);
-                    // compressed A: 128 stored bytes per row and step for fp8, 64 elements for 16-bit
-                    tma_load_2d_hint(a_s(s), &tmA, full_bar(s), ks * (F8 ? KSD / 2 : KS / 2), m0, pol_stream);
+                    mbar_arrive_expect_tx(full_bar(s), GATHER ? A_BYTES + M_BYTES : MT * A_BYTES + B_BYTES);
+                    // compressed A: 128 stored bytes per row and step for fp8, 64 elements for 16-bit;
+                    // rows past M (a last row tile of a pair) arrive zero-filled
+#pragma unroll
+                    for (int r = 0; r < MT; ++r)
+                        tma_load_2d_hint(a_s(s) + r * A_BYTES, &tmA, full_bar(s), ks * (F8 ? KSD / 2 : KS / 2),
+                                         m0 + r * BM, pol_stream);
                     if (GATHER) tma_load_2d_hint(mc_s(s), &tmMeta, full_bar(s), ks * (KS / 8), m0, pol_stream);
                     if constexpr (!GATHER && PLANES > 1) {
                         // lifted rows ks KS .. ks KS + 127: windows w0 .. w0 + 31 of plane j
@@ -332,14 +356,14 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
                 const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
                 const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
                 for (int c = 0; c < nch && ok; ++c, ++acc_i) {
-                    const int b = acc_i & 1;
-                    const uint32_t aph = static_cast<uint32_t>(acc_i >> 1) & 1u;
+                    const int b = acc_i % NAC;
+                    const uint32_t aph = static_cast<uint32_t>(acc_i / NAC) & 1u;
                     if (!mbar_wait(acce_bar(b), aph ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * MT * BN);
                     const int k_lo = c * CH, k_hi = min(nk, k_lo + CH);
                     for (int ks = k_lo; ks < k_hi; ++ks) {
                         if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT) ||
@@ -349,17 +373,24 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
                         }
                         tc_fence_after();
                         if (GATHER) fence_proxy_async_smem();  // B rows arrived through cp.async
-                        const uint32_t mcol = tmem + META_COL + META_STRIDE * 4u * s;
+                        const uint32_t mcol = tmem + META_COL + META_STRIDE * 4u * MT * s;
                         const uint64_t so = static_cast<uint64_t>(static_cast<uint32_t>(s) * (STAGE_BYTES >> 4));
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // MMA i: A +32 stored bytes; B +32 K rows (16-bit) or +64 K rows (fp8) of 128 B
-                            if constexpr (F8)
-                                mma_sp_f8(d, adesc0 + so + 2u * i, bdesc0 + so + 512u * i, mcol + META_STRIDE * i,
-                                          a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
-                            else
-                                mma_sp_f16(d, adesc0 + so + 2u * i, bdesc0 + so + 256u * i, mcol + META_STRIDE * i,
-                                           a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
+                        for (int r = 0; r < MT; ++r) {
+                            // row tile r: its A tile, accumulator and metadata columns; the stage's B
+                            const uint64_t ro = static_cast<uint64_t>(r) * (A_BYTES >> 4);
+                            const uint32_t dr = d + static_cast<uint32_t>(r * BN);
+                            const uint32_t mr = mcol + META_STRIDE * 4u * r;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                // MMA i: A +32 stored bytes; B +32 K rows (16-bit) or +64 K rows (fp8) of 128 B
+                                if constexpr (F8)
+                                    mma_sp_f8(dr, adesc0 + so + ro + 2u * i, bdesc0 + so + 512u * i,
+                                              mr + META_STRIDE * i, a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
+                                else
+                                    mma_sp_f16(dr, adesc0 + so + ro + 2u * i, bdesc0 + so + 256u * i,
+                                               mr + META_STRIDE * i, a.idesc, (ks > k_lo || i > 0) ? 1u : 0u);
+                            }
                         }
                         mma_commit(empty_bar(s));
                         if (++s == STAGES) {
@@ -410,19 +441,23 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
         Walk f = m;
         int f_step = 0;
         auto meta_copy = [&]() {
-            const int64_t grow = static_cast<int64_t>(f.mt) * BM + row;
-            const bool live = f.u < total && grow < a.M;
-            const uint8_t* src = live ? a.meta + grow * a.ldm + static_cast<int64_t>(f.ks) * (KSD / 8) : a.meta;
-            const uint32_t dst = s0 + RING_OFF + static_cast<uint32_t>(f_step % META_RING) * MB + (MB / BM) * row;
-            cp_async16(dst, src, live ? 16u : 0u);
-            if constexpr (F8) cp_async16(dst + 16u, live ? src + 16 : src, live ? 16u : 0u);
+#pragma unroll
+            for (int r = 0; r < MT; ++r) {
+                const int64_t grow = static_cast<int64_t>(f.mt) * BMG + r * BM + row;
+                const bool live = f.u < total && grow < a.M;
+                const uint8_t* src = live ? a.meta + grow * a.ldm + static_cast<int64_t>(f.ks) * (KSD / 8) : a.meta;
+                const uint32_t dst = s0 + RING_OFF + static_cast<uint32_t>(f_step % MRING) * (MT * MB) + r * MB +
+                                     (MB / BM) * row;
+                cp_async16(dst, src, live ? 16u : 0u);
+                if constexpr (F8) cp_async16(dst + 16u, live ? src + 16 : src, live ? 16u : 0u);
+            }
             cp_async_commit();
             ++f_step;
             if (f.u < total) advance(f);
         };
         int m_step = 0;
         if (!GATHER)
-            for (int i = 0; i < META_AHEAD; ++i) meta_copy();
+            for (int i = 0; i < MAHEAD; ++i) meta_copy();
         auto meta_step = [&]() -> bool {
             const int cmt = m.mt;
             const int slot = s;
@@ -432,51 +467,53 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
                 s = 0;
                 ph ^= 1u;
             }
-            const bool row_live = static_cast<int64_t>(cmt) * BM + row < a.M;
-            uint4 w;
+            uint4 wr[MT];
+            uint4 w2r[F8 ? MT : 1];
             if (GATHER) {
                 if (!mbar_wait(full_bar(slot), par, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
-                const uint8_t* mc = smem + slot * STAGE_BYTES + A_BYTES + B_BYTES;
-                w = *reinterpret_cast<const uint4*>(mc + 16 * row);
+                const uint8_t* mc = smem + slot * STAGE_BYTES + A_BYTES + B_BYTES;  // TVW: one row tile
+                wr[0] = *reinterpret_cast<const uint4*>(mc + 16 * row);
             } else {
-                cp_async_wait<META_AHEAD - 1>();  // this thread's copy for this step has landed
-                const uint8_t* mine = smem + RING_OFF + (m_step % META_RING) * MB + (MB / BM) * row;
-                w = *reinterpret_cast<const uint4*>(mine);
-                if constexpr (F8) {
-                    // kind::f8f6f4 reads row r's 64 bits of one MMA from TMEM lane r, two
-                    // consecutive columns, in stored order (measured): copy them as they are
-                    uint4 w2 = *reinterpret_cast<const uint4*>(mine + 16);
-                    ++m_step;
-                    meta_copy();
-                    if (!mbar_wait(empty_bar(slot), par ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
-                    if (!row_live) {
-                        w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
-                        w2 = w;
-                    }
-                    const uint32_t tb = tl + META_STRIDE * 4u * slot;
-                    tmem_st2(tb, w.x, w.y);
-                    tmem_st2(tb + META_STRIDE, w.z, w.w);
-                    tmem_st2(tb + 2 * META_STRIDE, w2.x, w2.y);
-                    tmem_st2(tb + 3 * META_STRIDE, w2.z, w2.w);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(mready_bar(slot));
-                    return true;
+                cp_async_wait<MAHEAD - 1>();  // this thread's copies for this step have landed
+                const uint8_t* mine = smem + RING_OFF + (m_step % MRING) * (MT * MB) + (MB / BM) * row;
+#pragma unroll
+                for (int r = 0; r < MT; ++r) {
+                    wr[r] = *reinterpret_cast<const uint4*>(mine + r * MB);
+                    if constexpr (F8) w2r[r] = *reinterpret_cast<const uint4*>(mine + r * MB + 16);
                 }
                 ++m_step;
                 meta_copy();
                 // the MMAs that read this slot's metadata columns last time are done
                 if (!mbar_wait(empty_bar(slot), par ^ 1u, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) return false;
             }
-            // rows past M arrive zero-filled; give them the valid (0, 1) pattern
-            if (!row_live) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
-            const uint32_t in[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t p = __shfl_xor_sync(0xffffffffu, in[i], 8);
-                const uint32_t o = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
-                tmem_st1(tl + META_STRIDE * (4u * slot + i), o);
+            for (int r = 0; r < MT; ++r) {
+                // rows past M arrive zero-filled; give them the valid (0, 1) pattern
+                const bool row_live = static_cast<int64_t>(cmt) * BMG + r * BM + row < a.M;
+                uint4 w = wr[r];
+                const uint32_t tb = tl + META_STRIDE * (4u * MT * slot + 4u * r);
+                if constexpr (F8) {
+                    // kind::f8f6f4 reads row r's 64 bits of one MMA from TMEM lane r, two
+                    // consecutive columns, in stored order (measured): copy them as they are
+                    uint4 w2 = w2r[r];
+                    if (!row_live) {
+                        w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+                        w2 = w;
+                    }
+                    tmem_st2(tb, w.x, w.y);
+                    tmem_st2(tb + META_STRIDE, w.z, w.w);
+                    tmem_st2(tb + 2 * META_STRIDE, w2.x, w2.y);
+                    tmem_st2(tb + 3 * META_STRIDE, w2.z, w2.w);
+                } else {
+                    if (!row_live) w = make_uint4(0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u);
+                    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t p = __shfl_xor_sync(0xffffffffu, in[i], 8);
+                        const uint32_t o = (lane & 8) ? __byte_perm(p, in[i], 0x7632) : __byte_perm(in[i], p, 0x5410);
+                        tmem_st1(tb + META_STRIDE * i, o);
+                    }
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -552,9 +589,7 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
             const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
-            const int64_t row = static_cast<int64_t>(mt) * BM + q * 32 + lane;
             const int64_t n0 = static_cast<int64_t>(nt) * BN;
-            const bool row_live = row < a.M;
             const bool full_n = n0 + BN <= a.N && a.vec_ok;
             const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
             int32_t run[INT_EXACT ? BN : 1];
@@ -562,41 +597,47 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
             for (int i = 0; i < (INT_EXACT ? BN : 1); ++i) run[i] = 0;
             bool ok = true;
             for (int c = 0; c < nch; ++c, ++acc_i) {
-                const int b = acc_i & 1;
-                const uint32_t aph = static_cast<uint32_t>(acc_i >> 1) & 1u;
+                const int b = acc_i % NAC;
+                const uint32_t aph = static_cast<uint32_t>(acc_i / NAC) & 1u;
                 if (!mbar_wait(accf_bar(b), aph, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tb = tl + static_cast<uint32_t>(b * BN);
+#pragma unroll 1
+                for (int r = 0; r < MT; ++r) {
+                    // row tile r of the output tile: this thread's row, its accumulator
+                    const int64_t row = static_cast<int64_t>(mt) * BMG + r * BM + q * 32 + lane;
+                    const bool row_live = row < a.M;
+                    const uint32_t tb = tl + static_cast<uint32_t>((b * MT + r) * BN);
 #pragma unroll
-                for (int j = 0; j < BN / 16; ++j) {
-                    uint32_t v[16];
-                    if (nk > 0) {
-                        tmem_ld16(tb + 16 * j, v);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = 0u;
-                    }
-                    if constexpr (INT_EXACT) {
-                        // every chunk partial is an integer of magnitude below 2^24, exact in
-                        // fp32; round-to-nearest conversion returns it unchanged
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) run[16 * j + i] += __float2int_rn(__uint_as_float(v[i]));
-                    } else if (row_live) {
-                        float* cp = static_cast<float*>(a.C) + row * a.ldc + n0 + 16 * j;
-                        if (full_n) {
-#pragma unroll
-                            for (int i = 0; i < 16; i += 4)
-                                __stcs(reinterpret_cast<float4*>(cp + i),
-                                       make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                   __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+                    for (int j = 0; j < BN / 16; ++j) {
+                        uint32_t v[16];
+                        if (nk > 0) {
+                            tmem_ld16(tb + 16 * j, v);
+                            tmem_ld_wait();
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (n0 + 16 * j + i < a.N) cp[i] = __uint_as_float(v[i]);
+                            for (int i = 0; i < 16; ++i) v[i] = 0u;
+                        }
+                        if constexpr (INT_EXACT) {
+                            // every chunk partial is an integer of magnitude below 2^24, exact in
+                            // fp32; round-to-nearest conversion returns it unchanged
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) run[16 * j + i] += __float2int_rn(__uint_as_float(v[i]));
+                        } else if (row_live) {
+                            float* cp = static_cast<float*>(a.C) + row * a.ldc + n0 + 16 * j;
+                            if (full_n) {
+#pragma unroll
+                                for (int i = 0; i < 16; i += 4)
+                                    __stcs(reinterpret_cast<float4*>(cp + i),
+                                           make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (n0 + 16 * j + i < a.N) cp[i] = __uint_as_float(v[i]);
+                            }
                         }
                     }
                 }
@@ -606,7 +647,8 @@ __global__ void __launch_bounds__(Tile<BNT, F8>::threads(GATHER), 1)
             }
             if (!ok) break;
             if constexpr (INT_EXACT) {
-                if (row_live) {
+                const int64_t row = static_cast<int64_t>(mt) * BM + q * 32 + lane;  // MT == 1
+                if (row < a.M) {
                     int32_t* cp = static_cast<int32_t*>(a.C) + row * a.ldc + n0;
                     if (full_n) {
 #pragma unroll
@@ -679,20 +721,20 @@ __global__ void widen_i8_kernel(const WidenJob j0, const WidenJob j1) {
     }
 }
 
-template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false>
+template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false, int MT = 1>
 spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const BMaps<PLANES>& tmB, const SpArgs& a,
                           cudaStream_t stream, int slot) {
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
-    constexpr int kSmem = Tile<BNT, F8>::SMEM;
+    constexpr int kSmem = Tile<BNT, F8, MT>::SMEM;
     if (dev->max_smem_optin < kSmem) return SPMM_ERR_UNSUPPORTED;
-    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES, BNT, F8>;
+    auto kern = sparse_spmm_kernel<GATHER, INT_EXACT, PLANES, BNT, F8, MT>;
     if (!set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem, slot)) return SPMM_ERR_CUDA;
     const int64_t units = static_cast<int64_t>(a.n_mtiles) * a.n_ntiles;
     if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_SPARSE, stream);
-    kern<<<grid, Tile<BNT, F8>::threads(GATHER), kSmem, stream>>>(tmA, tmM, tmB, a);
+    kern<<<grid, Tile<BNT, F8, MT>::threads(GATHER), kSmem, stream>>>(tmA, tmM, tmB, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_SPARSE, stream);
     return cuda_status(e);
@@ -756,13 +798,17 @@ bool wide_tile(bool i8, int64_t M, int64_t N, int sms) {
     return w192 * 144 < w128 * 100;
 }
 
+// Two 128-row tiles per CTA for plain fp16/bf16/fp8 2:4 whenever A has more
+// than one row tile: they share each B stage (see Tile).
+bool pair_tiles(bool i8, int64_t M) { return !i8 && M > BM; }
+
 SpArgs dense_b_args(const DeviceInfo* dev, int64_t M, int64_t K, int64_t N, int32_t dtype, const uint8_t* meta,
-                    void* C, int64_t ldc, int bn) {
+                    void* C, int64_t ldc, int bn, int mt = 1) {
     SpArgs a{};
     a.M = M;
     a.N = N;
     a.K = K;
-    a.n_mtiles = static_cast<int32_t>((M + BM - 1) / BM);
+    a.n_mtiles = static_cast<int32_t>((M + BM * mt - 1) / (BM * mt));  // output tiles of mt row tiles
     a.n_ntiles = static_cast<int32_t>((N + bn - 1) / bn);
     a.C = C;
     a.ldc = ldc;
@@ -796,8 +842,10 @@ spmm_status launch_spmm24_f8(const DeviceInfo* dev, const spmm_24_t* A, const vo
         !encode_tmap_2d(&tmB.m[0], u8, B, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
                         static_cast<uint64_t>(ldb), 128, 256, CU_TENSOR_MAP_SWIZZLE_128B))
         return SPMM_ERR_CUDA;
-    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, 128);
+    const bool pair = pair_tiles(false, A->M);
+    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, 128, pair ? 2 : 1);
     a.idesc = idesc_f8(128, 128, A->dtype == SPMM_E5M2, false, true, true);
+    if (pair) return launch_sparse<false, false, 1, 128, true, 2>(tmA, tmM, tmB, a, stream, 17);
     return launch_sparse<false, false, 1, 128, true>(tmA, tmM, tmB, a, stream, 15);
 }
 
@@ -833,10 +881,12 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
         (!b3d && !encode_tmap_2d(&tmB.m[0], t, bsrc, static_cast<uint64_t>(N), static_cast<uint64_t>(A->K),
                                  static_cast<uint64_t>(bld) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
         return SPMM_ERR_CUDA;
-    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, bn);
+    const bool pair = bn == 128 && pair_tiles(i8, A->M);
+    SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, bn, pair ? 2 : 1);
     a.b3d = b3d ? 1 : 0;
     if (i8) return launch_sparse<false, true, 1, 128>(tmA, tmM, tmB, a, stream, 2);
     if (bn == 192) return launch_sparse<false, false, 1, 192>(tmA, tmM, tmB, a, stream, 13);
+    if (pair) return launch_sparse<false, false, 1, 128, false, 2>(tmA, tmM, tmB, a, stream, 18);
     return launch_sparse<false, false, 1, 128>(tmA, tmM, tmB, a, stream, 1);
 }
 
@@ -866,7 +916,9 @@ spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void
     std::memset(&tmB, 0, sizeof(tmB));
     // Plane j: rows 2j + p + 2n g of B (p < 4, g < G).  Whole 64-column chunks:
     // one 4-D box {64, 4, 32, bn / 64}; otherwise one 3-D box {64, 4, 32} per chunk.
-    const int bn = wide_tile(i8, A->M, N, dev->sms) ? 192 : 128;
+    // fp16/bf16 with more than one row tile: two row tiles per CTA at 128 columns.
+    const bool pair = pair_tiles(i8, A->M);
+    const int bn = !pair && wide_tile(i8, A->M, N, dev->sms) ? 192 : 128;
     const bool b4d = N % 64 == 0;
     const uint64_t row = static_cast<uint64_t>(bld) * 2;
     for (int j = 0; j < n - 1; ++j) {
@@ -886,11 +938,12 @@ spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void
         if (!ok) return SPMM_ERR_CUDA;
     }
     if (!encode_a_maps(t, vals, A->meta, A->M, Kl, &tmA, &tmM)) return SPMM_ERR_CUDA;
-    SpArgs a = dense_b_args(dev, A->M, Kl, N, A->dtype, A->meta, C, ldc, bn);
+    SpArgs a = dense_b_args(dev, A->M, Kl, N, A->dtype, A->meta, C, ldc, bn, pair ? 2 : 1);
     a.b3d = b4d ? 1 : 0;
     a.planes = n - 1;
     a.plane_groups = static_cast<int32_t>(G);
     if (i8) return launch_sparse<false, true, kMaxPlanes, 128>(tmA, tmM, tmB, a, stream, 12);
+    if (pair) return launch_sparse<false, false, kMaxPlanes, 128, false, 2>(tmA, tmM, tmB, a, stream, 19);
     if (bn == 192) return launch_sparse<false, false, kMaxPlanes, 192>(tmA, tmM, tmB, a, stream, 14);
     return launch_sparse<false, false, kMaxPlanes, 128>(tmA, tmM, tmB, a, stream, 11);
 }
