@@ -116,7 +116,13 @@ struct Tile {
     __host__ __device__ static constexpr int epi_warp0(bool gather) {
         return META_WARP0 + kMetaWarps + gather_warps(gather);
     }
-    __host__ __device__ static constexpr int threads(bool gather) { return 32 * (epi_warp0(gather) + 4); }
+    // Epilogue warps: four (one per TMEM lane quarter) draining every row tile, or,
+    // for int8 with two row tiles, sixteen: one per (row tile, 64-column half,
+    // lane quarter), so each thread keeps 64 exact int32 sums instead of 128.
+    __host__ __device__ static constexpr int epi_warps(bool int_exact) { return (int_exact && MT_ > 1) ? 16 : 4; }
+    __host__ __device__ static constexpr int threads(bool gather, bool int_exact = false) {
+        return 32 * (epi_warp0(gather) + epi_warps(int_exact));
+    }
 };
 static_assert(Tile<128>::STAGES % Tile<128>::PRODUCERS == 0 && Tile<192>::STAGES % Tile<192>::PRODUCERS == 0,
               "every slot belongs to one producer");
@@ -198,12 +204,12 @@ __device__ __forceinline__ int tile_steps(const SpArgs& a, int mt, int& kb, int&
 }
 
 template <bool GATHER, bool INT_EXACT, int PLANES, int BNT, bool F8 = false, int MT = 1>
-__global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
+__global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER, INT_EXACT), 1)
     sparse_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmMeta,
                        const __grid_constant__ BMaps<PLANES> tmB, const SpArgs a) {
     using Cfg = Tile<BNT, F8, MT>;
-    static_assert(MT == 1 || (!GATHER && !INT_EXACT && BNT == 128),
-                  "two row tiles per CTA: 2:4 and lifted operands, 128-column tiles, no int8 epilogue");
+    static_assert(MT == 1 || (!GATHER && BNT == 128 && !(F8 && INT_EXACT)),
+                  "two row tiles per CTA: 2:4 and lifted operands, 128-column tiles");
     static_assert(!INT_EXACT || BNT == 128, "the int8 epilogue keeps 128 sums per thread");
     static_assert(!GATHER || BNT == 128, "TVW gathers two 64-column chunks");
     static_assert(!F8 || (BNT == 128 && !GATHER && !INT_EXACT && PLANES == 1), "fp8: plain 2:4, 128-column tiles");
@@ -222,6 +228,9 @@ __global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int kGatherWarps = gather_warps(GATHER);
     constexpr int kEpiWarp0 = Cfg::epi_warp0(GATHER);
+    constexpr int kEpiWarps = Cfg::epi_warps(INT_EXACT);
+    constexpr int kEpiTiles = kEpiWarps == 4 ? MT : 1;         // row tiles each epilogue warp drains
+    constexpr int kEpiCols = kEpiWarps == 16 ? BN / 2 : BN;    // accumulator columns each epilogue warp drains
     constexpr int kRowsPerWarp = KS / (GATHER ? kGatherWarps : 1);  // TVW: kept rows each gathering warp copies per step
     const uint32_t s0 = smem_u32(smem), bar0 = smem_u32(bars);
     // stage s: [A of row tile 0 .. MT - 1 | B chunks 0 .. BN/64 - 1 | stored metadata (TVW)]
@@ -243,7 +252,7 @@ __global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
         }
         for (int b = 0; b < NAC; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), kEpiWarps);
         }
         mbar_init(done_bar, 1);
         fence_mbar_init();
@@ -581,7 +590,10 @@ __global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
         }
     } else {
         // -------------------------------------------------------- epilogue
-        const int q = warp & 3;
+        const int q = warp & 3;                // TMEM lane quarter this warp may read
+        const int e = warp - kEpiWarp0;        // groups of four consecutive warps cover the four quarters
+        const int r0 = kEpiWarps == 4 ? 0 : e / 8;                           // first row tile this warp drains
+        const int c0 = kEpiWarps == 16 ? ((e / 4) & 1) * kEpiCols : 0;      // first accumulator column
         int acc_i = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             int mt, nt;
@@ -589,12 +601,12 @@ __global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
             int kb, kt;
             const int nk = tile_steps(a, mt, kb, kt, GATHER, KSD);
             const int nch = nk > 0 ? (nk + CH - 1) / CH : 1;
-            const int64_t n0 = static_cast<int64_t>(nt) * BN;
-            const bool full_n = n0 + BN <= a.N && a.vec_ok;
-            const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            int32_t run[INT_EXACT ? BN : 1];
+            const int64_t n0 = static_cast<int64_t>(nt) * BN + c0;           // this warp's first output column
+            const bool full_n = n0 + kEpiCols <= a.N && a.vec_ok;
+            const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c0);
+            int32_t run[INT_EXACT ? kEpiCols : 1];
 #pragma unroll
-            for (int i = 0; i < (INT_EXACT ? BN : 1); ++i) run[i] = 0;
+            for (int i = 0; i < (INT_EXACT ? kEpiCols : 1); ++i) run[i] = 0;
             bool ok = true;
             for (int c = 0; c < nch; ++c, ++acc_i) {
                 const int b = acc_i % NAC;
@@ -605,13 +617,13 @@ __global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int r = 0; r < MT; ++r) {
+                for (int r = r0; r < r0 + kEpiTiles; ++r) {
                     // row tile r of the output tile: this thread's row, its accumulator
                     const int64_t row = static_cast<int64_t>(mt) * BMG + r * BM + q * 32 + lane;
                     const bool row_live = row < a.M;
                     const uint32_t tb = tl + static_cast<uint32_t>((b * MT + r) * BN);
 #pragma unroll
-                    for (int j = 0; j < BN / 16; ++j) {
+                    for (int j = 0; j < kEpiCols / 16; ++j) {
                         uint32_t v[16];
                         if (nk > 0) {
                             tmem_ld16(tb + 16 * j, v);
@@ -647,17 +659,17 @@ __global__ void __launch_bounds__(Tile<BNT, F8, MT>::threads(GATHER), 1)
             }
             if (!ok) break;
             if constexpr (INT_EXACT) {
-                const int64_t row = static_cast<int64_t>(mt) * BM + q * 32 + lane;  // MT == 1
+                const int64_t row = static_cast<int64_t>(mt) * BMG + r0 * BM + q * 32 + lane;  // one row tile
                 if (row < a.M) {
                     int32_t* cp = static_cast<int32_t*>(a.C) + row * a.ldc + n0;
                     if (full_n) {
 #pragma unroll
-                        for (int i = 0; i < BN; i += 4)
+                        for (int i = 0; i < kEpiCols; i += 4)
                             __stcs(reinterpret_cast<int4*>(cp + i),
                                    make_int4(run[i], run[i + 1], run[i + 2], run[i + 3]));
                     } else {
 #pragma unroll
-                        for (int i = 0; i < BN; ++i)
+                        for (int i = 0; i < kEpiCols; ++i)
                             if (n0 + i < a.N) cp[i] = run[i];
                     }
                 }
@@ -734,7 +746,7 @@ spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const 
     if (units >= (int64_t(1) << 31) - dev->sms) return SPMM_ERR_UNSUPPORTED;  // 32-bit tile indices
     const int grid = static_cast<int>(units < dev->sms ? units : dev->sms);
     trace_begin(SPMM_KERNEL_SPARSE, stream);
-    kern<<<grid, Tile<BNT, F8, MT>::threads(GATHER), kSmem, stream>>>(tmA, tmM, tmB, a);
+    kern<<<grid, Tile<BNT, F8, MT>::threads(GATHER, INT_EXACT), kSmem, stream>>>(tmA, tmM, tmB, a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_SPARSE, stream);
     return cuda_status(e);
@@ -798,9 +810,12 @@ bool wide_tile(bool i8, int64_t M, int64_t N, int sms) {
     return w192 * 144 < w128 * 100;
 }
 
-// Two 128-row tiles per CTA for plain fp16/bf16/fp8 2:4 whenever A has more
-// than one row tile: they share each B stage (see Tile).
-bool pair_tiles(bool i8, int64_t M) { return !i8 && M > BM; }
+// Two 128-row tiles per CTA whenever A has more than one row tile: they share
+// each B stage (see Tile).  For int8 this is measured 2% faster per call than
+// one row tile (359 us against 366 us at 8192^2 x 4096, widening included): the
+// four exact-chunk drains per tile stall the MMAs on the single accumulator.
+constexpr bool kPairInt8 = true;
+bool pair_tiles(bool i8, int64_t M) { return M > BM && (!i8 || kPairInt8); }
 
 SpArgs dense_b_args(const DeviceInfo* dev, int64_t M, int64_t K, int64_t N, int32_t dtype, const uint8_t* meta,
                     void* C, int64_t ldc, int bn, int mt = 1) {
@@ -884,6 +899,7 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
     const bool pair = bn == 128 && pair_tiles(i8, A->M);
     SpArgs a = dense_b_args(dev, A->M, A->K, N, A->dtype, A->meta, C, ldc, bn, pair ? 2 : 1);
     a.b3d = b3d ? 1 : 0;
+    if (i8 && pair) return launch_sparse<false, true, 1, 128, false, 2>(tmA, tmM, tmB, a, stream, 20);
     if (i8) return launch_sparse<false, true, 1, 128>(tmA, tmM, tmB, a, stream, 2);
     if (bn == 192) return launch_sparse<false, false, 1, 192>(tmA, tmM, tmB, a, stream, 13);
     if (pair) return launch_sparse<false, false, 1, 128, false, 2>(tmA, tmM, tmB, a, stream, 18);
@@ -917,7 +933,7 @@ spmm_status launch_slide(const spmm_slide_t* A, const void* B, int64_t ldb, void
     // Plane j: rows 2j + p + 2n g of B (p < 4, g < G).  Whole 64-column chunks:
     // one 4-D box {64, 4, 32, bn / 64}; otherwise one 3-D box {64, 4, 32} per chunk.
     // fp16/bf16 with more than one row tile: two row tiles per CTA at 128 columns.
-    const bool pair = pair_tiles(i8, A->M);
+    const bool pair = !i8 && pair_tiles(i8, A->M);  // int8 lifted operands keep one row tile
     const int bn = !pair && wide_tile(i8, A->M, N, dev->sms) ? 192 : 128;
     const bool b4d = N % 64 == 0;
     const uint64_t row = static_cast<uint64_t>(bld) * 2;
