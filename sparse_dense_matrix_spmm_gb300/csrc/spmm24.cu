@@ -77,8 +77,9 @@ constexpr int META_RING = 8, META_AHEAD = 6;
 // int8 path, whose exact epilogue keeps BN int32 sums per thread, and N <= 128).
 // BN = 192: N = 192 sparse MMAs, which do about a quarter more useful work per
 // tensor-core cycle than N = 128 (measured), in three 66 KB stages with one
-// producer warp per stage; fp16/bf16 2:4 and lifted operands, where the count
-// of tile waves favours it (wide_tile).  Producer p fills
+// producer warp per stage; fp16/bf16 2:4 where the count of tile waves favours
+// it (wide_tile), and lifted operands with a single row tile (with more, two
+// row tiles per CTA measured faster at the 6:8 shape).  Producer p fills
 // the steps at positions t with t % PRODUCERS == p into slot t % STAGES, so each
 // slot has one producer.
 //

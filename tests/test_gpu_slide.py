@@ -134,10 +134,11 @@ def test_slide_degenerate_inputs():
 
 
 @pytest.mark.parametrize("dtype,N", [("f16", 384), ("bf16", 380)])
-def test_slide_192_column_tiles(dtype, N):
-    """The lifted product in the 192-column configuration (M = 128 x SM count,
-    three 128-column tiles of N): 4-D plane boxes at N = 384, per-chunk 3-D boxes
-    at N = 380.  Three 128-row tiles are checked."""
+def test_slide_many_row_tiles(dtype, N):
+    """The lifted product at M = 128 x SM count (two 128-row tiles per CTA, many
+    waves of output tiles) with three 128-column tiles of N: 4-D plane boxes at
+    N = 384, per-chunk 3-D boxes at N = 380.  Three 128-row tiles are checked
+    (the first, one in the middle, the last)."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
     sms = torch.cuda.get_device_properties(0).multi_processor_count
