@@ -60,11 +60,36 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(src: str) -> str:
+    """C/C++/CUDA source without comments or blank-line changes: what the compiler sees."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":                      # string or character literal
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def source_sha(*rel):
+    """Hash of the kernel sources' code (comments and blank lines ignored), so a
+    recorded DRAM traffic figure stays attached to the code it was measured on."""
     h = hashlib.sha256()
     for r in rel:
-        with open(os.path.join(ROOT, r), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, r), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
