@@ -148,6 +148,12 @@ typedef struct {
     int32_t dtype; /* SPMM_I8 (-> int32 C); SPMM_F16, SPMM_BF16, SPMM_E4M3 or SPMM_E5M2 (-> fp32 C) */
     void *vals;
     uint8_t *meta;
+    /* Optional, int8 only: vals widened to fp16 once (vals16[M][K/2], device
+     * memory, 16-byte aligned, written by spmm_widen_24 and owned by the caller).
+     * When set, spmm_24 multiplies with it instead of widening vals on every
+     * call (only B is widened per call).  NULL for every other dtype (else
+     * SPMM_ERR_DTYPE). */
+    void *vals16;
 } spmm_24_t;
 
 /* (2n-2):2n sparsity run as 2:4 ("SlideSparse", abstract: sliding window
@@ -242,6 +248,11 @@ SPMM_API spmm_status spmm_wcsr(const spmm_wcsr_t *A, const void *B, int64_t ldb,
 /* Workspace bytes spmm_24 needs (int8 operands are widened to fp16 for the
  * tensor core; 0 for fp16/bf16). */
 SPMM_API spmm_status spmm_24_workspace_size(const spmm_24_t *A, int64_t N, size_t *bytes);
+/* int8 2:4 operand: write its values widened to fp16 (exactly: every int8 is an
+ * fp16 integer) into vals16[M][K/2] (caller-allocated device memory, 16-byte
+ * aligned), for spmm_24_t.vals16.  A->vals16 is not read.  A dtype other than
+ * SPMM_I8 -> SPMM_ERR_DTYPE.  Asynchronous on `stream`. */
+SPMM_API spmm_status spmm_widen_24(const spmm_24_t *A, void *vals16, spmm_stream_t stream);
 /* C = A * B with A 2:4 ("Accelerating Sparse DNNs Based on Tiled GEMM": 2:4
  * executed inside the sparse tensor core).  int8: C is int32 and exact (the
  * kernel accumulates 2048-wide K chunks in fp32, every partial an integer of

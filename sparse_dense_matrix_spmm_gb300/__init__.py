@@ -31,7 +31,7 @@ from . import _lib
 from ._lib import SpmmError
 
 __all__ = ["BCSR", "Mat24", "Slide", "TVW", "CSR", "WCSR", "SpmmError", "spmm_bcsr", "spmm_build_bcsr_count",
-           "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_prune_24", "spmm_24", "spmm_24_workspace_size",
+           "spmm_build_bcsr_fill", "build_bcsr", "spmm_compress_24", "spmm_prune_24", "spmm_widen_24", "spmm_24", "spmm_24_workspace_size",
            "spmm_build_tvw", "spmm_prune_tvw", "spmm_tvw", "spmm_build_wcsr_workspace_size", "spmm_build_wcsr_count",
            "spmm_build_wcsr_fill", "build_wcsr", "spmm_wcsr", "spmm_wcsr_workspace_size",
            "spmm_build_slide", "spmm_slide", "spmm_slide_workspace_size",
@@ -92,9 +92,10 @@ class Mat24:
     dtype: torch.dtype
     vals: torch.Tensor
     meta: torch.Tensor
+    vals16: Optional[torch.Tensor] = None  # int8: vals widened to fp16 once (spmm_widen_24)
 
     def c(self) -> _lib.T24:
-        return _lib.T24(self.M, self.K, _code(self.dtype), _ptr(self.vals), _ptr(self.meta))
+        return _lib.T24(self.M, self.K, _code(self.dtype), _ptr(self.vals), _ptr(self.meta), _ptr(self.vals16))
 
 
 @dataclass
@@ -342,6 +343,15 @@ def spmm_24_workspace_size(A: Mat24, N: int) -> int:
     a = A.c()
     _lib.call("spmm_24_workspace_size", C.byref(a), N, C.byref(n))
     return n.value
+
+
+def spmm_widen_24(A: Mat24, stream=None) -> Mat24:
+    """int8 2:4 operand: the same operand with its values widened to fp16 once
+    (vals16), so that spmm_24 widens only B on each call."""
+    v16 = torch.empty((A.M, A.K // 2), dtype=torch.float16, device=A.vals.device)
+    a = A.c()
+    _lib.call("spmm_widen_24", C.byref(a), _ptr(v16), _stream(stream))
+    return Mat24(A.M, A.K, A.dtype, A.vals, A.meta, v16)
 
 
 def spmm_24(A: Mat24, B: torch.Tensor, C_: Optional[torch.Tensor] = None,

@@ -40,7 +40,7 @@ class WcsrT(C.Structure):
 
 
 class T24(C.Structure):
-    _fields_ = [("M", I64), ("K", I64), ("dtype", I32), ("vals", P), ("meta", P)]
+    _fields_ = [("M", I64), ("K", I64), ("dtype", I32), ("vals", P), ("meta", P), ("vals16", P)]
 
 
 class SlideT(C.Structure):
@@ -64,6 +64,7 @@ SIGNATURES = {
     "spmm_wcsr_workspace_size": (I32, [C.POINTER(WcsrT), I64, C.POINTER(SZ)]),
     "spmm_wcsr": (I32, [C.POINTER(WcsrT), P, I64, P, I64, I64, P, SZ, P]),
     "spmm_24_workspace_size": (I32, [C.POINTER(T24), I64, C.POINTER(SZ)]),
+    "spmm_widen_24": (I32, [C.POINTER(T24), P, P]),
     "spmm_24": (I32, [C.POINTER(T24), P, I64, P, I64, I64, P, SZ, P]),
     "spmm_24_noalloc": (I32, [C.POINTER(T24), P, I64, P, I64, I64, P]),
     "spmm_tvw": (I32, [C.POINTER(TvwT), P, I64, P, I64, I64, P]),

@@ -173,6 +173,7 @@ namespace {
 spmm_status check_24(const spmm_24_t* A, int64_t N) {
     if (!A) return SPMM_ERR_NULL;
     if (!dtype_24(A->dtype)) return SPMM_ERR_DTYPE;
+    if (A->vals16 && A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;  // pre-widened values: int8 only
     if (A->M < 0 || A->K <= 0 || N < 0) return SPMM_ERR_SHAPE;
     if (A->K % (is_fp8(A->dtype) ? 256 : 128)) return SPMM_ERR_SHAPE;  // whole K steps of the kernel
     if (A->M >= (int64_t(1) << 31) || A->K >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
@@ -189,6 +190,7 @@ spmm_status check_24_call(const spmm_24_t* A, const void* B, int64_t ldb, const 
     if (A->M > 0 && N > 0 && (!B || !C)) return SPMM_ERR_NULL;
     if (A->M > 0 && (!A->vals || !A->meta)) return SPMM_ERR_NULL;
     if (ldb < N || ldc < N || !aligned16(A->vals) || !aligned16(A->meta)) return SPMM_ERR_SHAPE;
+    if (A->vals16 && !aligned16(A->vals16)) return SPMM_ERR_SHAPE;
     // B is read by TMA (not for int8, which is widened first): 16-byte aligned rows
     if (A->dtype != SPMM_I8 && ((ldb * dtype_bytes(A->dtype)) % 16 || !aligned16(B))) return SPMM_ERR_SHAPE;
     return SPMM_OK;
@@ -534,6 +536,16 @@ spmm_status spmm_24_workspace_size(const spmm_24_t* A, int64_t N, size_t* bytes)
     if (st != SPMM_OK) return st;
     *bytes = spmm24_workspace_bytes(A, N);
     return SPMM_OK;
+}
+
+spmm_status spmm_widen_24(const spmm_24_t* A, void* vals16, spmm_stream_t stream) {
+    spmm_status st = check_24(A, 0);
+    if (st != SPMM_OK) return st;
+    if (A->dtype != SPMM_I8) return SPMM_ERR_DTYPE;
+    if (A->M == 0) return SPMM_OK;
+    if (!A->vals || !vals16) return SPMM_ERR_NULL;
+    if (!aligned16(A->vals) || !aligned16(vals16)) return SPMM_ERR_SHAPE;
+    return widen_values_24(A->vals, A->M, A->K / 2, vals16, reinterpret_cast<cudaStream_t>(stream));
 }
 
 spmm_status spmm_24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,

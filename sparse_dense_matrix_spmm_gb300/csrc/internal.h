@@ -71,6 +71,8 @@ spmm_status launch_bcsr(const spmm_bcsr_t* A, const void* B, int64_t ldb, float*
                         cudaStream_t stream, const int32_t* row_perm = nullptr);
 
 size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N);
+// int8 stored values (rows x kv, pitch kv) widened to fp16 into dst (pitch kv).
+spmm_status widen_values_24(const void* vals, int64_t rows, int64_t kv, void* dst, cudaStream_t stream);
 spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* C, int64_t ldc, int64_t N,
                           void* ws, cudaStream_t stream);
 size_t slide_workspace_bytes(const spmm_slide_t* A, int64_t N);

@@ -756,32 +756,36 @@ spmm_status launch_sparse(const CUtensorMap& tmA, const CUtensorMap& tmM, const 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // int8 operands: the stored values (rows x kv) and B (kb rows x N) widened to
-// fp16 in the workspace, B with pitch np = N rounded up to 8.
-size_t widen_bytes(int64_t rows, int64_t kv, int64_t kb, int64_t N) {
+// fp16 in the workspace, B with pitch np = N rounded up to 8.  With values
+// widened beforehand (have_a16) only B is.
+size_t widen_bytes(int64_t rows, int64_t kv, int64_t kb, int64_t N, bool have_a16 = false) {
     const int64_t np = (N + 7) / 8 * 8;
-    return align256(static_cast<size_t>(rows) * kv * 2) + align256(static_cast<size_t>(kb) * np * 2);
+    return (have_a16 ? 0 : align256(static_cast<size_t>(rows) * kv * 2)) + align256(static_cast<size_t>(kb) * np * 2);
 }
 
+WidenJob widen_job(const void* src, int64_t lds, __half* dst, int64_t ldd, int64_t r, int64_t cols) {
+    WidenJob j{static_cast<const int8_t*>(src), lds, dst, ldd, r, cols, (ldd + 15) / 16, 0};
+    j.threads = r * j.per_row;
+    return j;
+}
+
+// vals16: the values already widened (the workspace then holds only B), or null.
 spmm_status widen_operands(const void* vals, int64_t rows, int64_t kv, const void* B, int64_t ldb, int64_t kb,
                            int64_t N, void* ws, cudaStream_t stream, const void** vals16, const void** b16,
-                           int64_t* ld16) {
-    __half* wa = static_cast<__half*>(ws);
-    __half* wb = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(rows) * kv * 2));
+                           int64_t* ld16, const void* a16 = nullptr) {
+    __half* wa = a16 ? nullptr : static_cast<__half*>(ws);
+    __half* wb = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) +
+                                           (a16 ? 0 : align256(static_cast<size_t>(rows) * kv * 2)));
     const int64_t np = (N + 7) / 8 * 8;
-    auto job = [](const void* src, int64_t lds, __half* dst, int64_t ldd, int64_t r, int64_t cols) {
-        WidenJob j{static_cast<const int8_t*>(src), lds, dst, ldd, r, cols, (ldd + 15) / 16, 0};
-        j.threads = r * j.per_row;
-        return j;
-    };
-    const WidenJob ja = job(vals, kv, wa, kv, rows, kv);
-    const WidenJob jb = job(B, ldb, wb, np, kb, N);
+    const WidenJob ja = a16 ? widen_job(vals, kv, nullptr, kv, 0, kv) : widen_job(vals, kv, wa, kv, rows, kv);
+    const WidenJob jb = widen_job(B, ldb, wb, np, kb, N);
     const int64_t threads = ja.threads + jb.threads;
     trace_begin(SPMM_KERNEL_WIDEN, stream);
     widen_i8_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(ja, jb);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_WIDEN, stream);
     if (e != cudaSuccess) return SPMM_ERR_CUDA;
-    *vals16 = wa;
+    *vals16 = a16 ? a16 : wa;
     *b16 = wb;
     *ld16 = np;
     return SPMM_OK;
@@ -841,7 +845,17 @@ SpArgs dense_b_args(const DeviceInfo* dev, int64_t M, int64_t K, int64_t N, int3
 }  // namespace
 
 size_t spmm24_workspace_bytes(const spmm_24_t* A, int64_t N) {
-    return A->dtype == SPMM_I8 ? widen_bytes(A->M, A->K / 2, A->K, N) : 0;
+    return A->dtype == SPMM_I8 ? widen_bytes(A->M, A->K / 2, A->K, N, A->vals16 != nullptr) : 0;
+}
+
+spmm_status widen_values_24(const void* vals, int64_t rows, int64_t kv, void* dst, cudaStream_t stream) {
+    const WidenJob ja = widen_job(vals, kv, static_cast<__half*>(dst), kv, rows, kv);
+    const WidenJob jb = widen_job(vals, kv, nullptr, kv, 0, kv);
+    trace_begin(SPMM_KERNEL_WIDEN, stream);
+    widen_i8_kernel<<<static_cast<unsigned>((ja.threads + 255) / 256), 256, 0, stream>>>(ja, jb);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_WIDEN, stream);
+    return cuda_status(e);
 }
 
 // fp8 operands (kind::f8f6f4): A's stored bytes in 128 x 128-byte boxes, B in
@@ -877,7 +891,8 @@ spmm_status launch_spmm24(const spmm_24_t* A, const void* B, int64_t ldb, void* 
     int64_t bld = ldb;
     const CUtensorMapDataType t = i8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : half_type(A->dtype);
     if (i8) {
-        const spmm_status st = widen_operands(A->vals, A->M, A->K / 2, B, ldb, A->K, N, ws, stream, &vals, &bsrc, &bld);
+        const spmm_status st =
+            widen_operands(A->vals, A->M, A->K / 2, B, ldb, A->K, N, ws, stream, &vals, &bsrc, &bld, A->vals16);
         if (st != SPMM_OK) return st;
     }
     CUtensorMap tmA, tmM;

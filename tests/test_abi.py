@@ -53,7 +53,7 @@ def test_struct_layouts_match_c():
     # sizes of the format structs as laid out by the C compiler (x86-64 / aarch64 LP64)
     from sparse_dense_matrix_spmm_gb300 import _lib
     assert ctypes.sizeof(_lib.BcsrT) == 8 * 2 + 4 * 2 + 8 + 8 + 8 * 3
-    assert ctypes.sizeof(_lib.T24) == 8 * 2 + 8 + 8 * 2
+    assert ctypes.sizeof(_lib.T24) == 8 * 2 + 8 + 8 * 3
     assert ctypes.sizeof(_lib.TvwT) == 8 * 2 + 4 * 2 + 8 * 2 + 8 * 4
     assert ctypes.sizeof(_lib.WcsrT) == 8 * 3 + 4 * 3 + 4 + 8 * 3 + 8 * 9
     assert ctypes.sizeof(_lib.SlideT) == 8 * 2 + 4 * 2 + 8 * 2
@@ -130,3 +130,23 @@ def test_sddmm_validation():
     assert L.spmm_sddmm(ctypes.byref(SF), 16, 16, 16, 16, 16, 16, None) == 3     # fp8 -> SPMM_ERR_DTYPE
     E = _lib.CsrT(64, 64, 0, 1, None, None, None)
     assert L.spmm_sddmm(ctypes.byref(E), 16, None, 16, None, 16, None, None) == 0  # no entries: nothing to do
+
+
+def test_widened_values_validation():
+    """spmm_widen_24 and a pre-widened vals16 are int8 only; a NULL destination or
+    an unaligned vals16 is refused before any launch."""
+    from sparse_dense_matrix_spmm_gb300 import _lib
+    L = _lib.load()
+    f16 = _lib.T24(128, 256, 1, 16, 16, None)
+    assert L.spmm_widen_24(ctypes.byref(f16), 16, None) == 3                  # fp16 -> SPMM_ERR_DTYPE
+    i8 = _lib.T24(128, 256, 2, 16, 16, None)
+    assert L.spmm_widen_24(ctypes.byref(i8), None, None) == 1                 # no destination -> SPMM_ERR_NULL
+    assert L.spmm_widen_24(ctypes.byref(i8), 8, None) == 2                    # unaligned -> SPMM_ERR_SHAPE
+    f16w = _lib.T24(128, 256, 1, 16, 16, 32)
+    n = ctypes.c_size_t(0)
+    assert L.spmm_24_workspace_size(ctypes.byref(f16w), 64, ctypes.byref(n)) == 3  # vals16 on fp16 -> DTYPE
+    i8w = _lib.T24(128, 256, 2, 16, 16, 32)
+    assert L.spmm_24_workspace_size(ctypes.byref(i8w), 64, ctypes.byref(n)) == 0
+    m = ctypes.c_size_t(0)
+    assert L.spmm_24_workspace_size(ctypes.byref(i8), 64, ctypes.byref(m)) == 0
+    assert m.value > n.value > 0                                              # only B is widened per call

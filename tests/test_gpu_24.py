@@ -33,6 +33,29 @@ def test_24_int8_exact(M, K, N):
     assert np.array_equal(C.cpu().numpy().astype(np.int64), ref)
 
 
+@pytest.mark.parametrize("M,K,N", [(384, 2048, 520), (200, 1024, 136)])
+def test_24_int8_prewidened_values(M, K, N):
+    """Values widened to fp16 once (spmm_widen_24) are the int8 values exactly, and
+    spmm_24 with them (only B widened per call, a smaller workspace) equals the
+    per-call path and the oracle bit for bit, on two different right-hand sides."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.mask24_problem(M, K, N, seed=M + 7)
+    F, O = _compress(p, "i8")
+    W = spmm.spmm_widen_24(F)
+    torch.cuda.synchronize()
+    assert torch.equal(W.vals16.float(), F.vals.float())
+    assert spmm.spmm_24_workspace_size(W, N) < spmm.spmm_24_workspace_size(F, N)
+    B1 = dev(p["B"])
+    B2 = torch.flip(B1, dims=[1]).contiguous()
+    for B, Bh in ((B1, p["B"]), (B2, np.ascontiguousarray(p["B"][:, ::-1]))):
+        C = spmm.spmm_24(W, B)
+        torch.cuda.synchronize()
+        assert spmm.last_device_error() == 0
+        assert torch.equal(C, spmm.spmm_24(F, B))
+        assert np.array_equal(C.cpu().numpy().astype(np.int64), oracle.spmm24(O, Bh))
+
+
 def test_24_int8_extreme_values_stay_exact():
     """Every product 127*127 with equal signs: the kernel drains its fp32
     accumulator every 2048 dense K, so each chunk of 1024 products reaches the

@@ -95,3 +95,19 @@ def test_noalloc_bf16_needs_no_scratch():
     O = oracle.compress24(p["A"], "bf16")
     assert_close(C.cpu().numpy(), oracle.spmm24(O, p["B"]), "noalloc bf16")
     assert spmm.last_device_error() == 0
+
+
+def test_noalloc_with_prewidened_values():
+    """With values widened beforehand the entry point needs scratch for B only, and
+    its result equals the oracle's bit for bit."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    M, K, N = 256, 2048, 200
+    p = gen.mask24_problem(M, K, N, seed=9)
+    W = spmm.spmm_widen_24(spmm.spmm_compress_24(dev(p["A"])))
+    C = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
+    assert _call_noalloc(W, dev(p["B"]), C, N) == 0
+    torch.cuda.synchronize()
+    O = oracle.compress24(p["A"], "i8")
+    assert np.array_equal(C.cpu().numpy().astype(np.int64), oracle.spmm24(O, p["B"]))
+    assert spmm.last_device_error() == 0
