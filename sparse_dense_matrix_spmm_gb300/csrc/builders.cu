@@ -108,12 +108,44 @@ __device__ void bcsr_flags(const T* dense, int64_t ld, int br, int bh, int gk, i
     __syncthreads();
 }
 
+// Any element of a 16-byte piece nonzero (the rule of nz, per element).
 template <typename T>
+__device__ __forceinline__ bool nz16(const uint4& v);
+template <>
+__device__ __forceinline__ bool nz16<uint16_t>(const uint4& v) { return ((v.x | v.y | v.z | v.w) & 0x7FFF7FFFu) != 0u; }
+template <>
+__device__ __forceinline__ bool nz16<int8_t>(const uint4& v) { return (v.x | v.y | v.z | v.w) != 0u; }
+
+// The same flags from 16-byte pieces (VEC: rows and block columns 16-byte
+// aligned, bh * K / 8 < 2^31): consecutive threads read consecutive pieces of
+// a row, four loads in flight per thread, and a piece's block column comes
+// from 32-bit arithmetic.
+template <typename T>
+__device__ void bcsr_flags_vec(const T* dense, int64_t ld, int br, int bh, int gk, int bw, uint8_t* flags) {
+    for (int bc = threadIdx.x; bc < gk; bc += blockDim.x) flags[bc] = 0;
+    __syncthreads();
+    constexpr int E = 16 / static_cast<int>(sizeof(T));
+    const int ppr = gk * (bw / E), ppb = bw / E;  // pieces per row, per block column
+    const int total = bh * ppr;
+    const T* base = dense + static_cast<int64_t>(br) * bh * ld;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int r = i / ppr, pc = i - r * ppr;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(r) * ld) + pc);
+        if (nz16<T>(v)) flags[pc / ppb] = 1;  // benign same-value race
+    }
+    __syncthreads();
+}
+
+template <typename T, bool VEC>
 __global__ void bcsr_count_kernel(const T* dense, int64_t ld, int bh, int bw, int gk, int32_t* row_ptr) {
     extern __shared__ uint8_t flags[];
     __shared__ int32_t sh[33];
     const int br = blockIdx.x;
-    bcsr_flags<T>(dense, ld, br, bh, gk, bw, flags);
+    if constexpr (VEC)
+        bcsr_flags_vec<T>(dense, ld, br, bh, gk, bw, flags);
+    else
+        bcsr_flags<T>(dense, ld, br, bh, gk, bw, flags);
     int32_t cnt = 0;
     for (int bc = threadIdx.x; bc < gk; bc += blockDim.x) cnt += flags[bc];
     int32_t total = 0;
@@ -121,7 +153,7 @@ __global__ void bcsr_count_kernel(const T* dense, int64_t ld, int bh, int bw, in
     if (threadIdx.x == 0) row_ptr[br] = total;
 }
 
-template <typename T>
+template <typename T, bool VEC>
 __global__ void bcsr_fill_kernel(const T* dense, int64_t ld, int bh, int bw, int gk, const int32_t* row_ptr,
                                  int32_t* col_idx, T* vals) {
     extern __shared__ uint8_t smem[];
@@ -129,7 +161,10 @@ __global__ void bcsr_fill_kernel(const T* dense, int64_t ld, int bh, int bw, int
     int32_t* pos = reinterpret_cast<int32_t*>(smem + ((gk + 15) & ~15));
     __shared__ int32_t sh[33];
     const int br = blockIdx.x;
-    bcsr_flags<T>(dense, ld, br, bh, gk, bw, flags);
+    if constexpr (VEC)
+        bcsr_flags_vec<T>(dense, ld, br, bh, gk, bw, flags);
+    else
+        bcsr_flags<T>(dense, ld, br, bh, gk, bw, flags);
     // positions of the stored blocks inside this block row, in ascending bc
     const int per = (gk + blockDim.x - 1) / blockDim.x;
     const int b0 = min(gk, static_cast<int>(threadIdx.x) * per), b1 = min(gk, b0 + per);
@@ -147,12 +182,38 @@ __global__ void bcsr_fill_kernel(const T* dense, int64_t ld, int bh, int bw, int
     const int64_t blk = static_cast<int64_t>(bh) * bw;
     const int64_t K = static_cast<int64_t>(gk) * bw;
     const T* base = dense + static_cast<int64_t>(br) * bh * ld;
-    for (int64_t e = threadIdx.x; e < static_cast<int64_t>(bh) * K; e += blockDim.x) {
-        const int64_t r = e / K, c = e % K;
-        const int bc = static_cast<int>(c / bw);
-        if (!flags[bc]) continue;
-        vals[(first + pos[bc]) * blk + r * bw + (c % bw)] = base[r * ld + c];
+    if constexpr (VEC) {
+        // the stored blocks' 16-byte pieces, in the same order as the flag pass
+        constexpr int E = 16 / static_cast<int>(sizeof(T));
+        const int ppr = gk * (bw / E), ppb = bw / E;
+        const int total = bh * ppr;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < total; i += blockDim.x) {
+            const int r = i / ppr, pc = i - r * ppr, bc = pc / ppb;
+            if (!flags[bc]) continue;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(r) * ld) + pc);
+            *reinterpret_cast<uint4*>(vals + (first + pos[bc]) * blk + static_cast<int64_t>(r) * bw + (pc - bc * ppb) * E) = v;
+        }
+    } else {
+        for (int64_t e = threadIdx.x; e < static_cast<int64_t>(bh) * K; e += blockDim.x) {
+            const int64_t r = e / K, c = e % K;
+            const int bc = static_cast<int>(c / bw);
+            if (!flags[bc]) continue;
+            vals[(first + pos[bc]) * blk + r * bw + (c % bw)] = base[r * ld + c];
+        }
     }
+}
+
+// One CTA per block row; 1024 threads keep enough 16-byte loads in flight when
+// a matrix has only a few hundred block rows.
+constexpr int kBcsrBuildThreads = 1024;
+
+// 16-byte pieces for the BCSR builders: aligned base and row pitch, block
+// columns a whole number of pieces, piece indices of a block row in 32 bits.
+bool bcsr_vec(const void* dense, int64_t ld, int64_t K, int bh, int bw, int es, const void* vals) {
+    return reinterpret_cast<uintptr_t>(dense) % 16 == 0 && (ld * es) % 16 == 0 && (bw * es) % 16 == 0 &&
+           (vals == nullptr || reinterpret_cast<uintptr_t>(vals) % 16 == 0) &&
+           static_cast<int64_t>(bh) * K * es / 16 < (int64_t(1) << 31);
 }
 
 // ---------------------------------------------------------------- 2:4
@@ -501,12 +562,19 @@ spmm_status run_bcsr_count(const void* dense, int64_t M, int64_t K, int64_t ld, 
     const int nbr = static_cast<int>(M / bh), gk = static_cast<int>(K / bw);
     const int smem = gk;
     if (nbr > 0 && gk > 0) {
-        if (dtype == SPMM_I8)
-            bcsr_count_kernel<int8_t>
-                <<<nbr, 256, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk, row_ptr);
+        const bool vec = bcsr_vec(dense, ld, K, bh, bw, dtype == SPMM_I8 ? 1 : 2, nullptr);
+        if (dtype == SPMM_I8 && vec)
+            bcsr_count_kernel<int8_t, true>
+                <<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk, row_ptr);
+        else if (dtype == SPMM_I8)
+            bcsr_count_kernel<int8_t, false>
+                <<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk, row_ptr);
+        else if (vec)
+            bcsr_count_kernel<uint16_t, true>
+                <<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw, gk, row_ptr);
         else
-            bcsr_count_kernel<uint16_t>
-                <<<nbr, 256, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw, gk, row_ptr);
+            bcsr_count_kernel<uint16_t, false>
+                <<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw, gk, row_ptr);
         if (cudaGetLastError() != cudaSuccess) return SPMM_ERR_CUDA;
     } else if (nbr > 0) {
         if (cudaMemsetAsync(row_ptr, 0, sizeof(int32_t) * nbr, s) != cudaSuccess) return SPMM_ERR_CUDA;
@@ -527,12 +595,19 @@ spmm_status run_bcsr_fill(const void* dense, int64_t M, int64_t K, int64_t ld, i
     const int nbr = static_cast<int>(M / bh), gk = static_cast<int>(K / bw);
     const int smem = ((gk + 15) & ~15) + 4 * gk;
     if (nbr == 0 || gk == 0) return SPMM_OK;
-    if (dtype == SPMM_I8)
-        bcsr_fill_kernel<int8_t><<<nbr, 256, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk, row_ptr,
-                                                        col_idx, static_cast<int8_t*>(vals));
+    const bool vec = bcsr_vec(dense, ld, K, bh, bw, dtype == SPMM_I8 ? 1 : 2, vals);
+    if (dtype == SPMM_I8 && vec)
+        bcsr_fill_kernel<int8_t, true><<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk,
+                                                              row_ptr, col_idx, static_cast<int8_t*>(vals));
+    else if (dtype == SPMM_I8)
+        bcsr_fill_kernel<int8_t, false><<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const int8_t*>(dense), ld, bh, bw, gk,
+                                                               row_ptr, col_idx, static_cast<int8_t*>(vals));
+    else if (vec)
+        bcsr_fill_kernel<uint16_t, true><<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw,
+                                                                gk, row_ptr, col_idx, static_cast<uint16_t*>(vals));
     else
-        bcsr_fill_kernel<uint16_t><<<nbr, 256, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw, gk,
-                                                          row_ptr, col_idx, static_cast<uint16_t*>(vals));
+        bcsr_fill_kernel<uint16_t, false><<<nbr, kBcsrBuildThreads, smem, s>>>(static_cast<const uint16_t*>(dense), ld, bh, bw,
+                                                                 gk, row_ptr, col_idx, static_cast<uint16_t*>(vals));
     return cuda_status(cudaGetLastError());
 }
 

@@ -107,3 +107,33 @@ def test_bcsr_64_row_blocks_padded_strides():
     O = oracle.bcsr_build(p["A"], 64, 64, "bf16")
     assert_close(out.cpu().numpy(), oracle.bcsr_spmm(O, p["B"]), "64-row blocks, padded")
     assert (Cpad[:, 320:] == -1.0).all().item()
+
+
+@pytest.mark.parametrize("dtype,pad", [("bf16", 0), ("bf16", 4), ("i8", 0), ("i8", 3)])
+def test_bcsr_builder_pitches(dtype, pad):
+    """The builder's 16-byte path (aligned row pitch) and its element path (a pitch
+    of K + 4 bf16 or K + 3 int8 elements) both give the oracle's row_ptr, col_idx
+    and values bit for bit, for 16-bit and int8 operands (-0.0 and NaN included
+    for bf16)."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    M, K, bh, bw = 256, 512, 32, 64
+    p = gen.bcsr_problem(M, K, 8, bh, bw, 20, seed=31 + pad, dtype="bf16")
+    if dtype == "i8":
+        rng = np.random.default_rng(pad)
+        A = np.where(p["A"] != 0, rng.integers(-128, 128, size=(M, K)), 0).astype(np.int8)
+        Ad = torch.zeros((M, K + pad), dtype=torch.int8, device="cuda")
+        Ad[:, :K] = torch.from_numpy(A).cuda()
+    else:
+        A = p["A"].copy()
+        A[0, 0] = 0x8000                       # -0.0: zero, its block not stored unless other entries are
+        A[5, 70] = 0x7FC0                      # NaN: nonzero
+        Ad = torch.zeros((M, K + pad), dtype=torch.bfloat16, device="cuda")
+        Ad[:, :K] = dev_half(A, "bf16")
+    F = spmm.build_bcsr(Ad[:, :K], bh, bw)
+    O = oracle.bcsr_build(A, bh, bw, dtype)
+    assert F.nnzb == O["nnzb"]
+    assert np.array_equal(F.row_ptr.cpu().numpy(), O["row_ptr"])
+    assert np.array_equal(F.col_idx.cpu().numpy(), O["col_idx"])
+    got = F.vals.cpu().numpy() if dtype == "i8" else host_bits(F.vals)
+    assert np.array_equal(got.reshape(O["vals"].shape), O["vals"])
