@@ -7,8 +7,11 @@
 // into shared memory) and the 2:4 pattern executes inside the sparse tensor
 // core (here: tcgen05.mma.sp with the 2-bit indices in TMEM).
 //
-// Roles (one CTA per SM, persistent over 128 x 128 output tiles; 352 threads for
-// 2:4, 608 for TVW):
+// Roles (one CTA per SM, persistent over output tiles).  Described here for one
+// 128-row tile per CTA (352 threads for 2:4, 608 for TVW); with two row tiles
+// per CTA (see Tile: 256 x 128 output tiles) three producers own one stage
+// each, the other roles move up one warp, the MMA issuer issues each stage's
+// MMAs for both row tiles, and int8 uses sixteen epilogue warps (768 threads):
 //   warps 0-1  producers, taking alternate stages of one ring: per 128-wide
 //              dense-K step, TMA loads of the compressed A tile (128 x 64,
 //              K-major, 128B swizzle), for TVW its metadata (128 x 16 B) and, for
@@ -37,8 +40,9 @@
 // a TMEM column whose index is a multiple of 8.
 //
 // int8 operands: the tensor core on sm_103a has no integer MMA, so int8 values
-// (exact in fp16) are widened to fp16 in a workspace and multiplied with fp32
-// accumulation.  Every product is an integer of magnitude at most 127*127; the
+// (exact in fp16) are multiplied as fp16 with fp32 accumulation: B is widened in
+// the workspace on every call, the stored values too unless the operand carries
+// them widened already (spmm_24_t.vals16).  Every product is an integer of magnitude at most 127*127; the
 // accumulator is drained every 2048 dense K (1024 products, |partial| <=
 // 16 516 096 < 2^24, so every partial sum is an exactly representable integer)
 // and the chunks are summed in int32 by the epilogue, so C is exact.
