@@ -98,6 +98,7 @@ KERNEL_SOURCES = {
     "bcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/bcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "wcsr_spmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "wcsr_tc_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
+    "wcsr_ts_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/wcsr.cu", "sparse_dense_matrix_spmm_gb300/csrc/sm103.cuh"),
     "sddmm_kernel": ("sparse_dense_matrix_spmm_gb300/csrc/sddmm.cu",),
 }
 
@@ -598,7 +599,10 @@ def run_extra(name, args, ws, peaks, flush_buf):
         # the library's rule: tensor core when >= 4 nonzeros per window column and >= 384 per work unit
         tcore = F.nnz >= 4 * F.n_wcols and F.nnz >= 384 * F.n_units
         extra_fields["window_products"] = "tensor core" if tcore else "CUDA cores"
-        wkern = "wcsr_tc_kernel" if tcore else "wcsr_spmm_kernel"
+        # and of the tensor-core kernels, the streaming one for windows of <= 16 rows
+        # and <= 32 steps per unit
+        stream = F.h <= 16 and F.S <= 32
+        wkern = ("wcsr_ts_kernel" if stream else "wcsr_tc_kernel") if tcore else "wcsr_spmm_kernel"
         Cd = torch.empty((c["M"], c["N"]), dtype=torch.float32, device="cuda")
         wsp = torch.zeros(max(1, spmm.spmm_wcsr_workspace_size(F, c["N"])), dtype=torch.uint8, device="cuda")
         nnz = csr.nnz

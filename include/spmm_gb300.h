@@ -234,14 +234,20 @@ SPMM_API spmm_status spmm_bcsr(const spmm_bcsr_t *A, const void *B, int64_t ldb,
 SPMM_API spmm_status spmm_wcsr_workspace_size(const spmm_wcsr_t *A, int64_t N, size_t *bytes);
 /* C = A * B with A in row-window CSR ("AsyncSparse", abstract and Fig. 2:
  * the sparse operand loaded per row window, long windows split across thread
- * blocks).  Each window's product runs on the tensor core: for every 16 of its
- * column slots, D (128 output columns x h rows) += (the 16 gathered B rows)^T
- * x (the window's h x 16 value tile)^T with fp32 accumulation in TMEM.  Split
- * windows are summed in split order by the last unit to finish, so results are
- * run-to-run identical.  The workspace needs no clearing: its counters carry
- * a per-call tag, so a call that stopped early (a timed-out wait) does not
- * affect later ones; calls sharing one workspace must not overlap on the GPU.
- * h <= 64.  fp16/bf16 in, fp32 C. */
+ * blocks).  Where windows reuse their columns (at least 4 nonzeros per
+ * distinct window column and 384 per work unit) each window's product runs on
+ * the tensor core: for every 16 of its column slots, D (128 output columns x h
+ * rows) += (the 16 gathered B rows)^T x (the window's h x 16 value tile)^T with
+ * fp32 accumulation in TMEM (windows of <= 16 rows with S <= 32 in a streaming
+ * kernel whose gathers run ahead of the MMAs, taller windows per item);
+ * otherwise each nonzero's B row is gathered and multiplied on CUDA cores.
+ * Split windows are summed in split order by the last unit to finish, so
+ * results are run-to-run identical.  The workspace needs no clearing: its
+ * counters carry a per-call tag, so a call that stopped early (a timed-out
+ * wait) does not affect later ones; calls sharing one workspace must not
+ * overlap on the GPU.  h <= 64.  fp16/bf16 in, fp32 C.  B (K x N, row pitch
+ * ldb elements) must start on a 16-byte boundary with ldb a multiple of 8,
+ * else SPMM_ERR_SHAPE. */
 SPMM_API spmm_status spmm_wcsr(const spmm_wcsr_t *A, const void *B, int64_t ldb, float *C, int64_t ldc, int64_t N,
                                void *workspace, size_t workspace_bytes, spmm_stream_t stream);
 

@@ -1061,6 +1061,422 @@ __global__ void __launch_bounds__(kThreads, 1) wcsr_tc_kernel(const Args a) {
 
 }  // namespace tc
 
+// ---------------------------------------------------------------- streaming tensor-core product
+// The same window products as tc::wcsr_tc_kernel (D (128 x Np) += G (128 x 16)
+// W^T (16 x Np) per 16 column slots), with the work split by role instead of by
+// item, so that the gathers of later items proceed while earlier items are
+// prepared, multiplied and written out.  One CTA per SM, persistent over items
+// (unit, 128-column slab); windows of at most 16 rows (Np = 16).
+//   warps 0-7   preparation, one item per warp at a time (item i to warp i % 8,
+//               its own item slot): the unit header, its column list, its
+//               values into the slot's W tiles (all steps of the item: at most
+//               32, 16 KB), then the item record.  Each item's chain of dependent
+//               loads is several L2 round trips, so eight are prepared at once.
+//   warps 8-15  gathers: items alternate between two rings of 8 stages (4 KB
+//               each), one per MMA issuer; step t of a ring's sequence of (item,
+//               K step) goes to warp 8 + t % 8, which copies the step's 16 B rows
+//               into stage t % 8 of that ring with 16-byte cp.async copies (no
+//               registers held: both rings can be in flight).
+//   warps 16-17 MMA issuers, items alternating between them: one thread each
+//               issues its items' steps (M = 128 output columns, N = 16 window
+//               rows, K = 16 slots) into the item's accumulator (two per issuer
+//               in TMEM) and commits each stage back to the gathers.  With one
+//               issuer its per-step waits and issue latency bounded the kernel
+//               (clustered windows: 76 us against 62 us with two).
+//   warps 18-21 epilogue: per item, read the accumulator (TMEM lane quarter =
+//               32 output columns) and write C, or a partial tile and the
+//               split-window fix-up as in tc::wcsr_tc_kernel.
+// Every stage has exactly one filling warp and one consuming issuer, so no
+// party can run two phases ahead of a parity wait (a shared ring let one issuer
+// take a stage two fills early).  An item slot is reused once its gathers, both
+// issuers and its epilogue have all let go of it; every wait is bounded.
+namespace ts {
+
+constexpr int kPrepWarps = 8, kGatherWarps = 8, kEpiWarps = 4;
+constexpr int kIssuers = 2;  // MMA-issuing warps (alternate items, own stage ring, two accumulators each)
+constexpr int kGroup = 1;    // steps whose stages are waited for together before their MMAs (more: slower)
+constexpr int kGatherWarp0 = kPrepWarps, kMmaWarp = kGatherWarp0 + kGatherWarps, kEpiWarp0 = kMmaWarp + kIssuers;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kSlab = 128;
+constexpr int kNp = 16;                                  // MMA N: windows of at most 16 rows
+constexpr int kSlots = kPrepWarps;                       // item slots: one per preparing warp
+constexpr int kAcc = 2 * kIssuers;                       // TMEM accumulators (two per issuer)
+constexpr int kStages = 16;                              // gather stages, split into one ring per issuer
+constexpr int kRing = kStages / kIssuers;                // so every stage has one filler and one consumer
+static_assert(kStages % kIssuers == 0 && kGroup <= kRing, "ring split");
+// gathering warp g fills the steps t with t % kGatherWarps == g; a stage filled by two warps
+// could see one of them two fills ahead of the other, which a parity wait cannot tell apart
+static_assert(kRing % kGatherWarps == 0, "one filling warp per stage");
+constexpr uint32_t kStepBytes = 16 * kSlab * 2;          // 16 gathered rows of 256 bytes
+constexpr uint32_t kTile = kNp * 32;                     // one step's W tile (16 rows x 16 slots, fp16)
+constexpr int kMaxSteps = 32;                            // 512 column slots per unit at most (S <= 32)
+constexpr uint32_t kWBytes = kMaxSteps * kTile;          // 16 KB per item slot
+constexpr uint32_t kColBytes = kMaxSteps * 16 * 4;       // 2 KB per item slot
+constexpr uint32_t kRingOff = 0;
+constexpr uint32_t kWOff = kRingOff + kStages * kStepBytes;
+constexpr uint32_t kColOff = kWOff + kSlots * kWBytes;
+constexpr uint32_t kRecOff = kColOff + kSlots * kColBytes;
+constexpr uint32_t kBarOff = kRecOff + kSlots * 64;
+// barriers: item_full, item_empty [kSlots]; stage_full, stage_empty [kStages]; acc_full, acc_empty [kAcc];
+// done [kIssuers]
+constexpr int kBars = 2 * kSlots + 2 * kStages + 2 * kAcc + kIssuers;
+constexpr uint32_t kSmem = 1024 + kBarOff + 8 * kBars + 16 + 16;
+static_assert(kStepBytes % 1024 == 0 && kWOff % 1024 == 0, "swizzle alignment of the stages");
+static_assert(kSmem <= 232448, "shared memory per block");
+// item_empty: every gathering warp, every MMA issuer (each reads the step count) and every epilogue warp
+constexpr int kItemUsers = kGatherWarps + kIssuers + kEpiWarps;
+static_assert(kAcc % kIssuers == 0, "issuer j owns accumulators j, j + kIssuers, ...");
+
+struct Rec {
+    int32_t u, w, n0, r0, nrows, Tu, nk, U, u0, ok;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) wcsr_ts_kernel(const tc::Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t s0 = ptx::smem_u32(smem);
+    const uint32_t bar0 = s0 + kBarOff;
+    auto item_full = [&](int i) { return bar0 + 8u * i; };
+    auto item_empty = [&](int i) { return bar0 + 8u * (kSlots + i); };
+    auto stage_full = [&](int s) { return bar0 + 8u * (2 * kSlots + s); };
+    auto stage_empty = [&](int s) { return bar0 + 8u * (2 * kSlots + kStages + s); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 * kStages + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 * kStages + kAcc + b); };
+    auto done_bar = [&](int j) { return bar0 + 8u * (2 * kSlots + 2 * kStages + 2 * kAcc + j); };
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kBars);
+    int* s_last = reinterpret_cast<int*>(smem + kBarOff + 8 * kBars + 16);
+    Rec* recs = reinterpret_cast<Rec*>(smem + kRecOff);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kSlots; ++i) {
+            ptx::mbar_init(item_full(i), 1);
+            ptx::mbar_init(item_empty(i), kItemUsers);
+        }
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(stage_full(s), 32);  // one cp.async arrival per lane of the gathering warp
+            ptx::mbar_init(stage_empty(s), 1);
+        }
+        for (int b = 0; b < kAcc; ++b) {
+            ptx::mbar_init(acc_full(b), 1);
+            ptx::mbar_init(acc_empty(b), kEpiWarps);
+        }
+        for (int j = 0; j < kIssuers; ++j) ptx::mbar_init(done_bar(j), 1);
+        ptx::fence_mbar_init();
+    }
+    constexpr uint32_t kTmemCols = kAcc * kNp <= 32 ? 32u : (kAcc * kNp <= 64 ? 64u : 128u);
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tslot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (threadIdx.x < a.pf_n) {
+        // L2 warm-up: this CTA's share of one of the format arrays or B
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.pf_ptr[threadIdx.x]);
+        const int64_t n = a.pf_bytes[threadIdx.x];
+        const uintptr_t lo = (b0 + n * blockIdx.x / gridDim.x + 15) & ~uintptr_t(15);
+        uintptr_t hi = (b0 + n * (blockIdx.x + 1) / gridDim.x) & ~uintptr_t(15);
+        const uintptr_t end = (b0 + n) & ~uintptr_t(15);
+        if (hi > end) hi = end;
+        for (uintptr_t x = lo; x < hi; x += 65536u)
+            ptx::bulk_prefetch_l2(reinterpret_cast<const void*>(x), static_cast<uint32_t>(hi - x < 65536u ? hi - x : 65536u));
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+
+    if (warp < kPrepWarps) {
+        // -------------------------------------------------------- preparation
+        const int pw = warp;  // this warp prepares items pw, pw + kPrepWarps, ... in slot pw
+        bool ok = true;
+        for (int ic = pw; ok && first + static_cast<int64_t>(ic) * stride < a.n_items; ic += kPrepWarps) {
+            const int64_t id = first + static_cast<int64_t>(ic) * stride;
+            const int slot = ic % kSlots;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(item_empty(slot), (static_cast<uint32_t>(ic / kSlots) & 1u) ^ 1u,
+                                                        a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT))) {
+                ok = false;
+                break;
+            }
+            const tc::Item it = tc::load_item(a, id);
+            const int nk = it.ok ? it.nk : 0;
+            int32_t* cols = reinterpret_cast<int32_t*>(smem + kColOff + slot * kColBytes);
+            const uint32_t wt = s0 + kWOff + slot * kWBytes;
+            // the column list (at most 16 slots per lane, all loads in flight together)
+            int cv[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int e = lane + 32 * k;
+                cv[k] = (e < 16 * nk && e < it.Tu) ? __ldg(a.wcols + it.wbase + it.slot0 + e) : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int e = lane + 32 * k;
+                if (e < 16 * nk) {
+                    const bool good = cv[k] >= 0 && cv[k] < a.K;
+                    if (e < it.Tu && !good) atomicOr(a.err, SPMM_DEVERR_INDEX);
+                    cols[e] = good ? cv[k] : -1;
+                }
+            }
+            for (uint32_t o = 16u * lane; o < static_cast<uint32_t>(nk) * kTile; o += 16u * 32u)
+                ptx::st_shared_v4(wt + o, make_uint4(0u, 0u, 0u, 0u));
+            __syncwarp();
+            // the unit's nonzeros into their W tiles, eight per lane loaded together
+            if (it.ok) {
+                for (int e0 = it.nz0 + lane; e0 < it.nz1; e0 += 32 * 8) {
+                    int lr[8], sl[8];
+                    uint16_t v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int e = e0 + 32 * k;
+                        lr[k] = 255;
+                        sl[k] = -1;
+                        v[k] = 0;
+                        if (e < it.nz1) {
+                            lr[k] = a.lrow[e];
+                            sl[k] = __ldg(a.slot + e) - it.slot0;
+                            v[k] = __ldg(a.val + e);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if (e0 + 32 * k >= it.nz1) continue;
+                        if (sl[k] < 0 || sl[k] >= it.Tu || lr[k] >= it.nrows) {
+                            atomicOr(a.err, SPMM_DEVERR_INDEX);  // skipped
+                            continue;
+                        }
+                        const int kx = sl[k] & 15;
+                        tc::st_shared_u16(wt + (sl[k] >> 4) * kTile + (lr[k] >> 3) * 256u + (kx >> 3) * 128u +
+                                              (lr[k] & 7) * 16u + (kx & 7) * 2u,
+                                          v[k]);
+                    }
+                }
+            } else if (lane == 0) {
+                atomicOr(a.err, SPMM_DEVERR_INDEX);  // malformed unit list: the item is skipped
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                recs[slot] = Rec{it.u, it.w, it.n0, it.r0, it.nrows, it.Tu, nk, it.U, it.u0, it.ok ? 1 : 0};
+                ptx::mbar_arrive(item_full(slot));
+            }
+        }
+    } else if (warp < kMmaWarp) {
+        // -------------------------------------------------------- gathers
+        const int g = warp - kGatherWarp0;
+        const int hl = lane & 15, hi = lane >> 4, gq = hl % 8;
+        const uint32_t piece_off = static_cast<uint32_t>(hl / 8) * 2048u;
+        int ic = 0;
+        int64_t tr[kIssuers];  // steps of earlier items, per ring
+#pragma unroll
+        for (int r = 0; r < kIssuers; ++r) tr[r] = 0;
+        bool ok = true;
+        for (int64_t id = first; id < a.n_items && ok; id += stride, ++ic) {
+            const int slot = ic % kSlots, ring = ic % kIssuers;
+            int64_t t0 = tr[0];
+#pragma unroll
+            for (int r = 1; r < kIssuers; ++r)
+                if (ring == r) t0 = tr[r];
+            // every wait's outcome is made warp-uniform, so the warp leaves together
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(item_full(slot), static_cast<uint32_t>(ic / kSlots) & 1u,
+                                                        a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT))) {
+                ok = false;
+                break;
+            }
+            const int nk = recs[slot].nk;
+            const int64_t n = static_cast<int64_t>(recs[slot].n0) + 8 * hl;
+            const int32_t* cols = reinterpret_cast<const int32_t*>(smem + kColOff + slot * kColBytes);
+            for (int k = static_cast<int>((g - t0 % kGatherWarps + kGatherWarps) % kGatherWarps); k < nk;
+                 k += kGatherWarps) {
+                const int64_t t = t0 + k;
+                const int s = ring * kRing + static_cast<int>(t % kRing);
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(stage_empty(s), (static_cast<uint32_t>(t / kRing) & 1u) ^ 1u,
+                                                            a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT))) {
+                    ok = false;
+                    break;
+                }
+                // this lane's 8 pieces (16 bytes each) of rows 2 j + hi; zero-filled for
+                // slots past the unit's columns and columns past N
+                const uint32_t dst = s0 + kRingOff + s * kStepBytes + piece_off;
+                const int64_t left = a.N - n;
+                const uint32_t nb = left >= 8 ? 16u : (left > 0 ? static_cast<uint32_t>(left) * 2u : 0u);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int sr = 2 * j + hi;  // slot within the step
+                    const int col = cols[16 * k + sr];
+                    const uint16_t* src = col >= 0 && nb ? a.B + static_cast<int64_t>(col) * a.ldb + n : a.B;
+                    ptx::cp_async16(dst + sr * 128u + (static_cast<uint32_t>(gq ^ (sr & 7)) << 4), src,
+                                    col >= 0 ? nb : 0u);
+                }
+                ptx::cp_async_arrive_noinc(stage_full(s));
+            }
+#pragma unroll
+            for (int r = 0; r < kIssuers; ++r)
+                if (ring == r) tr[r] = t0 + nk;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(item_empty(slot));
+        }
+        ptx::cp_async_wait<0>();  // no copy into shared memory outstanding at exit
+    } else if (warp < kEpiWarp0) {
+        // -------------------------------------------------------- MMA issuers
+        // issuer j takes items j, j + kIssuers, ... and their steps from ring j; it
+        // waits for each group of kGroup stages before one proxy fence and their MMAs
+        const int j = warp - kMmaWarp;
+        if (lane == 0) {
+            const uint64_t adesc0 = ptx::smem_desc(s0 + kRingOff, 2048u, 1024u, ptx::SWZ_128B);
+            int ic = 0;
+            int64_t t = 0;
+            bool ok = true;
+            for (int64_t id = first; id < a.n_items && ok; id += stride, ++ic) {
+                const int slot = ic % kSlots;
+                if (!ptx::mbar_wait(item_full(slot), static_cast<uint32_t>(ic / kSlots) & 1u, a.timeout_ns, a.err,
+                                    SPMM_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                const int nk = recs[slot].nk;
+                if (ic % kIssuers != j) {  // another issuer's item
+                    ptx::mbar_arrive(item_empty(slot));
+                    continue;
+                }
+                const int b = ic % kAcc;
+                if (!ptx::mbar_wait(acc_empty(b), (static_cast<uint32_t>(ic / kAcc) & 1u) ^ 1u, a.timeout_ns, a.err,
+                                    SPMM_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint64_t bdesc0 = ptx::smem_desc(s0 + kWOff + slot * kWBytes, 128u, 256u, ptx::SWZ_NONE);
+                const uint32_t d = tmem + static_cast<uint32_t>(b * kNp);
+                for (int k0 = 0; k0 < nk && ok; k0 += kGroup) {
+                    const int kn = nk - k0 < kGroup ? nk - k0 : kGroup;
+                    for (int k = k0; k < k0 + kn; ++k) {
+                        const int64_t tt = t + k;
+                        if (!ptx::mbar_wait(stage_full(j * kRing + static_cast<int>(tt % kRing)),
+                                            static_cast<uint32_t>(tt / kRing) & 1u, a.timeout_ns, a.err,
+                                            SPMM_DEVERR_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    ptx::fence_proxy_async_smem();  // the stages arrived through cp.async (generic proxy)
+                    for (int k = k0; k < k0 + kn; ++k) {
+                        const int s = j * kRing + static_cast<int>((t + k) % kRing);
+                        ptx::mma_f16(d, adesc0 + static_cast<uint64_t>(s) * (kStepBytes >> 4),
+                                     bdesc0 + static_cast<uint64_t>(k) * (kTile >> 4), a.idesc, k > 0 ? 1u : 0u);
+                        ptx::mma_commit(stage_empty(s));
+                    }
+                }
+                if (!ok) break;
+                t += nk;
+                ptx::mma_commit(acc_full(b));
+                ptx::mbar_arrive(item_empty(slot));
+            }
+            // leave no MMA in flight (after a timeout too)
+            ptx::mma_commit(done_bar(j));
+            ptx::mbar_wait(done_bar(j), 0, a.timeout_ns, a.err, SPMM_DEVERR_TIMEOUT);
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter: output columns 32 q .. 32 q + 31 of the slab
+        const int et = threadIdx.x - 32 * kEpiWarp0;  // 0 .. 127
+        int ic = 0;
+        bool ok = true;
+        for (int64_t id = first; id < a.n_items && ok; id += stride, ++ic) {
+            const int slot = ic % kSlots, b = ic % kAcc;
+            const bool waited = ptx::mbar_wait(item_full(slot), static_cast<uint32_t>(ic / kSlots) & 1u, a.timeout_ns,
+                                               a.err, SPMM_DEVERR_TIMEOUT) &&
+                                ptx::mbar_wait(acc_full(b), static_cast<uint32_t>(ic / kAcc) & 1u, a.timeout_ns, a.err,
+                                               SPMM_DEVERR_TIMEOUT);
+            if (!tc::bar_and(2, 32 * kEpiWarps, waited)) {  // the four warps leave together
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const Rec it = recs[slot];
+            const int64_t ncol = static_cast<int64_t>(it.n0) + 32 * q + lane;
+            const bool split = it.U > 1;
+            float* base = split ? a.partial + static_cast<int64_t>(it.u) * a.h * a.N
+                                : a.C + static_cast<int64_t>(it.r0) * a.ldc;
+            const int64_t ld = split ? a.N : a.ldc;
+            uint32_t v[16];
+            if (it.nk > 0) {
+                ptx::tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * kNp), v);
+                ptx::tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0u;  // a window without nonzeros
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(acc_empty(b));
+                ptx::mbar_arrive(item_empty(slot));
+            }
+            if (!it.ok) continue;
+            if (ncol < a.N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < it.nrows) {
+                        float* p = base + j * ld + ncol;
+                        if (split)
+                            __stcg(p, __uint_as_float(v[j]));
+                        else
+                            __stcs(p, __uint_as_float(v[j]));
+                    }
+            }
+            if (!split) continue;
+            // split window: the last of its units (arrival counter) sums the partials
+            // of all units in unit order
+            __threadfence();
+            ptx::named_barrier(2, 32 * kEpiWarps);
+            if (et == 0) {
+                unsigned long long* tk = a.ticket + static_cast<int64_t>(it.w) * a.nslabs + it.n0 / kSlab;
+                int last = 0;
+                if (open_tag(tk, a.gen, a.err)) {
+                    const unsigned long long old = atomicAdd(tk, 1ull);
+                    last = static_cast<int>(old & 0xffffffffull) == it.U - 1;
+                }
+                *s_last = last;
+            }
+            ptx::named_barrier(2, 32 * kEpiWarps);
+            const int last = *s_last;
+            ptx::named_barrier(2, 32 * kEpiWarps);  // s_last is rewritten by the next split item
+            if (!last) continue;
+            __threadfence();
+            if (ncol < a.N) {
+                for (int rb = 0; rb < it.nrows; rb += 8) {
+                    float acc[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+                    for (int k = 0; k < it.U; ++k) {
+                        const float* pp = a.partial + (static_cast<int64_t>(it.u0 + k) * a.h + rb) * a.N + ncol;
+                        float x[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) x[j] = rb + j < it.nrows ? __ldcg(pp + j * a.N) : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[j] += x[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (rb + j < it.nrows) a.C[(static_cast<int64_t>(it.r0) + rb + j) * a.ldc + ncol] = acc[j];
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace ts
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BuildWs {
@@ -1261,6 +1677,51 @@ spmm_status launch_wcsr_tc(const DeviceInfo* dev, const spmm_wcsr_t* A, const vo
     return cuda_status(e);
 }
 
+spmm_status launch_wcsr_ts(const DeviceInfo* dev, const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C,
+                           int64_t ldc, int64_t N, void* ws, cudaStream_t s) {
+    tc::Args a{};
+    a.wcol_ptr = A->wcol_ptr;
+    a.wcols = A->wcols;
+    a.unit_ptr = A->unit_ptr;
+    a.unit_win = A->unit_win;
+    a.unit_nz_ptr = A->unit_nz_ptr;
+    a.lrow = A->lrow;
+    a.slot = A->slot;
+    a.val = static_cast<const uint16_t*>(A->val);
+    a.B = static_cast<const uint16_t*>(B);
+    a.ldb = ldb;
+    a.C = C;
+    a.ldc = ldc;
+    a.M = A->M;
+    a.K = A->K;
+    a.N = N;
+    a.h = A->h;
+    a.S = A->S;
+    a.Np = ts::kNp;
+    a.nslabs = static_cast<int32_t>(wcsr_nslabs(N));
+    a.n_windows = A->n_windows;
+    a.n_units = A->n_units;
+    a.n_items = A->n_units * a.nslabs;
+    a.b_vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 8 == 0);
+    a.idesc = ptx::idesc_f16(128, ts::kNp, A->dtype == SPMM_BF16, true, false, false);
+    a.gen = next_gen();
+    const SpmmWs w = carve_spmm(ws, A, N);
+    a.ticket = w.ticket;
+    a.partial = w.partial;
+    a.err = dev->err;
+    a.timeout_ns = kWaitTimeoutNs;
+    warmup_set(a, A, B, ldb, N);
+    const unsigned grid = static_cast<unsigned>(a.n_items < dev->sms ? a.n_items : dev->sms);
+    const int smem = static_cast<int>(ts::kSmem);
+    if (dev->max_smem_optin < smem) return SPMM_ERR_UNSUPPORTED;
+    if (!set_smem_attr_once(reinterpret_cast<const void*>(ts::wcsr_ts_kernel), smem, 21)) return SPMM_ERR_CUDA;
+    trace_begin(SPMM_KERNEL_WCSR, s);
+    ts::wcsr_ts_kernel<<<grid, ts::kThreads, smem, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(SPMM_KERNEL_WCSR, s);
+    return cuda_status(e);
+}
+
 spmm_status launch_wcsr_cc(const DeviceInfo* dev, const spmm_wcsr_t* A, const void* B, int64_t ldb, float* C,
                            int64_t ldc, int64_t N, void* ws, cudaStream_t s) {
     cc::WcsrArgs a{};
@@ -1328,8 +1789,12 @@ spmm_status launch_wcsr(const spmm_wcsr_t* A, const void* B, int64_t ldb, float*
     const DeviceInfo* dev = device_info();
     if (!dev) return SPMM_ERR_CUDA;
     if (A->M == 0 || N == 0) return SPMM_OK;
-    if (wcsr_uses_tensor_core(A)) return launch_wcsr_tc(dev, A, B, ldb, C, ldc, N, ws, s);
-    return launch_wcsr_cc(dev, A, B, ldb, C, ldc, N, ws, s);
+    if (!wcsr_uses_tensor_core(A)) return launch_wcsr_cc(dev, A, B, ldb, C, ldc, N, ws, s);
+    // windows of at most 16 rows and at most 32 steps per unit: the streaming kernel
+    // (clustered windows, 65536 x 65536, N = 128: 62 us against 66); B rows start on
+    // 16-byte boundaries (checked by the entry point), as its 16-byte copies need
+    if (A->h <= ts::kNp && A->S <= ts::kMaxSteps) return launch_wcsr_ts(dev, A, B, ldb, C, ldc, N, ws, s);
+    return launch_wcsr_tc(dev, A, B, ldb, C, ldc, N, ws, s);
 }
 
 bool wcsr_uses_tensor_core(const spmm_wcsr_t* A) {
