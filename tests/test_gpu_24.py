@@ -56,14 +56,44 @@ def test_24_int8_prewidened_values(M, K, N):
         assert np.array_equal(C.cpu().numpy().astype(np.int64), oracle.spmm24(O, Bh))
 
 
-def test_24_int8_extreme_values_stay_exact():
+def _int8_b(B, ld):
+    """int8 B on the device as a K x N view of rows ld bytes apart."""
+    import torch
+    K, N = B.shape
+    full = torch.zeros((K, ld), dtype=torch.int8, device="cuda")
+    full[:, :N] = dev(B)
+    return full[:, :N]
+
+
+@pytest.mark.parametrize("M,K,N", [(328, 1024, 200), (128, 512, 72), (256, 2048, 128)])
+def test_24_int8_b_row_pitch(M, K, N):
+    """int8 B with rows padded past N (pitch a multiple of 16 bytes) and with an odd
+    pitch equals the oracle bit for bit: ragged N, a ragged last pair of row tiles,
+    one row tile, with and without values widened beforehand."""
+    torch = need_gpu()
+    import sparse_dense_matrix_spmm_gb300 as spmm
+    p = gen.mask24_problem(M, K, N, seed=M + K + N + 1)
+    F, O = _compress(p, "i8")
+    W = spmm.spmm_widen_24(F)
+    ref = oracle.spmm24(O, p["B"])
+    ld16 = -(-N // 16) * 16 + 16          # rows on 16-byte boundaries, padded past N
+    for B in (_int8_b(p["B"], ld16), _int8_b(p["B"], N + 1)):
+        for A in (F, W):
+            C = spmm.spmm_24(A, B)
+            torch.cuda.synchronize()
+            assert spmm.last_device_error() == 0
+            assert np.array_equal(C.cpu().numpy().astype(np.int64), ref), (B.stride(0), A is W)
+
+
+@pytest.mark.parametrize("M", [128, 256])  # one row tile, a pair of row tiles
+def test_24_int8_extreme_values_stay_exact(M):
     """Every product 127*127 with equal signs: the kernel drains its fp32
     accumulator every 2048 dense K, so each chunk of 1024 products reaches the
     largest partial sum it can hold exactly (1024 * 16129 < 2^24), and any lost
     bit would show."""
     torch = need_gpu()
     import sparse_dense_matrix_spmm_gb300 as spmm
-    M, K, N = 128, 4096, 128
+    K, N = 4096, 128
     A = np.zeros((M, K), np.int8)
     A[:, 0::4] = 127
     A[:, 3::4] = 127
