@@ -10,11 +10,14 @@
 // serialise on one warp), finds the slice's first row by binary search in
 // row_ptr (a dependent chain of about log2(M) loads, so slices are long), and
 // preloads the slice's (row, column) pairs with coalesced loads into shared
-// memory, where the lane groups read them.  L = min(32, K / E) lanes form one
-// output's group: each lane loads E elements (16 bytes: E = 8 for 16-bit
-// types, 16 for int8) of A's row and of Bt's row per step, and the group sums
-// by shuffles.  Each lane keeps ILP outputs in
-// flight to hide the latency of the Bt row gathers.
+// memory, where the lane groups read them.  Four lanes form one output's group:
+// each lane loads E elements (16 bytes: E = 8 for 16-bit types, 16 for int8)
+// of A's row and of Bt's row per step, K / (4 E) steps, and the group sums by
+// two shuffle rounds.  Each lane keeps kIlp outputs in flight to hide the
+// latency of the Bt row gathers.  The kernel is bound by instruction issue, and
+// few lanes per output spend few shuffles on it (measured at K = 128 on the
+// 65536^2 log-normal pattern: 4 lanes 53.9 us fp16 / 33.4 us int8, 16 and 8
+// lanes 70.3 / 37.5 us, 2 lanes 58.0 / 39.6 us, 1 lane 92.8 / 56.0 us).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -24,12 +27,10 @@ namespace spmm {
 namespace {
 
 constexpr int kIlp = 4;
-// passes of G * kIlp entries per warp: the slice's binary search is amortised
-// over them.  int8 rows are half as long, so its passes are shorter and more
-// warps share the entries (measured on the 65536^2 log-normal pattern, K = 128:
-// 8 passes 47.8 us, 16 passes 56.0 us; fp16 keeps 16: 78.5 us vs 92.8 us).
-template <typename T>
-__host__ __device__ constexpr int passes() { return sizeof(T) == 1 ? 8 : 16; }
+constexpr int kLanes = 4;     // lanes per output
+// entries per warp: passes of (32 / kLanes) * kIlp entries amortise the slice's
+// binary search (128 entries measured best at 16 lanes per output too)
+constexpr int kSliceEntries = 128;
 constexpr int kThreads = 256;
 
 template <typename T>
@@ -99,16 +100,18 @@ struct SddmmArgs {
 
 // Four CTAs (32 warps) per SM: the register cap of 64 fits the kernel without
 // spills and keeps a third more gathers in flight than the 80 registers it
-// takes unbounded (measured at K = 128: 68 us against 79 us for fp16, 38 us
-// against 48 us for int8; five or more CTAs spill and run slower).
+// takes unbounded (measured at K = 128 with 16 lanes per output: 68 us against
+// 79 us for fp16, 38 us against 48 us for int8; five or more CTAs spilled and ran
+// slower).
 template <typename T, int L>
 __global__ void __launch_bounds__(kThreads, 4) sddmm_kernel(const SddmmArgs a) {
     using Acc = typename Sd<T>::Acc;
     constexpr int E = Sd<T>::E;
     constexpr int G = 32 / L;                   // outputs per warp per pass
     constexpr int kPer = G * kIlp;              // entries per pass
-    constexpr int kPasses = passes<T>();
+    constexpr int kPasses = kSliceEntries / kPer;
     constexpr int kSlice = kPer * kPasses;      // entries per warp
+    static_assert(kPasses > 0 && kSlice == kSliceEntries, "whole passes per slice");
     constexpr int kRegs = kSlice / 32;          // (row, column) pairs each lane preloads
     static_assert(kSlice % 32 == 0, "whole warp loads of the slice's indices");
     const int lane = threadIdx.x & 31, sub = lane / L, sl = lane % L;
@@ -211,12 +214,6 @@ __global__ void __launch_bounds__(kThreads, 4) sddmm_kernel(const SddmmArgs a) {
     }
 }
 
-template <typename T>
-void launch_lanes(const SddmmArgs& a, int lanes, unsigned grid, cudaStream_t s) {
-    if (lanes == 8) sddmm_kernel<T, 8><<<grid, kThreads, 0, s>>>(a);
-    else if (lanes == 16) sddmm_kernel<T, 16><<<grid, kThreads, 0, s>>>(a);
-    else sddmm_kernel<T, 32><<<grid, kThreads, 0, s>>>(a);
-}
 
 }  // namespace
 
@@ -238,21 +235,17 @@ spmm_status launch_sddmm(const spmm_csr_t* S, int64_t K, const void* A, int64_t 
     a.ldb = ldbt;
     a.out = out;
     a.err = dev->err;
-    // lanes per output: one 16-byte load each covers E elements of K
-    const int E = S->dtype == SPMM_I8 ? 16 : 8;
-    const int lanes = K >= 32 * E ? 32 : (K >= 16 * E ? 16 : 8);
-    const int np = S->dtype == SPMM_I8 ? passes<int8_t>() : passes<__half>();
-    const int64_t slice = static_cast<int64_t>(32 / lanes) * kIlp * np;
-    const int64_t warps = (S->nnz + slice - 1) / slice;
+    const int64_t warps = (S->nnz + kSliceEntries - 1) / kSliceEntries;
     const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     if (blocks >= (int64_t(1) << 31)) return SPMM_ERR_UNSUPPORTED;
     trace_begin(SPMM_KERNEL_SDDMM, s);
+    const unsigned grid = static_cast<unsigned>(blocks);
     if (S->dtype == SPMM_I8)
-        launch_lanes<int8_t>(a, lanes, static_cast<unsigned>(blocks), s);
+        sddmm_kernel<int8_t, kLanes><<<grid, kThreads, 0, s>>>(a);
     else if (S->dtype == SPMM_BF16)
-        launch_lanes<__nv_bfloat16>(a, lanes, static_cast<unsigned>(blocks), s);
+        sddmm_kernel<__nv_bfloat16, kLanes><<<grid, kThreads, 0, s>>>(a);
     else
-        launch_lanes<__half>(a, lanes, static_cast<unsigned>(blocks), s);
+        sddmm_kernel<__half, kLanes><<<grid, kThreads, 0, s>>>(a);
     const cudaError_t e = cudaGetLastError();
     trace_end(SPMM_KERNEL_SDDMM, s);
     return cuda_status(e);
