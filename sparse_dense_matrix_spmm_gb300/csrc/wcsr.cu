@@ -16,27 +16,37 @@
 //           position of e = window start + nonzeros of earlier units + nonzeros of
 //                           earlier rows in e's unit + rank inside its row segment
 //
-// SpMM.  On the synthetic power-law workload the windows are about 6% dense
-// (uniform columns), so the contraction per window is not a dense tile: the
-// kernel runs on CUDA cores.  Each nonzero gathers one B row (N * 2 bytes) from
-// L2; with one CTA per work unit the kernel is bound by instruction issue and
-// by the chain of dependent loads per unit (unit header, window header and
-// nonzeros, column list, B rows), so occupancy (8 CTAs of 4 warps per SM) and
-// instructions per nonzero decide its rate.  The CTA stages the unit's sparse
-// operand in shared memory as {column, local row | value} (all of a thread's
-// slots requested before any column is resolved), then cuts it into eight
-// contiguous streams, one per half-warp.  The 16 lanes of a half read one B
-// row per load (8 columns, 16 bytes, each), accumulate with one mixed-precision
-// FMA per element (16-bit operands, fp32 accumulator; the same result as
-// converting both and using fmaf), write rows that lie inside the stream into
-// a shared-memory tile, and hand the two rows at the stream's ends to a fix-up
-// that adds them in stream order, so every sum has a fixed order.  Rows never
-// decrease along a stream, so a batch whose last entry is on the current row
-// needs no per-entry row test.  Unsplit windows write C from the tile; a split
-// window's units write partial tiles to the workspace, and the last unit to
-// finish (ticket counter) sums them in unit order, with several loads in
-// flight per thread, and resets the counter.  The first wave of CTAs prefetches
-// the format arrays and B into L2 with bulk prefetches.
+// SpMM: three kernels, chosen from the format's counts (wcsr_uses_tensor_core).
+//  - Windows whose columns hold about one nonzero each (the synthetic power-law
+//    workload: windows ~6% dense) run on CUDA cores (cc::wcsr_spmm_kernel): a
+//    dense tile per window would gather as many B rows as the plain product.
+//    Each nonzero gathers one B row (N * 2 bytes) from L2; with one CTA per work
+//    unit the kernel is bound by instruction issue and by the chain of dependent
+//    loads per unit (unit header, window header and nonzeros, column list, B
+//    rows), so occupancy (8 CTAs of 4 warps per SM) and instructions per nonzero
+//    decide its rate.  The CTA stages the unit's sparse operand in shared memory
+//    as {column, local row | value} (all of a thread's slots requested before
+//    any column is resolved), then cuts it into eight contiguous streams, one
+//    per half-warp.  The 16 lanes of a half read one B row per load (8 columns,
+//    16 bytes, each), accumulate with one mixed-precision FMA per element
+//    (16-bit operands, fp32 accumulator; the same result as converting both and
+//    using fmaf), write rows that lie inside the stream into a shared-memory
+//    tile, and hand the two rows at the stream's ends to a fix-up that adds them
+//    in stream order, so every sum has a fixed order.  Rows never decrease along
+//    a stream, so a batch whose last entry is on the current row needs no
+//    per-entry row test.  The first wave of CTAs prefetches the format arrays
+//    and B into L2 with bulk prefetches.
+//  - Windows that reuse their columns run their window products on the tensor
+//    core: per 16 column slots, the 16 gathered B rows (128 output columns on
+//    the MMA's M) times the window's value tile (window rows on N), fp32 in
+//    TMEM.  Windows of at most 16 rows take the streaming kernel
+//    (ts::wcsr_ts_kernel: preparation, gathers, MMA issue and epilogue in
+//    separate warps over a persistent item sequence), taller ones the per-item
+//    kernel (tc::wcsr_tc_kernel: four warpgroups, each on its own items).
+// In every kernel, unsplit windows write C directly; a split window's units
+// write partial tiles to the workspace, and the last unit to finish (an
+// arrival counter tagged with the call's generation, so the workspace needs no
+// clearing) sums them in unit order.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
