@@ -7,8 +7,8 @@
 // A dot product of two contiguous K-vectors per output: HBM- and
 // gather-bound work for CUDA cores, not a contraction for the tensor core.
 // Each warp takes a fixed slice of the nonzero array (so one long row does not
-// serialise on one warp), finds the slice's first row by binary search in
-// row_ptr (a dependent chain of about log2(M) loads, so slices are long), and
+// serialise on one warp), finds the slice's first row by a 32-way search in
+// row_ptr (about log32(M) rounds of dependent loads, so slices are long), and
 // preloads the slice's (row, column) pairs with coalesced loads into shared
 // memory, where the lane groups read them.  Four lanes form one output's group:
 // each lane loads E elements (16 bytes: E = 8 for 16-bit types, 16 for int8)
