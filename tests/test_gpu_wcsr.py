@@ -161,6 +161,7 @@ def _tensor_core_path(W):
     (333, 5000, 72, 16, 2, 64, 56),        # ragged last window, ragged N, S = 2: every window split in two
     (500, 9000, 200, 32, 4, 96, 32),       # taller windows, two slabs (128 + 72 columns), splits
     (260, 3000, 136, 8, 4, 64, 56),        # h = 8 (MMA N rounded up to 16)
+    (384, 6000, 200, 16, 4, 96, 56),       # 16-row windows (streaming kernel) over two slabs, every window split
     (200, 2500, 64, 48, 32, 200, 20),      # h = 48: several chunks of W tiles per unit
     (320, 4000, 128, 64, 4, 128, 40),      # h = 64, the largest window (MMA N = 64), split windows
 ])
